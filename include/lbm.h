@@ -1,0 +1,177 @@
+/*
+ * lbm.h -- C ABI of the GB300 D3Q19 BGK lattice Boltzmann library (liblbm.so).
+ *
+ * One context = one dense nx*ny*nz lattice on the current CUDA device, advanced by fused
+ * stream-collide kernels on one CUDA stream.  Sources, cited by page title and section:
+ *
+ *  [PortLBM]  "PortLBM: A Portable Lattice Boltzmann Tool Leveraging SYCL on AMD, NVIDIA, and
+ *             Intel GPUs": §3.1 Eq. 1 (BGK update, time step 1), Eq. 2 (second-order
+ *             equilibrium, 2D incompressible variant), last paragraph of §3.1 (equilibrium inlet,
+ *             halfway bounce-back, outlet), §3.2 and Fig. 2 (stream / collision / bundle
+ *             layouts), §3.3 Eq. 3 (collision + streaming; one-step pull, two lattices).
+ *  [Layout]   "GPU lattice Boltzmann: streaming layout and performance": the "In place" bullet
+ *             (AA addressing, 152 population bytes per cell update), the "Two buffers" bullet
+ *             (collide in place, then pull: 304 bytes), the paragraph after them (the same
+ *             per-link wall / reflection / open-face rules in both; gather before scatter; the
+ *             momentum exchange of a submission's last step), and `Streaming::Auto`.
+ *  [Blog]     "GPU加速LBM流体仿真：从原理到150倍性能优化实战": §2.2 (D3Q19 weights 1/3, 1/18,
+ *             1/36), §5.1 (omega = 1/(3 nu + 1/2): stability requires tau > 1/2).
+ *
+ * Velocity set (fixed by this ABI; [Blog] §2.2 gives the classes rest / 6 axis / 12 diagonal):
+ *   q : 0 (0,0,0)   1 (+1,0,0)  2 (-1,0,0)  3 (0,+1,0)  4 (0,-1,0)  5 (0,0,+1)  6 (0,0,-1)
+ *       7 (+1,+1,0) 8 (-1,-1,0) 9 (+1,0,+1) 10 (-1,0,-1) 11 (0,+1,+1) 12 (0,-1,-1)
+ *       13 (+1,-1,0) 14 (-1,+1,0) 15 (+1,0,-1) 16 (-1,0,+1) 17 (0,+1,-1) 18 (0,-1,+1)
+ *   weights w0 = 1/3, w1..w6 = 1/18, w7..w18 = 1/36; opposite(q) = q+1 for odd q, q-1 for even
+ *   q > 0, opposite(0) = 0.
+ *
+ * Canonical array conventions at this ABI (the internal layout is never visible):
+ *   cell index  n = x + nx*(y + ny*z), N = nx*ny*nz;
+ *   populations f[q*N + n], fp32, absolute values, the natural (pre-collision) state f(x, t);
+ *   flags       uint8 per cell: LBM_FLUID, LBM_SOLID (bounce-back), LBM_INLET (reservoir held at
+ *               f_eq(rho_in, u_in), never updated);
+ *   rho[n], u[a*N + n] (a = 0,1,2), fp32.
+ *
+ * The step.  Per time step every FLUID cell x collides (BGK, relaxation omega = 1/tau,
+ * equilibrium w rho [1 + 3 c.u + 9/2 (c.u)^2 - 3/2 u.u], c_s^2 = 1/3; with a body acceleration g
+ * Guo forcing: F = rho g, u = j/rho + g/2, source (1 - omega/2) w [3 (c - u).F + 9 (c.u)(c.F)])
+ * and then receives population q from s = x - c_q, wrapped on PERIODIC axes and clamped onto the
+ * last layer on OPEN axes (zero-gradient): FLUID s gives its post-collision f*_q(s); SOLID s
+ * reflects x's own f*_opposite(q)(x) (halfway bounce-back); INLET s gives f_eq,q(rho_in, u_in).
+ *
+ * Ownership and threading.  The caller owns every array it passes; the library keeps no caller
+ * pointer after a call returns.  Array arguments may be device pointers or host pointers (pinned
+ * or pageable); host data is staged through the library's own buffers.  A context is used by one
+ * host thread at a time.  Calls that only enqueue work (lbm_step) are asynchronous on the
+ * context's stream; calls that return data to the caller synchronise that stream.
+ *
+ * Errors.  Functions returning int give LBM_OK (0) or a negative LBM_E* code; lbm_create returns
+ * NULL on failure.  The message for the calling thread's last failure is lbm_last_error().  A call
+ * that fails argument validation changes nothing; a CUDA failure (LBM_ECUDA) leaves the context
+ * usable only for lbm_destroy.
+ */
+#ifndef LBM_H
+#define LBM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct lbm_ctx lbm_ctx;
+
+/* Population layouts ([PortLBM] §3.2, Fig. 2).  STREAM: SoA, f[q][n].  COLLISION: AoS,
+ * f[n][q].  BUNDLE: SoAoS; the populations are grouped by (c_y, c_z) into 9 bundles (the x-rows
+ * of the stencil: five of three members ordered c_x = -1, 0, +1, four of one), and bundle b of
+ * size m_b stores f[b-offset*N + n*m_b + j]. */
+enum { LBM_LAYOUT_STREAM = 0, LBM_LAYOUT_BUNDLE = 1, LBM_LAYOUT_COLLISION = 2 };
+
+/* Streaming schemes.  AA ([Layout] "In place"): one buffer; even steps read (q, x) and write the
+ * collided value at (opposite(q), x); odd steps read (opposite(q), x - c_q) and write (q, x + c_q);
+ * 152 population bytes per cell update.  AB: two buffers, fused pull-collide ([PortLBM] §3.3
+ * one-step pull two-lattice), also 152 bytes per update.  AB2: two buffers, [Layout] "Two
+ * buffers" form: collide in place, then pull into the other buffer, 304 bytes per update.  AUTO
+ * resolves to AA, as [Layout]'s `Streaming::Auto` does. */
+enum { LBM_STREAMING_AUTO = 0, LBM_STREAMING_AA = 1, LBM_STREAMING_AB = 2, LBM_STREAMING_AB2 = 3 };
+
+enum {
+    LBM_OK = 0,
+    LBM_EINVAL = -1,     /* invalid argument                                               */
+    LBM_ENOMEM = -2,     /* device or host allocation failed                               */
+    LBM_ECUDA = -3,      /* CUDA runtime error (message in lbm_last_error)                  */
+    LBM_ESTATE = -4,     /* call not valid in the current state (e.g. force before a step)  */
+    LBM_ENOTFINITE = -5  /* lbm_check_finite found a NaN or infinity                         */
+};
+
+enum { LBM_FLUID = 0, LBM_SOLID = 1, LBM_INLET = 2 };
+enum { LBM_PERIODIC = 0, LBM_OPEN = 1 };
+
+/* Create a context on the current CUDA device.  nx, ny, nz >= 1, nz <= 65535, N <= 2^31 - 1,
+ * tau > 1/2 and finite ([Blog] §5.1: omega = 1/tau must stay below 2).  Allocates the population
+ * buffer(s) (AA: one, AB/AB2: two, 76 N bytes each) and the flag array.  Initial state: every cell
+ * FLUID, all faces PERIODIC, g = 0, inlet (1, 0, 0, 0), f = w_q (rest at rho = 1), step count 0,
+ * stream 0 (the legacy default stream).  Returns NULL on error (see lbm_last_error). */
+lbm_ctx* lbm_create(int nx, int ny, int nz, float tau, int layout, int streaming);
+
+/* Message for the calling thread's most recent failure ("" if none).  Valid until that thread's
+ * next call into the library. */
+const char* lbm_last_error(void);
+
+/* Use `cuda_stream` (a cudaStream_t, e.g. torch.cuda.current_stream().cuda_stream) for all later
+ * work of this context.  Work already enqueued on the previous stream is synchronised first. */
+int lbm_set_stream(lbm_ctx* ctx, void* cuda_stream);
+
+/* Cell flags, N bytes, LBM_FLUID / LBM_SOLID / LBM_INLET ([PortLBM] §3.1 boundary treatment;
+ * [Layout]: the per-link rules are driven by the cell type).  Any other value -> LBM_EINVAL.
+ * Changing flags does not touch the populations.  Synchronous. */
+int lbm_set_flags(lbm_ctx* ctx, const uint8_t* flags);
+
+/* Face type per axis: LBM_PERIODIC (wrap) or LBM_OPEN (zero-gradient: a population whose source
+ * lies beyond the face comes from the source clamped onto the last layer).  An OPEN axis needs at
+ * least 2 cells. */
+int lbm_set_faces(lbm_ctx* ctx, int face_x, int face_y, int face_z);
+
+/* State held by every INLET cell: f = f_eq(rho, (ux, uy, uz)).  rho > 0 and finite. */
+int lbm_set_inlet(lbm_ctx* ctx, float rho, float ux, float uy, float uz);
+
+/* Body acceleration g (force density F = rho g), applied with Guo forcing.  0 disables it. */
+int lbm_set_body_force(lbm_ctx* ctx, float gx, float gy, float gz);
+
+/* Load the natural state f(x, t) from f[19*N] (canonical, absolute fp32).  Values of SOLID and
+ * INLET cells are ignored.  Resets the step count to 0 (AA even parity).  Synchronous. */
+int lbm_set_populations(lbm_ctx* ctx, const float* f);
+
+/* Load f = f_eq(rho[n], u[.][n]) for every FLUID cell, computed on the device in fp32
+ * ([PortLBM] Eq. 2 in its 3D compressible form).  rho[N] > 0, u[3*N].  Resets the step count to 0.
+ * Synchronous. */
+int lbm_set_equilibrium(lbm_ctx* ctx, const float* rho, const float* u);
+
+/* Read the natural state f(x, t) into f[19*N] (canonical, absolute fp32), whatever the AA parity
+ * or A-B buffer state: after an odd AA step count the streaming half of the next step is applied
+ * on the fly.  SOLID cells read 0, INLET cells f_eq(rho_in, u_in).  Synchronous. */
+int lbm_get_populations(lbm_ctx* ctx, float* f);
+
+/* Enqueue n >= 0 time steps ([PortLBM] Eq. 1 with the per-link rules above) on the context
+ * stream.  The last of the n steps also computes the momentum-exchange force of its
+ * post-collision state (read with lbm_force_momentum_exchange).  Asynchronous; n = 0 is a no-op
+ * that leaves the last force unchanged. */
+int lbm_step(lbm_ctx* ctx, int n);
+
+/* Density and velocity of the natural state: rho[N], u[3*N] (fp32).  FLUID: rho = sum f,
+ * u = j/rho + g/2 (Guo's half-force shift).  SOLID: 0, 0.  INLET: rho_in, u_in.  Synchronous. */
+int lbm_macroscopic(lbm_ctx* ctx, float* rho, float* u);
+
+/* Force on all SOLID cells (one body) from the last step of the last lbm_step call
+ * ([Layout]: the momentum exchange is taken in the step whose forces are read back): the sum
+ * over every bounce-back link of a FLUID cell of 2 c_q f*_q, accumulated in fp32 per cell and in
+ * fp64 across cells, in a fixed order.  F[3] in lattice units.  LBM_ESTATE before the first step
+ * or after the state was reloaded.  Synchronous. */
+int lbm_force_momentum_exchange(lbm_ctx* ctx, double F[3]);
+
+/* LBM_OK if every population of every FLUID cell is finite, LBM_ENOTFINITE otherwise.
+ * Synchronous. */
+int lbm_check_finite(lbm_ctx* ctx);
+
+/* Time steps taken since the last state load (lbm_set_populations / lbm_set_equilibrium). */
+int64_t lbm_step_count(lbm_ctx* ctx);
+
+/* Number of this library's kernels launched for this context so far (for accounting). */
+int64_t lbm_kernel_launches(lbm_ctx* ctx);
+
+/* Per-kernel timing ([Layout] "Measuring": per-kernel GPU time on request).  enable != 0 records
+ * a CUDA event pair around every step kernel launched afterwards; lbm_profile_read returns, for
+ * kernel kind `kind` (0 AA even, 1 AA odd, 2 A-B pull, 3 A-B collide, 4 stream, 5 open-face
+ * gather, 6 force reduce), the number of launches and their summed milliseconds since profiling
+ * was enabled, and synchronises the stream. */
+int lbm_profile_enable(lbm_ctx* ctx, int enable);
+int lbm_profile_read(lbm_ctx* ctx, int kind, int64_t* launches, double* total_ms);
+
+/* Release every resource of the context.  NULL-safe.  Synchronises its stream first. */
+void lbm_destroy(lbm_ctx* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LBM_H */
