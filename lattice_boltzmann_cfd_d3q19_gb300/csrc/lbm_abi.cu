@@ -1,0 +1,614 @@
+// C ABI of the D3Q19 BGK library: context, buffers, the step sequence and host/device transfers.
+// The arithmetic lives in the kernels (lbm_kernels.cuh); this file only validates arguments,
+// owns device memory and enqueues launches on the context's stream.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <string>
+#include <utility>
+#include <vector>
+
+#include "lbm.h"
+#include "lbm_launch.h"
+
+using namespace lbm;
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+    if (e == cudaErrorMemoryAllocation)
+        return fail(LBM_ENOMEM, "%s: out of device memory (%s)", what, cudaGetErrorString(e));
+    return fail(LBM_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define LBM_CUDA(call, what)                                  \
+    do {                                                      \
+        cudaError_t e_ = (call);                              \
+        if (e_ != cudaSuccess) return cuda_fail(e_, (what));  \
+    } while (0)
+
+bool is_device_pointer(const void* p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
+// f_eq(rho, u) - w in double, rounded once (host-side inlet constant).
+void shifted_equilibrium(double rho, const double u[3], float out[19]) {
+    const double uu = u[0] * u[0] + u[1] * u[1] + u[2] * u[2];
+    for (int q = 0; q < 19; ++q) {
+        const double cu = cx(q) * u[0] + cy(q) * u[1] + cz(q) * u[2];
+        const double w = q == 0 ? 1.0 / 3.0 : q <= 6 ? 1.0 / 18.0 : 1.0 / 36.0;
+        out[q] = (float)(w * (rho - 1.0 + rho * (3.0 * cu + 4.5 * cu * cu - 1.5 * uu)));
+    }
+}
+
+constexpr size_t kStagingFloats = size_t(32) << 20;  // 128 MiB host-transfer staging
+
+}  // namespace
+
+struct lbm_ctx {
+    int n[3] = {0, 0, 0};
+    size_t N = 0;
+    float tau = 0.f, omega = 0.f;
+    int layout = 0, streaming = 0;
+    const LayoutOps* ops = nullptr;
+    int face[3] = {LBM_PERIODIC, LBM_PERIODIC, LBM_PERIODIC};
+    float g[3] = {0.f, 0.f, 0.f};
+    float inlet[4] = {1.f, 0.f, 0.f, 0.f};
+    float heq_in[19] = {};
+    float* buf[2] = {nullptr, nullptr};
+    int cur = 0;
+    int state = ST_NATURAL;
+    uint8_t* types = nullptr;
+    uint8_t* flags = nullptr;
+    float* scratch = nullptr;
+    size_t face_base[3][2] = {};
+    double* partial = nullptr;
+    size_t nblocks = 0;
+    double* force_dev = nullptr;
+    double* force_host = nullptr;
+    int* err_dev = nullptr;
+    int* err_host = nullptr;
+    float* staging = nullptr;
+    cudaStream_t stream = nullptr;
+    int64_t steps = 0;
+    bool force_valid = false;
+    int64_t launches = 0;
+    dim3 grid, block;
+    bool profiling = false;
+    std::vector<std::pair<cudaEvent_t, cudaEvent_t>> prof[K_NUM_KINDS];
+    std::vector<cudaEvent_t> event_pool;
+
+    Params params(float* A, float* B) const {
+        Params p;
+        p.A = A;
+        p.B = B;
+        p.flags = flags;
+        p.scratch = scratch;
+        p.partial = partial;
+        p.nx = n[0];
+        p.ny = n[1];
+        p.nz = n[2];
+        for (int a = 0; a < 3; ++a) p.open[a] = face[a] == LBM_OPEN;
+        p.N = N;
+        for (int a = 0; a < 3; ++a)
+            for (int s = 0; s < 2; ++s) p.face_base[a][s] = face_base[a][s];
+        p.omega = omega;
+        for (int a = 0; a < 3; ++a) p.g[a] = g[a];
+        for (int q = 0; q < 19; ++q) p.heq_in[q] = heq_in[q];
+        return p;
+    }
+    bool body() const { return g[0] != 0.f || g[1] != 0.f || g[2] != 0.f; }
+    bool any_open() const { return face[0] == LBM_OPEN || face[1] == LBM_OPEN || face[2] == LBM_OPEN; }
+    // buffer holding the current state and its meaning
+    float* state_buffer() const { return streaming == LBM_STREAMING_AA ? buf[0] : buf[cur]; }
+
+    cudaEvent_t take_event() {
+        cudaEvent_t e = nullptr;
+        if (!event_pool.empty()) {
+            e = event_pool.back();
+            event_pool.pop_back();
+        } else if (cudaEventCreate(&e) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        return e;
+    }
+    void release_profile() {
+        for (auto& v : prof) {
+            for (auto& pr : v) {
+                event_pool.push_back(pr.first);
+                event_pool.push_back(pr.second);
+            }
+            v.clear();
+        }
+    }
+    void free_all() {
+        if (stream) cudaStreamSynchronize(stream);
+        release_profile();
+        for (cudaEvent_t e : event_pool) cudaEventDestroy(e);
+        event_pool.clear();
+        cudaFree(buf[0]);
+        cudaFree(buf[1]);
+        cudaFree(types);
+        cudaFree(flags);
+        cudaFree(scratch);
+        cudaFree(partial);
+        cudaFree(force_dev);
+        cudaFree(err_dev);
+        cudaFree(staging);
+        cudaFreeHost(force_host);
+        cudaFreeHost(err_host);
+    }
+};
+
+namespace {
+
+const LayoutOps* ops_for(int layout) {
+    switch (layout) {
+        case LBM_LAYOUT_STREAM: return &layout_ops_stream();
+        case LBM_LAYOUT_BUNDLE: return &layout_ops_bundle();
+        case LBM_LAYOUT_COLLISION: return &layout_ops_collision();
+    }
+    return nullptr;
+}
+
+int ensure_staging(lbm_ctx* c) {
+    if (!c->staging) LBM_CUDA(cudaMalloc(&c->staging, kStagingFloats * sizeof(float)), "staging buffer");
+    return LBM_OK;
+}
+
+int classify(lbm_ctx* c) {
+    LBM_CUDA(launch_classify(c->params(nullptr, nullptr), c->types, c->flags, c->grid, c->block,
+                             c->stream), "classify flags");
+    ++c->launches;
+    return LBM_OK;
+}
+
+// Launch a step kernel, timed when profiling is on.
+int launch_kind(lbm_ctx* c, int kind, const Params& p, bool force) {
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    if (c->profiling) {
+        e0 = c->take_event();
+        e1 = c->take_event();
+        if (e0) cudaEventRecord(e0, c->stream);
+    }
+    cudaError_t e = cudaSuccess;
+    if (kind == K_PREGATHER) {
+        for (int a = 0; a < 3 && e == cudaSuccess; ++a)
+            if (c->face[a] == LBM_OPEN)
+                for (int s = 0; s < 2 && e == cudaSuccess; ++s) {
+                    e = c->ops->pregather(p, a, s, c->stream);
+                    ++c->launches;
+                }
+    } else if (kind == K_FORCE) {
+        e = launch_force_finalize(c->partial, c->nblocks, c->force_dev, c->stream);
+        ++c->launches;
+    } else {
+        e = c->ops->cells(kind, p, force, c->body(), c->grid, c->block, c->stream);
+        ++c->launches;
+    }
+    if (c->profiling && e0 && e1) {
+        cudaEventRecord(e1, c->stream);
+        c->prof[kind].emplace_back(e0, e1);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+    return LBM_OK;
+}
+
+int step_once(lbm_ctx* c, bool last) {
+    int rc = LBM_OK;
+    if (c->streaming == LBM_STREAMING_AA) {
+        const Params p = c->params(c->buf[0], c->buf[0]);
+        if (c->state == ST_NATURAL) {
+            rc = launch_kind(c, K_AA_EVEN, p, last);
+            c->state = ST_POST_AA;
+        } else {
+            if (c->any_open()) rc = launch_kind(c, K_PREGATHER, p, false);
+            if (rc == LBM_OK) rc = launch_kind(c, K_AA_ODD, p, last);
+            c->state = ST_NATURAL;
+        }
+    } else if (c->streaming == LBM_STREAMING_AB) {
+        const Params p = c->params(c->buf[c->cur], c->buf[c->cur ^ 1]);
+        rc = launch_kind(c, c->state == ST_NATURAL ? K_AB_COLLIDE : K_AB_PULL, p, last);
+        c->cur ^= 1;
+        c->state = ST_POST_AB;
+    } else {  // two-pass: collide in place, then pull into the other buffer
+        const Params pc = c->params(c->buf[c->cur], c->buf[c->cur]);
+        rc = launch_kind(c, K_AB_COLLIDE, pc, last);
+        if (rc == LBM_OK) {
+            const Params ps = c->params(c->buf[c->cur], c->buf[c->cur ^ 1]);
+            rc = launch_kind(c, K_STREAM, ps, false);
+        }
+        c->cur ^= 1;
+        c->state = ST_NATURAL;
+    }
+    if (rc == LBM_OK && last) rc = launch_kind(c, K_FORCE, c->params(nullptr, nullptr), false);
+    return rc;
+}
+
+int sync(lbm_ctx* c, const char* what) {
+    LBM_CUDA(cudaStreamSynchronize(c->stream), what);
+    return LBM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* lbm_last_error(void) { return g_err.c_str(); }
+
+lbm_ctx* lbm_create(int nx, int ny, int nz, float tau, int layout, int streaming) {
+    g_err.clear();
+    if (nx < 1 || ny < 1 || nz < 1) {
+        fail(LBM_EINVAL, "lbm_create: grid %d x %d x %d: every extent must be >= 1", nx, ny, nz);
+        return nullptr;
+    }
+    if (ny > 65535 || nz > 65535) {
+        fail(LBM_EINVAL, "lbm_create: ny and nz must be <= 65535 (got %d, %d)", ny, nz);
+        return nullptr;
+    }
+    const size_t N = (size_t)nx * (size_t)ny * (size_t)nz;
+    if (N > 2147483647u) {
+        fail(LBM_EINVAL, "lbm_create: %zu cells exceed the limit of 2^31 - 1", N);
+        return nullptr;
+    }
+    if (!std::isfinite(tau) || !(tau > 0.5f)) {
+        fail(LBM_EINVAL, "lbm_create: tau = %g: need a finite tau > 1/2 (omega = 1/tau < 2)",
+             (double)tau);
+        return nullptr;
+    }
+    const LayoutOps* ops = ops_for(layout);
+    if (!ops) {
+        fail(LBM_EINVAL, "lbm_create: unknown layout %d", layout);
+        return nullptr;
+    }
+    if (streaming < LBM_STREAMING_AUTO || streaming > LBM_STREAMING_AB2) {
+        fail(LBM_EINVAL, "lbm_create: unknown streaming scheme %d", streaming);
+        return nullptr;
+    }
+    if (std::getenv("LBM_FAIL_ALLOC")) {
+        fail(LBM_ENOMEM, "lbm_create: allocation refused (LBM_FAIL_ALLOC is set)");
+        return nullptr;
+    }
+    lbm_ctx* c = new (std::nothrow) lbm_ctx();
+    if (!c) {
+        fail(LBM_ENOMEM, "lbm_create: host allocation failed");
+        return nullptr;
+    }
+    c->n[0] = nx;
+    c->n[1] = ny;
+    c->n[2] = nz;
+    c->N = N;
+    c->tau = tau;
+    c->omega = 1.0f / tau;
+    c->layout = layout;
+    c->streaming = streaming == LBM_STREAMING_AUTO ? LBM_STREAMING_AA : streaming;
+    c->ops = ops;
+    const double u0[3] = {0.0, 0.0, 0.0};
+    shifted_equilibrium(1.0, u0, c->heq_in);
+    unsigned bx = 32;
+    while (bx < (unsigned)nx && bx < 256) bx *= 2;
+    c->block = dim3(bx, 256 / bx, 1);
+    c->grid = dim3((unsigned)((nx + bx - 1) / bx), (unsigned)((ny + c->block.y - 1) / c->block.y),
+                   (unsigned)nz);
+    c->nblocks = (size_t)c->grid.x * c->grid.y * c->grid.z;
+
+    auto bad = [&](cudaError_t e, const char* what) {
+        cuda_fail(e, what);
+        c->free_all();
+        delete c;
+        return nullptr;
+    };
+    cudaError_t e;
+    const size_t pop_bytes = 19 * N * sizeof(float);
+    if ((e = cudaMalloc(&c->buf[0], pop_bytes)) != cudaSuccess) return bad(e, "lbm_create: population buffer");
+    if (c->streaming != LBM_STREAMING_AA &&
+        (e = cudaMalloc(&c->buf[1], pop_bytes)) != cudaSuccess)
+        return bad(e, "lbm_create: second population buffer");
+    if ((e = cudaMalloc(&c->types, N)) != cudaSuccess) return bad(e, "lbm_create: cell types");
+    if ((e = cudaMalloc(&c->flags, N)) != cudaSuccess) return bad(e, "lbm_create: cell flags");
+    if ((e = cudaMalloc(&c->partial, 3 * c->nblocks * sizeof(double))) != cudaSuccess)
+        return bad(e, "lbm_create: force partials");
+    if ((e = cudaMalloc(&c->force_dev, 3 * sizeof(double))) != cudaSuccess) return bad(e, "lbm_create: force");
+    if ((e = cudaMalloc(&c->err_dev, sizeof(int))) != cudaSuccess) return bad(e, "lbm_create: error word");
+    if ((e = cudaMallocHost(&c->force_host, 3 * sizeof(double))) != cudaSuccess) return bad(e, "lbm_create: pinned force");
+    if ((e = cudaMallocHost(&c->err_host, sizeof(int))) != cudaSuccess) return bad(e, "lbm_create: pinned error word");
+    // rest state: h = f - w = 0 everywhere; all cells FLUID
+    if ((e = cudaMemsetAsync(c->buf[0], 0, pop_bytes, c->stream)) != cudaSuccess) return bad(e, "lbm_create: init");
+    if (c->buf[1] && (e = cudaMemsetAsync(c->buf[1], 0, pop_bytes, c->stream)) != cudaSuccess)
+        return bad(e, "lbm_create: init");
+    if ((e = cudaMemsetAsync(c->types, 0, N, c->stream)) != cudaSuccess) return bad(e, "lbm_create: init");
+    if (classify(c) != LBM_OK) {
+        c->free_all();
+        delete c;
+        return nullptr;
+    }
+    if ((e = cudaStreamSynchronize(c->stream)) != cudaSuccess) return bad(e, "lbm_create: init");
+    return c;
+}
+
+int lbm_set_stream(lbm_ctx* c, void* cuda_stream) {
+    if (!c) return fail(LBM_EINVAL, "lbm_set_stream: NULL context");
+    if (int rc = sync(c, "lbm_set_stream")) return rc;
+    c->stream = (cudaStream_t)cuda_stream;
+    return LBM_OK;
+}
+
+int lbm_set_flags(lbm_ctx* c, const uint8_t* flags) {
+    if (!c || !flags) return fail(LBM_EINVAL, "lbm_set_flags: NULL argument");
+    uint8_t* tmp = nullptr;
+    LBM_CUDA(cudaMalloc(&tmp, c->N), "lbm_set_flags: temporary");
+    int rc = LBM_OK;
+    cudaError_t e = cudaMemcpyAsync(tmp, flags, c->N, cudaMemcpyDefault, c->stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(c->err_dev, 0, sizeof(int), c->stream);
+    if (e == cudaSuccess) e = launch_validate_types(tmp, c->N, c->err_dev, c->stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(c->err_host, c->err_dev, sizeof(int), cudaMemcpyDeviceToHost, c->stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);
+    if (e != cudaSuccess) {
+        rc = cuda_fail(e, "lbm_set_flags");
+    } else if (*c->err_host) {
+        rc = fail(LBM_EINVAL, "lbm_set_flags: flag values must be 0 (FLUID), 1 (SOLID) or 2 (INLET)");
+    } else {
+        ++c->launches;
+        e = cudaMemcpyAsync(c->types, tmp, c->N, cudaMemcpyDeviceToDevice, c->stream);
+        if (e != cudaSuccess) rc = cuda_fail(e, "lbm_set_flags");
+        if (rc == LBM_OK) rc = classify(c);
+        if (rc == LBM_OK) rc = sync(c, "lbm_set_flags");
+    }
+    cudaFree(tmp);
+    return rc;
+}
+
+int lbm_set_faces(lbm_ctx* c, int fx, int fy, int fz) {
+    if (!c) return fail(LBM_EINVAL, "lbm_set_faces: NULL context");
+    const int f[3] = {fx, fy, fz};
+    for (int a = 0; a < 3; ++a) {
+        if (f[a] != LBM_PERIODIC && f[a] != LBM_OPEN)
+            return fail(LBM_EINVAL, "lbm_set_faces: face type %d on axis %d", f[a], a);
+        if (f[a] == LBM_OPEN && c->n[a] < 2)
+            return fail(LBM_EINVAL, "lbm_set_faces: an OPEN axis needs >= 2 cells (axis %d)", a);
+    }
+    // scratch for the AA odd step's open-face pre-gather: 19 values per face cell and side
+    size_t area[3] = {(size_t)c->n[1] * c->n[2], (size_t)c->n[0] * c->n[2], (size_t)c->n[0] * c->n[1]};
+    size_t total = 0, base[3][2] = {};
+    for (int a = 0; a < 3; ++a)
+        for (int s = 0; s < 2; ++s) {
+            base[a][s] = total;
+            if (f[a] == LBM_OPEN) total += 19 * area[a];
+        }
+    float* scratch = nullptr;
+    if (total > 0 && c->streaming == LBM_STREAMING_AA)
+        LBM_CUDA(cudaMalloc(&scratch, total * sizeof(float)), "lbm_set_faces: open-face scratch");
+    if (int rc = sync(c, "lbm_set_faces")) {
+        cudaFree(scratch);
+        return rc;
+    }
+    cudaFree(c->scratch);
+    c->scratch = scratch;
+    for (int a = 0; a < 3; ++a) {
+        c->face[a] = f[a];
+        for (int s = 0; s < 2; ++s) c->face_base[a][s] = base[a][s];
+    }
+    if (int rc = classify(c)) return rc;
+    return sync(c, "lbm_set_faces");
+}
+
+int lbm_set_inlet(lbm_ctx* c, float rho, float ux, float uy, float uz) {
+    if (!c) return fail(LBM_EINVAL, "lbm_set_inlet: NULL context");
+    if (!std::isfinite(rho) || !(rho > 0.f) || !std::isfinite(ux) || !std::isfinite(uy) ||
+        !std::isfinite(uz))
+        return fail(LBM_EINVAL, "lbm_set_inlet: need finite rho > 0 and finite u");
+    c->inlet[0] = rho;
+    c->inlet[1] = ux;
+    c->inlet[2] = uy;
+    c->inlet[3] = uz;
+    const double u[3] = {ux, uy, uz};
+    shifted_equilibrium(rho, u, c->heq_in);
+    return LBM_OK;
+}
+
+int lbm_set_body_force(lbm_ctx* c, float gx, float gy, float gz) {
+    if (!c) return fail(LBM_EINVAL, "lbm_set_body_force: NULL context");
+    if (!std::isfinite(gx) || !std::isfinite(gy) || !std::isfinite(gz))
+        return fail(LBM_EINVAL, "lbm_set_body_force: g must be finite");
+    c->g[0] = gx;
+    c->g[1] = gy;
+    c->g[2] = gz;
+    return LBM_OK;
+}
+
+static void reset_state(lbm_ctx* c) {
+    c->state = ST_NATURAL;
+    c->steps = 0;
+    c->force_valid = false;
+}
+
+int lbm_set_populations(lbm_ctx* c, const float* f) {
+    if (!c || !f) return fail(LBM_EINVAL, "lbm_set_populations: NULL argument");
+    float* dst = c->state_buffer();
+    const Params p = c->params(dst, dst);
+    const size_t total = 19 * c->N;
+    if (is_device_pointer(f)) {
+        LBM_CUDA(c->ops->pack(p, f, 0, total, c->stream), "lbm_set_populations: pack");
+        ++c->launches;
+    } else {
+        if (int rc = ensure_staging(c)) return rc;
+        for (size_t i0 = 0; i0 < total; i0 += kStagingFloats) {
+            const size_t cnt = total - i0 < kStagingFloats ? total - i0 : kStagingFloats;
+            LBM_CUDA(cudaMemcpyAsync(c->staging, f + i0, cnt * sizeof(float), cudaMemcpyDefault,
+                                     c->stream), "lbm_set_populations: copy");
+            LBM_CUDA(c->ops->pack(p, c->staging, i0, cnt, c->stream), "lbm_set_populations: pack");
+            ++c->launches;
+        }
+    }
+    reset_state(c);
+    return sync(c, "lbm_set_populations");
+}
+
+int lbm_set_equilibrium(lbm_ctx* c, const float* rho, const float* u) {
+    if (!c || !rho || !u) return fail(LBM_EINVAL, "lbm_set_equilibrium: NULL argument");
+    float* dst = c->state_buffer();
+    const Params p = c->params(dst, dst);
+    const size_t N = c->N;
+    if (is_device_pointer(rho) && is_device_pointer(u)) {
+        LBM_CUDA(c->ops->equilibrium(p, rho, u, u + N, u + 2 * N, 0, (uint32_t)N, c->stream),
+                 "lbm_set_equilibrium");
+        ++c->launches;
+    } else {
+        if (int rc = ensure_staging(c)) return rc;
+        const size_t chunk = kStagingFloats / 4;
+        for (size_t n0 = 0; n0 < N; n0 += chunk) {
+            const size_t cnt = N - n0 < chunk ? N - n0 : chunk;
+            float* s = c->staging;
+            LBM_CUDA(cudaMemcpyAsync(s, rho + n0, cnt * 4, cudaMemcpyDefault, c->stream), "lbm_set_equilibrium: copy");
+            for (int a = 0; a < 3; ++a)
+                LBM_CUDA(cudaMemcpyAsync(s + (a + 1) * chunk, u + a * N + n0, cnt * 4, cudaMemcpyDefault,
+                                         c->stream), "lbm_set_equilibrium: copy");
+            LBM_CUDA(c->ops->equilibrium(p, s, s + chunk, s + 2 * chunk, s + 3 * chunk, (uint32_t)n0,
+                                         (uint32_t)cnt, c->stream), "lbm_set_equilibrium");
+            ++c->launches;
+        }
+    }
+    reset_state(c);
+    return sync(c, "lbm_set_equilibrium");
+}
+
+int lbm_get_populations(lbm_ctx* c, float* f) {
+    if (!c || !f) return fail(LBM_EINVAL, "lbm_get_populations: NULL argument");
+    float* src = c->state_buffer();
+    const Params p = c->params(src, src);
+    const size_t total = 19 * c->N;
+    if (is_device_pointer(f)) {
+        LBM_CUDA(c->ops->unpack(p, c->state, f, 0, total, c->stream), "lbm_get_populations");
+        ++c->launches;
+    } else {
+        if (int rc = ensure_staging(c)) return rc;
+        for (size_t i0 = 0; i0 < total; i0 += kStagingFloats) {
+            const size_t cnt = total - i0 < kStagingFloats ? total - i0 : kStagingFloats;
+            LBM_CUDA(c->ops->unpack(p, c->state, c->staging, i0, cnt, c->stream), "lbm_get_populations");
+            ++c->launches;
+            LBM_CUDA(cudaMemcpyAsync(f + i0, c->staging, cnt * sizeof(float), cudaMemcpyDefault,
+                                     c->stream), "lbm_get_populations: copy");
+        }
+    }
+    return sync(c, "lbm_get_populations");
+}
+
+int lbm_step(lbm_ctx* c, int n) {
+    if (!c) return fail(LBM_EINVAL, "lbm_step: NULL context");
+    if (n < 0) return fail(LBM_EINVAL, "lbm_step: n = %d < 0", n);
+    for (int i = 0; i < n; ++i)
+        if (int rc = step_once(c, i == n - 1)) return rc;
+    if (n > 0) {
+        c->steps += n;
+        c->force_valid = true;
+    }
+    return LBM_OK;
+}
+
+int lbm_macroscopic(lbm_ctx* c, float* rho, float* u) {
+    if (!c || !rho || !u) return fail(LBM_EINVAL, "lbm_macroscopic: NULL argument");
+    float* src = c->state_buffer();
+    const Params p = c->params(src, src);
+    const size_t N = c->N;
+    if (is_device_pointer(rho) && is_device_pointer(u)) {
+        LBM_CUDA(c->ops->macro(p, c->state, c->inlet, rho, u, u + N, u + 2 * N, 0, (uint32_t)N,
+                               c->stream), "lbm_macroscopic");
+        ++c->launches;
+    } else {
+        if (int rc = ensure_staging(c)) return rc;
+        const size_t chunk = kStagingFloats / 4;
+        float* s = c->staging;
+        for (size_t n0 = 0; n0 < N; n0 += chunk) {
+            const size_t cnt = N - n0 < chunk ? N - n0 : chunk;
+            LBM_CUDA(c->ops->macro(p, c->state, c->inlet, s, s + chunk, s + 2 * chunk, s + 3 * chunk,
+                                   (uint32_t)n0, (uint32_t)cnt, c->stream), "lbm_macroscopic");
+            ++c->launches;
+            LBM_CUDA(cudaMemcpyAsync(rho + n0, s, cnt * 4, cudaMemcpyDefault, c->stream), "lbm_macroscopic: copy");
+            for (int a = 0; a < 3; ++a)
+                LBM_CUDA(cudaMemcpyAsync(u + a * N + n0, s + (a + 1) * chunk, cnt * 4, cudaMemcpyDefault,
+                                         c->stream), "lbm_macroscopic: copy");
+        }
+    }
+    return sync(c, "lbm_macroscopic");
+}
+
+int lbm_force_momentum_exchange(lbm_ctx* c, double F[3]) {
+    if (!c || !F) return fail(LBM_EINVAL, "lbm_force_momentum_exchange: NULL argument");
+    if (!c->force_valid)
+        return fail(LBM_ESTATE, "lbm_force_momentum_exchange: no step since the state was loaded");
+    LBM_CUDA(cudaMemcpyAsync(c->force_host, c->force_dev, 3 * sizeof(double), cudaMemcpyDeviceToHost,
+                             c->stream), "lbm_force_momentum_exchange");
+    if (int rc = sync(c, "lbm_force_momentum_exchange")) return rc;
+    for (int a = 0; a < 3; ++a) F[a] = c->force_host[a];
+    return LBM_OK;
+}
+
+int lbm_check_finite(lbm_ctx* c) {
+    if (!c) return fail(LBM_EINVAL, "lbm_check_finite: NULL context");
+    float* src = c->state_buffer();
+    LBM_CUDA(cudaMemsetAsync(c->err_dev, 0, sizeof(int), c->stream), "lbm_check_finite");
+    LBM_CUDA(c->ops->check_finite(c->params(src, src), c->err_dev, c->grid, c->block, c->stream),
+             "lbm_check_finite");
+    ++c->launches;
+    LBM_CUDA(cudaMemcpyAsync(c->err_host, c->err_dev, sizeof(int), cudaMemcpyDeviceToHost, c->stream),
+             "lbm_check_finite");
+    if (int rc = sync(c, "lbm_check_finite")) return rc;
+    if (*c->err_host) return fail(LBM_ENOTFINITE, "lbm_check_finite: a population is NaN or infinite");
+    return LBM_OK;
+}
+
+int64_t lbm_step_count(lbm_ctx* c) { return c ? c->steps : -1; }
+
+int64_t lbm_kernel_launches(lbm_ctx* c) { return c ? c->launches : -1; }
+
+int lbm_profile_enable(lbm_ctx* c, int enable) {
+    if (!c) return fail(LBM_EINVAL, "lbm_profile_enable: NULL context");
+    if (int rc = sync(c, "lbm_profile_enable")) return rc;
+    c->release_profile();
+    c->profiling = enable != 0;
+    return LBM_OK;
+}
+
+int lbm_profile_read(lbm_ctx* c, int kind, int64_t* launches, double* total_ms) {
+    if (!c || !launches || !total_ms) return fail(LBM_EINVAL, "lbm_profile_read: NULL argument");
+    if (kind < 0 || kind >= K_NUM_KINDS) return fail(LBM_EINVAL, "lbm_profile_read: kind %d", kind);
+    if (int rc = sync(c, "lbm_profile_read")) return rc;
+    double ms = 0.0;
+    for (auto& pr : c->prof[kind]) {
+        float t = 0.f;
+        LBM_CUDA(cudaEventElapsedTime(&t, pr.first, pr.second), "lbm_profile_read");
+        ms += t;
+    }
+    *launches = (int64_t)c->prof[kind].size();
+    *total_ms = ms;
+    return LBM_OK;
+}
+
+void lbm_destroy(lbm_ctx* c) {
+    if (!c) return;
+    c->free_all();
+    delete c;
+}
+
+}  // extern "C"

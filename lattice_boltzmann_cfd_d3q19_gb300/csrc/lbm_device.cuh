@@ -1,0 +1,192 @@
+// Device-side building blocks of the D3Q19 BGK step: velocity set, weights, layout addressing,
+// per-link geometry and the collision.  Everything that depends on q is a constexpr function of
+// q, so fully unrolled loops over the 19 populations fold it into immediates.
+//
+// Populations are stored SHIFTED: h_q = f_q - w_q (fp32).  At rest (rho = 1, u = 0) h = 0, and
+// the values a step adds or subtracts are small against h, which keeps fp32 rounding of the
+// near-unity density out of long runs.  The C ABI always exchanges absolute f.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace lbm {
+
+enum : int { LAYOUT_STREAM = 0, LAYOUT_BUNDLE = 1, LAYOUT_COLLISION = 2 };
+
+// internal flag byte: bits 0-1 cell type, bit 7 "bulk" (FLUID, and all 18 neighbours exist inside
+// the domain -- wrapped on periodic axes, not beyond an open face -- and are FLUID).
+enum : uint8_t { T_FLUID = 0, T_SOLID = 1, T_INLET = 2, TYPE_MASK = 3, F_BULK = 0x80 };
+
+// what the population buffer holds between steps
+enum : int {
+    ST_NATURAL = 0,  // natural h_q(x) at slot (q, x)
+    ST_POST_AA = 1,  // post-collision h*_q(x) at slot (opposite(q), x): AA after an even step
+    ST_POST_AB = 2   // post-collision h*_q(x) at slot (q, x): two-buffer pull state
+};
+
+// ---- D3Q19 velocity set ---------------------------------------------------------------------
+// Member order: rest, then each moving velocity followed by its opposite.  The velocity is coded
+// as (cx+1) + 3 (cy+1) + 9 (cz+1).
+__host__ __device__ constexpr int vcode(int q) {
+    return q == 0 ? 13 : q == 1 ? 14 : q == 2 ? 12 : q == 3 ? 16 : q == 4 ? 10 : q == 5 ? 22
+         : q == 6 ? 4 : q == 7 ? 17 : q == 8 ? 9 : q == 9 ? 23 : q == 10 ? 3 : q == 11 ? 25
+         : q == 12 ? 1 : q == 13 ? 11 : q == 14 ? 15 : q == 15 ? 5 : q == 16 ? 21 : q == 17 ? 7
+         : 19;
+}
+__host__ __device__ constexpr int cx(int q) { return vcode(q) % 3 - 1; }
+__host__ __device__ constexpr int cy(int q) { return (vcode(q) / 3) % 3 - 1; }
+__host__ __device__ constexpr int cz(int q) { return vcode(q) / 9 - 1; }
+__host__ __device__ constexpr int opp(int q) { return q == 0 ? 0 : (q & 1) ? q + 1 : q - 1; }
+__host__ __device__ constexpr float wq(int q) {
+    return q == 0 ? 1.0f / 3.0f : q <= 6 ? 1.0f / 18.0f : 1.0f / 36.0f;
+}
+
+// ---- layout addressing ------------------------------------------------------------------------
+// STREAM (SoA): q*N + n.  COLLISION (AoS): n*19 + q.  BUNDLE (SoAoS): the populations sharing
+// (cy, cz) form one bundle -- an x-row of the stencil, members ordered cx = -1, 0, +1 -- stored as
+// boff*N + n*size + j.
+__host__ __device__ constexpr int bundle_size(int q) { return (cy(q) == 0 || cz(q) == 0) ? 3 : 1; }
+__host__ __device__ constexpr int bundle_off(int q) {
+    return (cy(q) == 0 && cz(q) == 0) ? 0 : (cy(q) == 1 && cz(q) == 0) ? 3
+         : (cy(q) == -1 && cz(q) == 0) ? 6 : (cy(q) == 0 && cz(q) == 1) ? 9
+         : (cy(q) == 0 && cz(q) == -1) ? 12 : (cy(q) == 1 && cz(q) == 1) ? 15
+         : (cy(q) == -1 && cz(q) == -1) ? 16 : (cy(q) == 1 && cz(q) == -1) ? 17 : 18;
+}
+__host__ __device__ constexpr int bundle_j(int q) { return bundle_size(q) == 3 ? cx(q) + 1 : 0; }
+
+template <int L>
+__host__ __device__ __forceinline__ size_t idx(int q, uint32_t n, size_t N) {
+    if (L == LAYOUT_STREAM) return (size_t)q * N + n;
+    if (L == LAYOUT_COLLISION) return (size_t)n * 19u + (size_t)q;
+    return (size_t)bundle_off(q) * N + (size_t)n * (size_t)bundle_size(q) + (size_t)bundle_j(q);
+}
+// runtime-q variant (off the hot path)
+template <int L>
+__host__ __device__ __forceinline__ size_t idx_rt(int q, uint32_t n, size_t N) {
+    if (L == LAYOUT_STREAM) return (size_t)q * N + n;
+    if (L == LAYOUT_COLLISION) return (size_t)n * 19u + (size_t)q;
+    int s = 0, o = 0, j = 0;
+    switch (q) {
+#define LBM_BCASE(Q) case Q: s = bundle_size(Q); o = bundle_off(Q); j = bundle_j(Q); break;
+        LBM_BCASE(0) LBM_BCASE(1) LBM_BCASE(2) LBM_BCASE(3) LBM_BCASE(4) LBM_BCASE(5)
+        LBM_BCASE(6) LBM_BCASE(7) LBM_BCASE(8) LBM_BCASE(9) LBM_BCASE(10) LBM_BCASE(11)
+        LBM_BCASE(12) LBM_BCASE(13) LBM_BCASE(14) LBM_BCASE(15) LBM_BCASE(16) LBM_BCASE(17)
+        LBM_BCASE(18)
+#undef LBM_BCASE
+    }
+    return (size_t)o * N + (size_t)n * (size_t)s + (size_t)j;
+}
+
+// ---- kernel parameters (passed by value) ---------------------------------------------------------
+struct Params {
+    float* A;              // buffer read (AA: the only buffer; A-B: source)
+    float* B;              // A-B destination (may equal A for the in-place collision)
+    const uint8_t* flags;  // internal flag bytes
+    float* scratch;        // open-face pre-gathered values (AA odd step)
+    double* partial;       // per-block momentum-exchange partial sums, 3 per block
+    int nx, ny, nz;
+    int open[3];           // axis has OPEN faces
+    size_t N;
+    size_t face_base[3][2];  // scratch offset of face (axis, side); 19 * area values each
+    float omega;
+    float g[3];
+    float heq_in[19];      // shifted inlet state f_eq(rho_in, u_in) - w
+};
+
+// ---- per-link geometry ----------------------------------------------------------------------------
+// Coordinate v + c along an axis of n cells: wrapped on a periodic axis; on an open axis a value
+// beyond the face is clamped onto the last layer and *beyond is set.
+__device__ __forceinline__ int clampwrap(int v, int n, int open, bool& beyond) {
+    if (v < 0) {
+        if (open) { beyond = true; return 0; }
+        return v + n;
+    }
+    if (v >= n) {
+        if (open) { beyond = true; return n - 1; }
+        return v - n;
+    }
+    return v;
+}
+
+// ---- collision -------------------------------------------------------------------------------------
+// BGK with the second-order equilibrium (c_s^2 = 1/3) on shifted populations, plus Guo forcing
+// when BODY: u = j/rho + g/2, F = rho g, source (1 - omega/2) w [3 (c - u).F + 9 (c.u)(c.F)].
+// h[] holds h_q on entry and h*_q on exit.
+template <bool BODY>
+__device__ __forceinline__ void collide(float (&h)[19], const Params& p) {
+    float drho = 0.f, jx = 0.f, jy = 0.f, jz = 0.f;
+#pragma unroll
+    for (int q = 0; q < 19; ++q) {
+        drho += h[q];
+        if (cx(q) > 0) jx += h[q]; else if (cx(q) < 0) jx -= h[q];
+        if (cy(q) > 0) jy += h[q]; else if (cy(q) < 0) jy -= h[q];
+        if (cz(q) > 0) jz += h[q]; else if (cz(q) < 0) jz -= h[q];
+    }
+    const float rho = 1.0f + drho;
+    const float inv = 1.0f / rho;
+    float ux = jx * inv, uy = jy * inv, uz = jz * inv;
+    float Fx = 0.f, Fy = 0.f, Fz = 0.f, uF = 0.f, src = 0.f;
+    if (BODY) {
+        ux = fmaf(0.5f, p.g[0], ux);
+        uy = fmaf(0.5f, p.g[1], uy);
+        uz = fmaf(0.5f, p.g[2], uz);
+        Fx = rho * p.g[0];
+        Fy = rho * p.g[1];
+        Fz = rho * p.g[2];
+        uF = ux * Fx + uy * Fy + uz * Fz;
+        src = 1.0f - 0.5f * p.omega;
+    }
+    const float uu15 = 1.5f * (ux * ux + uy * uy + uz * uz);
+    const float om = p.omega;
+#pragma unroll
+    for (int q = 0; q < 19; ++q) {
+        float cu = 0.f;
+        if (cx(q) > 0) cu += ux; else if (cx(q) < 0) cu -= ux;
+        if (cy(q) > 0) cu += uy; else if (cy(q) < 0) cu -= uy;
+        if (cz(q) > 0) cu += uz; else if (cz(q) < 0) cu -= uz;
+        // f_eq - w = w (rho - 1 + rho (3 cu + 4.5 cu^2 - 1.5 u.u))
+        const float poly = fmaf(cu, fmaf(4.5f, cu, 3.0f), -uu15);
+        const float heq = wq(q) * fmaf(rho, poly, drho);
+        float hn = fmaf(-om, h[q] - heq, h[q]);
+        if (BODY) {
+            float cF = 0.f;
+            if (cx(q) > 0) cF += Fx; else if (cx(q) < 0) cF -= Fx;
+            if (cy(q) > 0) cF += Fy; else if (cy(q) < 0) cF -= Fy;
+            if (cz(q) > 0) cF += Fz; else if (cz(q) < 0) cF -= Fz;
+            hn = fmaf(src * wq(q), fmaf(9.0f * cu, cF, 3.0f * (cF - uF)), hn);
+        }
+        h[q] = hn;
+    }
+}
+
+// ---- momentum-exchange block reduction ----------------------------------------------------------------
+// Every thread of the block must call this.  Warp shuffles, then one fp64 partial per block.
+__device__ __forceinline__ void block_force(float fx, float fy, float fz, double* partial) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        fx += __shfl_xor_sync(0xffffffffu, fx, o);
+        fy += __shfl_xor_sync(0xffffffffu, fy, o);
+        fz += __shfl_xor_sync(0xffffffffu, fz, o);
+    }
+    __shared__ float warp_sum[3][32];
+    const int t = threadIdx.x + blockDim.x * threadIdx.y;
+    const int nwarps = (blockDim.x * blockDim.y + 31) >> 5;
+    if ((t & 31) == 0) {
+        warp_sum[0][t >> 5] = fx;
+        warp_sum[1][t >> 5] = fy;
+        warp_sum[2][t >> 5] = fz;
+    }
+    __syncthreads();
+    if (t == 0) {
+        double s[3] = {0.0, 0.0, 0.0};
+        for (int w = 0; w < nwarps; ++w)
+            for (int a = 0; a < 3; ++a) s[a] += (double)warp_sum[a][w];
+        const size_t b = blockIdx.x + (size_t)gridDim.x * (blockIdx.y + (size_t)gridDim.y * blockIdx.z);
+        partial[3 * b + 0] = s[0];
+        partial[3 * b + 1] = s[1];
+        partial[3 * b + 2] = s[2];
+    }
+}
+
+}  // namespace lbm

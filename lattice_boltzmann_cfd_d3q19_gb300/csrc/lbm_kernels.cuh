@@ -1,0 +1,454 @@
+// Kernels of the D3Q19 BGK step, templated on the population layout L.  Included by one
+// translation unit per layout, which instantiates them and defines the launch functions.
+//
+// Cell kernels use a 3D grid: threads along x (blockDim.x), rows along y (blockDim.y), one z
+// plane per blockIdx.z; a thread owns cell n = x + nx (y + ny z).
+//
+// The per-link rules, the same in every scheme ("GPU lattice Boltzmann: streaming layout and
+// performance", paragraph after the layout bullets): population q of FLUID cell x comes from
+// s = x - c_q (wrapped on periodic axes, clamped onto the last layer beyond an OPEN face):
+// FLUID s streams its post-collision value, SOLID s reflects x's own post-collision population
+// opposite(q) (halfway bounce-back, PortLBM §3.1), INLET s supplies f_eq(rho_in, u_in).
+#pragma once
+
+#include "lbm_device.cuh"
+
+namespace lbm {
+
+struct Link {
+    uint32_t cell;
+    int face;  // -1: inside the domain; otherwise 2*axis + side of the first axis clamped
+};
+
+// Cell x + d with the face rules; `face` records the first axis (x, then y, then z) whose
+// coordinate lay beyond an OPEN face.
+__device__ __forceinline__ Link link_cell(const Params& p, int x, int y, int z, int dx, int dy,
+                                          int dz) {
+    int face = -1;
+    int v = x + dx;
+    if (v < 0) { if (p.open[0]) { v = 0; face = 0; } else v += p.nx; }
+    else if (v >= p.nx) { if (p.open[0]) { v = p.nx - 1; face = 1; } else v -= p.nx; }
+    int w = y + dy;
+    if (w < 0) { if (p.open[1]) { w = 0; if (face < 0) face = 2; } else w += p.ny; }
+    else if (w >= p.ny) { if (p.open[1]) { w = p.ny - 1; if (face < 0) face = 3; } else w -= p.ny; }
+    int u = z + dz;
+    if (u < 0) { if (p.open[2]) { u = 0; if (face < 0) face = 4; } else u += p.nz; }
+    else if (u >= p.nz) { if (p.open[2]) { u = p.nz - 1; if (face < 0) face = 5; } else u -= p.nz; }
+    Link l;
+    l.cell = (uint32_t)v + (uint32_t)p.nx * ((uint32_t)w + (uint32_t)p.ny * (uint32_t)u);
+    l.face = face;
+    return l;
+}
+
+// Position of cell (x, y, z) on the face layers of `axis` (row-major over the other two axes).
+__device__ __forceinline__ size_t face_pos(const Params& p, int axis, int x, int y, int z) {
+    return axis == 0 ? (size_t)y + (size_t)p.ny * z
+         : axis == 1 ? (size_t)x + (size_t)p.nx * z : (size_t)x + (size_t)p.nx * y;
+}
+__device__ __forceinline__ size_t face_area(const Params& p, int axis) {
+    return axis == 0 ? (size_t)p.ny * p.nz : axis == 1 ? (size_t)p.nx * p.nz : (size_t)p.nx * p.ny;
+}
+__device__ __forceinline__ size_t scratch_slot(const Params& p, int face, int q, int x, int y,
+                                               int z) {
+    const int axis = face >> 1;
+    return p.face_base[axis][face & 1] + (size_t)q * face_area(p, axis) + face_pos(p, axis, x, y, z);
+}
+
+// Wrapped neighbour coordinates of a bulk cell (a bulk cell never reaches an open face).
+struct Nbr {
+    uint32_t X[3], R[3][3];  // X[cx+1]; R[cy+1][cz+1] = nx (Y + ny Z)
+    __device__ __forceinline__ Nbr(const Params& p, int x, int y, int z) {
+        X[0] = x == 0 ? p.nx - 1 : x - 1;
+        X[1] = x;
+        X[2] = x == p.nx - 1 ? 0 : x + 1;
+        const uint32_t Y[3] = {(uint32_t)(y == 0 ? p.ny - 1 : y - 1), (uint32_t)y,
+                               (uint32_t)(y == p.ny - 1 ? 0 : y + 1)};
+        const uint32_t Z[3] = {(uint32_t)(z == 0 ? p.nz - 1 : z - 1), (uint32_t)z,
+                               (uint32_t)(z == p.nz - 1 ? 0 : z + 1)};
+#pragma unroll
+        for (int b = 0; b < 3; ++b)
+#pragma unroll
+            for (int c = 0; c < 3; ++c) R[b][c] = (uint32_t)p.nx * (Y[b] + (uint32_t)p.ny * Z[c]);
+    }
+    // cell x + s c_q, s = +1 or -1
+    template <int Q, int S>
+    __device__ __forceinline__ uint32_t at() const {
+        return X[S * cx(Q) + 1] + R[S * cy(Q) + 1][S * cz(Q) + 1];
+    }
+};
+
+// Momentum exchange of a non-bulk FLUID cell: every link along which post-collision population q
+// bounces back (x + c_q, wrapped or clamped, is SOLID) adds 2 c_q f*_q, f* = h* + w.
+template <int Q>
+__device__ __forceinline__ void accumulate_force(float h_post, float& fx, float& fy, float& fz) {
+    const float t = 2.0f * (h_post + wq(Q));
+    if (cx(Q) > 0) fx += t; else if (cx(Q) < 0) fx -= t;
+    if (cy(Q) > 0) fy += t; else if (cy(Q) < 0) fy -= t;
+    if (cz(Q) > 0) fz += t; else if (cz(Q) < 0) fz -= t;
+}
+
+template <int Q>
+__device__ __forceinline__ void local_force(const Params& p, const float (&h)[19], int x, int y,
+                                            int z, float& fx, float& fy, float& fz) {
+    const Link d = link_cell(p, x, y, z, cx(Q), cy(Q), cz(Q));
+    if ((p.flags[d.cell] & TYPE_MASK) == T_SOLID) accumulate_force<Q>(h[Q], fx, fy, fz);
+}
+
+template <int Q = 1>
+__device__ __forceinline__ void all_local_forces(const Params& p, const float (&h)[19], int x,
+                                                 int y, int z, float& fx, float& fy, float& fz) {
+    local_force<Q>(p, h, x, y, z, fx, fy, fz);
+    if constexpr (Q < 18) all_local_forces<Q + 1>(p, h, x, y, z, fx, fy, fz);
+}
+
+// ============================== AA pattern, even step ===========================================
+// "In place" bullet: read population q of x at (q, x); write the collided one at (opposite(q), x).
+template <int L, bool FORCE, bool BODY>
+__global__ void __launch_bounds__(256) k_aa_even(Params p) {
+    const int x = blockIdx.x * blockDim.x + threadIdx.x;
+    const int y = blockIdx.y * blockDim.y + threadIdx.y;
+    const int z = blockIdx.z;
+    float fx = 0.f, fy = 0.f, fz = 0.f;
+    if (x < p.nx && y < p.ny) {
+        const uint32_t n = (uint32_t)x + (uint32_t)p.nx * ((uint32_t)y + (uint32_t)p.ny * z);
+        const uint8_t fl = p.flags[n];
+        if ((fl & TYPE_MASK) == T_FLUID) {
+            float h[19];
+#pragma unroll
+            for (int q = 0; q < 19; ++q) h[q] = p.A[idx<L>(q, n, p.N)];
+            collide<BODY>(h, p);
+#pragma unroll
+            for (int q = 0; q < 19; ++q) p.A[idx<L>(opp(q), n, p.N)] = h[q];
+            if (FORCE && !(fl & F_BULK)) all_local_forces(p, h, x, y, z, fx, fy, fz);
+        }
+    }
+    if (FORCE) block_force(fx, fy, fz, p.partial);
+}
+
+// ============================== AA pattern, odd step ============================================
+// "In place" bullet: read population q of x at (opposite(q), x - c_q); write the collided value at
+// (q, x + c_q).  Cell x reads and writes exactly the same 19 slots, so cells never race.
+// Boundary links use x's own mirrored slots; populations whose source lies beyond an OPEN face
+// were copied to scratch by k_pregather before this kernel (gather before scatter), and the
+// post-collision values of cells on an OPEN face layer are also written to the neighbours that
+// take them as their clamped (zero-gradient) source.
+
+template <int L, int Q>
+__device__ __forceinline__ float aa_odd_gather(const Params& p, uint32_t n, int x, int y, int z) {
+    const Link s = link_cell(p, x, y, z, -cx(Q), -cy(Q), -cz(Q));
+    const int t = p.flags[s.cell] & TYPE_MASK;
+    if (t == T_SOLID) return p.A[idx<L>(Q, n, p.N)];           // f*_opp(q)(x) sits at (q, x)
+    if (t == T_INLET) return p.heq_in[Q];
+    if (s.face >= 0) return p.scratch[scratch_slot(p, s.face, Q, x, y, z)];
+    return p.A[idx<L>(opp(Q), s.cell, p.N)];
+}
+
+template <int L, int Q>
+__device__ __forceinline__ void aa_odd_face_copies(const Params& p, float v, int x, int y, int z) {
+    // axes on which x sits on the layer where c_q points into the domain from an OPEN face
+    int M = 0;
+    if (cx(Q) != 0 && p.open[0] && ((cx(Q) > 0 && x == 0) || (cx(Q) < 0 && x == p.nx - 1))) M |= 1;
+    if (cy(Q) != 0 && p.open[1] && ((cy(Q) > 0 && y == 0) || (cy(Q) < 0 && y == p.ny - 1))) M |= 2;
+    if (cz(Q) != 0 && p.open[2] && ((cz(Q) > 0 && z == 0) || (cz(Q) < 0 && z == p.nz - 1))) M |= 4;
+    if (M == 0) return;
+    for (int S = 1; S < 8; ++S) {
+        if ((S & M) != S) continue;
+        // receiver r: on axes in S it shares x's coordinate (its source clamps back onto x)
+        int r[3] = {x, y, z};
+        const int c[3] = {cx(Q), cy(Q), cz(Q)};
+        const int nn[3] = {p.nx, p.ny, p.nz};
+        bool valid = true;
+        for (int a = 0; a < 3; ++a) {
+            if (S & (1 << a)) continue;
+            int v2 = r[a] + c[a];
+            if (v2 < 0 || v2 >= nn[a]) {
+                if (p.open[a]) valid = false;
+                else v2 = v2 < 0 ? v2 + nn[a] : v2 - nn[a];
+            }
+            r[a] = v2;
+        }
+        if (!valid) continue;
+        const uint32_t rc = (uint32_t)r[0] + (uint32_t)p.nx * ((uint32_t)r[1] + (uint32_t)p.ny * r[2]);
+        if ((p.flags[rc] & TYPE_MASK) == T_FLUID) p.A[idx<L>(Q, rc, p.N)] = v;
+    }
+}
+
+template <int L, bool FORCE, int Q>
+__device__ __forceinline__ void aa_odd_scatter(const Params& p, float v, uint32_t n, int x, int y,
+                                               int z, float& fx, float& fy, float& fz) {
+    const Link d = link_cell(p, x, y, z, cx(Q), cy(Q), cz(Q));
+    const int t = p.flags[d.cell] & TYPE_MASK;
+    if (t == T_SOLID) {
+        p.A[idx<L>(opp(Q), n, p.N)] = v;                          // bounces back into x
+        if (FORCE) accumulate_force<Q>(v, fx, fy, fz);
+    } else if (t == T_INLET) {
+        p.A[idx<L>(opp(Q), n, p.N)] = p.heq_in[opp(Q)];            // the reservoir feeds x
+    } else if (d.face < 0) {
+        p.A[idx<L>(Q, d.cell, p.N)] = v;
+    }
+    if (p.open[0] | p.open[1] | p.open[2]) aa_odd_face_copies<L, Q>(p, v, x, y, z);
+}
+
+template <int L, int Q = 0>
+__device__ __forceinline__ void aa_odd_gather_all(const Params& p, float (&h)[19], uint32_t n,
+                                                  int x, int y, int z) {
+    h[Q] = aa_odd_gather<L, Q>(p, n, x, y, z);
+    if constexpr (Q < 18) aa_odd_gather_all<L, Q + 1>(p, h, n, x, y, z);
+}
+
+template <int L, bool FORCE, int Q = 0>
+__device__ __forceinline__ void aa_odd_scatter_all(const Params& p, const float (&h)[19],
+                                                   uint32_t n, int x, int y, int z, float& fx,
+                                                   float& fy, float& fz) {
+    aa_odd_scatter<L, FORCE, Q>(p, h[Q], n, x, y, z, fx, fy, fz);
+    if constexpr (Q < 18) aa_odd_scatter_all<L, FORCE, Q + 1>(p, h, n, x, y, z, fx, fy, fz);
+}
+
+template <int L, int Q = 0>
+__device__ __forceinline__ void aa_odd_bulk_load(const Params& p, const Nbr& nb, float (&h)[19]) {
+    h[Q] = p.A[idx<L>(opp(Q), nb.template at<Q, -1>(), p.N)];
+    if constexpr (Q < 18) aa_odd_bulk_load<L, Q + 1>(p, nb, h);
+}
+
+template <int L, int Q = 0>
+__device__ __forceinline__ void aa_odd_bulk_store(const Params& p, const Nbr& nb,
+                                                  const float (&h)[19]) {
+    p.A[idx<L>(Q, nb.template at<Q, 1>(), p.N)] = h[Q];
+    if constexpr (Q < 18) aa_odd_bulk_store<L, Q + 1>(p, nb, h);
+}
+
+template <int L, bool FORCE, bool BODY>
+__global__ void __launch_bounds__(256) k_aa_odd(Params p) {
+    const int x = blockIdx.x * blockDim.x + threadIdx.x;
+    const int y = blockIdx.y * blockDim.y + threadIdx.y;
+    const int z = blockIdx.z;
+    float fx = 0.f, fy = 0.f, fz = 0.f;
+    if (x < p.nx && y < p.ny) {
+        const uint32_t n = (uint32_t)x + (uint32_t)p.nx * ((uint32_t)y + (uint32_t)p.ny * z);
+        const uint8_t fl = p.flags[n];
+        if ((fl & TYPE_MASK) == T_FLUID) {
+            float h[19];
+            if (fl & F_BULK) {
+                const Nbr nb(p, x, y, z);
+                aa_odd_bulk_load<L>(p, nb, h);
+                collide<BODY>(h, p);
+                aa_odd_bulk_store<L>(p, nb, h);
+            } else {
+                aa_odd_gather_all<L>(p, h, n, x, y, z);
+                collide<BODY>(h, p);
+                aa_odd_scatter_all<L, FORCE>(p, h, n, x, y, z, fx, fy, fz);
+            }
+        }
+    }
+    if (FORCE) block_force(fx, fy, fz, p.partial);
+}
+
+// Open-face pre-gather for the AA odd step: for every FLUID cell x on face layer (axis, side) and
+// every q whose source x - c_q lies beyond that face first, copy the clamped source's
+// post-collision population q -- at (opposite(q), s) -- into scratch, before the odd kernel
+// overwrites that slot.
+template <int L>
+__global__ void __launch_bounds__(256) k_pregather(Params p, int axis, int side) {
+    const size_t area = face_area(p, axis);
+    const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= 19 * area) return;
+    const int q = (int)(i / area);
+    const size_t pos = i - (size_t)q * area;
+    int x, y, z;
+    if (axis == 0) { x = side ? p.nx - 1 : 0; y = (int)(pos % p.ny); z = (int)(pos / p.ny); }
+    else if (axis == 1) { y = side ? p.ny - 1 : 0; x = (int)(pos % p.nx); z = (int)(pos / p.nx); }
+    else { z = side ? p.nz - 1 : 0; x = (int)(pos % p.nx); y = (int)(pos / p.nx); }
+    const uint32_t n = (uint32_t)x + (uint32_t)p.nx * ((uint32_t)y + (uint32_t)p.ny * z);
+    if ((p.flags[n] & TYPE_MASK) != T_FLUID) return;
+    const Link s = link_cell(p, x, y, z, -cx(q), -cy(q), -cz(q));
+    if (s.face != 2 * axis + side) return;
+    if ((p.flags[s.cell] & TYPE_MASK) != T_FLUID) return;
+    p.scratch[p.face_base[axis][side] + (size_t)q * area + pos] = p.A[idx_rt<L>(opp(q), s.cell, p.N)];
+}
+
+// ============================== two buffers (A-B) ===============================================
+// FROM_NATURAL: collide the natural state in place of the cell (first step after a state load,
+// and the first pass of the two-pass scheme).  Otherwise: pull-collide (PortLBM §3.3 one-step pull,
+// two lattices): gather the 19 populations from the neighbours' post-collision values in A,
+// collide, and write the post-collision values to B at (q, x).
+template <int L, int Q = 0>
+__device__ __forceinline__ void ab_gather_all(const Params& p, float (&h)[19], uint32_t n, int x,
+                                              int y, int z) {
+    const Link s = link_cell(p, x, y, z, -cx(Q), -cy(Q), -cz(Q));
+    const int t = p.flags[s.cell] & TYPE_MASK;
+    if (t == T_SOLID) h[Q] = p.A[idx<L>(opp(Q), n, p.N)];
+    else if (t == T_INLET) h[Q] = p.heq_in[Q];
+    else h[Q] = p.A[idx<L>(Q, s.cell, p.N)];
+    if constexpr (Q < 18) ab_gather_all<L, Q + 1>(p, h, n, x, y, z);
+}
+
+template <int L, int Q = 0>
+__device__ __forceinline__ void ab_bulk_load(const Params& p, const Nbr& nb, float (&h)[19]) {
+    h[Q] = p.A[idx<L>(Q, nb.template at<Q, -1>(), p.N)];
+    if constexpr (Q < 18) ab_bulk_load<L, Q + 1>(p, nb, h);
+}
+
+template <int L, bool FORCE, bool BODY, bool FROM_NATURAL>
+__global__ void __launch_bounds__(256) k_ab(Params p) {
+    const int x = blockIdx.x * blockDim.x + threadIdx.x;
+    const int y = blockIdx.y * blockDim.y + threadIdx.y;
+    const int z = blockIdx.z;
+    float fx = 0.f, fy = 0.f, fz = 0.f;
+    if (x < p.nx && y < p.ny) {
+        const uint32_t n = (uint32_t)x + (uint32_t)p.nx * ((uint32_t)y + (uint32_t)p.ny * z);
+        const uint8_t fl = p.flags[n];
+        if ((fl & TYPE_MASK) == T_FLUID) {
+            float h[19];
+            if (FROM_NATURAL) {
+#pragma unroll
+                for (int q = 0; q < 19; ++q) h[q] = p.A[idx<L>(q, n, p.N)];
+            } else if (fl & F_BULK) {
+                const Nbr nb(p, x, y, z);
+                ab_bulk_load<L>(p, nb, h);
+            } else {
+                ab_gather_all<L>(p, h, n, x, y, z);
+            }
+            collide<BODY>(h, p);
+#pragma unroll
+            for (int q = 0; q < 19; ++q) p.B[idx<L>(q, n, p.N)] = h[q];
+            if (FORCE && !(fl & F_BULK)) all_local_forces(p, h, x, y, z, fx, fy, fz);
+        }
+    }
+    if (FORCE) block_force(fx, fy, fz, p.partial);
+}
+
+// Streaming only: natural state into B from the post-collision state in A (two-pass scheme's
+// second pass).
+template <int L>
+__global__ void __launch_bounds__(256) k_stream(Params p) {
+    const int x = blockIdx.x * blockDim.x + threadIdx.x;
+    const int y = blockIdx.y * blockDim.y + threadIdx.y;
+    const int z = blockIdx.z;
+    if (x >= p.nx || y >= p.ny) return;
+    const uint32_t n = (uint32_t)x + (uint32_t)p.nx * ((uint32_t)y + (uint32_t)p.ny * z);
+    const uint8_t fl = p.flags[n];
+    if ((fl & TYPE_MASK) != T_FLUID) return;
+    float h[19];
+    if (fl & F_BULK) {
+        const Nbr nb(p, x, y, z);
+        ab_bulk_load<L>(p, nb, h);
+    } else {
+        ab_gather_all<L>(p, h, n, x, y, z);
+    }
+#pragma unroll
+    for (int q = 0; q < 19; ++q) p.B[idx<L>(q, n, p.N)] = h[q];
+}
+
+// ============================== state access off the step path ==================================
+// Natural shifted population q of FLUID cell (x, y, z) for a buffer in state `state`.
+template <int L>
+__device__ __forceinline__ float natural_h(const Params& p, int state, int q, uint32_t n, int x,
+                                           int y, int z) {
+    if (state == ST_NATURAL) return p.A[idx_rt<L>(q, n, p.N)];
+    const Link s = link_cell(p, x, y, z, -cx(q), -cy(q), -cz(q));
+    const int t = p.flags[s.cell] & TYPE_MASK;
+    if (t == T_INLET) return p.heq_in[q];
+    if (state == ST_POST_AA) {
+        if (t == T_SOLID) return p.A[idx_rt<L>(q, n, p.N)];
+        return p.A[idx_rt<L>(opp(q), s.cell, p.N)];
+    }
+    if (t == T_SOLID) return p.A[idx_rt<L>(opp(q), n, p.N)];
+    return p.A[idx_rt<L>(q, s.cell, p.N)];
+}
+
+// Canonical absolute f[q*N + n] for flat indices [i0, i0 + count) into out[0, count).
+template <int L>
+__global__ void __launch_bounds__(256) k_unpack(Params p, int state, float* out, size_t i0,
+                                                size_t count) {
+    const size_t k = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (k >= count) return;
+    const size_t i = i0 + k;
+    const int q = (int)(i / p.N);
+    const uint32_t n = (uint32_t)(i - (size_t)q * p.N);
+    const int x = (int)(n % (uint32_t)p.nx);
+    const int y = (int)((n / (uint32_t)p.nx) % (uint32_t)p.ny);
+    const int z = (int)(n / ((uint32_t)p.nx * (uint32_t)p.ny));
+    const int t = p.flags[n] & TYPE_MASK;
+    float v;
+    if (t == T_SOLID) v = 0.0f;
+    else if (t == T_INLET) v = p.heq_in[q] + wq(q);
+    else v = natural_h<L>(p, state, q, n, x, y, z) + wq(q);
+    out[k] = v;
+}
+
+// Canonical absolute f[q*N + n], flat indices [i0, i0 + count), into the natural shifted state.
+template <int L>
+__global__ void __launch_bounds__(256) k_pack(Params p, const float* in, size_t i0, size_t count) {
+    const size_t k = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (k >= count) return;
+    const size_t i = i0 + k;
+    const int q = (int)(i / p.N);
+    const uint32_t n = (uint32_t)(i - (size_t)q * p.N);
+    p.A[idx_rt<L>(q, n, p.N)] = in[k] - wq(q);
+}
+
+// Natural shifted state f_eq(rho, u) - w for cells [n0, n0 + count).
+template <int L>
+__global__ void __launch_bounds__(256) k_equilibrium(Params p, const float* rho, const float* u0,
+                                                     const float* u1, const float* u2,
+                                                     uint32_t n0, uint32_t count) {
+    const uint32_t k = blockIdx.x * blockDim.x + threadIdx.x;
+    if (k >= count) return;
+    const uint32_t n = n0 + k;
+    const float r = rho[k], ux = u0[k], uy = u1[k], uz = u2[k];
+    const float drho = r - 1.0f;
+    const float uu15 = 1.5f * (ux * ux + uy * uy + uz * uz);
+#pragma unroll
+    for (int q = 0; q < 19; ++q) {
+        const float cu = (float)cx(q) * ux + (float)cy(q) * uy + (float)cz(q) * uz;
+        const float poly = fmaf(cu, fmaf(4.5f, cu, 3.0f), -uu15);
+        p.A[idx<L>(q, n, p.N)] = wq(q) * fmaf(r, poly, drho);
+    }
+}
+
+// rho and u (Guo-shifted) of the natural state for cells [n0, n0 + count).
+template <int L>
+__global__ void __launch_bounds__(256) k_macro(Params p, int state, float rho_in, float ux_in,
+                                               float uy_in, float uz_in, float* rho, float* u0,
+                                               float* u1, float* u2, uint32_t n0, uint32_t count) {
+    const uint32_t k = blockIdx.x * blockDim.x + threadIdx.x;
+    if (k >= count) return;
+    const uint32_t n = n0 + k;
+    const int t = p.flags[n] & TYPE_MASK;
+    if (t == T_SOLID) { rho[k] = 0.f; u0[k] = u1[k] = u2[k] = 0.f; return; }
+    if (t == T_INLET) { rho[k] = rho_in; u0[k] = ux_in; u1[k] = uy_in; u2[k] = uz_in; return; }
+    const int x = (int)(n % (uint32_t)p.nx);
+    const int y = (int)((n / (uint32_t)p.nx) % (uint32_t)p.ny);
+    const int z = (int)(n / ((uint32_t)p.nx * (uint32_t)p.ny));
+    float drho = 0.f, jx = 0.f, jy = 0.f, jz = 0.f;
+#pragma unroll
+    for (int q = 0; q < 19; ++q) {
+        const float h = natural_h<L>(p, state, q, n, x, y, z);
+        drho += h;
+        jx += (float)cx(q) * h;
+        jy += (float)cy(q) * h;
+        jz += (float)cz(q) * h;
+    }
+    const float r = 1.0f + drho;
+    rho[k] = r;
+    u0[k] = jx / r + 0.5f * p.g[0];
+    u1[k] = jy / r + 0.5f * p.g[1];
+    u2[k] = jz / r + 0.5f * p.g[2];
+}
+
+// Sets *bad when any stored population of a FLUID cell is not finite.
+template <int L>
+__global__ void __launch_bounds__(256) k_check_finite(Params p, int* bad) {
+    const int x = blockIdx.x * blockDim.x + threadIdx.x;
+    const int y = blockIdx.y * blockDim.y + threadIdx.y;
+    const int z = blockIdx.z;
+    if (x >= p.nx || y >= p.ny) return;
+    const uint32_t n = (uint32_t)x + (uint32_t)p.nx * ((uint32_t)y + (uint32_t)p.ny * z);
+    if ((p.flags[n] & TYPE_MASK) != T_FLUID) return;
+    bool ok = true;
+#pragma unroll
+    for (int q = 0; q < 19; ++q) ok &= isfinite(p.A[idx<L>(q, n, p.N)]);
+    if (!ok) *bad = 1;
+}
+
+}  // namespace lbm

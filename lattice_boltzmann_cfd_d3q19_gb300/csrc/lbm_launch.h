@@ -1,0 +1,50 @@
+// Host-side launch interface between the C ABI and the layout-specific kernel instantiations.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "lbm_device.cuh"
+
+namespace lbm {
+
+// kernel kinds (also the profiling kinds of the C ABI)
+enum : int {
+    K_AA_EVEN = 0,
+    K_AA_ODD = 1,
+    K_AB_PULL = 2,
+    K_AB_COLLIDE = 3,
+    K_STREAM = 4,
+    K_PREGATHER = 5,
+    K_FORCE = 6,
+    K_NUM_KINDS = 7
+};
+
+struct LayoutOps {
+    // step kernels: K_AA_EVEN, K_AA_ODD, K_AB_PULL, K_AB_COLLIDE, K_STREAM
+    cudaError_t (*cells)(int kind, const Params& p, bool force, bool body, dim3 grid, dim3 block,
+                         cudaStream_t s);
+    cudaError_t (*pregather)(const Params& p, int axis, int side, cudaStream_t s);
+    cudaError_t (*pack)(const Params& p, const float* in, size_t i0, size_t count, cudaStream_t s);
+    cudaError_t (*unpack)(const Params& p, int state, float* out, size_t i0, size_t count,
+                          cudaStream_t s);
+    cudaError_t (*equilibrium)(const Params& p, const float* rho, const float* u0, const float* u1,
+                               const float* u2, uint32_t n0, uint32_t count, cudaStream_t s);
+    cudaError_t (*macro)(const Params& p, int state, const float inlet[4], float* rho, float* u0,
+                         float* u1, float* u2, uint32_t n0, uint32_t count, cudaStream_t s);
+    cudaError_t (*check_finite)(const Params& p, int* bad, dim3 grid, dim3 block, cudaStream_t s);
+};
+
+const LayoutOps& layout_ops_stream();
+const LayoutOps& layout_ops_bundle();
+const LayoutOps& layout_ops_collision();
+
+// layout-independent kernels
+cudaError_t launch_validate_types(const uint8_t* types, size_t N, int* bad, cudaStream_t s);
+cudaError_t launch_classify(const Params& p, const uint8_t* types, uint8_t* flags, dim3 grid,
+                            dim3 block, cudaStream_t s);
+cudaError_t launch_force_finalize(const double* partial, size_t nblocks, double* out,
+                                  cudaStream_t s);
+
+}  // namespace lbm

@@ -1,0 +1,359 @@
+"""GPU (CUDA library through the C ABI) against the fp64 CPU oracle on identical seeded inputs.
+
+Bar: max |f_gpu - f_oracle| <= 1e-5 on FLUID cells after N steps (fp32 storage and arithmetic
+against fp64, rho ~ 1); bit-exact where the update is a pure permutation of integer labels."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from lattice_boltzmann_cfd_d3q19_gb300 import binding as B
+from lattice_boltzmann_cfd_d3q19_gb300 import workloads as wl
+from lbm_harness import (LAYOUTS, SCHEMES, TOL_F, Case, max_fluid_diff, random_state, window)
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+
+def mixed_case(nx, ny, nz, faces, seed, solid=0.15, inlet_layer=True, g=(2e-5, -1e-5, 1e-5),
+               tau=0.62):
+    r = np.random.default_rng(seed)
+    N = nx * ny * nz
+    flags = (r.uniform(size=N) < solid).astype(np.uint8)
+    if inlet_layer:
+        x, _, _ = wl.coords(nx, ny, nz)
+        flags[x == 0] = wl.INLET
+    return Case(nx, ny, nz, tau, random_state(N, seed + 1), flags=flags, faces=faces,
+                inlet=(1.01, 0.04, -0.01, 0.02), g=g)
+
+
+# ---- small cases: every scheme x layout, all link types, ragged grids, even and odd counts -------
+
+SMALL = [
+    # nx, ny, nz, faces, solid fraction, inlet layer
+    (37, 23, 19, (0, 0, 0), 0.0, False),
+    (37, 23, 19, (0, 0, 0), 0.2, False),
+    (33, 17, 9, (1, 0, 0), 0.15, True),
+    (20, 19, 11, (1, 1, 0), 0.15, True),
+    (13, 14, 15, (1, 1, 1), 0.1, False),
+    (300, 3, 2, (1, 0, 1), 0.1, True),
+]
+
+
+@pytest.mark.parametrize("scheme", ["AA", "AB", "AB2"])
+@pytest.mark.parametrize("layout", ["stream", "bundle", "collision"])
+@pytest.mark.parametrize("ci", range(len(SMALL)))
+def test_small_cases_match_oracle(ci, layout, scheme):
+    nx, ny, nz, faces, solid, inlet = SMALL[ci]
+    case = mixed_case(nx, ny, nz, faces, 300 + ci, solid=solid, inlet_layer=inlet)
+    for steps in (1, 4, 7):
+        fo, Fo = case.run_oracle(steps, want_force=True)
+        fg, Fg = case.run_gpu(steps, layout, scheme, want_force=True)
+        assert max_fluid_diff(case, fg, fo) <= TOL_F, (steps, max_fluid_diff(case, fg, fo))
+        scale = max(1.0, float(np.abs(Fo).max()))
+        assert np.abs(Fg - Fo).max() <= 1e-4 * scale, (Fg, Fo)
+
+
+def test_degenerate_grids():
+    for (nx, ny, nz) in [(1, 1, 1), (2, 1, 1), (1, 3, 1), (2, 2, 2), (5, 1, 7)]:
+        case = Case(nx, ny, nz, 0.7, random_state(nx * ny * nz, 7), g=(1e-4, 0, 0))
+        fo, _ = case.run_oracle(5)
+        for scheme in SCHEMES:
+            fg, _ = case.run_gpu(5, "stream", scheme)
+            assert max_fluid_diff(case, fg, fo) <= TOL_F
+
+
+def test_zero_steps_is_identity_and_force_unavailable():
+    case = mixed_case(9, 8, 7, (1, 0, 0), 5)
+    ctx = case.gpu_context()
+    try:
+        B.lbm_step(ctx, 0)
+        f = np.zeros((19, case.N), np.float32)
+        B.lbm_get_populations(ctx, f)
+        fl = case.fluid
+        assert np.array_equal(f[:, fl], case.f0_32[:, fl])
+        with pytest.raises(B.LbmError) as ei:
+            B.lbm_force_momentum_exchange(ctx)
+        assert ei.value.code == B.ESTATE
+    finally:
+        B.lbm_destroy(ctx)
+
+
+@pytest.mark.parametrize("scheme", ["AA", "AB"])
+def test_split_step_calls_equal_one_call(scheme):
+    case = mixed_case(17, 9, 10, (1, 0, 0), 11)
+    f1, F1 = case.run_gpu(9, "stream", scheme, want_force=True)
+    f2, F2 = case.run_gpu(9, "stream", scheme, want_force=True, chunks=[2, 3, 1, 3])
+    assert np.array_equal(f1, f2)
+    assert np.array_equal(F1, F2)
+
+
+# ---- streaming is an exact permutation ---------------------------------------------------------------
+
+@pytest.mark.parametrize("scheme", ["AA", "AB", "AB2"])
+@pytest.mark.parametrize("layout", ["stream", "bundle", "collision"])
+def test_streaming_permutation_bit_exact(layout, scheme):
+    """Collision off (tau = 1e30, g = 0), integer labels: every label must land exactly where the
+    oracle (pinned to forward particle tracing) puts it -- neighbour indexing is bit-exact."""
+    nx, ny, nz = 21, 10, 7
+    r = np.random.default_rng(41)
+    flags = (r.uniform(size=nx * ny * nz) < 0.2).astype(np.uint8)
+    case = Case(nx, ny, nz, 1e30, wl.labels(nx * ny * nz), flags=flags)
+    for steps in (1, 2, 5):
+        fo, _ = case.run_oracle(steps)
+        fg, _ = case.run_gpu(steps, layout, scheme)
+        fl = case.fluid
+        assert np.array_equal(fg[:, fl], fo[:, fl]), steps
+
+
+# ---- configuration 1: periodic 32^3 Taylor-Green, 100 steps -----------------------------------------
+
+@pytest.mark.parametrize("scheme", ["AA", "AB"])
+def test_taylor_green_32_full(scheme):
+    rho, u = wl.taylor_green(32, 32, 32, 0.02, noise=1e-4, seed=wl.SEED_TG32)
+    case = Case(32, 32, 32, 0.6, oracle.equilibrium_field(rho, u))
+    fo, _ = case.run_oracle(100)
+    fg, _ = case.run_gpu(100, "stream", scheme)
+    assert max_fluid_diff(case, fg, fo) <= TOL_F
+
+
+# ---- configuration 2: 64^3 channel, Guo forcing, 20000 steps -------------------------------------------
+
+def test_channel_64_full_against_reduced_oracle():
+    """The channel is invariant along x and z, so the 64^3 oracle equals the 1 x 64 x 1 oracle
+    broadcast (pinned bit-exactly on the CPU); the GPU runs the full 64^3 problem."""
+    n, tau, g, steps = 64, 0.8, 1e-6, 20000
+    f0 = oracle.equilibrium_field(*wl.uniform_fields(n))
+    col = Case(1, n, 1, tau, f0, flags=wl.channel_flags(1, n, 1), g=(g, 0, 0))
+    fo, Fo = col.run_oracle(steps, want_force=True)
+    full = Case(n, n, n, tau, oracle.equilibrium_field(*wl.uniform_fields(n ** 3)),
+                flags=wl.channel_flags(n, n, n), g=(g, 0, 0))
+    fg, Fg = full.run_gpu(steps, "stream", "AA", want_force=True)
+    fo_full = np.broadcast_to(fo.reshape(19, 1, n, 1), (19, n, n, n)).reshape(19, -1)
+    assert max_fluid_diff(full, fg, fo_full) <= TOL_F
+    assert abs(Fg[0] - Fo[0] * n * n) <= 1e-3 * abs(Fo[0] * n * n)
+    # the profile: parabola with the startup transient (same bar as the oracle's own pin)
+    ctx = full.gpu_context()
+    try:
+        B.lbm_step(ctx, steps)
+        rho = np.zeros(full.N, np.float32)
+        u = np.zeros(3 * full.N, np.float32)
+        B.lbm_macroscopic(ctx, rho, u)
+    finally:
+        B.lbm_destroy(ctx)
+    ux = u[:full.N].reshape(n, n, n)[:, 1:n - 1, :].mean(axis=(0, 2))
+    nu, H = (tau - 0.5) / 3, n - 2
+    eta = np.arange(1, n - 1) - 0.5
+    expect = g / (2 * nu) * eta * (H - eta)
+    for m in range(1, 400, 2):
+        expect -= (4 * g * H * H / (nu * math.pi ** 3 * m ** 3)) * np.sin(m * math.pi * eta / H) \
+            * math.exp(-m * m * math.pi ** 2 * nu * steps / (H * H))
+    assert np.abs(ux - expect).max() < 0.01 * g * H * H / (8 * nu)
+
+
+# ---- configuration 3: periodic 128^3 Taylor-Green, AA vs A-B across layouts -----------------------
+
+def test_taylor_green_128_layouts_and_schemes():
+    rho, u = wl.taylor_green(128, 128, 128, 0.05)
+    case = Case(128, 128, 128, 0.6, oracle.equilibrium_field(rho, u))
+    steps = 20
+    fo, _ = case.run_oracle(steps)
+    ref = None
+    for layout in LAYOUTS:
+        for scheme in ("AA", "AB"):
+            fg, _ = case.run_gpu(steps, layout, scheme)
+            assert max_fluid_diff(case, fg, fo) <= TOL_F, (layout, scheme)
+            if ref is None:
+                ref = fg
+            else:
+                assert np.abs(fg - ref).max() <= 1e-6, (layout, scheme)
+
+
+# ---- configuration 4: sphere with inlet and open outlet ---------------------------------------------
+
+def sphere_case(nx, ny, nz, center, r, tau=0.56, u_in=0.05):
+    flags = wl.sphere_flags(nx, ny, nz, center, r)
+    f0 = oracle.equilibrium_field(*wl.uniform_fields(nx * ny * nz, 1.0, (u_in, 0, 0)))
+    return Case(nx, ny, nz, tau, f0, flags=flags, faces=(1, 0, 0), inlet=(1.0, u_in, 0.0, 0.0))
+
+
+@pytest.mark.parametrize("scheme", ["AA", "AB"])
+def test_sphere_reduced_full_run(scheme):
+    case = sphere_case(48, 32, 32, (15, 16, 16), 5)
+    fo, Fo = case.run_oracle(300, want_force=True)
+    fg, Fg = case.run_gpu(300, "stream", scheme, want_force=True)
+    assert max_fluid_diff(case, fg, fo) <= TOL_F
+    assert np.abs(Fg - Fo).max() <= 1e-4 * abs(Fo[0])
+    assert Fg[0] > 0
+
+
+def test_sphere_128_windows_and_symmetry():
+    case = sphere_case(128, 128, 128, (40, 64, 64), 16)
+    k = 3
+    fg, _ = case.run_gpu(k, "stream", "AA")
+    centers = [(40, 64, 48 - 1), (24, 64, 64), (56, 70, 64), (100, 5, 120), (64, 64, 81)]
+    for c in centers:
+        sub, ci, _ = window(case, c, k + 1, case.f0_32)
+        fo, _ = sub.run_oracle(k)
+        if sub.flags[ci] != wl.FLUID:
+            continue
+        n = c[0] + 128 * (c[1] + 128 * c[2])
+        assert np.abs(fg[:, n] - fo[:, ci]).max() <= TOL_F, c
+    # full run: the drag is along +x, the transverse force vanishes by mirror symmetry
+    ctx = case.gpu_context()
+    try:
+        B.lbm_step(ctx, 2000)
+        F = B.lbm_force_momentum_exchange(ctx)
+        assert B.lbm_check_finite(ctx)
+    finally:
+        B.lbm_destroy(ctx)
+    assert F[0] > 0
+    assert abs(F[1]) <= 1e-4 * F[0] and abs(F[2]) <= 1e-4 * F[0]
+
+
+# ---- configuration 5: porous medium with body force ----------------------------------------------------
+
+@pytest.mark.parametrize("scheme", ["AA", "AB"])
+def test_porous_reduced_full_run(scheme):
+    n = 48
+    flags = wl.porous_flags(n, n, n, 0.30, 3, seed=wl.SEED_POROUS512)
+    case = Case(n, n, n, 0.7, random_state(n ** 3, 77, amp=5e-3, du=0.02), flags=flags,
+                g=(1e-4, 0, 0))
+    fo, Fo = case.run_oracle(60, want_force=True)
+    fg, Fg = case.run_gpu(60, "stream", scheme, want_force=True)
+    assert max_fluid_diff(case, fg, fo) <= TOL_F
+    assert np.abs(Fg - Fo).max() <= 1e-4 * np.abs(Fo).max()
+
+
+@pytest.mark.slow
+def test_porous_512_windows():
+    """Full 512^3 porous problem in the benchmark's configuration (AA, stream layout), checked on
+    sampled cells against the oracle on their light cones; a random initial state makes every
+    link carry a distinct value."""
+    n = 512
+    flags = wl.porous_flags(n, n, n, 0.30, 3, seed=wl.SEED_POROUS512)
+    N = n ** 3
+    # near-equilibrium random state: one random field, shifted differently per population
+    r = np.random.default_rng(5).uniform(-1, 1, N).astype(np.float32)
+    _, w, _ = oracle.tables()
+    f0 = np.empty((19, N), np.float32)
+    for q in range(19):
+        f0[q] = np.float32(w[q]) * (1 + np.float32(0.01) * np.roll(r, 7919 * q))
+    case = Case(n, n, n, 0.7, f0, flags=flags, g=(1e-6, 0, 0))
+    k = 4
+    fg, _ = case.run_gpu(k, "stream", "AA")
+    rs = np.random.default_rng(9)
+    centers = [tuple(int(v) for v in rs.integers(0, n, 3)) for _ in range(12)]
+    centers += [(0, 0, 0), (511, 511, 511), (0, 255, 511)]
+    checked = 0
+    for c in centers:
+        sub, ci, _ = window(case, c, k + 1, f0)
+        if sub.flags[ci] != wl.FLUID:
+            continue
+        fo, _ = sub.run_oracle(k)
+        nn = c[0] + n * (c[1] + n * c[2])
+        assert np.abs(fg[:, nn] - fo[:, ci]).max() <= TOL_F, c
+        checked += 1
+    assert checked >= 5
+
+
+# ---- state handling ---------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("layout", ["stream", "bundle", "collision"])
+def test_macroscopic_and_host_paths(layout):
+    case = mixed_case(19, 13, 11, (1, 0, 0), 21)
+    P = case.oracle_problem()
+    for steps in (0, 3, 4):
+        fo, _ = P.step_ab(case.f0_32.astype(np.float64), steps)
+        ro, uo = P.macroscopic(fo)
+        for device_input in (True, False):
+            ctx = case.gpu_context(layout, "AA", device_input=device_input)
+            try:
+                B.lbm_step(ctx, steps)
+                rho = np.zeros(case.N, np.float32)
+                u = np.zeros(3 * case.N, np.float32)
+                B.lbm_macroscopic(ctx, rho, u)
+                rho_d = torch.zeros(case.N, dtype=torch.float32, device="cuda")
+                u_d = torch.zeros(3 * case.N, dtype=torch.float32, device="cuda")
+                B.lbm_macroscopic(ctx, rho_d, u_d)
+                f_d = torch.zeros(19 * case.N, dtype=torch.float32, device="cuda")
+                B.lbm_get_populations(ctx, f_d)
+            finally:
+                B.lbm_destroy(ctx)
+            assert np.array_equal(rho, rho_d.cpu().numpy())
+            assert np.array_equal(u, u_d.cpu().numpy())
+            assert np.abs(rho - ro).max() <= 1e-5
+            assert np.abs(u.reshape(3, -1) - uo).max() <= 1e-5
+            fl = case.fluid
+            assert np.abs(f_d.cpu().numpy().reshape(19, -1)[:, fl] - fo[:, fl]).max() <= TOL_F
+
+
+def test_set_equilibrium_matches_oracle():
+    n = 24
+    rho, u = wl.taylor_green(n, n, n, 0.05, noise=1e-3, seed=3)
+    feq = oracle.equilibrium_field(rho, u)
+    ctx = B.lbm_create(n, n, n, 0.6)
+    try:
+        B.lbm_set_equilibrium(ctx, rho.astype(np.float32), u.astype(np.float32).reshape(-1))
+        f = np.zeros((19, n ** 3), np.float32)
+        B.lbm_get_populations(ctx, f)
+    finally:
+        B.lbm_destroy(ctx)
+    assert np.abs(f - feq).max() <= 1e-6
+
+
+def test_invalid_flags_leave_state_unchanged():
+    case = mixed_case(9, 8, 7, (0, 0, 0), 31, inlet_layer=False)
+    ctx = case.gpu_context()
+    try:
+        bad = case.flags.copy()
+        bad[17] = 7
+        with pytest.raises(B.LbmError) as ei:
+            B.lbm_set_flags(ctx, bad)
+        assert ei.value.code == B.EINVAL
+        B.lbm_step(ctx, 3)
+        f = np.zeros((19, case.N), np.float32)
+        B.lbm_get_populations(ctx, f)
+    finally:
+        B.lbm_destroy(ctx)
+    fo, _ = case.run_oracle(3)
+    assert max_fluid_diff(case, f.astype(np.float64), fo) <= TOL_F
+
+
+def test_check_finite_flags_nan():
+    case = mixed_case(8, 8, 8, (0, 0, 0), 33, solid=0.0, inlet_layer=False)
+    f0 = case.f0_32.copy()
+    f0[5, 100] = np.nan
+    ctx = B.lbm_create(8, 8, 8, 0.7)
+    try:
+        B.lbm_set_populations(ctx, case.f0_32)
+        assert B.lbm_check_finite(ctx)
+        B.lbm_set_populations(ctx, f0)
+        assert not B.lbm_check_finite(ctx)
+    finally:
+        B.lbm_destroy(ctx)
+
+
+def test_stream_profile_and_launch_counts():
+    case = mixed_case(16, 16, 16, (1, 0, 0), 35)
+    ctx = case.gpu_context()
+    try:
+        s = torch.cuda.Stream()
+        B.lbm_set_stream(ctx, s.cuda_stream)
+        B.lbm_profile_enable(ctx, True)
+        before = B.lbm_kernel_launches(ctx)
+        B.lbm_step(ctx, 4)
+        s.synchronize()
+        launched = B.lbm_kernel_launches(ctx) - before
+        # 2 even + 2 odd + 2 x 2 open-face pre-gathers + 1 force reduction
+        assert launched == 2 + 2 + 4 + 1
+        n_even, ms_even = B.lbm_profile_read(ctx, B.K_AA_EVEN)
+        n_odd, ms_odd = B.lbm_profile_read(ctx, B.K_AA_ODD)
+        assert n_even == 2 and n_odd == 2 and ms_even > 0 and ms_odd > 0
+        assert B.lbm_step_count(ctx) == 4
+    finally:
+        B.lbm_destroy(ctx)
