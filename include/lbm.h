@@ -162,8 +162,9 @@ int64_t lbm_kernel_launches(lbm_ctx* ctx);
 /* Per-kernel timing ([Layout] "Measuring": per-kernel GPU time on request).  enable != 0 records
  * a CUDA event pair around every step kernel launched afterwards; lbm_profile_read returns, for
  * kernel kind `kind` (0 AA even, 1 AA odd, 2 A-B pull, 3 A-B collide, 4 stream, 5 open-face
- * gather, 6 force reduce), the number of launches and their summed milliseconds since profiling
- * was enabled, and synchronises the stream. */
+ * gather, 6 force reduce, 7 boundary kernels of cells next to an inlet or an open face), the
+ * number of launches and their summed milliseconds since profiling was enabled, and
+ * synchronises the stream. */
 int lbm_profile_enable(lbm_ctx* ctx, int enable);
 int lbm_profile_read(lbm_ctx* ctx, int kind, int64_t* launches, double* total_ms);
 

@@ -21,7 +21,7 @@ OK, EINVAL, ENOMEM, ECUDA, ESTATE, ENOTFINITE = 0, -1, -2, -3, -4, -5
 FLUID, SOLID, INLET = 0, 1, 2
 PERIODIC, OPEN = 0, 1
 # profiling kinds of lbm_profile_read
-K_AA_EVEN, K_AA_ODD, K_AB_PULL, K_AB_COLLIDE, K_STREAM, K_PREGATHER, K_FORCE = range(7)
+K_AA_EVEN, K_AA_ODD, K_AB_PULL, K_AB_COLLIDE, K_STREAM, K_PREGATHER, K_FORCE, K_BOUNDARY = range(8)
 
 # every function declared in include/lbm.h, with (restype, argtypes)
 _P, _I, _F, _D, _I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_double, ctypes.c_int64

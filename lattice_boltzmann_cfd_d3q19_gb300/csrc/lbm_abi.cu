@@ -6,6 +6,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <algorithm>
 #include <new>
 #include <string>
 #include <utility>
@@ -80,10 +81,17 @@ struct lbm_ctx {
     int state = ST_NATURAL;
     uint8_t* types = nullptr;
     uint8_t* flags = nullptr;
+    uint32_t* mask = nullptr;
+    uint32_t* special = nullptr;  // sorted indices of the special FLUID cells
+    uint32_t n_special = 0;
+    uint32_t* count_dev = nullptr;
     float* scratch = nullptr;
     size_t face_base[3][2] = {};
-    double* partial = nullptr;
+    double* partial = nullptr;    // nblocks main-kernel partials, then the boundary kernels'
+    size_t partial_cap = 0;       // triples allocated
     size_t nblocks = 0;
+    size_t force_blocks = 0;      // partial triples written by the step that computes the force
+    double* stage = nullptr;
     double* force_dev = nullptr;
     double* force_host = nullptr;
     int* err_dev = nullptr;
@@ -103,8 +111,12 @@ struct lbm_ctx {
         p.A = A;
         p.B = B;
         p.flags = flags;
+        p.mask = mask;
+        p.special = special;
+        p.n_special = n_special;
         p.scratch = scratch;
         p.partial = partial;
+        p.part_special = nblocks;
         p.nx = n[0];
         p.ny = n[1];
         p.nz = n[2];
@@ -151,6 +163,10 @@ struct lbm_ctx {
         cudaFree(buf[1]);
         cudaFree(types);
         cudaFree(flags);
+        cudaFree(mask);
+        cudaFree(special);
+        cudaFree(count_dev);
+        cudaFree(stage);
         cudaFree(scratch);
         cudaFree(partial);
         cudaFree(force_dev);
@@ -177,15 +193,66 @@ int ensure_staging(lbm_ctx* c) {
     return LBM_OK;
 }
 
+unsigned special_blocks(uint32_t n_special) { return (n_special + 255) / 256; }
+
+// Recompute flags, solid-link masks and the sorted special-cell list from the cell types and
+// faces.  Synchronous.
 int classify(lbm_ctx* c) {
-    LBM_CUDA(launch_classify(c->params(nullptr, nullptr), c->types, c->flags, c->grid, c->block,
+    Params p = c->params(nullptr, nullptr);
+    LBM_CUDA(cudaMemsetAsync(c->count_dev, 0, sizeof(uint32_t), c->stream), "classify");
+    LBM_CUDA(launch_classify(p, c->types, c->flags, c->mask, c->count_dev, c->grid, c->block,
                              c->stream), "classify flags");
     ++c->launches;
+    uint32_t count = 0;
+    LBM_CUDA(cudaMemcpyAsync(&count, c->count_dev, sizeof(uint32_t), cudaMemcpyDeviceToHost,
+                             c->stream), "classify");
+    LBM_CUDA(cudaStreamSynchronize(c->stream), "classify");
+    std::vector<uint32_t> list(count);
+    uint32_t* dev_list = nullptr;
+    if (count > 0) {
+        LBM_CUDA(cudaMalloc(&dev_list, count * sizeof(uint32_t)), "classify: special-cell list");
+        cudaError_t e = cudaMemsetAsync(c->count_dev, 0, sizeof(uint32_t), c->stream);
+        if (e == cudaSuccess)
+            e = launch_list_special(p, c->flags, dev_list, c->count_dev, c->grid, c->block, c->stream);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(list.data(), dev_list, count * sizeof(uint32_t),
+                                cudaMemcpyDeviceToHost, c->stream);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);
+        if (e == cudaSuccess) {
+            ++c->launches;
+            // a fixed cell order keeps the boundary kernels' force partial sums reproducible
+            std::sort(list.begin(), list.end());
+            e = cudaMemcpyAsync(dev_list, list.data(), count * sizeof(uint32_t),
+                                cudaMemcpyHostToDevice, c->stream);
+        }
+        if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);
+        if (e != cudaSuccess) {
+            cudaFree(dev_list);
+            return cuda_fail(e, "classify: special-cell list");
+        }
+    }
+    const size_t need = c->nblocks + special_blocks(count);
+    if (need > c->partial_cap) {
+        double* np_ = nullptr;
+        cudaError_t e = cudaMalloc(&np_, 3 * need * sizeof(double));
+        if (e != cudaSuccess) {
+            cudaFree(dev_list);
+            return cuda_fail(e, "classify: force partials");
+        }
+        cudaFree(c->partial);
+        c->partial = np_;
+        c->partial_cap = need;
+    }
+    cudaFree(c->special);
+    c->special = dev_list;
+    c->n_special = count;
     return LBM_OK;
 }
 
-// Launch a step kernel, timed when profiling is on.
-int launch_kind(lbm_ctx* c, int kind, const Params& p, bool force) {
+// Launch a step kernel (or, for K_BOUNDARY, the boundary kernel of step kind `main_kind`), timed
+// when profiling is on.
+int launch_kind(lbm_ctx* c, int kind, const Params& p, bool force, int main_kind = -1) {
+    if (kind == K_BOUNDARY && c->n_special == 0) return LBM_OK;
     cudaEvent_t e0 = nullptr, e1 = nullptr;
     if (c->profiling) {
         e0 = c->take_event();
@@ -201,11 +268,16 @@ int launch_kind(lbm_ctx* c, int kind, const Params& p, bool force) {
                     ++c->launches;
                 }
     } else if (kind == K_FORCE) {
-        e = launch_force_finalize(c->partial, c->nblocks, c->force_dev, c->stream);
+        e = launch_force_finalize(c->partial, c->force_blocks, c->stage, c->force_dev, c->stream);
+        c->launches += 2;
+    } else if (kind == K_BOUNDARY) {
+        e = c->ops->special(main_kind, p, force, c->body(), c->stream);
         ++c->launches;
+        if (force) c->force_blocks = c->nblocks + special_blocks(c->n_special);
     } else {
         e = c->ops->cells(kind, p, force, c->body(), c->grid, c->block, c->stream);
         ++c->launches;
+        if (force) c->force_blocks = c->nblocks;
     }
     if (c->profiling && e0 && e1) {
         cudaEventRecord(e1, c->stream);
@@ -223,22 +295,28 @@ int step_once(lbm_ctx* c, bool last) {
             rc = launch_kind(c, K_AA_EVEN, p, last);
             c->state = ST_POST_AA;
         } else {
+            // open-face sources are copied before either odd kernel writes
             if (c->any_open()) rc = launch_kind(c, K_PREGATHER, p, false);
             if (rc == LBM_OK) rc = launch_kind(c, K_AA_ODD, p, last);
+            if (rc == LBM_OK) rc = launch_kind(c, K_BOUNDARY, p, last, K_AA_ODD);
             c->state = ST_NATURAL;
         }
     } else if (c->streaming == LBM_STREAMING_AB) {
         const Params p = c->params(c->buf[c->cur], c->buf[c->cur ^ 1]);
-        rc = launch_kind(c, c->state == ST_NATURAL ? K_AB_COLLIDE : K_AB_PULL, p, last);
+        if (c->state == ST_NATURAL) {
+            rc = launch_kind(c, K_AB_COLLIDE, p, last);
+        } else {
+            rc = launch_kind(c, K_AB_PULL, p, last);
+            if (rc == LBM_OK) rc = launch_kind(c, K_BOUNDARY, p, last, K_AB_PULL);
+        }
         c->cur ^= 1;
         c->state = ST_POST_AB;
     } else {  // two-pass: collide in place, then pull into the other buffer
         const Params pc = c->params(c->buf[c->cur], c->buf[c->cur]);
         rc = launch_kind(c, K_AB_COLLIDE, pc, last);
-        if (rc == LBM_OK) {
-            const Params ps = c->params(c->buf[c->cur], c->buf[c->cur ^ 1]);
-            rc = launch_kind(c, K_STREAM, ps, false);
-        }
+        const Params ps = c->params(c->buf[c->cur], c->buf[c->cur ^ 1]);
+        if (rc == LBM_OK) rc = launch_kind(c, K_STREAM, ps, false);
+        if (rc == LBM_OK) rc = launch_kind(c, K_BOUNDARY, ps, false, K_STREAM);
         c->cur ^= 1;
         c->state = ST_NATURAL;
     }
@@ -327,8 +405,10 @@ lbm_ctx* lbm_create(int nx, int ny, int nz, float tau, int layout, int streaming
         return bad(e, "lbm_create: second population buffer");
     if ((e = cudaMalloc(&c->types, N)) != cudaSuccess) return bad(e, "lbm_create: cell types");
     if ((e = cudaMalloc(&c->flags, N)) != cudaSuccess) return bad(e, "lbm_create: cell flags");
-    if ((e = cudaMalloc(&c->partial, 3 * c->nblocks * sizeof(double))) != cudaSuccess)
-        return bad(e, "lbm_create: force partials");
+    if ((e = cudaMalloc(&c->mask, N * sizeof(uint32_t))) != cudaSuccess) return bad(e, "lbm_create: link masks");
+    if ((e = cudaMalloc(&c->count_dev, sizeof(uint32_t))) != cudaSuccess) return bad(e, "lbm_create: counter");
+    if ((e = cudaMalloc(&c->stage, 3 * kForceStage * sizeof(double))) != cudaSuccess)
+        return bad(e, "lbm_create: force stage");
     if ((e = cudaMalloc(&c->force_dev, 3 * sizeof(double))) != cudaSuccess) return bad(e, "lbm_create: force");
     if ((e = cudaMalloc(&c->err_dev, sizeof(int))) != cudaSuccess) return bad(e, "lbm_create: error word");
     if ((e = cudaMallocHost(&c->force_host, 3 * sizeof(double))) != cudaSuccess) return bad(e, "lbm_create: pinned force");

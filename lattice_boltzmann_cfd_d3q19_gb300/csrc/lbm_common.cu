@@ -10,9 +10,11 @@ __global__ void __launch_bounds__(256) k_validate_types(const uint8_t* types, si
     if (n < N && types[n] > T_INLET) *bad = 1;
 }
 
-// flags = type | F_BULK when the cell is FLUID and all 18 neighbours are inside the domain
-// (wrapped on periodic axes, not beyond an open face) and FLUID.
-__global__ void __launch_bounds__(256) k_classify(Params p, const uint8_t* types, uint8_t* flags) {
+// Internal flags and solid-link masks.  For a FLUID cell: mask bit q when x + c_q (wrapped, or
+// clamped at an OPEN face) is SOLID; F_SPECIAL when some x + c_q is INLET or lies beyond an OPEN
+// face; F_BULK when no link rule applies at all.
+__global__ void __launch_bounds__(256) k_classify(Params p, const uint8_t* types, uint8_t* flags,
+                                                  uint32_t* mask, uint32_t* count) {
     const int x = blockIdx.x * blockDim.x + threadIdx.x;
     const int y = blockIdx.y * blockDim.y + threadIdx.y;
     const int z = blockIdx.z;
@@ -20,24 +22,46 @@ __global__ void __launch_bounds__(256) k_classify(Params p, const uint8_t* types
     const uint32_t n = (uint32_t)x + (uint32_t)p.nx * ((uint32_t)y + (uint32_t)p.ny * z);
     const uint8_t t = types[n];
     uint8_t out = t;
+    uint32_t m = 0;
     if (t == T_FLUID) {
-        bool bulk = true;
+        bool special = false;
         for (int q = 1; q < 19; ++q) {
             const Link s = link_cell(p, x, y, z, cx(q), cy(q), cz(q));
-            if (s.face >= 0 || types[s.cell] != T_FLUID) bulk = false;
+            const uint8_t ts = types[s.cell];
+            if (s.face >= 0 || ts == T_INLET) special = true;
+            if (ts == T_SOLID) m |= 1u << q;
         }
-        if (bulk) out |= F_BULK;
+        if (special) {
+            out |= F_SPECIAL;
+            atomicAdd(count, 1u);
+        } else if (m == 0) {
+            out |= F_BULK;
+        }
     }
     flags[n] = out;
+    mask[n] = m;
 }
 
-// Sums the per-block partials in a fixed order (strided per thread, then a tree), in fp64.
-__global__ void __launch_bounds__(256) k_force_finalize(const double* partial, size_t nblocks,
-                                                        double* out) {
+__global__ void __launch_bounds__(256) k_list_special(Params p, const uint8_t* flags,
+                                                      uint32_t* list, uint32_t* count) {
+    const int x = blockIdx.x * blockDim.x + threadIdx.x;
+    const int y = blockIdx.y * blockDim.y + threadIdx.y;
+    const int z = blockIdx.z;
+    if (x >= p.nx || y >= p.ny) return;
+    const uint32_t n = (uint32_t)x + (uint32_t)p.nx * ((uint32_t)y + (uint32_t)p.ny * z);
+    if (flags[n] & F_SPECIAL) list[atomicAdd(count, 1u)] = n;
+}
+
+// Stage 1: block b sums the partials of chunk b in a fixed order (thread-strided, then a tree).
+// Stage 2: one block sums the stage values the same way.
+__global__ void __launch_bounds__(256) k_force_sum(const double* partial, size_t nblocks,
+                                                   size_t chunk, double* out) {
     __shared__ double s[3][256];
     const int t = threadIdx.x;
+    const size_t b0 = (size_t)blockIdx.x * chunk;
+    const size_t b1 = b0 + chunk < nblocks ? b0 + chunk : nblocks;
     double a0 = 0.0, a1 = 0.0, a2 = 0.0;
-    for (size_t b = t; b < nblocks; b += 256) {
+    for (size_t b = b0 + t; b < b1; b += 256) {
         a0 += partial[3 * b + 0];
         a1 += partial[3 * b + 1];
         a2 += partial[3 * b + 2];
@@ -51,7 +75,7 @@ __global__ void __launch_bounds__(256) k_force_finalize(const double* partial, s
             for (int a = 0; a < 3; ++a) s[a][t] += s[a][t + w];
         __syncthreads();
     }
-    if (t < 3) out[t] = s[t][0];
+    if (t < 3) out[3 * blockIdx.x + t] = s[t][0];
 }
 
 }  // namespace
@@ -61,15 +85,25 @@ cudaError_t launch_validate_types(const uint8_t* types, size_t N, int* bad, cuda
     return cudaGetLastError();
 }
 
-cudaError_t launch_classify(const Params& p, const uint8_t* types, uint8_t* flags, dim3 grid,
-                            dim3 block, cudaStream_t s) {
-    k_classify<<<grid, block, 0, s>>>(p, types, flags);
+cudaError_t launch_classify(const Params& p, const uint8_t* types, uint8_t* flags, uint32_t* mask,
+                            uint32_t* count, dim3 grid, dim3 block, cudaStream_t s) {
+    k_classify<<<grid, block, 0, s>>>(p, types, flags, mask, count);
     return cudaGetLastError();
 }
 
-cudaError_t launch_force_finalize(const double* partial, size_t nblocks, double* out,
-                                  cudaStream_t s) {
-    k_force_finalize<<<1, 256, 0, s>>>(partial, nblocks, out);
+cudaError_t launch_list_special(const Params& p, const uint8_t* flags, uint32_t* list,
+                                uint32_t* count, dim3 grid, dim3 block, cudaStream_t s) {
+    k_list_special<<<grid, block, 0, s>>>(p, flags, list, count);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_force_finalize(const double* partial, size_t nblocks, double* stage,
+                                  double* out, cudaStream_t s) {
+    const size_t chunk = (nblocks + kForceStage - 1) / kForceStage;
+    k_force_sum<<<kForceStage, 256, 0, s>>>(partial, nblocks, chunk > 0 ? chunk : 1, stage);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    k_force_sum<<<1, 256, 0, s>>>(stage, kForceStage, kForceStage, out);
     return cudaGetLastError();
 }
 

@@ -14,9 +14,15 @@ namespace lbm {
 
 enum : int { LAYOUT_STREAM = 0, LAYOUT_BUNDLE = 1, LAYOUT_COLLISION = 2 };
 
-// internal flag byte: bits 0-1 cell type, bit 7 "bulk" (FLUID, and all 18 neighbours exist inside
-// the domain -- wrapped on periodic axes, not beyond an open face -- and are FLUID).
-enum : uint8_t { T_FLUID = 0, T_SOLID = 1, T_INLET = 2, TYPE_MASK = 3, F_BULK = 0x80 };
+// internal flag byte: bits 0-1 cell type; for FLUID cells
+//  bit 6 "special": a neighbour x + c_q is INLET or lies beyond an OPEN face -- the cell takes the
+//        general per-link path in the boundary kernels;
+//  bit 7 "bulk": all 18 neighbours exist inside the domain (wrapped on periodic axes) and are
+//        FLUID -- no link rule applies.
+// FLUID cells that are neither have SOLID neighbours only; their links are described by the
+// per-cell solid-link mask (bit q set when x + c_q, wrapped or clamped, is SOLID).
+enum : uint8_t { T_FLUID = 0, T_SOLID = 1, T_INLET = 2, TYPE_MASK = 3, F_SPECIAL = 0x40,
+                 F_BULK = 0x80 };
 
 // what the population buffer holds between steps
 enum : int {
@@ -55,11 +61,13 @@ __host__ __device__ constexpr int bundle_off(int q) {
 }
 __host__ __device__ constexpr int bundle_j(int q) { return bundle_size(q) == 3 ? cx(q) + 1 : 0; }
 
-template <int L>
-__host__ __device__ __forceinline__ size_t idx(int q, uint32_t n, size_t N) {
-    if (L == LAYOUT_STREAM) return (size_t)q * N + n;
-    if (L == LAYOUT_COLLISION) return (size_t)n * 19u + (size_t)q;
-    return (size_t)bundle_off(q) * N + (size_t)n * (size_t)bundle_size(q) + (size_t)bundle_j(q);
+// Element offset of population q of cell n.  I is the offset type: uint32_t when 19 N < 2^32
+// (every offset and every intermediate product then fits), size_t otherwise.
+template <int L, typename I = size_t>
+__host__ __device__ __forceinline__ I idx(int q, uint32_t n, I N) {
+    if (L == LAYOUT_STREAM) return (I)q * N + (I)n;
+    if (L == LAYOUT_COLLISION) return (I)n * (I)19 + (I)q;
+    return (I)bundle_off(q) * N + (I)n * (I)bundle_size(q) + (I)bundle_j(q);
 }
 // runtime-q variant (off the hot path)
 template <int L>
@@ -83,8 +91,12 @@ struct Params {
     float* A;              // buffer read (AA: the only buffer; A-B: source)
     float* B;              // A-B destination (may equal A for the in-place collision)
     const uint8_t* flags;  // internal flag bytes
+    const uint32_t* mask;  // per-cell solid-link mask (read for non-bulk FLUID cells)
+    const uint32_t* special;  // indices of the special FLUID cells
+    uint32_t n_special;
     float* scratch;        // open-face pre-gathered values (AA odd step)
     double* partial;       // per-block momentum-exchange partial sums, 3 per block
+    size_t part_special;   // first partial slot of the boundary kernels' blocks
     int nx, ny, nz;
     int open[3];           // axis has OPEN faces
     size_t N;
@@ -162,7 +174,8 @@ __device__ __forceinline__ void collide(float (&h)[19], const Params& p) {
 
 // ---- momentum-exchange block reduction ----------------------------------------------------------------
 // Every thread of the block must call this.  Warp shuffles, then one fp64 partial per block.
-__device__ __forceinline__ void block_force(float fx, float fy, float fz, double* partial) {
+__device__ __forceinline__ void block_force(float fx, float fy, float fz, double* partial,
+                                            size_t slot_base = 0) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         fx += __shfl_xor_sync(0xffffffffu, fx, o);
@@ -182,7 +195,8 @@ __device__ __forceinline__ void block_force(float fx, float fy, float fz, double
         double s[3] = {0.0, 0.0, 0.0};
         for (int w = 0; w < nwarps; ++w)
             for (int a = 0; a < 3; ++a) s[a] += (double)warp_sum[a][w];
-        const size_t b = blockIdx.x + (size_t)gridDim.x * (blockIdx.y + (size_t)gridDim.y * blockIdx.z);
+        const size_t b = slot_base + blockIdx.x +
+                         (size_t)gridDim.x * (blockIdx.y + (size_t)gridDim.y * blockIdx.z);
         partial[3 * b + 0] = s[0];
         partial[3 * b + 1] = s[1];
         partial[3 * b + 2] = s[2];

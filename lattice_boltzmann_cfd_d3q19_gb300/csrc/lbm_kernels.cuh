@@ -54,31 +54,32 @@ __device__ __forceinline__ size_t scratch_slot(const Params& p, int face, int q,
     return p.face_base[axis][face & 1] + (size_t)q * face_area(p, axis) + face_pos(p, axis, x, y, z);
 }
 
-// Wrapped neighbour coordinates of a bulk cell (a bulk cell never reaches an open face).
+// Neighbour cell indices of a cell whose 18 neighbours are inside the domain (wrapped on periodic
+// axes): n + d, with d the sum of one per-axis delta per velocity component.
 struct Nbr {
-    uint32_t X[3], R[3][3];  // X[cx+1]; R[cy+1][cz+1] = nx (Y + ny Z)
+    int dx[3], dy[3], dz[3];  // delta for c = -1, 0, +1 along each axis
     __device__ __forceinline__ Nbr(const Params& p, int x, int y, int z) {
-        X[0] = x == 0 ? p.nx - 1 : x - 1;
-        X[1] = x;
-        X[2] = x == p.nx - 1 ? 0 : x + 1;
-        const uint32_t Y[3] = {(uint32_t)(y == 0 ? p.ny - 1 : y - 1), (uint32_t)y,
-                               (uint32_t)(y == p.ny - 1 ? 0 : y + 1)};
-        const uint32_t Z[3] = {(uint32_t)(z == 0 ? p.nz - 1 : z - 1), (uint32_t)z,
-                               (uint32_t)(z == p.nz - 1 ? 0 : z + 1)};
-#pragma unroll
-        for (int b = 0; b < 3; ++b)
-#pragma unroll
-            for (int c = 0; c < 3; ++c) R[b][c] = (uint32_t)p.nx * (Y[b] + (uint32_t)p.ny * Z[c]);
+        const int sx = 1, sy = p.nx, sz = p.nx * p.ny;
+        dx[0] = x == 0 ? (p.nx - 1) * sx : -sx;
+        dx[1] = 0;
+        dx[2] = x == p.nx - 1 ? -(p.nx - 1) * sx : sx;
+        dy[0] = y == 0 ? (p.ny - 1) * sy : -sy;
+        dy[1] = 0;
+        dy[2] = y == p.ny - 1 ? -(p.ny - 1) * sy : sy;
+        dz[0] = z == 0 ? (p.nz - 1) * sz : -sz;
+        dz[1] = 0;
+        dz[2] = z == p.nz - 1 ? -(p.nz - 1) * sz : sz;
     }
-    // cell x + s c_q, s = +1 or -1
+    // cell n + s c_q, s = +1 or -1
     template <int Q, int S>
-    __device__ __forceinline__ uint32_t at() const {
-        return X[S * cx(Q) + 1] + R[S * cy(Q) + 1][S * cz(Q) + 1];
+    __device__ __forceinline__ uint32_t at(uint32_t n) const {
+        return n + (uint32_t)(dx[S * cx(Q) + 1] + dy[S * cy(Q) + 1] + dz[S * cz(Q) + 1]);
     }
 };
 
-// Momentum exchange of a non-bulk FLUID cell: every link along which post-collision population q
-// bounces back (x + c_q, wrapped or clamped, is SOLID) adds 2 c_q f*_q, f* = h* + w.
+// Momentum exchange of a FLUID cell: every link along which post-collision population q bounces
+// back (bit q of the solid-link mask: x + c_q, wrapped or clamped, is SOLID) adds 2 c_q f*_q,
+// f* = h* + w.
 template <int Q>
 __device__ __forceinline__ void accumulate_force(float h_post, float& fx, float& fy, float& fz) {
     const float t = 2.0f * (h_post + wq(Q));
@@ -87,39 +88,57 @@ __device__ __forceinline__ void accumulate_force(float h_post, float& fx, float&
     if (cz(Q) > 0) fz += t; else if (cz(Q) < 0) fz -= t;
 }
 
-template <int Q>
-__device__ __forceinline__ void local_force(const Params& p, const float (&h)[19], int x, int y,
-                                            int z, float& fx, float& fy, float& fz) {
-    const Link d = link_cell(p, x, y, z, cx(Q), cy(Q), cz(Q));
-    if ((p.flags[d.cell] & TYPE_MASK) == T_SOLID) accumulate_force<Q>(h[Q], fx, fy, fz);
+template <int Q = 1>
+__device__ __forceinline__ void mask_forces(uint32_t m, const float (&h)[19], float& fx, float& fy,
+                                            float& fz) {
+    if ((m >> Q) & 1u) accumulate_force<Q>(h[Q], fx, fy, fz);
+    if constexpr (Q < 18) mask_forces<Q + 1>(m, h, fx, fy, fz);
 }
 
-template <int Q = 1>
-__device__ __forceinline__ void all_local_forces(const Params& p, const float (&h)[19], int x,
-                                                 int y, int z, float& fx, float& fy, float& fz) {
-    local_force<Q>(p, h, x, y, z, fx, fy, fz);
-    if constexpr (Q < 18) all_local_forces<Q + 1>(p, h, x, y, z, fx, fy, fz);
+template <int Q>
+__device__ __forceinline__ bool solid_link(uint32_t m) { return (m >> Q) & 1u; }
+
+// Thread -> cell of the 3D launch; false for the ragged tail.
+struct CellCoord {
+    int x, y, z;
+    uint32_t n;
+};
+__device__ __forceinline__ bool grid_cell(const Params& p, CellCoord& c) {
+    c.x = blockIdx.x * blockDim.x + threadIdx.x;
+    c.y = blockIdx.y * blockDim.y + threadIdx.y;
+    c.z = blockIdx.z;
+    c.n = (uint32_t)c.x + (uint32_t)p.nx * ((uint32_t)c.y + (uint32_t)p.ny * c.z);
+    return c.x < p.nx && c.y < p.ny;
+}
+// Thread -> i-th special cell of the 1D boundary launch.
+__device__ __forceinline__ bool special_cell(const Params& p, CellCoord& c) {
+    const uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= p.n_special) return false;
+    c.n = p.special[i];
+    c.x = (int)(c.n % (uint32_t)p.nx);
+    c.y = (int)((c.n / (uint32_t)p.nx) % (uint32_t)p.ny);
+    c.z = (int)(c.n / ((uint32_t)p.nx * (uint32_t)p.ny));
+    return true;
 }
 
 // ============================== AA pattern, even step ===========================================
 // "In place" bullet: read population q of x at (q, x); write the collided one at (opposite(q), x).
-template <int L, bool FORCE, bool BODY>
+// Purely local, so every FLUID cell (special ones included) is handled here.
+template <int L, bool FORCE, bool BODY, typename I>
 __global__ void __launch_bounds__(256) k_aa_even(Params p) {
-    const int x = blockIdx.x * blockDim.x + threadIdx.x;
-    const int y = blockIdx.y * blockDim.y + threadIdx.y;
-    const int z = blockIdx.z;
+    CellCoord c;
     float fx = 0.f, fy = 0.f, fz = 0.f;
-    if (x < p.nx && y < p.ny) {
-        const uint32_t n = (uint32_t)x + (uint32_t)p.nx * ((uint32_t)y + (uint32_t)p.ny * z);
-        const uint8_t fl = p.flags[n];
+    if (grid_cell(p, c)) {
+        const uint8_t fl = p.flags[c.n];
         if ((fl & TYPE_MASK) == T_FLUID) {
+            const I N = (I)p.N;
             float h[19];
 #pragma unroll
-            for (int q = 0; q < 19; ++q) h[q] = p.A[idx<L>(q, n, p.N)];
+            for (int q = 0; q < 19; ++q) h[q] = p.A[idx<L, I>(q, c.n, N)];
             collide<BODY>(h, p);
 #pragma unroll
-            for (int q = 0; q < 19; ++q) p.A[idx<L>(opp(q), n, p.N)] = h[q];
-            if (FORCE && !(fl & F_BULK)) all_local_forces(p, h, x, y, z, fx, fy, fz);
+            for (int q = 0; q < 19; ++q) p.A[idx<L, I>(opp(q), c.n, N)] = h[q];
+            if (FORCE && !(fl & F_BULK)) mask_forces(p.mask[c.n], h, fx, fy, fz);
         }
     }
     if (FORCE) block_force(fx, fy, fz, p.partial);
@@ -127,12 +146,56 @@ __global__ void __launch_bounds__(256) k_aa_even(Params p) {
 
 // ============================== AA pattern, odd step ============================================
 // "In place" bullet: read population q of x at (opposite(q), x - c_q); write the collided value at
-// (q, x + c_q).  Cell x reads and writes exactly the same 19 slots, so cells never race.
-// Boundary links use x's own mirrored slots; populations whose source lies beyond an OPEN face
-// were copied to scratch by k_pregather before this kernel (gather before scatter), and the
-// post-collision values of cells on an OPEN face layer are also written to the neighbours that
-// take them as their clamped (zero-gradient) source.
+// (q, x + c_q).  Cell x reads and writes exactly the same 19 slots, so cells never race.  A link
+// whose partner cell is SOLID uses x's own mirrored slot instead: the gather of q reads (q, x),
+// which holds f*_opposite(q)(x) after the even step, and the scatter of q writes (opposite(q), x).
+//
+// Main kernel: FLUID cells that are not special.  The solid-link mask selects, per population,
+// between the neighbour's slot and the cell's own mirrored slot, so bulk and near-wall cells run
+// the same branch-free code.
+template <int L, typename I, int Q = 0>
+__device__ __forceinline__ void aa_odd_load(const Params& p, const Nbr& nb, uint32_t n, uint32_t m,
+                                            I N, float (&h)[19]) {
+    const I own = idx<L, I>(Q, n, N);
+    const I far = idx<L, I>(opp(Q), nb.template at<Q, -1>(n), N);
+    h[Q] = p.A[solid_link<opp(Q)>(m) ? own : far];
+    if constexpr (Q < 18) aa_odd_load<L, I, Q + 1>(p, nb, n, m, N, h);
+}
 
+template <int L, typename I, int Q = 0>
+__device__ __forceinline__ void aa_odd_store(const Params& p, const Nbr& nb, uint32_t n, uint32_t m,
+                                             I N, const float (&h)[19]) {
+    const I own = idx<L, I>(opp(Q), n, N);
+    const I far = idx<L, I>(Q, nb.template at<Q, 1>(n), N);
+    p.A[solid_link<Q>(m) ? own : far] = h[Q];
+    if constexpr (Q < 18) aa_odd_store<L, I, Q + 1>(p, nb, n, m, N, h);
+}
+
+template <int L, bool FORCE, bool BODY, typename I>
+__global__ void __launch_bounds__(256) k_aa_odd(Params p) {
+    CellCoord c;
+    float fx = 0.f, fy = 0.f, fz = 0.f;
+    if (grid_cell(p, c)) {
+        const uint8_t fl = p.flags[c.n];
+        if ((fl & (TYPE_MASK | F_SPECIAL)) == T_FLUID) {
+            const uint32_t m = (fl & F_BULK) ? 0u : p.mask[c.n];
+            const Nbr nb(p, c.x, c.y, c.z);
+            const I N = (I)p.N;
+            float h[19];
+            aa_odd_load<L, I>(p, nb, c.n, m, N, h);
+            collide<BODY>(h, p);
+            aa_odd_store<L, I>(p, nb, c.n, m, N, h);
+            if (FORCE && m) mask_forces(m, h, fx, fy, fz);
+        }
+    }
+    if (FORCE) block_force(fx, fy, fz, p.partial);
+}
+
+// Boundary kernel of the odd step: special cells (an INLET neighbour or a link across an OPEN
+// face), general per-link rules.  Populations whose source lies beyond an OPEN face were copied
+// to scratch by k_pregather before both kernels (gather before scatter), and the post-collision
+// values of cells on an OPEN face layer are also written to the neighbours that take them as their
+// clamped (zero-gradient) source.
 template <int L, int Q>
 __device__ __forceinline__ float aa_odd_gather(const Params& p, uint32_t n, int x, int y, int z) {
     const Link s = link_cell(p, x, y, z, -cx(Q), -cy(Q), -cz(Q));
@@ -173,14 +236,13 @@ __device__ __forceinline__ void aa_odd_face_copies(const Params& p, float v, int
     }
 }
 
-template <int L, bool FORCE, int Q>
+template <int L, int Q>
 __device__ __forceinline__ void aa_odd_scatter(const Params& p, float v, uint32_t n, int x, int y,
-                                               int z, float& fx, float& fy, float& fz) {
+                                               int z) {
     const Link d = link_cell(p, x, y, z, cx(Q), cy(Q), cz(Q));
     const int t = p.flags[d.cell] & TYPE_MASK;
     if (t == T_SOLID) {
         p.A[idx<L>(opp(Q), n, p.N)] = v;                          // bounces back into x
-        if (FORCE) accumulate_force<Q>(v, fx, fy, fz);
     } else if (t == T_INLET) {
         p.A[idx<L>(opp(Q), n, p.N)] = p.heq_in[opp(Q)];            // the reservoir feeds x
     } else if (d.face < 0) {
@@ -196,57 +258,31 @@ __device__ __forceinline__ void aa_odd_gather_all(const Params& p, float (&h)[19
     if constexpr (Q < 18) aa_odd_gather_all<L, Q + 1>(p, h, n, x, y, z);
 }
 
-template <int L, bool FORCE, int Q = 0>
+template <int L, int Q = 0>
 __device__ __forceinline__ void aa_odd_scatter_all(const Params& p, const float (&h)[19],
-                                                   uint32_t n, int x, int y, int z, float& fx,
-                                                   float& fy, float& fz) {
-    aa_odd_scatter<L, FORCE, Q>(p, h[Q], n, x, y, z, fx, fy, fz);
-    if constexpr (Q < 18) aa_odd_scatter_all<L, FORCE, Q + 1>(p, h, n, x, y, z, fx, fy, fz);
-}
-
-template <int L, int Q = 0>
-__device__ __forceinline__ void aa_odd_bulk_load(const Params& p, const Nbr& nb, float (&h)[19]) {
-    h[Q] = p.A[idx<L>(opp(Q), nb.template at<Q, -1>(), p.N)];
-    if constexpr (Q < 18) aa_odd_bulk_load<L, Q + 1>(p, nb, h);
-}
-
-template <int L, int Q = 0>
-__device__ __forceinline__ void aa_odd_bulk_store(const Params& p, const Nbr& nb,
-                                                  const float (&h)[19]) {
-    p.A[idx<L>(Q, nb.template at<Q, 1>(), p.N)] = h[Q];
-    if constexpr (Q < 18) aa_odd_bulk_store<L, Q + 1>(p, nb, h);
+                                                   uint32_t n, int x, int y, int z) {
+    aa_odd_scatter<L, Q>(p, h[Q], n, x, y, z);
+    if constexpr (Q < 18) aa_odd_scatter_all<L, Q + 1>(p, h, n, x, y, z);
 }
 
 template <int L, bool FORCE, bool BODY>
-__global__ void __launch_bounds__(256) k_aa_odd(Params p) {
-    const int x = blockIdx.x * blockDim.x + threadIdx.x;
-    const int y = blockIdx.y * blockDim.y + threadIdx.y;
-    const int z = blockIdx.z;
+__global__ void __launch_bounds__(256) k_aa_odd_special(Params p) {
+    CellCoord c;
     float fx = 0.f, fy = 0.f, fz = 0.f;
-    if (x < p.nx && y < p.ny) {
-        const uint32_t n = (uint32_t)x + (uint32_t)p.nx * ((uint32_t)y + (uint32_t)p.ny * z);
-        const uint8_t fl = p.flags[n];
-        if ((fl & TYPE_MASK) == T_FLUID) {
-            float h[19];
-            if (fl & F_BULK) {
-                const Nbr nb(p, x, y, z);
-                aa_odd_bulk_load<L>(p, nb, h);
-                collide<BODY>(h, p);
-                aa_odd_bulk_store<L>(p, nb, h);
-            } else {
-                aa_odd_gather_all<L>(p, h, n, x, y, z);
-                collide<BODY>(h, p);
-                aa_odd_scatter_all<L, FORCE>(p, h, n, x, y, z, fx, fy, fz);
-            }
-        }
+    if (special_cell(p, c)) {
+        float h[19];
+        aa_odd_gather_all<L>(p, h, c.n, c.x, c.y, c.z);
+        collide<BODY>(h, p);
+        aa_odd_scatter_all<L>(p, h, c.n, c.x, c.y, c.z);
+        if (FORCE) mask_forces(p.mask[c.n], h, fx, fy, fz);
     }
-    if (FORCE) block_force(fx, fy, fz, p.partial);
+    if (FORCE) block_force(fx, fy, fz, p.partial, p.part_special);
 }
 
 // Open-face pre-gather for the AA odd step: for every FLUID cell x on face layer (axis, side) and
 // every q whose source x - c_q lies beyond that face first, copy the clamped source's
-// post-collision population q -- at (opposite(q), s) -- into scratch, before the odd kernel
-// overwrites that slot.
+// post-collision population q -- at (opposite(q), s) -- into scratch, before the odd kernels
+// overwrite that slot.
 template <int L>
 __global__ void __launch_bounds__(256) k_pregather(Params p, int axis, int side) {
     const size_t area = face_area(p, axis);
@@ -267,10 +303,19 @@ __global__ void __launch_bounds__(256) k_pregather(Params p, int axis, int side)
 }
 
 // ============================== two buffers (A-B) ===============================================
-// FROM_NATURAL: collide the natural state in place of the cell (first step after a state load,
-// and the first pass of the two-pass scheme).  Otherwise: pull-collide (PortLBM §3.3 one-step pull,
-// two lattices): gather the 19 populations from the neighbours' post-collision values in A,
-// collide, and write the post-collision values to B at (q, x).
+// Pull (PortLBM §3.3 one-step pull, two lattices): gather the 19 incoming populations from the
+// neighbours' post-collision values in A -- SOLID source: x's own opposite population, at
+// (opposite(q), x) -- collide, and write the post-collision values to B at (q, x).
+template <int L, typename I, int Q = 0>
+__device__ __forceinline__ void ab_load(const Params& p, const Nbr& nb, uint32_t n, uint32_t m, I N,
+                                        float (&h)[19]) {
+    const I own = idx<L, I>(opp(Q), n, N);
+    const I far = idx<L, I>(Q, nb.template at<Q, -1>(n), N);
+    h[Q] = p.A[solid_link<opp(Q)>(m) ? own : far];
+    if constexpr (Q < 18) ab_load<L, I, Q + 1>(p, nb, n, m, N, h);
+}
+
+// general per-link gather (special cells)
 template <int L, int Q = 0>
 __device__ __forceinline__ void ab_gather_all(const Params& p, float (&h)[19], uint32_t n, int x,
                                               int y, int z) {
@@ -282,61 +327,76 @@ __device__ __forceinline__ void ab_gather_all(const Params& p, float (&h)[19], u
     if constexpr (Q < 18) ab_gather_all<L, Q + 1>(p, h, n, x, y, z);
 }
 
-template <int L, int Q = 0>
-__device__ __forceinline__ void ab_bulk_load(const Params& p, const Nbr& nb, float (&h)[19]) {
-    h[Q] = p.A[idx<L>(Q, nb.template at<Q, -1>(), p.N)];
-    if constexpr (Q < 18) ab_bulk_load<L, Q + 1>(p, nb, h);
-}
-
-template <int L, bool FORCE, bool BODY, bool FROM_NATURAL>
+// FROM_NATURAL: collide the natural state of the cell (first step after a state load, and the
+// first pass of the two-pass scheme, where B may equal A); every FLUID cell.  Otherwise
+// pull-collide for the FLUID cells that are not special.
+template <int L, bool FORCE, bool BODY, bool FROM_NATURAL, typename I>
 __global__ void __launch_bounds__(256) k_ab(Params p) {
-    const int x = blockIdx.x * blockDim.x + threadIdx.x;
-    const int y = blockIdx.y * blockDim.y + threadIdx.y;
-    const int z = blockIdx.z;
+    CellCoord c;
     float fx = 0.f, fy = 0.f, fz = 0.f;
-    if (x < p.nx && y < p.ny) {
-        const uint32_t n = (uint32_t)x + (uint32_t)p.nx * ((uint32_t)y + (uint32_t)p.ny * z);
-        const uint8_t fl = p.flags[n];
-        if ((fl & TYPE_MASK) == T_FLUID) {
+    if (grid_cell(p, c)) {
+        const uint8_t fl = p.flags[c.n];
+        const uint8_t want = FROM_NATURAL ? TYPE_MASK : (TYPE_MASK | F_SPECIAL);
+        if ((fl & want) == T_FLUID) {
+            // the natural-state collision needs the links only for the force
+            const uint32_t m = ((fl & F_BULK) || (FROM_NATURAL && !FORCE)) ? 0u : p.mask[c.n];
+            const I N = (I)p.N;
             float h[19];
             if (FROM_NATURAL) {
 #pragma unroll
-                for (int q = 0; q < 19; ++q) h[q] = p.A[idx<L>(q, n, p.N)];
-            } else if (fl & F_BULK) {
-                const Nbr nb(p, x, y, z);
-                ab_bulk_load<L>(p, nb, h);
+                for (int q = 0; q < 19; ++q) h[q] = p.A[idx<L, I>(q, c.n, N)];
             } else {
-                ab_gather_all<L>(p, h, n, x, y, z);
+                const Nbr nb(p, c.x, c.y, c.z);
+                ab_load<L, I>(p, nb, c.n, m, N, h);
             }
             collide<BODY>(h, p);
 #pragma unroll
-            for (int q = 0; q < 19; ++q) p.B[idx<L>(q, n, p.N)] = h[q];
-            if (FORCE && !(fl & F_BULK)) all_local_forces(p, h, x, y, z, fx, fy, fz);
+            for (int q = 0; q < 19; ++q) p.B[idx<L, I>(q, c.n, N)] = h[q];
+            if (FORCE && m) mask_forces(m, h, fx, fy, fz);
         }
     }
     if (FORCE) block_force(fx, fy, fz, p.partial);
 }
 
-// Streaming only: natural state into B from the post-collision state in A (two-pass scheme's
-// second pass).
+template <int L, bool FORCE, bool BODY>
+__global__ void __launch_bounds__(256) k_ab_special(Params p) {
+    CellCoord c;
+    float fx = 0.f, fy = 0.f, fz = 0.f;
+    if (special_cell(p, c)) {
+        float h[19];
+        ab_gather_all<L>(p, h, c.n, c.x, c.y, c.z);
+        collide<BODY>(h, p);
+#pragma unroll
+        for (int q = 0; q < 19; ++q) p.B[idx<L>(q, c.n, p.N)] = h[q];
+        if (FORCE) mask_forces(p.mask[c.n], h, fx, fy, fz);
+    }
+    if (FORCE) block_force(fx, fy, fz, p.partial, p.part_special);
+}
+
+// Streaming only: natural state into B from the post-collision state in A (second pass of the
+// two-pass scheme).  Main kernel (non-special FLUID cells) and boundary kernel (special cells).
 template <int L>
 __global__ void __launch_bounds__(256) k_stream(Params p) {
-    const int x = blockIdx.x * blockDim.x + threadIdx.x;
-    const int y = blockIdx.y * blockDim.y + threadIdx.y;
-    const int z = blockIdx.z;
-    if (x >= p.nx || y >= p.ny) return;
-    const uint32_t n = (uint32_t)x + (uint32_t)p.nx * ((uint32_t)y + (uint32_t)p.ny * z);
-    const uint8_t fl = p.flags[n];
-    if ((fl & TYPE_MASK) != T_FLUID) return;
+    CellCoord c;
+    if (!grid_cell(p, c)) return;
+    const uint8_t fl = p.flags[c.n];
+    if ((fl & (TYPE_MASK | F_SPECIAL)) != T_FLUID) return;
+    const uint32_t m = (fl & F_BULK) ? 0u : p.mask[c.n];
+    const Nbr nb(p, c.x, c.y, c.z);
     float h[19];
-    if (fl & F_BULK) {
-        const Nbr nb(p, x, y, z);
-        ab_bulk_load<L>(p, nb, h);
-    } else {
-        ab_gather_all<L>(p, h, n, x, y, z);
-    }
+    ab_load<L, size_t>(p, nb, c.n, m, p.N, h);
 #pragma unroll
-    for (int q = 0; q < 19; ++q) p.B[idx<L>(q, n, p.N)] = h[q];
+    for (int q = 0; q < 19; ++q) p.B[idx<L>(q, c.n, p.N)] = h[q];
+}
+
+template <int L>
+__global__ void __launch_bounds__(256) k_stream_special(Params p) {
+    CellCoord c;
+    if (!special_cell(p, c)) return;
+    float h[19];
+    ab_gather_all<L>(p, h, c.n, c.x, c.y, c.z);
+#pragma unroll
+    for (int q = 0; q < 19; ++q) p.B[idx<L>(q, c.n, p.N)] = h[q];
 }
 
 // ============================== state access off the step path ==================================

@@ -18,13 +18,16 @@ enum : int {
     K_STREAM = 4,
     K_PREGATHER = 5,
     K_FORCE = 6,
-    K_NUM_KINDS = 7
+    K_BOUNDARY = 7,  // special-cell kernels of the AA odd, A-B pull and streaming steps
+    K_NUM_KINDS = 8
 };
 
 struct LayoutOps {
     // step kernels: K_AA_EVEN, K_AA_ODD, K_AB_PULL, K_AB_COLLIDE, K_STREAM
     cudaError_t (*cells)(int kind, const Params& p, bool force, bool body, dim3 grid, dim3 block,
                          cudaStream_t s);
+    // boundary kernel over the special-cell list for main kind K_AA_ODD, K_AB_PULL or K_STREAM
+    cudaError_t (*special)(int kind, const Params& p, bool force, bool body, cudaStream_t s);
     cudaError_t (*pregather)(const Params& p, int axis, int side, cudaStream_t s);
     cudaError_t (*pack)(const Params& p, const float* in, size_t i0, size_t count, cudaStream_t s);
     cudaError_t (*unpack)(const Params& p, int state, float* out, size_t i0, size_t count,
@@ -42,9 +45,16 @@ const LayoutOps& layout_ops_collision();
 
 // layout-independent kernels
 cudaError_t launch_validate_types(const uint8_t* types, size_t N, int* bad, cudaStream_t s);
-cudaError_t launch_classify(const Params& p, const uint8_t* types, uint8_t* flags, dim3 grid,
-                            dim3 block, cudaStream_t s);
-cudaError_t launch_force_finalize(const double* partial, size_t nblocks, double* out,
-                                  cudaStream_t s);
+// flags, solid-link masks and the number of special cells (added to *count)
+cudaError_t launch_classify(const Params& p, const uint8_t* types, uint8_t* flags, uint32_t* mask,
+                            uint32_t* count, dim3 grid, dim3 block, cudaStream_t s);
+// appends the index of every special cell to list (order unspecified), *count as the cursor
+cudaError_t launch_list_special(const Params& p, const uint8_t* flags, uint32_t* list,
+                                uint32_t* count, dim3 grid, dim3 block, cudaStream_t s);
+// fixed-order fp64 sum of nblocks partial triples: per-chunk sums into stage (kForceStage
+// triples), then one block -> out[3].  Two launches.
+constexpr unsigned kForceStage = 256;
+cudaError_t launch_force_finalize(const double* partial, size_t nblocks, double* stage,
+                                  double* out, cudaStream_t s);
 
 }  // namespace lbm

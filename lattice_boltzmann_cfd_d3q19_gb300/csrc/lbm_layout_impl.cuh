@@ -9,25 +9,37 @@ namespace {
 
 constexpr int L = LBM_LAYOUT;
 
-#define LBM_LAUNCH_FB(KERNEL, EXTRA)                                                   \
-    do {                                                                               \
-        if (force) {                                                                   \
-            if (body) KERNEL<L, true, true EXTRA><<<grid, block, 0, s>>>(p);           \
-            else KERNEL<L, true, false EXTRA><<<grid, block, 0, s>>>(p);               \
-        } else {                                                                       \
-            if (body) KERNEL<L, false, true EXTRA><<<grid, block, 0, s>>>(p);          \
-            else KERNEL<L, false, false EXTRA><<<grid, block, 0, s>>>(p);              \
-        }                                                                              \
-    } while (0)
-#define LBM_COMMA ,
+template <bool F, bool B, typename I>
+void launch_main(int kind, const Params& p, dim3 grid, dim3 block, cudaStream_t s) {
+    switch (kind) {
+        case K_AA_EVEN: k_aa_even<L, F, B, I><<<grid, block, 0, s>>>(p); break;
+        case K_AA_ODD: k_aa_odd<L, F, B, I><<<grid, block, 0, s>>>(p); break;
+        case K_AB_PULL: k_ab<L, F, B, false, I><<<grid, block, 0, s>>>(p); break;
+        case K_AB_COLLIDE: k_ab<L, F, B, true, I><<<grid, block, 0, s>>>(p); break;
+    }
+}
+
+// 64-bit element offsets: with them the compiler strength-reduces the 19 per-population bases
+template <bool F, bool B>
+void launch_main_offsets(int kind, const Params& p, dim3 grid, dim3 block, cudaStream_t s) {
+    launch_main<F, B, size_t>(kind, p, grid, block, s);
+}
 
 cudaError_t cells(int kind, const Params& p, bool force, bool body, dim3 grid, dim3 block,
                   cudaStream_t s) {
     switch (kind) {
-        case K_AA_EVEN: LBM_LAUNCH_FB(k_aa_even, ); break;
-        case K_AA_ODD: LBM_LAUNCH_FB(k_aa_odd, ); break;
-        case K_AB_PULL: LBM_LAUNCH_FB(k_ab, LBM_COMMA false); break;
-        case K_AB_COLLIDE: LBM_LAUNCH_FB(k_ab, LBM_COMMA true); break;
+        case K_AA_EVEN:
+        case K_AA_ODD:
+        case K_AB_PULL:
+        case K_AB_COLLIDE:
+            if (force) {
+                if (body) launch_main_offsets<true, true>(kind, p, grid, block, s);
+                else launch_main_offsets<true, false>(kind, p, grid, block, s);
+            } else {
+                if (body) launch_main_offsets<false, true>(kind, p, grid, block, s);
+                else launch_main_offsets<false, false>(kind, p, grid, block, s);
+            }
+            break;
         case K_STREAM: k_stream<L><<<grid, block, 0, s>>>(p); break;
         default: return cudaErrorInvalidValue;
     }
@@ -35,6 +47,30 @@ cudaError_t cells(int kind, const Params& p, bool force, bool body, dim3 grid, d
 }
 
 unsigned blocks_for(size_t count) { return (unsigned)((count + 255) / 256); }
+
+#define LBM_LAUNCH_SPECIAL(KERNEL)                                                     \
+    do {                                                                               \
+        if (force) {                                                                   \
+            if (body) KERNEL<L, true, true><<<grid, 256, 0, s>>>(p);                   \
+            else KERNEL<L, true, false><<<grid, 256, 0, s>>>(p);                       \
+        } else {                                                                       \
+            if (body) KERNEL<L, false, true><<<grid, 256, 0, s>>>(p);                  \
+            else KERNEL<L, false, false><<<grid, 256, 0, s>>>(p);                      \
+        }                                                                              \
+    } while (0)
+
+cudaError_t special(int kind, const Params& p, bool force, bool body, cudaStream_t s) {
+    if (p.n_special == 0) return cudaSuccess;
+    const unsigned grid = blocks_for(p.n_special);
+    switch (kind) {
+        case K_AA_ODD: LBM_LAUNCH_SPECIAL(k_aa_odd_special); break;
+        case K_AB_PULL: LBM_LAUNCH_SPECIAL(k_ab_special); break;
+        case K_STREAM: k_stream_special<L><<<grid, 256, 0, s>>>(p); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+#undef LBM_LAUNCH_SPECIAL
 
 cudaError_t pregather(const Params& p, int axis, int side, cudaStream_t s) {
     const size_t area = axis == 0 ? (size_t)p.ny * p.nz
@@ -76,9 +112,7 @@ cudaError_t check_finite(const Params& p, int* bad, dim3 grid, dim3 block, cudaS
     return cudaGetLastError();
 }
 
-const LayoutOps kOps = {cells, pregather, pack, unpack, equilibrium, macro, check_finite};
+const LayoutOps kOps = {cells, special, pregather, pack, unpack, equilibrium, macro, check_finite};
 
-#undef LBM_LAUNCH_FB
-#undef LBM_COMMA
 }  // namespace
 }  // namespace lbm
