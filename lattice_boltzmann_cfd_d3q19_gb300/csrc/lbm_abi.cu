@@ -127,7 +127,21 @@ struct lbm_ctx {
         p.omega = omega;
         for (int a = 0; a < 3; ++a) p.g[a] = g[a];
         for (int q = 0; q < 19; ++q) p.heq_in[q] = heq_in[q];
+        for (int q = 0; q < 19; ++q) {
+            const size_t off = plane_offset(q), off_opp = plane_offset(opp(q));
+            p.pa[q] = A ? A + off : nullptr;
+            p.pb[q] = B ? B + off : nullptr;
+            p.pdiff[q] = (long long)off - (long long)off_opp;
+        }
         return p;
+    }
+    // element offset of population q of cell 0 in the population layout
+    size_t plane_offset(int q) const {
+        switch (layout) {
+            case LBM_LAYOUT_BUNDLE: return idx<LAYOUT_BUNDLE>(q, 0, N);
+            case LBM_LAYOUT_COLLISION: return idx<LAYOUT_COLLISION>(q, 0, N);
+            default: return idx<LAYOUT_STREAM>(q, 0, N);
+        }
     }
     bool body() const { return g[0] != 0.f || g[1] != 0.f || g[2] != 0.f; }
     bool any_open() const { return face[0] == LBM_OPEN || face[1] == LBM_OPEN || face[2] == LBM_OPEN; }

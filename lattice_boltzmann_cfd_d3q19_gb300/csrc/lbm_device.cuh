@@ -61,13 +61,18 @@ __host__ __device__ constexpr int bundle_off(int q) {
 }
 __host__ __device__ constexpr int bundle_j(int q) { return bundle_size(q) == 3 ? cx(q) + 1 : 0; }
 
-// Element offset of population q of cell n.  I is the offset type: uint32_t when 19 N < 2^32
-// (every offset and every intermediate product then fits), size_t otherwise.
+// Element offset of population q of cell n.
 template <int L, typename I = size_t>
 __host__ __device__ __forceinline__ I idx(int q, uint32_t n, I N) {
     if (L == LAYOUT_STREAM) return (I)q * N + (I)n;
     if (L == LAYOUT_COLLISION) return (I)n * (I)19 + (I)q;
     return (I)bundle_off(q) * N + (I)n * (I)bundle_size(q) + (I)bundle_j(q);
+}
+// In every layout population q of cell n sits at plane(q) + n * cell_stride(q), with
+// plane(q) = idx(q, 0); opposite populations share their stride.
+template <int L>
+__host__ __device__ constexpr int cell_stride(int q) {
+    return L == LAYOUT_STREAM ? 1 : L == LAYOUT_COLLISION ? 19 : bundle_size(q);
 }
 // runtime-q variant (off the hot path)
 template <int L>
@@ -104,6 +109,11 @@ struct Params {
     float omega;
     float g[3];
     float heq_in[19];      // shifted inlet state f_eq(rho_in, u_in) - w
+    // hot-path addressing: population q of cell n is pa[q][n * cell_stride(q)] in A and
+    // pb[q][n * cell_stride(q)] in B; pdiff[q] = pa[q] - pa[opposite(q)] in elements
+    float* pa[19];
+    float* pb[19];
+    long long pdiff[19];
 };
 
 // ---- per-link geometry ----------------------------------------------------------------------------
@@ -138,16 +148,15 @@ __device__ __forceinline__ void collide(float (&h)[19], const Params& p) {
     const float rho = 1.0f + drho;
     const float inv = 1.0f / rho;
     float ux = jx * inv, uy = jy * inv, uz = jz * inv;
-    float Fx = 0.f, Fy = 0.f, Fz = 0.f, uF = 0.f, src = 0.f;
+    // Guo forcing with F = rho g: the source is (1 - omega/2) rho w [3 (c.g - u.g) + 9 (c.u)(c.g)];
+    // g stays a launch parameter (warp-uniform), so only u.g and (1 - omega/2) rho are per cell
+    float ug = 0.f, srho = 0.f;
     if (BODY) {
         ux = fmaf(0.5f, p.g[0], ux);
         uy = fmaf(0.5f, p.g[1], uy);
         uz = fmaf(0.5f, p.g[2], uz);
-        Fx = rho * p.g[0];
-        Fy = rho * p.g[1];
-        Fz = rho * p.g[2];
-        uF = ux * Fx + uy * Fy + uz * Fz;
-        src = 1.0f - 0.5f * p.omega;
+        ug = ux * p.g[0] + uy * p.g[1] + uz * p.g[2];
+        srho = (1.0f - 0.5f * p.omega) * rho;
     }
     const float uu15 = 1.5f * (ux * ux + uy * uy + uz * uz);
     const float om = p.omega;
@@ -162,11 +171,11 @@ __device__ __forceinline__ void collide(float (&h)[19], const Params& p) {
         const float heq = wq(q) * fmaf(rho, poly, drho);
         float hn = fmaf(-om, h[q] - heq, h[q]);
         if (BODY) {
-            float cF = 0.f;
-            if (cx(q) > 0) cF += Fx; else if (cx(q) < 0) cF -= Fx;
-            if (cy(q) > 0) cF += Fy; else if (cy(q) < 0) cF -= Fy;
-            if (cz(q) > 0) cF += Fz; else if (cz(q) < 0) cF -= Fz;
-            hn = fmaf(src * wq(q), fmaf(9.0f * cu, cF, 3.0f * (cF - uF)), hn);
+            float cg = 0.f;
+            if (cx(q) > 0) cg += p.g[0]; else if (cx(q) < 0) cg -= p.g[0];
+            if (cy(q) > 0) cg += p.g[1]; else if (cy(q) < 0) cg -= p.g[1];
+            if (cz(q) > 0) cg += p.g[2]; else if (cz(q) < 0) cg -= p.g[2];
+            hn = fmaf(srho * wq(q), fmaf(9.0f * cu, cg, 3.0f * (cg - ug)), hn);
         }
         h[q] = hn;
     }

@@ -124,6 +124,13 @@ __device__ __forceinline__ bool special_cell(const Params& p, CellCoord& c) {
 // ============================== AA pattern, even step ===========================================
 // "In place" bullet: read population q of x at (q, x); write the collided one at (opposite(q), x).
 // Purely local, so every FLUID cell (special ones included) is handled here.
+// Hot-path addressing: element offset, relative to a population's plane pointer, of cell n
+// (I = int when every offset of the launch fits, else long long).
+template <int L, typename I>
+__device__ __forceinline__ I cell_off(int q, uint32_t n) {
+    return (I)n * (I)cell_stride<L>(q);
+}
+
 template <int L, bool FORCE, bool BODY, typename I>
 __global__ void __launch_bounds__(256) k_aa_even(Params p) {
     CellCoord c;
@@ -131,13 +138,15 @@ __global__ void __launch_bounds__(256) k_aa_even(Params p) {
     if (grid_cell(p, c)) {
         const uint8_t fl = p.flags[c.n];
         if ((fl & TYPE_MASK) == T_FLUID) {
-            const I N = (I)p.N;
             float h[19];
 #pragma unroll
-            for (int q = 0; q < 19; ++q) h[q] = p.A[idx<L, I>(q, c.n, N)];
+            for (int q = 0; q < 19; ++q) h[q] = p.pa[q][cell_off<L, I>(q, c.n)];
             collide<BODY>(h, p);
+            // store addresses formed after the collision, not kept from the loads
+            uint32_t ns = c.n;
+            asm volatile("" : "+r"(ns) : "f"(h[0]), "f"(h[18]));
 #pragma unroll
-            for (int q = 0; q < 19; ++q) p.A[idx<L, I>(opp(q), c.n, N)] = h[q];
+            for (int q = 0; q < 19; ++q) p.pa[opp(q)][cell_off<L, I>(q, ns)] = h[q];
             if (FORCE && !(fl & F_BULK)) mask_forces(p.mask[c.n], h, fx, fy, fz);
         }
     }
@@ -155,20 +164,22 @@ __global__ void __launch_bounds__(256) k_aa_even(Params p) {
 // the same branch-free code.
 template <int L, typename I, int Q = 0>
 __device__ __forceinline__ void aa_odd_load(const Params& p, const Nbr& nb, uint32_t n, uint32_t m,
-                                            I N, float (&h)[19]) {
-    const I own = idx<L, I>(Q, n, N);
-    const I far = idx<L, I>(opp(Q), nb.template at<Q, -1>(n), N);
-    h[Q] = p.A[solid_link<opp(Q)>(m) ? own : far];
-    if constexpr (Q < 18) aa_odd_load<L, I, Q + 1>(p, nb, n, m, N, h);
+                                            float (&h)[19]) {
+    // own slot (q, x) = pa[opp q] + pdiff[q] + n s; neighbour slot (opp q, x - c_q)
+    const I own = (I)p.pdiff[Q] + cell_off<L, I>(Q, n);
+    const I far = cell_off<L, I>(Q, nb.template at<Q, -1>(n));
+    h[Q] = p.pa[opp(Q)][solid_link<opp(Q)>(m) ? own : far];
+    if constexpr (Q < 18) aa_odd_load<L, I, Q + 1>(p, nb, n, m, h);
 }
 
 template <int L, typename I, int Q = 0>
 __device__ __forceinline__ void aa_odd_store(const Params& p, const Nbr& nb, uint32_t n, uint32_t m,
-                                             I N, const float (&h)[19]) {
-    const I own = idx<L, I>(opp(Q), n, N);
-    const I far = idx<L, I>(Q, nb.template at<Q, 1>(n), N);
-    p.A[solid_link<Q>(m) ? own : far] = h[Q];
-    if constexpr (Q < 18) aa_odd_store<L, I, Q + 1>(p, nb, n, m, N, h);
+                                             const float (&h)[19]) {
+    // own slot (opp q, x) = pa[q] - pdiff[q] + n s; neighbour slot (q, x + c_q)
+    const I own = cell_off<L, I>(Q, n) - (I)p.pdiff[Q];
+    const I far = cell_off<L, I>(Q, nb.template at<Q, 1>(n));
+    p.pa[Q][solid_link<Q>(m) ? own : far] = h[Q];
+    if constexpr (Q < 18) aa_odd_store<L, I, Q + 1>(p, nb, n, m, h);
 }
 
 template <int L, bool FORCE, bool BODY, typename I>
@@ -180,12 +191,15 @@ __global__ void __launch_bounds__(256) k_aa_odd(Params p) {
         if ((fl & (TYPE_MASK | F_SPECIAL)) == T_FLUID) {
             const uint32_t m = (fl & F_BULK) ? 0u : p.mask[c.n];
             const Nbr nb(p, c.x, c.y, c.z);
-            const I N = (I)p.N;
             float h[19];
-            aa_odd_load<L, I>(p, nb, c.n, m, N, h);
+            aa_odd_load<L, I>(p, nb, c.n, m, h);
             collide<BODY>(h, p);
-            aa_odd_store<L, I>(p, nb, c.n, m, N, h);
-            if (FORCE && m) mask_forces(m, h, fx, fy, fz);
+            // the store addresses are formed after the collision (keeps them out of registers
+            // while the loads are in flight)
+            uint32_t ns = c.n, ms = m;
+            asm volatile("" : "+r"(ns), "+r"(ms) : "f"(h[0]), "f"(h[18]));
+            aa_odd_store<L, I>(p, nb, ns, ms, h);
+            if (FORCE && ms) mask_forces(ms, h, fx, fy, fz);
         }
     }
     if (FORCE) block_force(fx, fy, fz, p.partial);
@@ -307,12 +321,13 @@ __global__ void __launch_bounds__(256) k_pregather(Params p, int axis, int side)
 // neighbours' post-collision values in A -- SOLID source: x's own opposite population, at
 // (opposite(q), x) -- collide, and write the post-collision values to B at (q, x).
 template <int L, typename I, int Q = 0>
-__device__ __forceinline__ void ab_load(const Params& p, const Nbr& nb, uint32_t n, uint32_t m, I N,
+__device__ __forceinline__ void ab_load(const Params& p, const Nbr& nb, uint32_t n, uint32_t m,
                                         float (&h)[19]) {
-    const I own = idx<L, I>(opp(Q), n, N);
-    const I far = idx<L, I>(Q, nb.template at<Q, -1>(n), N);
-    h[Q] = p.A[solid_link<opp(Q)>(m) ? own : far];
-    if constexpr (Q < 18) ab_load<L, I, Q + 1>(p, nb, n, m, N, h);
+    // own slot (opp q, x) = pa[q] - pdiff[q] + n s; neighbour slot (q, x - c_q)
+    const I own = cell_off<L, I>(Q, n) - (I)p.pdiff[Q];
+    const I far = cell_off<L, I>(Q, nb.template at<Q, -1>(n));
+    h[Q] = p.pa[Q][solid_link<opp(Q)>(m) ? own : far];
+    if constexpr (Q < 18) ab_load<L, I, Q + 1>(p, nb, n, m, h);
 }
 
 // general per-link gather (special cells)
@@ -340,18 +355,19 @@ __global__ void __launch_bounds__(256) k_ab(Params p) {
         if ((fl & want) == T_FLUID) {
             // the natural-state collision needs the links only for the force
             const uint32_t m = ((fl & F_BULK) || (FROM_NATURAL && !FORCE)) ? 0u : p.mask[c.n];
-            const I N = (I)p.N;
             float h[19];
             if (FROM_NATURAL) {
 #pragma unroll
-                for (int q = 0; q < 19; ++q) h[q] = p.A[idx<L, I>(q, c.n, N)];
+                for (int q = 0; q < 19; ++q) h[q] = p.pa[q][cell_off<L, I>(q, c.n)];
             } else {
                 const Nbr nb(p, c.x, c.y, c.z);
-                ab_load<L, I>(p, nb, c.n, m, N, h);
+                ab_load<L, I>(p, nb, c.n, m, h);
             }
             collide<BODY>(h, p);
+            uint32_t ns = c.n;
+            asm volatile("" : "+r"(ns) : "f"(h[0]), "f"(h[18]));
 #pragma unroll
-            for (int q = 0; q < 19; ++q) p.B[idx<L, I>(q, c.n, N)] = h[q];
+            for (int q = 0; q < 19; ++q) p.pb[q][cell_off<L, I>(q, ns)] = h[q];
             if (FORCE && m) mask_forces(m, h, fx, fy, fz);
         }
     }
@@ -375,7 +391,7 @@ __global__ void __launch_bounds__(256) k_ab_special(Params p) {
 
 // Streaming only: natural state into B from the post-collision state in A (second pass of the
 // two-pass scheme).  Main kernel (non-special FLUID cells) and boundary kernel (special cells).
-template <int L>
+template <int L, typename I>
 __global__ void __launch_bounds__(256) k_stream(Params p) {
     CellCoord c;
     if (!grid_cell(p, c)) return;
@@ -384,9 +400,9 @@ __global__ void __launch_bounds__(256) k_stream(Params p) {
     const uint32_t m = (fl & F_BULK) ? 0u : p.mask[c.n];
     const Nbr nb(p, c.x, c.y, c.z);
     float h[19];
-    ab_load<L, size_t>(p, nb, c.n, m, p.N, h);
+    ab_load<L, I>(p, nb, c.n, m, h);
 #pragma unroll
-    for (int q = 0; q < 19; ++q) p.B[idx<L>(q, c.n, p.N)] = h[q];
+    for (int q = 0; q < 19; ++q) p.pb[q][cell_off<L, I>(q, c.n)] = h[q];
 }
 
 template <int L>

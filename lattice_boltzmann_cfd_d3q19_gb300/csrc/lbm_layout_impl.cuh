@@ -19,10 +19,11 @@ void launch_main(int kind, const Params& p, dim3 grid, dim3 block, cudaStream_t 
     }
 }
 
-// 64-bit element offsets: with them the compiler strength-reduces the 19 per-population bases
+// The hot kernels address populations as plane pointer + 64-bit element offset (measured faster
+// than 32-bit offsets in the odd kernel, whose registers they keep lower).
 template <bool F, bool B>
 void launch_main_offsets(int kind, const Params& p, dim3 grid, dim3 block, cudaStream_t s) {
-    launch_main<F, B, size_t>(kind, p, grid, block, s);
+    launch_main<F, B, long long>(kind, p, grid, block, s);
 }
 
 cudaError_t cells(int kind, const Params& p, bool force, bool body, dim3 grid, dim3 block,
@@ -40,7 +41,7 @@ cudaError_t cells(int kind, const Params& p, bool force, bool body, dim3 grid, d
                 else launch_main_offsets<false, false>(kind, p, grid, block, s);
             }
             break;
-        case K_STREAM: k_stream<L><<<grid, block, 0, s>>>(p); break;
+        case K_STREAM: k_stream<L, long long><<<grid, block, 0, s>>>(p); break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
