@@ -171,6 +171,30 @@ int lbm_profile_read(lbm_ctx* ctx, int kind, int64_t* launches, double* total_ms
 /* Release every resource of the context.  NULL-safe.  Synchronises its stream first. */
 void lbm_destroy(lbm_ctx* ctx);
 
+/* Momentum-exchange force of ONE collision of a caller-held state, without allocating any memory.
+ * The source papers and pages describe no counterpart to this entry point; it exists for callers
+ * that cannot call cudaMalloc (code running while a CUDA graph is captured on their stream,
+ * plug-ins whose host application owns all device memory through its own pool, tools that must
+ * not grow an embedding process's footprint).  It computes what lbm_force_momentum_exchange
+ * reports after lbm_set_populations(f) and lbm_step(1) on a context with the same grid, tau,
+ * flags, faces and body force: the sum over every bounce-back link of a FLUID cell of
+ * 2 c_q f*_q, f* the post-collision state.
+ *   f       device memory, canonical natural state f[q*N + n] (absolute fp32), 19*N floats;
+ *   flags   device memory, N bytes, LBM_FLUID / LBM_SOLID / LBM_INLET (others -> LBM_EINVAL);
+ *   face_*  LBM_PERIODIC or LBM_OPEN per axis; tau > 1/2; g the body acceleration (Guo forcing);
+ *   F       host memory, 3 doubles, written on success;
+ *   cuda_stream  the stream to run on (NULL: the legacy default stream); synchronised on return.
+ * Working memory: one fixed array of about 1.5 MiB in the library's static device memory, held
+ * by every GPU that loads the library until the process exits.  Grids of more than 16,777,216
+ * cells (256^3) exceed it and are rejected with LBM_EINVAL before any CUDA call.  The first call
+ * on each device looks the array's device address up (cudaGetSymbolAddress); make that first
+ * call before any stream capture.  All calls share the array: calls that overlap on the GPU
+ * (on different streams or host threads) race and give wrong results; serialise them. */
+int lbm_force_momentum_exchange_noalloc(const float* f, const uint8_t* flags, int nx, int ny,
+                                        int nz, int face_x, int face_y, int face_z, float tau,
+                                        float gx, float gy, float gz, double F[3],
+                                        void* cuda_stream);
+
 #ifdef __cplusplus
 }
 #endif

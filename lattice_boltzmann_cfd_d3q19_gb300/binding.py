@@ -45,6 +45,8 @@ SIGNATURES = {
     "lbm_profile_enable": (_I, [_P, _I]),
     "lbm_profile_read": (_I, [_P, _I, _P, _P]),
     "lbm_destroy": (None, [_P]),
+    "lbm_force_momentum_exchange_noalloc": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _F, _F, _F, _F,
+                                                 _P, _P]),
 }
 
 
@@ -206,3 +208,15 @@ def lbm_profile_read(ctx: int, kind: int):
 def lbm_destroy(ctx: int) -> None:
     if ctx:
         load().lbm_destroy(ctx)
+
+
+def lbm_force_momentum_exchange_noalloc(f, flags, nx: int, ny: int, nz: int, faces=(0, 0, 0),
+                                        tau: float = 0.6, g=(0.0, 0.0, 0.0),
+                                        cuda_stream: int = 0) -> np.ndarray:
+    """Force of one collision of the device state f with no allocation (see include/lbm.h)."""
+    F = np.zeros(3, np.float64)
+    _check(load().lbm_force_momentum_exchange_noalloc(
+        _ptr(f, np.float32), _ptr(flags, np.uint8), int(nx), int(ny), int(nz), int(faces[0]),
+        int(faces[1]), int(faces[2]), float(tau), float(g[0]), float(g[1]), float(g[2]),
+        F.ctypes.data, cuda_stream or None))
+    return F

@@ -66,6 +66,12 @@ constexpr size_t kStagingFloats = size_t(32) << 20;  // 128 MiB host-transfer st
 
 }  // namespace
 
+void lbm::set_last_error_v(const char* fmt, va_list ap) {
+    char buf[512];
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    g_err = buf;
+}
+
 struct lbm_ctx {
     int n[3] = {0, 0, 0};
     size_t N = 0;

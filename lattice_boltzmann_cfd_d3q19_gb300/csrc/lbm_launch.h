@@ -1,6 +1,7 @@
 // Host-side launch interface between the C ABI and the layout-specific kernel instantiations.
 #pragma once
 
+#include <cstdarg>
 #include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -56,5 +57,8 @@ cudaError_t launch_list_special(const Params& p, const uint8_t* flags, uint32_t*
 constexpr unsigned kForceStage = 256;
 cudaError_t launch_force_finalize(const double* partial, size_t nblocks, double* stage,
                                   double* out, cudaStream_t s);
+
+// Sets the calling thread's lbm_last_error() message (printf-style).
+void set_last_error_v(const char* fmt, va_list ap);
 
 }  // namespace lbm
