@@ -1,0 +1,79 @@
+"""Host logic of bench.py (no GPU): roofline arithmetic against the pages' worked examples, the
+whole-job throughput rule, and the max-over-ranks timing across two gloo ranks."""
+import os
+import sys
+
+import pytest
+
+import bench
+
+
+def golden_map(golden, name):
+    return {r[0]: float(r[1]) for r in golden(name)}
+
+
+def test_bytes_per_update_match_page(golden):
+    g = golden_map(golden, "bytes_per_update.txt")
+    # 19 fp32 populations read and written once per cell update
+    assert bench.POP_BYTES == 2 * 19 * 4 == g["in_place"]
+    assert bench.algorithmic_bytes(1, "AA") == g["in_place"] + bench.FLAG_BYTES
+    assert bench.algorithmic_bytes(1, "AB2") == g["two_buffers"] + bench.FLAG_BYTES
+    assert bench.fluid_bytes(10, 7) == 7 * 152 + 10
+
+
+def test_code_balance_roofline_reproduces_portlbm_example(golden):
+    g = golden_map(golden, "portlbm_code_balance.txt")
+    assert g["read_bytes"] + g["write_bytes"] == g["code_balance"]
+    for bw, glups in (("a30_peak_gbs", "a30_peak_glups"), ("a30_measured_gbs", "a30_measured_glups"),
+                      ("mi210_peak_gbs", "mi210_peak_glups")):
+        assert abs(bench.roofline_glups(g[bw], g["code_balance"]) - g[glups]) < 0.006
+
+
+def test_whole_job_throughput_counts_all_ranks():
+    # 2 ranks x 100 cells x 10 steps = 2000 updates in 1 ms (the slowest rank) -> 2 MLUPS
+    assert bench.whole_job_mlups(100, 10, 2, 1e-3) == pytest.approx(2.0)
+
+
+def _rank_main(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world))
+    import torch.distributed as dist
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    got = bench.reduce_max(0.5 + rank, world)
+    out.put((rank, got))
+    dist.destroy_process_group()
+
+
+def test_reduce_max_over_two_gloo_ranks():
+    import multiprocessing as mp
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = dict(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert res == {0: 1.5, 1: 1.5}
+
+
+def test_dist_env_defaults(monkeypatch):
+    for k in ("WORLD_SIZE", "RANK", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+    assert bench.dist_env() == (1, 0, 0)
+
+
+def test_recorded_traffic_requires_matching_sources(tmp_path, monkeypatch):
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    (prof / "ncu_traffic.txt").write_text("kernel_source_sha256: deadbeef\naa_odd_dram_bytes_per_cell: 150\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "deadbeef")
+    assert bench.recorded_traffic("aa_odd") == 150.0
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "changed")
+    assert bench.recorded_traffic("aa_odd") is None
