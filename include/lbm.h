@@ -144,8 +144,8 @@ int lbm_macroscopic(lbm_ctx* ctx, float* rho, float* u);
 
 /* Force on all SOLID cells (one body) from the last step of the last lbm_step call
  * ([Layout]: the momentum exchange is taken in the step whose forces are read back): the sum
- * over every bounce-back link of a FLUID cell of 2 c_q f*_q, accumulated in fp32 per cell and in
- * fp64 across cells, in a fixed order.  F[3] in lattice units.  LBM_ESTATE before the first step
+ * over every bounce-back link of a FLUID cell of 2 c_q f*_q, accumulated in fp32 within each warp
+ * of 32 cells and in fp64 across warps, in a fixed order.  F[3] in lattice units.  LBM_ESTATE before the first step
  * or after the state was reloaded.  Synchronous. */
 int lbm_force_momentum_exchange(lbm_ctx* ctx, double F[3]);
 

@@ -96,7 +96,7 @@ struct lbm_ctx {
     double* partial = nullptr;    // nblocks main-kernel partials, then the boundary kernels'
     size_t partial_cap = 0;       // triples allocated
     size_t nblocks = 0;
-    size_t force_blocks = 0;      // partial triples written by the step that computes the force
+    size_t force_triples = 0;     // partial triples written by the step that computes the force
     double* stage = nullptr;
     double* force_dev = nullptr;
     double* force_host = nullptr;
@@ -122,7 +122,7 @@ struct lbm_ctx {
         p.n_special = n_special;
         p.scratch = scratch;
         p.partial = partial;
-        p.part_special = nblocks;
+        p.part_special = nblocks * kWarpsPerBlock;
         p.nx = n[0];
         p.ny = n[1];
         p.nz = n[2];
@@ -215,6 +215,11 @@ int ensure_staging(lbm_ctx* c) {
 
 unsigned special_blocks(uint32_t n_special) { return (n_special + 255) / 256; }
 
+// one fp64 partial triple per warp of the step kernels and of the boundary kernels
+size_t partial_triples(size_t main_blocks, uint32_t n_special) {
+    return (main_blocks + special_blocks(n_special)) * kWarpsPerBlock;
+}
+
 // Recompute flags, solid-link masks and the sorted special-cell list from the cell types and
 // faces.  Synchronous.
 int classify(lbm_ctx* c) {
@@ -251,7 +256,7 @@ int classify(lbm_ctx* c) {
             return cuda_fail(e, "classify: special-cell list");
         }
     }
-    const size_t need = c->nblocks + special_blocks(count);
+    const size_t need = partial_triples(c->nblocks, count);
     if (need > c->partial_cap) {
         double* np_ = nullptr;
         cudaError_t e = cudaMalloc(&np_, 3 * need * sizeof(double));
@@ -288,16 +293,16 @@ int launch_kind(lbm_ctx* c, int kind, const Params& p, bool force, int main_kind
                     ++c->launches;
                 }
     } else if (kind == K_FORCE) {
-        e = launch_force_finalize(c->partial, c->force_blocks, c->stage, c->force_dev, c->stream);
+        e = launch_force_finalize(c->partial, c->force_triples, c->stage, c->force_dev, c->stream);
         c->launches += 2;
     } else if (kind == K_BOUNDARY) {
         e = c->ops->special(main_kind, p, force, c->body(), c->stream);
         ++c->launches;
-        if (force) c->force_blocks = c->nblocks + special_blocks(c->n_special);
+        if (force) c->force_triples = partial_triples(c->nblocks, c->n_special);
     } else {
         e = c->ops->cells(kind, p, force, c->body(), c->grid, c->block, c->stream);
         ++c->launches;
-        if (force) c->force_blocks = c->nblocks;
+        if (force) c->force_triples = partial_triples(c->nblocks, 0);
     }
     if (c->profiling && e0 && e1) {
         cudaEventRecord(e1, c->stream);

@@ -101,7 +101,7 @@ struct Params {
     uint32_t n_special;
     float* scratch;        // open-face pre-gathered values (AA odd step)
     double* partial;       // per-block momentum-exchange partial sums, 3 per block
-    size_t part_special;   // first partial slot of the boundary kernels' blocks
+    size_t part_special;   // first partial slot (triple) of the boundary kernels' warps
     int nx, ny, nz;
     int open[3];           // axis has OPEN faces
     size_t N;
@@ -178,6 +178,29 @@ __device__ __forceinline__ void collide(float (&h)[19], const Params& p) {
             hn = fmaf(srho * wq(q), fmaf(9.0f * cu, cg, 3.0f * (cg - ug)), hn);
         }
         h[q] = hn;
+    }
+}
+
+// ---- momentum-exchange warp reduction ----------------------------------------------------------------
+// Every thread of the warp must call this (full-warp shuffles, no block barrier, so a warp that
+// is done leaves at once).  Lane 0 stores the warp's sum as one fp64 triple at slot
+// slot_base + (linear block index) * (warps per block) + (warp in block).
+constexpr int kWarpsPerBlock = 8;  // step kernels launch 256-thread blocks
+__device__ __forceinline__ void warp_force(float fx, float fy, float fz, double* partial,
+                                           size_t slot_base = 0) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        fx += __shfl_xor_sync(0xffffffffu, fx, o);
+        fy += __shfl_xor_sync(0xffffffffu, fy, o);
+        fz += __shfl_xor_sync(0xffffffffu, fz, o);
+    }
+    const int t = threadIdx.x + blockDim.x * threadIdx.y;
+    if ((t & 31) == 0) {
+        const size_t b = blockIdx.x + (size_t)gridDim.x * (blockIdx.y + (size_t)gridDim.y * blockIdx.z);
+        const size_t w = slot_base + b * kWarpsPerBlock + (size_t)(t >> 5);
+        partial[3 * w + 0] = (double)fx;
+        partial[3 * w + 1] = (double)fy;
+        partial[3 * w + 2] = (double)fz;
     }
 }
 

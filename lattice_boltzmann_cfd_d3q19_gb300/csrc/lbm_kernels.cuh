@@ -150,7 +150,7 @@ __global__ void __launch_bounds__(256) k_aa_even(Params p) {
             if (FORCE && !(fl & F_BULK)) mask_forces(p.mask[c.n], h, fx, fy, fz);
         }
     }
-    if (FORCE) block_force(fx, fy, fz, p.partial);
+    if (FORCE) warp_force(fx, fy, fz, p.partial);
 }
 
 // ============================== AA pattern, odd step ============================================
@@ -172,14 +172,18 @@ __device__ __forceinline__ void aa_odd_load(const Params& p, const Nbr& nb, uint
     if constexpr (Q < 18) aa_odd_load<L, I, Q + 1>(p, nb, n, m, h);
 }
 
-template <int L, typename I, int Q = 0>
+template <int L, typename I, bool FORCE, int Q = 0>
 __device__ __forceinline__ void aa_odd_store(const Params& p, const Nbr& nb, uint32_t n, uint32_t m,
-                                             const float (&h)[19]) {
-    // own slot (opp q, x) = pa[q] - pdiff[q] + n s; neighbour slot (q, x + c_q)
+                                             const float (&h)[19], float& fx, float& fy,
+                                             float& fz) {
+    // own slot (opp q, x) = pa[q] - pdiff[q] + n s; neighbour slot (q, x + c_q); a bounced link
+    // also carries its momentum-exchange term
+    const bool bounce = solid_link<Q>(m);
     const I own = cell_off<L, I>(Q, n) - (I)p.pdiff[Q];
     const I far = cell_off<L, I>(Q, nb.template at<Q, 1>(n));
-    p.pa[Q][solid_link<Q>(m) ? own : far] = h[Q];
-    if constexpr (Q < 18) aa_odd_store<L, I, Q + 1>(p, nb, n, m, h);
+    p.pa[Q][bounce ? own : far] = h[Q];
+    if (FORCE && Q > 0 && bounce) accumulate_force<Q>(h[Q], fx, fy, fz);
+    if constexpr (Q < 18) aa_odd_store<L, I, FORCE, Q + 1>(p, nb, n, m, h, fx, fy, fz);
 }
 
 template <int L, bool FORCE, bool BODY, typename I>
@@ -198,11 +202,10 @@ __global__ void __launch_bounds__(256) k_aa_odd(Params p) {
             // while the loads are in flight)
             uint32_t ns = c.n, ms = m;
             asm volatile("" : "+r"(ns), "+r"(ms) : "f"(h[0]), "f"(h[18]));
-            aa_odd_store<L, I>(p, nb, ns, ms, h);
-            if (FORCE && ms) mask_forces(ms, h, fx, fy, fz);
+            aa_odd_store<L, I, FORCE>(p, nb, ns, ms, h, fx, fy, fz);
         }
     }
-    if (FORCE) block_force(fx, fy, fz, p.partial);
+    if (FORCE) warp_force(fx, fy, fz, p.partial);
 }
 
 // Boundary kernel of the odd step: special cells (an INLET neighbour or a link across an OPEN
@@ -290,7 +293,7 @@ __global__ void __launch_bounds__(256) k_aa_odd_special(Params p) {
         aa_odd_scatter_all<L>(p, h, c.n, c.x, c.y, c.z);
         if (FORCE) mask_forces(p.mask[c.n], h, fx, fy, fz);
     }
-    if (FORCE) block_force(fx, fy, fz, p.partial, p.part_special);
+    if (FORCE) warp_force(fx, fy, fz, p.partial, p.part_special);
 }
 
 // Open-face pre-gather for the AA odd step: for every FLUID cell x on face layer (axis, side) and
@@ -371,7 +374,7 @@ __global__ void __launch_bounds__(256) k_ab(Params p) {
             if (FORCE && m) mask_forces(m, h, fx, fy, fz);
         }
     }
-    if (FORCE) block_force(fx, fy, fz, p.partial);
+    if (FORCE) warp_force(fx, fy, fz, p.partial);
 }
 
 template <int L, bool FORCE, bool BODY>
@@ -386,7 +389,7 @@ __global__ void __launch_bounds__(256) k_ab_special(Params p) {
         for (int q = 0; q < 19; ++q) p.B[idx<L>(q, c.n, p.N)] = h[q];
         if (FORCE) mask_forces(p.mask[c.n], h, fx, fy, fz);
     }
-    if (FORCE) block_force(fx, fy, fz, p.partial, p.part_special);
+    if (FORCE) warp_force(fx, fy, fz, p.partial, p.part_special);
 }
 
 // Streaming only: natural state into B from the post-collision state in A (second pass of the
