@@ -90,7 +90,8 @@ struct lbm_ctx {
     uint32_t* mask = nullptr;
     uint32_t* special = nullptr;  // sorted indices of the special FLUID cells
     uint32_t n_special = 0;
-    uint32_t* count_dev = nullptr;
+    uint32_t* count_dev = nullptr;  // 2 counters: special cells, cells with a SOLID link
+    int any_solid_link = 0;
     float* scratch = nullptr;
     size_t face_base[3][2] = {};
     double* partial = nullptr;    // nblocks main-kernel partials, then the boundary kernels'
@@ -118,6 +119,7 @@ struct lbm_ctx {
         p.B = B;
         p.flags = flags;
         p.mask = mask;
+        p.any_solid_link = any_solid_link;
         p.special = special;
         p.n_special = n_special;
         p.scratch = scratch;
@@ -224,14 +226,15 @@ size_t partial_triples(size_t main_blocks, uint32_t n_special) {
 // faces.  Synchronous.
 int classify(lbm_ctx* c) {
     Params p = c->params(nullptr, nullptr);
-    LBM_CUDA(cudaMemsetAsync(c->count_dev, 0, sizeof(uint32_t), c->stream), "classify");
+    LBM_CUDA(cudaMemsetAsync(c->count_dev, 0, 2 * sizeof(uint32_t), c->stream), "classify");
     LBM_CUDA(launch_classify(p, c->types, c->flags, c->mask, c->count_dev, c->grid, c->block,
                              c->stream), "classify flags");
     ++c->launches;
-    uint32_t count = 0;
-    LBM_CUDA(cudaMemcpyAsync(&count, c->count_dev, sizeof(uint32_t), cudaMemcpyDeviceToHost,
+    uint32_t counts[2] = {0, 0};
+    LBM_CUDA(cudaMemcpyAsync(counts, c->count_dev, 2 * sizeof(uint32_t), cudaMemcpyDeviceToHost,
                              c->stream), "classify");
     LBM_CUDA(cudaStreamSynchronize(c->stream), "classify");
+    const uint32_t count = counts[0];
     std::vector<uint32_t> list(count);
     uint32_t* dev_list = nullptr;
     if (count > 0) {
@@ -271,6 +274,7 @@ int classify(lbm_ctx* c) {
     cudaFree(c->special);
     c->special = dev_list;
     c->n_special = count;
+    c->any_solid_link = counts[1] > 0;
     return LBM_OK;
 }
 
@@ -431,7 +435,7 @@ lbm_ctx* lbm_create(int nx, int ny, int nz, float tau, int layout, int streaming
     if ((e = cudaMalloc(&c->types, N)) != cudaSuccess) return bad(e, "lbm_create: cell types");
     if ((e = cudaMalloc(&c->flags, N)) != cudaSuccess) return bad(e, "lbm_create: cell flags");
     if ((e = cudaMalloc(&c->mask, N * sizeof(uint32_t))) != cudaSuccess) return bad(e, "lbm_create: link masks");
-    if ((e = cudaMalloc(&c->count_dev, sizeof(uint32_t))) != cudaSuccess) return bad(e, "lbm_create: counter");
+    if ((e = cudaMalloc(&c->count_dev, 2 * sizeof(uint32_t))) != cudaSuccess) return bad(e, "lbm_create: counter");
     if ((e = cudaMalloc(&c->stage, 3 * kForceStage * sizeof(double))) != cudaSuccess)
         return bad(e, "lbm_create: force stage");
     if ((e = cudaMalloc(&c->force_dev, 3 * sizeof(double))) != cudaSuccess) return bad(e, "lbm_create: force");

@@ -13,6 +13,7 @@ __global__ void __launch_bounds__(256) k_validate_types(const uint8_t* types, si
 // Internal flags and solid-link masks.  For a FLUID cell: mask bit q when x + c_q (wrapped, or
 // clamped at an OPEN face) is SOLID; F_SPECIAL when some x + c_q is INLET or lies beyond an OPEN
 // face; F_BULK when no link rule applies at all.
+// count[0]: special cells; count[1]: FLUID cells with a SOLID link (not special)
 __global__ void __launch_bounds__(256) k_classify(Params p, const uint8_t* types, uint8_t* flags,
                                                   uint32_t* mask, uint32_t* count) {
     const int x = blockIdx.x * blockDim.x + threadIdx.x;
@@ -37,6 +38,7 @@ __global__ void __launch_bounds__(256) k_classify(Params p, const uint8_t* types
         } else if (m == 0) {
             out |= F_BULK;
         }
+        if (m != 0) atomicAdd(count + 1, 1u);
     }
     flags[n] = out;
     mask[n] = m;

@@ -96,7 +96,8 @@ struct Params {
     float* A;              // buffer read (AA: the only buffer; A-B: source)
     float* B;              // A-B destination (may equal A for the in-place collision)
     const uint8_t* flags;  // internal flag bytes
-    const uint32_t* mask;  // per-cell solid-link mask (read for non-bulk FLUID cells)
+    const uint32_t* mask;  // per-cell solid-link mask (0 for bulk cells)
+    int any_solid_link;    // some FLUID cell has a SOLID neighbour (else every mask is 0)
     const uint32_t* special;  // indices of the special FLUID cells
     uint32_t n_special;
     float* scratch;        // open-face pre-gathered values (AA odd step)

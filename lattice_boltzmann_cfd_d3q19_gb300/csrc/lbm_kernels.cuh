@@ -191,9 +191,10 @@ __global__ void __launch_bounds__(256) k_aa_odd(Params p) {
     CellCoord c;
     float fx = 0.f, fy = 0.f, fz = 0.f;
     if (grid_cell(p, c)) {
+        // the mask is loaded beside the flag byte, not after it (one round trip less)
+        const uint32_t m = p.any_solid_link ? p.mask[c.n] : 0u;
         const uint8_t fl = p.flags[c.n];
         if ((fl & (TYPE_MASK | F_SPECIAL)) == T_FLUID) {
-            const uint32_t m = (fl & F_BULK) ? 0u : p.mask[c.n];
             const Nbr nb(p, c.x, c.y, c.z);
             float h[19];
             aa_odd_load<L, I>(p, nb, c.n, m, h);
@@ -353,11 +354,12 @@ __global__ void __launch_bounds__(256) k_ab(Params p) {
     CellCoord c;
     float fx = 0.f, fy = 0.f, fz = 0.f;
     if (grid_cell(p, c)) {
+        // the natural-state collision needs the links only for the force; the mask is loaded
+        // beside the flag byte, not after it
+        const uint32_t m = (p.any_solid_link && (FORCE || !FROM_NATURAL)) ? p.mask[c.n] : 0u;
         const uint8_t fl = p.flags[c.n];
         const uint8_t want = FROM_NATURAL ? TYPE_MASK : (TYPE_MASK | F_SPECIAL);
         if ((fl & want) == T_FLUID) {
-            // the natural-state collision needs the links only for the force
-            const uint32_t m = ((fl & F_BULK) || (FROM_NATURAL && !FORCE)) ? 0u : p.mask[c.n];
             float h[19];
             if (FROM_NATURAL) {
 #pragma unroll
@@ -398,9 +400,9 @@ template <int L, typename I>
 __global__ void __launch_bounds__(256) k_stream(Params p) {
     CellCoord c;
     if (!grid_cell(p, c)) return;
+    const uint32_t m = p.any_solid_link ? p.mask[c.n] : 0u;
     const uint8_t fl = p.flags[c.n];
     if ((fl & (TYPE_MASK | F_SPECIAL)) != T_FLUID) return;
-    const uint32_t m = (fl & F_BULK) ? 0u : p.mask[c.n];
     const Nbr nb(p, c.x, c.y, c.z);
     float h[19];
     ab_load<L, I>(p, nb, c.n, m, h);
