@@ -357,3 +357,84 @@ def test_stream_profile_and_launch_counts():
         assert B.lbm_step_count(ctx) == 4
     finally:
         B.lbm_destroy(ctx)
+
+
+# ---- full-length runs: properties that hold at any size ------------------------------------------
+
+def gpu_moments(ctx, N, g):
+    """(mass, momentum[3]) of the natural state from lbm_macroscopic, summed in fp64:
+    j = rho (u - g/2) undoes the reported half-force shift."""
+    rho = torch.zeros(N, dtype=torch.float32, device="cuda")
+    u = torch.zeros(3 * N, dtype=torch.float32, device="cuda")
+    B.lbm_macroscopic(ctx, rho, u)
+    r = rho.double()
+    u = u.double().view(3, N)
+    j = [(r * (u[a] - 0.5 * g[a])).sum().item() for a in range(3)]
+    return r.sum().item(), np.array(j)
+
+
+@pytest.mark.slow
+def test_taylor_green_128_full_length_properties():
+    """1000 steps at 128^3: every scheme and layout agrees, mass and momentum are conserved."""
+    n = 128
+    rho, u = wl.taylor_green(n, n, n, 0.05)
+    case = Case(n, n, n, 0.6, oracle.equilibrium_field(rho, u))
+    ref = None
+    for layout in LAYOUTS:
+        for scheme in ("AA", "AB"):
+            ctx = case.gpu_context(layout, scheme)
+            try:
+                m0, j0 = gpu_moments(ctx, case.N, (0, 0, 0))
+                B.lbm_step(ctx, 1000)
+                m1, j1 = gpu_moments(ctx, case.N, (0, 0, 0))
+                f = torch.zeros(19 * case.N, dtype=torch.float32, device="cuda")
+                B.lbm_get_populations(ctx, f)
+            finally:
+                B.lbm_destroy(ctx)
+            assert abs(m1 / m0 - 1) < 1e-6
+            assert np.abs(j1 - j0).max() < 1e-6 * m0
+            if ref is None:
+                ref = f
+            else:
+                assert (f - ref).abs().max().item() <= 1e-6, (layout, scheme)
+
+
+@pytest.mark.slow
+def test_sphere_128_full_length_aa_equals_ab():
+    case = sphere_case(128, 128, 128, (40, 64, 64), 16)
+    fa, Fa = case.run_gpu(2000, "stream", "AA", want_force=True)
+    fb, Fb = case.run_gpu(2000, "stream", "AB", want_force=True)
+    assert max_fluid_diff(case, fa, fb) <= 1e-6
+    assert np.abs(Fa - Fb).max() <= 1e-5 * abs(Fa[0])
+
+
+@pytest.mark.slow
+def test_porous_512_conservation_and_momentum_balance():
+    """The benchmark configuration (porous 512^3, AA, stream layout, Guo g = 1e-6, tau 0.7):
+    bounce-back conserves mass exactly, and over every step the fluid momentum grows by the body
+    force minus the momentum handed to the solids (the momentum-exchange force of that step)."""
+    n, g = 512, (1e-6, 0.0, 0.0)
+    N = n ** 3
+    flags = wl.porous_flags(n, n, n, 0.30, 3, seed=wl.SEED_POROUS512)
+    ctx = B.lbm_create(n, n, n, 0.7, B.LAYOUT_STREAM, B.STREAMING_AA)
+    try:
+        B.lbm_set_flags(ctx, flags)
+        B.lbm_set_body_force(ctx, *g)
+        rho = torch.ones(N, dtype=torch.float32, device="cuda")
+        u = torch.zeros(3 * N, dtype=torch.float32, device="cuda")
+        B.lbm_set_equilibrium(ctx, rho, u)
+        B.lbm_step(ctx, 20)
+        m_prev, j_prev = gpu_moments(ctx, N, g)
+        for _ in range(3):
+            B.lbm_step(ctx, 1)
+            F = B.lbm_force_momentum_exchange(ctx)
+            m, j = gpu_moments(ctx, N, g)
+            body = m_prev * g[0]
+            assert abs(m / m_prev - 1) < 1e-6
+            assert abs((j[0] - j_prev[0]) - (body - F[0])) <= 1e-3 * body
+            assert abs((j[1] - j_prev[1]) + F[1]) <= 1e-3 * body
+            assert abs((j[2] - j_prev[2]) + F[2]) <= 1e-3 * body
+            m_prev, j_prev = m, j
+        assert B.lbm_check_finite(ctx)
+    finally:
+        B.lbm_destroy(ctx)
