@@ -66,6 +66,24 @@ constexpr size_t kStagingFloats = size_t(32) << 20;  // 128 MiB host-transfer st
 
 }  // namespace
 
+// Launch constants of the Guo forcing as the collision applies it (see collide() in
+// lbm_device.cuh): the equilibrium velocity shift tau g and, per population,
+// -omega (tau - 1/2)^2 w_q (4.5 (c_q.g)^2 - 1.5 g.g); computed in double, rounded once.
+void lbm::guo_constants(float tau, const float g[3], float tau_g[3], float wk[19]) {
+    const double t = tau, om = 1.0 / t, a = t - 0.5;
+    const double gg = (double)g[0] * g[0] + (double)g[1] * g[1] + (double)g[2] * g[2];
+    for (int k = 0; k < 3; ++k) tau_g[k] = (float)(t * g[k]);
+    for (int q = 0; q < 19; ++q) {
+        const double cg = cx(q) * (double)g[0] + cy(q) * (double)g[1] + cz(q) * (double)g[2];
+        const double w = q == 0 ? 1.0 / 3.0 : q <= 6 ? 1.0 / 18.0 : 1.0 / 36.0;
+        wk[q] = (float)(-om * a * a * w * (4.5 * cg * cg - 1.5 * gg));
+    }
+}
+
+namespace {
+
+}  // namespace
+
 void lbm::set_last_error_v(const char* fmt, va_list ap) {
     char buf[512];
     vsnprintf(buf, sizeof buf, fmt, ap);
@@ -134,6 +152,7 @@ struct lbm_ctx {
             for (int s = 0; s < 2; ++s) p.face_base[a][s] = face_base[a][s];
         p.omega = omega;
         for (int a = 0; a < 3; ++a) p.g[a] = g[a];
+        guo_constants(tau, g, p.tau_g, p.wk);
         for (int q = 0; q < 19; ++q) p.heq_in[q] = heq_in[q];
         for (int q = 0; q < 19; ++q) {
             const size_t off = plane_offset(q), off_opp = plane_offset(opp(q));

@@ -109,6 +109,8 @@ struct Params {
     size_t face_base[3][2];  // scratch offset of face (axis, side); 19 * area values each
     float omega;
     float g[3];
+    float tau_g[3];        // tau g: equilibrium velocity shift of the Guo forcing
+    float wk[19];          // -omega (tau - 1/2)^2 w_q (4.5 (c_q.g)^2 - 1.5 g.g)
     float heq_in[19];      // shifted inlet state f_eq(rho_in, u_in) - w
     // hot-path addressing: population q of cell n is pa[q][n * cell_stride(q)] in A and
     // pb[q][n * cell_stride(q)] in B; pdiff[q] = pa[q] - pa[opposite(q)] in elements
@@ -149,15 +151,15 @@ __device__ __forceinline__ void collide(float (&h)[19], const Params& p) {
     const float rho = 1.0f + drho;
     const float inv = 1.0f / rho;
     float ux = jx * inv, uy = jy * inv, uz = jz * inv;
-    // Guo forcing with F = rho g: the source is (1 - omega/2) rho w [3 (c.g - u.g) + 9 (c.u)(c.g)];
-    // g stays a launch parameter (warp-uniform), so only u.g and (1 - omega/2) rho are per cell
-    float ug = 0.f, srho = 0.f;
+    // Guo forcing, F = rho g, u = j/rho + g/2, source S_q = (1 - omega/2) d f_eq,q/du . g.
+    // Because f_eq is quadratic in u, omega f_eq(u) + (1 - omega/2) d f_eq/du . g equals
+    // omega f_eq(u + a g) - omega a^2 w rho (4.5 (c.g)^2 - 1.5 g.g) with a = tau - 1/2 exactly:
+    // relax toward the equilibrium at j/rho + tau g and add rho wk_q, wk_q = -omega a^2 w_q
+    // (4.5 (c_q.g)^2 - 1.5 g.g) (launch constants).
     if (BODY) {
-        ux = fmaf(0.5f, p.g[0], ux);
-        uy = fmaf(0.5f, p.g[1], uy);
-        uz = fmaf(0.5f, p.g[2], uz);
-        ug = ux * p.g[0] + uy * p.g[1] + uz * p.g[2];
-        srho = (1.0f - 0.5f * p.omega) * rho;
+        ux += p.tau_g[0];
+        uy += p.tau_g[1];
+        uz += p.tau_g[2];
     }
     const float uu15 = 1.5f * (ux * ux + uy * uy + uz * uz);
     const float om = p.omega;
@@ -171,13 +173,7 @@ __device__ __forceinline__ void collide(float (&h)[19], const Params& p) {
         const float poly = fmaf(cu, fmaf(4.5f, cu, 3.0f), -uu15);
         const float heq = wq(q) * fmaf(rho, poly, drho);
         float hn = fmaf(-om, h[q] - heq, h[q]);
-        if (BODY) {
-            float cg = 0.f;
-            if (cx(q) > 0) cg += p.g[0]; else if (cx(q) < 0) cg -= p.g[0];
-            if (cy(q) > 0) cg += p.g[1]; else if (cy(q) < 0) cg -= p.g[1];
-            if (cz(q) > 0) cg += p.g[2]; else if (cz(q) < 0) cg -= p.g[2];
-            hn = fmaf(srho * wq(q), fmaf(9.0f * cu, cg, 3.0f * (cg - ug)), hn);
-        }
+        if (BODY) hn = fmaf(rho, p.wk[q], hn);
         h[q] = hn;
     }
 }

@@ -58,6 +58,9 @@ constexpr unsigned kForceStage = 256;
 cudaError_t launch_force_finalize(const double* partial, size_t nblocks, double* stage,
                                   double* out, cudaStream_t s);
 
+// Launch constants of the Guo forcing for relaxation time tau and body acceleration g.
+void guo_constants(float tau, const float g[3], float tau_g[3], float wk[19]);
+
 // Sets the calling thread's lbm_last_error() message (printf-style).
 void set_last_error_v(const char* fmt, va_list ap);
 

@@ -152,6 +152,7 @@ extern "C" int lbm_force_momentum_exchange_noalloc(const float* f, const uint8_t
     p.g[0] = gx;
     p.g[1] = gy;
     p.g[2] = gz;
+    guo_constants(tau, p.g, p.tau_g, p.wk);
     const bool body = gx != 0.f || gy != 0.f || gz != 0.f;
     const unsigned blocks = (unsigned)((N + kThreads - 1) / kThreads);
 
