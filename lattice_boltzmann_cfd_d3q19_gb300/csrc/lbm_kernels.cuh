@@ -374,6 +374,11 @@ __global__ void __launch_bounds__(256) k_ab(Params p) {
 #pragma unroll
             for (int q = 0; q < 19; ++q) p.pb[q][cell_off<L, I>(q, ns)] = h[q];
             if (FORCE && m) mask_forces(m, h, fx, fy, fz);
+        } else if ((fl & TYPE_MASK) != T_FLUID && p.pb[0] != p.pa[0]) {
+            // SOLID and INLET slots are never read; writing them keeps every 32-byte sector of
+            // the destination fully written (no fill from DRAM for partly written sectors)
+#pragma unroll
+            for (int q = 0; q < 19; ++q) p.pb[q][cell_off<L, I>(q, c.n)] = 0.0f;
         }
     }
     if (FORCE) warp_force(fx, fy, fz, p.partial);
@@ -402,7 +407,13 @@ __global__ void __launch_bounds__(256) k_stream(Params p) {
     if (!grid_cell(p, c)) return;
     const uint32_t m = p.any_solid_link ? p.mask[c.n] : 0u;
     const uint8_t fl = p.flags[c.n];
-    if ((fl & (TYPE_MASK | F_SPECIAL)) != T_FLUID) return;
+    if ((fl & TYPE_MASK) != T_FLUID) {
+        // never-read SOLID / INLET slots written to keep the destination's sectors whole
+#pragma unroll
+        for (int q = 0; q < 19; ++q) p.pb[q][cell_off<L, I>(q, c.n)] = 0.0f;
+        return;
+    }
+    if (fl & F_SPECIAL) return;
     const Nbr nb(p, c.x, c.y, c.z);
     float h[19];
     ab_load<L, I>(p, nb, c.n, m, h);

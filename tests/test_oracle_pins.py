@@ -119,6 +119,24 @@ def test_guo_source_moments():
     assert np.abs(c.T @ post - (c.T @ f + rho * g)).max() < 1e-15
 
 
+def test_guo_equals_shifted_velocity_relaxation_plus_constant():
+    """The forcing identity the GPU collision uses: with a quadratic equilibrium, the literal Guo
+    collision equals BGK relaxation toward f_eq(j/rho + tau g) plus
+    -omega (tau - 1/2)^2 w rho (4.5 (c.g)^2 - 1.5 g.g) per population."""
+    c, _, w, _ = frac_weights()
+    r = np.random.default_rng(12)
+    for tau in (0.55, 0.7, 1.3):
+        om, a = 1 / tau, tau - 0.5
+        g = r.uniform(-1e-3, 1e-3, 3)
+        f = oracle.equilibrium(1.03, [0.02, -0.01, 0.03]) + r.normal(size=19) * 1e-4
+        rho = f.sum()
+        j = c.T.astype(float) @ f
+        feq = oracle.equilibrium(rho, j / rho + tau * g)
+        cg = c.astype(float) @ g
+        alt = f - om * (f - feq) - om * a * a * w * rho * (4.5 * cg ** 2 - 1.5 * g @ g)
+        assert np.abs(alt - oracle.collide(f, tau, g)).max() < 1e-15
+
+
 # ---- whole-lattice invariants ----------------------------------------------------------------
 
 def random_state(N, seed, amp=1e-2):
