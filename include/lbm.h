@@ -135,8 +135,15 @@ int lbm_get_populations(lbm_ctx* ctx, float* f);
 /* Enqueue n >= 0 time steps ([PortLBM] Eq. 1 with the per-link rules above) on the context
  * stream.  The last of the n steps also computes the momentum-exchange force of its
  * post-collision state (read with lbm_force_momentum_exchange).  Asynchronous; n = 0 is a no-op
- * that leaves the last force unchanged. */
+ * that leaves the last force unchanged.  With graph launch on (the default) the steps are
+ * replayed from CUDA graphs of up to 32 steps, captured on a private stream on first use and
+ * cached per (length, buffer state); the setters of flags, faces, inlet and body force drop the
+ * cache.  Results are identical with graph launch on or off. */
 int lbm_step(lbm_ctx* ctx, int n);
+
+/* Turn graph replay of lbm_step on (enable != 0, the default) or off (one launch per kernel).
+ * While per-kernel profiling is enabled, steps are always launched one by one. */
+int lbm_set_graph_launch(lbm_ctx* ctx, int enable);
 
 /* Density and velocity of the natural state: rho[N], u[3*N] (fp32).  FLUID: rho = sum f,
  * u = j/rho + g/2 (Guo's half-force shift).  SOLID: 0, 0.  INLET: rho_in, u_in.  Synchronous. */

@@ -37,6 +37,7 @@ SIGNATURES = {
     "lbm_set_equilibrium": (_I, [_P, _P, _P]),
     "lbm_get_populations": (_I, [_P, _P]),
     "lbm_step": (_I, [_P, _I]),
+    "lbm_set_graph_launch": (_I, [_P, _I]),
     "lbm_macroscopic": (_I, [_P, _P, _P]),
     "lbm_force_momentum_exchange": (_I, [_P, _P]),
     "lbm_check_finite": (_I, [_P]),
@@ -166,6 +167,10 @@ def lbm_get_populations(ctx: int, f) -> None:
 
 def lbm_step(ctx: int, n: int) -> None:
     _check(load().lbm_step(ctx, int(n)))
+
+
+def lbm_set_graph_launch(ctx: int, enable: bool) -> None:
+    _check(load().lbm_set_graph_launch(ctx, 1 if enable else 0))
 
 
 def lbm_macroscopic(ctx: int, rho, u) -> None:

@@ -128,6 +128,19 @@ struct lbm_ctx {
     int64_t launches = 0;
     dim3 grid, block;
     bool profiling = false;
+    // CUDA graphs of step sequences, captured on a private stream and launched on `stream`
+    struct GraphEntry {
+        int len, state, cur, force;
+        cudaGraphExec_t exec;
+        int64_t kernels;  // kernel launches one replay performs
+    };
+    bool use_graphs = true;
+    cudaStream_t capture_stream = nullptr;
+    std::vector<GraphEntry> graphs;
+    void drop_graphs() {
+        for (auto& g : graphs) cudaGraphExecDestroy(g.exec);
+        graphs.clear();
+    }
     std::vector<std::pair<cudaEvent_t, cudaEvent_t>> prof[K_NUM_KINDS];
     std::vector<cudaEvent_t> event_pool;
 
@@ -197,6 +210,8 @@ struct lbm_ctx {
     }
     void free_all() {
         if (stream) cudaStreamSynchronize(stream);
+        drop_graphs();
+        if (capture_stream) cudaStreamDestroy(capture_stream);
         release_profile();
         for (cudaEvent_t e : event_pool) cudaEventDestroy(e);
         event_pool.clear();
@@ -377,6 +392,75 @@ int sync(lbm_ctx* c, const char* what) {
     return LBM_OK;
 }
 
+// Steps per graph: even, so a chunk returns the AA parity and the A-B buffer index to where it
+// started and one captured graph serves every chunk of a long run.
+constexpr int kGraphChunk = 32;
+
+// Capture `len` steps (the last one with the force when `force`) from the context's current
+// state into an executable graph.  The context's state is left as it was.
+int capture_steps(lbm_ctx* c, int len, bool force, lbm_ctx::GraphEntry* out) {
+    if (!c->capture_stream)
+        LBM_CUDA(cudaStreamCreateWithFlags(&c->capture_stream, cudaStreamNonBlocking),
+                 "lbm_step: capture stream");
+    const int state = c->state, cur = c->cur;
+    const size_t triples = c->force_triples;
+    const int64_t launches = c->launches;
+    cudaStream_t user = c->stream;
+    c->stream = c->capture_stream;
+    cudaGraph_t graph = nullptr;
+    int rc = LBM_OK;
+    cudaError_t e = cudaStreamBeginCapture(c->stream, cudaStreamCaptureModeThreadLocal);
+    if (e == cudaSuccess) {
+        for (int i = 0; i < len && rc == LBM_OK; ++i) rc = step_once(c, force && i == len - 1);
+        cudaError_t e2 = cudaStreamEndCapture(c->stream, &graph);
+        if (rc == LBM_OK && e2 != cudaSuccess) rc = cuda_fail(e2, "lbm_step: end capture");
+    } else {
+        rc = cuda_fail(e, "lbm_step: begin capture");
+    }
+    c->stream = user;
+    out->len = len;
+    out->state = state;
+    out->cur = cur;
+    out->force = force;
+    out->kernels = c->launches - launches;
+    const size_t force_triples = c->force_triples;
+    c->state = state;
+    c->cur = cur;
+    c->force_triples = force ? force_triples : triples;
+    c->launches = launches;
+    if (rc == LBM_OK) {
+        e = cudaGraphInstantiate(&out->exec, graph, 0);
+        if (e != cudaSuccess) rc = cuda_fail(e, "lbm_step: instantiate");
+    }
+    if (graph) cudaGraphDestroy(graph);
+    return rc;
+}
+
+// Replays `len` steps through a cached graph (captured on first use), then advances the state
+// the way the steps do.
+int graph_steps(lbm_ctx* c, int len, bool force) {
+    lbm_ctx::GraphEntry* g = nullptr;
+    for (auto& ge : c->graphs)
+        if (ge.len == len && ge.state == c->state && ge.cur == c->cur && ge.force == (int)force)
+            g = &ge;
+    if (!g) {
+        lbm_ctx::GraphEntry ne{};
+        if (int rc = capture_steps(c, len, force, &ne)) return rc;
+        c->graphs.push_back(ne);
+        g = &c->graphs.back();
+    }
+    LBM_CUDA(cudaGraphLaunch(g->exec, c->stream), "lbm_step: graph launch");
+    c->launches += g->kernels;
+    // state after `len` steps
+    if (c->streaming == LBM_STREAMING_AA) {
+        if (len & 1) c->state = c->state == ST_NATURAL ? ST_POST_AA : ST_NATURAL;
+    } else {
+        if (len & 1) c->cur ^= 1;
+        if (c->streaming == LBM_STREAMING_AB) c->state = ST_POST_AB;
+    }
+    return LBM_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -498,6 +582,7 @@ int lbm_set_flags(lbm_ctx* c, const uint8_t* flags) {
         rc = fail(LBM_EINVAL, "lbm_set_flags: flag values must be 0 (FLUID), 1 (SOLID) or 2 (INLET)");
     } else {
         ++c->launches;
+        c->drop_graphs();
         e = cudaMemcpyAsync(c->types, tmp, c->N, cudaMemcpyDeviceToDevice, c->stream);
         if (e != cudaSuccess) rc = cuda_fail(e, "lbm_set_flags");
         if (rc == LBM_OK) rc = classify(c);
@@ -531,6 +616,7 @@ int lbm_set_faces(lbm_ctx* c, int fx, int fy, int fz) {
         cudaFree(scratch);
         return rc;
     }
+    c->drop_graphs();
     cudaFree(c->scratch);
     c->scratch = scratch;
     for (int a = 0; a < 3; ++a) {
@@ -546,6 +632,7 @@ int lbm_set_inlet(lbm_ctx* c, float rho, float ux, float uy, float uz) {
     if (!std::isfinite(rho) || !(rho > 0.f) || !std::isfinite(ux) || !std::isfinite(uy) ||
         !std::isfinite(uz))
         return fail(LBM_EINVAL, "lbm_set_inlet: need finite rho > 0 and finite u");
+    c->drop_graphs();
     c->inlet[0] = rho;
     c->inlet[1] = ux;
     c->inlet[2] = uy;
@@ -559,6 +646,7 @@ int lbm_set_body_force(lbm_ctx* c, float gx, float gy, float gz) {
     if (!c) return fail(LBM_EINVAL, "lbm_set_body_force: NULL context");
     if (!std::isfinite(gx) || !std::isfinite(gy) || !std::isfinite(gz))
         return fail(LBM_EINVAL, "lbm_set_body_force: g must be finite");
+    c->drop_graphs();
     c->g[0] = gx;
     c->g[1] = gy;
     c->g[2] = gz;
@@ -645,8 +733,16 @@ int lbm_get_populations(lbm_ctx* c, float* f) {
 int lbm_step(lbm_ctx* c, int n) {
     if (!c) return fail(LBM_EINVAL, "lbm_step: NULL context");
     if (n < 0) return fail(LBM_EINVAL, "lbm_step: n = %d < 0", n);
-    for (int i = 0; i < n; ++i)
-        if (int rc = step_once(c, i == n - 1)) return rc;
+    if (c->use_graphs && !c->profiling) {
+        for (int done = 0; done < n;) {
+            const int len = n - done > kGraphChunk ? kGraphChunk : n - done;
+            if (int rc = graph_steps(c, len, done + len == n)) return rc;
+            done += len;
+        }
+    } else {
+        for (int i = 0; i < n; ++i)
+            if (int rc = step_once(c, i == n - 1)) return rc;
+    }
     if (n > 0) {
         c->steps += n;
         c->force_valid = true;
@@ -730,6 +826,12 @@ int lbm_profile_read(lbm_ctx* c, int kind, int64_t* launches, double* total_ms) 
     }
     *launches = (int64_t)c->prof[kind].size();
     *total_ms = ms;
+    return LBM_OK;
+}
+
+int lbm_set_graph_launch(lbm_ctx* c, int enable) {
+    if (!c) return fail(LBM_EINVAL, "lbm_set_graph_launch: NULL context");
+    c->use_graphs = enable != 0;
     return LBM_OK;
 }
 

@@ -438,3 +438,34 @@ def test_porous_512_conservation_and_momentum_balance():
         assert B.lbm_check_finite(ctx)
     finally:
         B.lbm_destroy(ctx)
+
+
+# ---- graph replay --------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("scheme", ["AA", "AB", "AB2"])
+def test_graph_replay_equals_direct_launches(scheme):
+    """lbm_step replays captured CUDA graphs in chunks; the result must equal one-by-one
+    launches bit for bit, for step counts below, at and across the chunk length, and across
+    a change of body force (which drops the cached graphs)."""
+    case = mixed_case(23, 12, 9, (1, 0, 0), 61)
+    out = []
+    for graphs in (True, False):
+        ctx = case.gpu_context("stream", scheme)
+        try:
+            B.lbm_set_graph_launch(ctx, graphs)
+            res = []
+            for n in (1, 2, 5, 32, 33, 70):
+                B.lbm_step(ctx, n)
+                res.append(B.lbm_force_momentum_exchange(ctx))
+            B.lbm_set_body_force(ctx, -3e-5, 1e-5, 0.0)
+            B.lbm_step(ctx, 9)
+            res.append(B.lbm_force_momentum_exchange(ctx))
+            f = np.zeros((19, case.N), np.float32)
+            B.lbm_get_populations(ctx, f)
+            assert B.lbm_step_count(ctx) == 1 + 2 + 5 + 32 + 33 + 70 + 9
+        finally:
+            B.lbm_destroy(ctx)
+        out.append((f, res))
+    assert np.array_equal(out[0][0], out[1][0])
+    for a, b in zip(out[0][1], out[1][1]):
+        assert np.array_equal(a, b)
