@@ -172,6 +172,7 @@ struct lbm_ctx {
             p.pa[q] = A ? A + off : nullptr;
             p.pb[q] = B ? B + off : nullptr;
             p.pdiff[q] = (long long)off - (long long)off_opp;
+            p.plane32[q] = (uint32_t)off;  // used only while 19 N <= 2^32
         }
         return p;
     }

@@ -117,6 +117,9 @@ struct Params {
     float* pa[19];
     float* pb[19];
     long long pdiff[19];
+    // compact addressing while every element offset fits in 32 bits (19 N <= 2^32): population q
+    // of cell n is A[plane32[q] + n * cell_stride(q)] (one base, one 32-bit offset per access)
+    uint32_t plane32[19];
 };
 
 // ---- per-link geometry ----------------------------------------------------------------------------

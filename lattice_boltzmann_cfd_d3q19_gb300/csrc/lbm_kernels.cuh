@@ -11,6 +11,8 @@
 // opposite(q) (halfway bounce-back, PortLBM §3.1), INLET s supplies f_eq(rho_in, u_in).
 #pragma once
 
+#include <type_traits>
+
 #include "lbm_device.cuh"
 
 namespace lbm {
@@ -162,13 +164,22 @@ __global__ void __launch_bounds__(256) k_aa_even(Params p) {
 // Main kernel: FLUID cells that are not special.  The solid-link mask selects, per population,
 // between the neighbour's slot and the cell's own mirrored slot, so bulk and near-wall cells run
 // the same branch-free code.
+// I = uint32_t: one base and 32-bit element offsets (fewer instructions per access); otherwise
+// per-population plane pointers with 64-bit offsets.
 template <int L, typename I, int Q = 0>
 __device__ __forceinline__ void aa_odd_load(const Params& p, const Nbr& nb, uint32_t n, uint32_t m,
                                             float (&h)[19]) {
-    // own slot (q, x) = pa[opp q] + pdiff[q] + n s; neighbour slot (opp q, x - c_q)
-    const I own = (I)p.pdiff[Q] + cell_off<L, I>(Q, n);
-    const I far = cell_off<L, I>(Q, nb.template at<Q, -1>(n));
-    h[Q] = p.pa[opp(Q)][solid_link<opp(Q)>(m) ? own : far];
+    constexpr uint32_t S = cell_stride<L>(Q);
+    if constexpr (std::is_same<I, uint32_t>::value) {
+        // own slot (q, x); neighbour slot (opp q, x - c_q)
+        const uint32_t own = p.plane32[Q] + n * S;
+        const uint32_t far = p.plane32[opp(Q)] + nb.template at<Q, -1>(n) * S;
+        h[Q] = p.A[solid_link<opp(Q)>(m) ? own : far];
+    } else {
+        const I own = (I)p.pdiff[Q] + cell_off<L, I>(Q, n);
+        const I far = cell_off<L, I>(Q, nb.template at<Q, -1>(n));
+        h[Q] = p.pa[opp(Q)][solid_link<opp(Q)>(m) ? own : far];
+    }
     if constexpr (Q < 18) aa_odd_load<L, I, Q + 1>(p, nb, n, m, h);
 }
 
@@ -176,12 +187,19 @@ template <int L, typename I, bool FORCE, int Q = 0>
 __device__ __forceinline__ void aa_odd_store(const Params& p, const Nbr& nb, uint32_t n, uint32_t m,
                                              const float (&h)[19], float& fx, float& fy,
                                              float& fz) {
-    // own slot (opp q, x) = pa[q] - pdiff[q] + n s; neighbour slot (q, x + c_q); a bounced link
-    // also carries its momentum-exchange term
+    // own slot (opp q, x); neighbour slot (q, x + c_q); a bounced link also carries its
+    // momentum-exchange term
+    constexpr uint32_t S = cell_stride<L>(Q);
     const bool bounce = solid_link<Q>(m);
-    const I own = cell_off<L, I>(Q, n) - (I)p.pdiff[Q];
-    const I far = cell_off<L, I>(Q, nb.template at<Q, 1>(n));
-    p.pa[Q][bounce ? own : far] = h[Q];
+    if constexpr (std::is_same<I, uint32_t>::value) {
+        const uint32_t own = p.plane32[opp(Q)] + n * S;
+        const uint32_t far = p.plane32[Q] + nb.template at<Q, 1>(n) * S;
+        p.A[bounce ? own : far] = h[Q];
+    } else {
+        const I own = cell_off<L, I>(Q, n) - (I)p.pdiff[Q];
+        const I far = cell_off<L, I>(Q, nb.template at<Q, 1>(n));
+        p.pa[Q][bounce ? own : far] = h[Q];
+    }
     if (FORCE && Q > 0 && bounce) accumulate_force<Q>(h[Q], fx, fy, fz);
     if constexpr (Q < 18) aa_odd_store<L, I, FORCE, Q + 1>(p, nb, n, m, h, fx, fy, fz);
 }
@@ -327,10 +345,17 @@ __global__ void __launch_bounds__(256) k_pregather(Params p, int axis, int side)
 template <int L, typename I, int Q = 0>
 __device__ __forceinline__ void ab_load(const Params& p, const Nbr& nb, uint32_t n, uint32_t m,
                                         float (&h)[19]) {
-    // own slot (opp q, x) = pa[q] - pdiff[q] + n s; neighbour slot (q, x - c_q)
-    const I own = cell_off<L, I>(Q, n) - (I)p.pdiff[Q];
-    const I far = cell_off<L, I>(Q, nb.template at<Q, -1>(n));
-    h[Q] = p.pa[Q][solid_link<opp(Q)>(m) ? own : far];
+    // own slot (opp q, x); neighbour slot (q, x - c_q)
+    constexpr uint32_t S = cell_stride<L>(Q);
+    if constexpr (std::is_same<I, uint32_t>::value) {
+        const uint32_t own = p.plane32[opp(Q)] + n * S;
+        const uint32_t far = p.plane32[Q] + nb.template at<Q, -1>(n) * S;
+        h[Q] = p.A[solid_link<opp(Q)>(m) ? own : far];
+    } else {
+        const I own = cell_off<L, I>(Q, n) - (I)p.pdiff[Q];
+        const I far = cell_off<L, I>(Q, nb.template at<Q, -1>(n));
+        h[Q] = p.pa[Q][solid_link<opp(Q)>(m) ? own : far];
+    }
     if constexpr (Q < 18) ab_load<L, I, Q + 1>(p, nb, n, m, h);
 }
 

@@ -23,7 +23,11 @@ void launch_main(int kind, const Params& p, dim3 grid, dim3 block, cudaStream_t 
 // than 32-bit offsets in the odd kernel, whose registers they keep lower).
 template <bool F, bool B>
 void launch_main_offsets(int kind, const Params& p, dim3 grid, dim3 block, cudaStream_t s) {
-    launch_main<F, B, long long>(kind, p, grid, block, s);
+    // the even kernel keeps plane pointers (it already streams at the copy bandwidth); the
+    // neighbour-addressing kernels take one base with 32-bit offsets whenever all 19 N fit
+    const bool compact = 19 * p.N <= (size_t(1) << 32) && kind != K_AA_EVEN;
+    if (compact) launch_main<F, B, uint32_t>(kind, p, grid, block, s);
+    else launch_main<F, B, long long>(kind, p, grid, block, s);
 }
 
 cudaError_t cells(int kind, const Params& p, bool force, bool body, dim3 grid, dim3 block,
@@ -41,7 +45,10 @@ cudaError_t cells(int kind, const Params& p, bool force, bool body, dim3 grid, d
                 else launch_main_offsets<false, false>(kind, p, grid, block, s);
             }
             break;
-        case K_STREAM: k_stream<L, long long><<<grid, block, 0, s>>>(p); break;
+        case K_STREAM:
+            if (19 * p.N <= (size_t(1) << 32)) k_stream<L, uint32_t><<<grid, block, 0, s>>>(p);
+            else k_stream<L, long long><<<grid, block, 0, s>>>(p);
+            break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
