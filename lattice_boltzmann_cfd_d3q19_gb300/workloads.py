@@ -20,7 +20,7 @@ import math
 
 import numpy as np
 
-FLUID, SOLID, INLET = 0, 1, 2
+FLUID, SOLID, INLET, MOVING_WALL = 0, 1, 2, 3
 
 # seed of each named workload: 1000 + its position in the list of workloads
 SEED_TG32 = 1001

@@ -17,7 +17,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "d3q19_oracle.cpp")
 _LIB = os.path.join(_HERE, "liboracle.so")
 
-FLUID, SOLID, INLET = 0, 1, 2
+FLUID, SOLID, INLET, MOVING_WALL = 0, 1, 2, 3
 PERIODIC, OPEN = 0, 1
 
 _lib = None
@@ -45,13 +45,13 @@ def _load():
         lib.oracle_equilibrium.argtypes = [d, P, P]
         lib.oracle_collide.argtypes = [P, d, P, P]
         lib.oracle_equilibrium_field.argtypes = [i64, P, P, P]
-        lib.oracle_step_ab.argtypes = [i, i, i, d, P, P, P, P, P, i, P, i]
+        lib.oracle_step_ab.argtypes = [i, i, i, d, P, P, P, P, P, P, i, P, i]
         lib.oracle_step_ab.restype = i
-        lib.oracle_step_aa.argtypes = [i, i, i, d, P, P, P, P, P, i, i, P, i]
+        lib.oracle_step_aa.argtypes = [i, i, i, d, P, P, P, P, P, P, i, i, P, i]
         lib.oracle_step_aa.restype = i
-        lib.oracle_aa_natural.argtypes = [i, i, i, P, P, P, P, P]
+        lib.oracle_aa_natural.argtypes = [i, i, i, P, P, P, P, P, P]
         lib.oracle_aa_natural.restype = i
-        lib.oracle_macroscopic.argtypes = [i, i, i, P, P, P, P, P, P]
+        lib.oracle_macroscopic.argtypes = [i, i, i, P, P, P, P, P, P, P]
         lib.oracle_macroscopic.restype = i
         lib.oracle_max_threads.restype = i
         _lib = lib
@@ -104,10 +104,11 @@ def equilibrium_field(rho, u) -> np.ndarray:
 
 
 class Problem:
-    """Grid, relaxation time, flags, faces, inlet state and body acceleration."""
+    """Grid, relaxation time, flags, faces, inlet state, body acceleration, wall velocity."""
 
     def __init__(self, nx, ny, nz, tau, flags=None, faces=(PERIODIC, PERIODIC, PERIODIC),
-                 inlet=(1.0, 0.0, 0.0, 0.0), g=(0.0, 0.0, 0.0), threads=0):
+                 inlet=(1.0, 0.0, 0.0, 0.0), g=(0.0, 0.0, 0.0), threads=0,
+                 wall=(0.0, 0.0, 0.0)):
         self.nx, self.ny, self.nz = int(nx), int(ny), int(nz)
         self.N = self.nx * self.ny * self.nz
         self.tau = float(tau)
@@ -118,11 +119,12 @@ class Problem:
         self.faces = np.ascontiguousarray(faces, dtype=np.int32).reshape(3)
         self.inlet = _f64(inlet, (4,))
         self.g = _f64(g, (3,))
+        self.wall = _f64(wall, (3,))
         self.threads = int(threads)
 
     def _args(self):
         return (self.nx, self.ny, self.nz, self.tau, _ptr(self.flags), _ptr(self.faces),
-                _ptr(self.inlet), _ptr(self.g))
+                _ptr(self.inlet), _ptr(self.g), _ptr(self.wall))
 
     def step_ab(self, f, nsteps: int, want_force: bool = False):
         """Two-lattice steps on a copy of natural f[19, N]; returns (f_new, force or None)."""
@@ -148,7 +150,8 @@ class Problem:
         A = _f64(A).reshape(19, self.N)
         f = np.zeros_like(A)
         rc = _load().oracle_aa_natural(self.nx, self.ny, self.nz, _ptr(self.flags),
-                                       _ptr(self.faces), _ptr(self.inlet), _ptr(A), _ptr(f))
+                                       _ptr(self.faces), _ptr(self.inlet), _ptr(self.wall),
+                                       _ptr(A), _ptr(f))
         if rc != 0:
             raise ValueError("oracle_aa_natural: invalid arguments")
         return f
@@ -158,8 +161,8 @@ class Problem:
         rho = np.zeros(self.N, np.float64)
         u = np.zeros((3, self.N), np.float64)
         rc = _load().oracle_macroscopic(self.nx, self.ny, self.nz, _ptr(self.flags),
-                                        _ptr(self.inlet), _ptr(self.g), _ptr(f), _ptr(rho),
-                                        _ptr(u))
+                                        _ptr(self.inlet), _ptr(self.wall), _ptr(self.g),
+                                        _ptr(f), _ptr(rho), _ptr(u))
         if rc != 0:
             raise ValueError("oracle_macroscopic: invalid arguments")
         return rho, u

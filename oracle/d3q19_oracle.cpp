@@ -24,7 +24,10 @@
 //  * SOLID cells reflect (halfway bounce-back), INLET cells are fixed reservoirs at
 //    f_eq(rho_in, u_in), an OPEN face is zero-gradient: a population whose source lies beyond the
 //    face is taken from the source clamped onto the last layer of that axis;
-//  * momentum exchange on the solid: sum over bounce-back links of 2 c_q f*_q (f* = post-collision).
+//  * MOVING_WALL cells reflect like SOLID ones plus the moving-wall term of the mirror method
+//    ("GPU加速LBM流体仿真", §4.2): 2 w_q rho (c_q.u_w) / c_s^2 with rho the reference density 1;
+//  * momentum exchange on the solid: sum over bounce-back links of 2 c_q f*_q (f* = post-collision),
+//    and on a moving-wall link c_q (2 f*_q - 6 w_q (c_q.u_w)) (what the fluid gives up there).
 //
 // Parity pins: every function here is checked by tests/test_oracle_pins.py against closed forms,
 // invariants and brute force (weights and moments, equilibrium fixed point, exact conservation,
@@ -65,7 +68,7 @@ int opposite(int q) {
     return -1;
 }
 
-enum { FLUID = 0, SOLID = 1, INLET = 2 };
+enum { FLUID = 0, SOLID = 1, INLET = 2, MOVING_WALL = 3 };
 enum { PERIODIC = 0, OPEN = 1 };
 
 struct Grid {
@@ -133,11 +136,19 @@ struct Problem {
     double omega;
     double g[3];
     double feq_in[19];
+    double uw[3];  // velocity of the MOVING_WALL cells
     const uint8_t* flags;
 };
 
+// Moving-wall term of a link whose population q leaves the wall toward the fluid: the mirror
+// method's 2 w_q rho (c_q.u_w) / c_s^2 with c_s^2 = 1/3 and the reference density 1.
+double wall_term(const Problem& P, int q) {
+    double cu = C[q][0] * P.uw[0] + C[q][1] * P.uw[1] + C[q][2] * P.uw[2];
+    return 6.0 * weight(q) * cu;
+}
+
 int setup(Problem* P, int nx, int ny, int nz, double tau, const uint8_t* flags, const int* faces,
-          const double* inlet, const double* g) {
+          const double* inlet, const double* g, const double* wall) {
     if (nx < 1 || ny < 1 || nz < 1 || !(tau > 0.5) || !flags || !faces) return -1;
     P->grid.n[0] = nx;
     P->grid.n[1] = ny;
@@ -148,12 +159,13 @@ int setup(Problem* P, int nx, int ny, int nz, double tau, const uint8_t* flags, 
         P->grid.face[a] = faces[a];
     }
     for (int64_t n = 0; n < P->grid.N; ++n)
-        if (flags[n] > INLET) return -1;
+        if (flags[n] > MOVING_WALL) return -1;
     P->omega = 1.0 / tau;
     for (int a = 0; a < 3; ++a) P->g[a] = g ? g[a] : 0.0;
     double rho_in = inlet ? inlet[0] : 1.0;
     double u_in[3] = {inlet ? inlet[1] : 0.0, inlet ? inlet[2] : 0.0, inlet ? inlet[3] : 0.0};
     equilibrium(rho_in, u_in, P->feq_in);
+    for (int a = 0; a < 3; ++a) P->uw[a] = wall ? wall[a] : 0.0;
     P->flags = flags;
     return 0;
 }
@@ -186,9 +198,12 @@ void momentum_exchange(const Problem& P, const double* post, double force[3]) {
                     int s[3];
                     bool beyond;
                     displaced(G, X, C[q], s, &beyond);
-                    if (P.flags[G.cell(s)] != SOLID) continue;
+                    uint8_t partner = P.flags[G.cell(s)];
+                    if (partner != SOLID && partner != MOVING_WALL) continue;
                     double fq = post[(int64_t)q * G.N + n];
-                    for (int a = 0; a < 3; ++a) acc[a] += 2.0 * C[q][a] * fq;
+                    // what the fluid gives up: f*_q leaves, the reflected population returns
+                    double back = partner == SOLID ? fq : fq + wall_term(P, opposite(q));
+                    for (int a = 0; a < 3; ++a) acc[a] += C[q][a] * (fq + back);
                 }
             }
         for (int a = 0; a < 3; ++a) plane[3 * (size_t)z + a] = acc[a];
@@ -211,6 +226,8 @@ double incoming(const Problem& P, const int X[3], int q, PostAt post_at) {
     switch (P.flags[ns]) {
         case FLUID: return post_at(q, ns);                     // streamed from the source
         case SOLID: return post_at(opposite(q), G.cell(X));   // halfway bounce-back
+        case MOVING_WALL:                                      // bounce-back off a moving wall
+            return post_at(opposite(q), G.cell(X)) + wall_term(P, q);
         default: return P.feq_in[q];                          // equilibrium reservoir
     }
 }
@@ -255,10 +272,11 @@ void oracle_equilibrium_field(int64_t N, const double* rho, const double* u, dou
 //   force  : if not NULL, momentum exchange of the last step's post-collision state.
 // Returns 0, or -1 on invalid arguments.
 int oracle_step_ab(int nx, int ny, int nz, double tau, const uint8_t* flags, const int* faces,
-                   const double* inlet, const double* g, double* f, int nsteps, double* force,
-                   int nthreads) {
+                   const double* inlet, const double* g, const double* wall, double* f,
+                   int nsteps, double* force, int nthreads) {
     Problem P;
-    if (setup(&P, nx, ny, nz, tau, flags, faces, inlet, g) != 0 || nsteps < 0 || !f) return -1;
+    if (setup(&P, nx, ny, nz, tau, flags, faces, inlet, g, wall) != 0 || nsteps < 0 || !f)
+        return -1;
     set_threads(nthreads);
     const Grid& G = P.grid;
     const int64_t N = G.N;
@@ -305,10 +323,10 @@ int oracle_step_ab(int nx, int ny, int nz, double tau, const uint8_t* flags, con
 // After an odd number of total steps the buffer holds post-collision values at (opposite(q), x);
 // oracle_aa_natural() turns that into natural populations.
 int oracle_step_aa(int nx, int ny, int nz, double tau, const uint8_t* flags, const int* faces,
-                   const double* inlet, const double* g, double* A, int parity, int nsteps,
-                   double* force, int nthreads) {
+                   const double* inlet, const double* g, const double* wall, double* A,
+                   int parity, int nsteps, double* force, int nthreads) {
     Problem P;
-    if (setup(&P, nx, ny, nz, tau, flags, faces, inlet, g) != 0 || nsteps < 0 || !A ||
+    if (setup(&P, nx, ny, nz, tau, flags, faces, inlet, g, wall) != 0 || nsteps < 0 || !A ||
         (parity != 0 && parity != 1))
         return -1;
     set_threads(nthreads);
@@ -377,6 +395,8 @@ int oracle_step_aa(int nx, int ny, int nz, double tau, const uint8_t* flags, con
                             slot(q, G.cell(d)) = pq;              // streamed to the neighbour
                         } else if (fd == SOLID) {
                             slot(p, n) = pq;                       // bounced back into x
+                        } else if (fd == MOVING_WALL) {
+                            slot(p, n) = pq + wall_term(P, p);     // off the moving wall
                         } else if (fd == INLET) {
                             slot(p, n) = P.feq_in[p];              // reservoir feeds x
                         }
@@ -408,9 +428,10 @@ int oracle_step_aa(int nx, int ny, int nz, double tau, const uint8_t* flags, con
 // (opposite(q), x)): the streaming half of the next odd step, without its collision.
 // Non-FLUID cells are copied unchanged.
 int oracle_aa_natural(int nx, int ny, int nz, const uint8_t* flags, const int* faces,
-                      const double* inlet, const double* A, double* f) {
+                      const double* inlet, const double* wall, const double* A, double* f) {
     Problem P;
-    if (setup(&P, nx, ny, nz, 1.0, flags, faces, inlet, nullptr) != 0 || !A || !f) return -1;
+    if (setup(&P, nx, ny, nz, 1.0, flags, faces, inlet, nullptr, wall) != 0 || !A || !f)
+        return -1;
     const Grid& G = P.grid;
     const int64_t N = G.N;
     auto post_at = [&](int q, int64_t n) { return A[(int64_t)opposite(q) * N + n]; };
@@ -427,9 +448,11 @@ int oracle_aa_natural(int nx, int ny, int nz, const uint8_t* flags, const int* f
 }
 
 // Density and velocity of a natural state.  FLUID: rho = sum f, u = j/rho + g/2 (Guo's
-// half-force shift).  SOLID: 0, 0.  INLET: rho_in, u_in.   rho[N], u[3][N].
+// half-force shift).  SOLID: 0, 0.  INLET: rho_in, u_in.  MOVING_WALL: 1, u_w.
+// rho[N], u[3][N].
 int oracle_macroscopic(int nx, int ny, int nz, const uint8_t* flags, const double* inlet,
-                       const double* g, const double* f, double* rho, double* u) {
+                       const double* wall, const double* g, const double* f, double* rho,
+                       double* u) {
     if (nx < 1 || ny < 1 || nz < 1 || !flags || !f || !rho || !u) return -1;
     const int64_t N = (int64_t)nx * ny * nz;
     double gg[3] = {g ? g[0] : 0.0, g ? g[1] : 0.0, g ? g[2] : 0.0};
@@ -441,6 +464,9 @@ int oracle_macroscopic(int nx, int ny, int nz, const uint8_t* flags, const doubl
         } else if (flags[n] == INLET) {
             rho[n] = inlet ? inlet[0] : 1.0;
             for (int a = 0; a < 3; ++a) u[a * N + n] = inlet ? inlet[1 + a] : 0.0;
+        } else if (flags[n] == MOVING_WALL) {
+            rho[n] = 1.0;
+            for (int a = 0; a < 3; ++a) u[a * N + n] = wall ? wall[a] : 0.0;
         } else {
             double r = 0.0, j[3] = {0.0, 0.0, 0.0};
             for (int q = 0; q < 19; ++q) {

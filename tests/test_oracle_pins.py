@@ -405,7 +405,9 @@ AA_CASES = [
     (5, 6, 4, (1, 1, 0), 0.15, True, (3e-5, 2e-5, 0)),
     (4, 5, 6, (1, 1, 1), 0.2, False, (0, 0, 1e-5)),
     (3, 3, 3, (0, 1, 1), 0.25, True, (0, 0, 0)),
+    (6, 5, 4, (1, 0, 0), 0.3, True, (2e-5, 0, 0)),   # with moving walls (see below)
 ]
+MOVING_CASES = {6}
 
 
 @pytest.mark.parametrize("case", range(len(AA_CASES)))
@@ -418,8 +420,10 @@ def test_aa_in_place_equals_two_lattice(case, steps):
     if inlet_layer:
         x, _, _ = wl.coords(nx, ny, nz)
         flags[x == 0] = wl.INLET
+    if case in MOVING_CASES:
+        flags[(flags == wl.SOLID) & (r.uniform(size=N) < 0.5)] = wl.MOVING_WALL
     P = oracle.Problem(nx, ny, nz, 0.62, flags=flags, faces=faces,
-                       inlet=(1.01, 0.03, -0.01, 0.02), g=g)
+                       inlet=(1.01, 0.03, -0.01, 0.02), g=g, wall=(0.03, -0.02, 0.01))
     f0 = random_state(N, 200 + case)
     fb, Fb = P.step_ab(f0, steps, want_force=True)
     A, Fa = P.step_aa(f0, 0, steps, want_force=True)
@@ -465,3 +469,69 @@ def test_porous_generator_reaches_target():
     assert 0.30 <= frac < 0.30 + 27 / flags.size + 1e-12
     again = wl.porous_flags(24, 20, 16, 0.30, 3, seed=5)
     assert np.array_equal(flags, again)
+
+
+# ---- moving walls (GPU加速LBM §4.2 mirror method, reference density 1) ----------------------------
+
+def couette(ny, tau, U, steps, nx=1, nz=1):
+    flags = np.zeros(nx * ny * nz, np.uint8)
+    _, y, _ = wl.coords(nx, ny, nz)
+    flags[y == 0] = wl.SOLID
+    flags[y == ny - 1] = wl.MOVING_WALL
+    P = oracle.Problem(nx, ny, nz, tau, flags=flags, wall=(U, 0.0, 0.0))
+    f0 = oracle.equilibrium_field(*wl.uniform_fields(P.N))
+    f, F = P.step_ab(f0, steps, want_force=True)
+    return P, f, F
+
+
+def test_couette_steady_profile_is_linear_and_wall_forces_balance():
+    """Plane Couette flow between a resting wall (y = 0) and a wall moving at U (y = ny - 1):
+    halfway bounce-back reproduces the linear profile u = U (y - 1/2) / H exactly, and at steady
+    state the fluid's momentum no longer changes, so the forces on the two walls cancel."""
+    ny, tau, U = 18, 0.9, 0.02
+    H = ny - 2
+    P, f, F = couette(ny, tau, U, 40000)
+    rho, u = P.macroscopic(f)
+    y = np.arange(1, ny - 1)
+    assert np.abs(u[0][1:ny - 1] - U * (y - 0.5) / H).max() < 1e-9 * U
+    assert np.abs(u[1:]).max() < 1e-12
+    nu = (tau - 0.5) / 3
+    assert abs(F[0]) < 1e-9 * nu * U / H   # resting wall gets +rho nu U/H, moving wall the opposite
+    # shear stress from the non-equilibrium populations equals rho nu U / H in every fluid cell
+    c, w, _ = oracle.tables()
+    feq = oracle.equilibrium_field(rho, u)
+    sxy = -(1 - 0.5 / tau) * ((c[:, 0] * c[:, 1])[:, None] * (f - feq)).sum(axis=0)
+    assert np.abs(sxy[1:ny - 1] - nu * U / H).max() < 1e-6 * nu * U / H
+
+
+def test_moving_wall_at_rest_equals_solid():
+    nx, ny, nz = 6, 7, 5
+    r = np.random.default_rng(31)
+    flags = (r.uniform(size=nx * ny * nz) < 0.2).astype(np.uint8)
+    moving = flags.copy()
+    moving[moving == wl.SOLID] = wl.MOVING_WALL
+    f0 = random_state(nx * ny * nz, 32)
+    fs, Fs = oracle.Problem(nx, ny, nz, 0.7, flags=flags).step_ab(f0, 5, want_force=True)
+    fm, Fm = oracle.Problem(nx, ny, nz, 0.7, flags=moving).step_ab(f0, 5, want_force=True)
+    assert np.array_equal(fs, fm) and np.array_equal(Fs, Fm)
+
+
+def test_lid_driven_cavity_conserves_mass():
+    n = 10
+    x, y, z = wl.coords(n, n, n)
+    flags = np.zeros(n ** 3, np.uint8)
+    flags[(x == 0) | (x == n - 1) | (y == 0) | (z == 0) | (z == n - 1)] = wl.SOLID
+    flags[y == n - 1] = wl.MOVING_WALL
+    P = oracle.Problem(n, n, n, 0.6, flags=flags, wall=(0.05, 0.0, 0.0))
+    f0 = oracle.equilibrium_field(*wl.uniform_fields(P.N))
+    fl = flags == wl.FLUID
+    f, _ = P.step_ab(f0, 200)
+    assert abs(f[:, fl].sum() / f0[:, fl].sum() - 1) < 1e-13
+    _, u = P.macroscopic(f)
+    assert u[0][fl].max() > 0.005          # the lid drags the fluid along
+    # over one step the fluid's momentum changes by minus the momentum handed to the walls
+    # (resting and moving) -- checks the moving-wall correction of the momentum exchange
+    c, _, _ = oracle.tables()
+    f2, F = P.step_ab(f, 1, want_force=True)
+    dP = (c.T.astype(float) @ f2[:, fl]).sum(axis=1) - (c.T.astype(float) @ f[:, fl]).sum(axis=1)
+    assert np.abs(dP + F).max() < 1e-13
