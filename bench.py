@@ -247,15 +247,20 @@ def timed_steps(B, torch, ctx, steps, warmup, per_step=2, profile=True, sampler=
     return ms, launches, prof, clocks
 
 
-def variant(B, torch, n, scheme, steps=10, warmup=3):
-    """Periodic box without solids, g = 0, uniform flow: the clean roofline point."""
+def variant(B, torch, n, scheme, steps=10, warmup=3, cavity=False):
+    """Periodic box without solids, g = 0, uniform flow: the clean roofline point.  With
+    cavity=True: a lid-driven cavity (resting walls, lid moving at 0.05 along x), fluid at rest."""
     ctx = B.lbm_create(n, n, n, 0.6, B.LAYOUT_STREAM,
                        B.STREAMING_AA if scheme == "AA" else B.STREAMING_AB)
     try:
         N = n ** 3
+        if cavity:
+            B.lbm_set_flags(ctx, wl.cavity_flags(n, n, n))
+            B.lbm_set_wall_velocity(ctx, 0.05, 0.0, 0.0)
         rho = torch.ones(N, dtype=torch.float32, device="cuda")
         u = torch.zeros(3 * N, dtype=torch.float32, device="cuda")
-        u[:N] = 0.02
+        if not cavity:
+            u[:N] = 0.02
         B.lbm_set_equilibrium(ctx, rho, u)
         # throughput with graph replay (no per-kernel events), then per-kernel event timing
         ms, _, _, _ = timed_steps(B, torch, ctx, steps, warmup, profile=False)
@@ -410,6 +415,7 @@ def run_ours(args):
         log("[bench] variants")
         out["variants"] = {f"{s}_{m}^3_periodic": variant(B, torch, m, s)
                            for m in (128, 512) for s in ("AA", "AB")}
+        out["variants"]["AA_256^3_lid_driven_cavity"] = variant(B, torch, 256, "AA", cavity=True)
     if not args.no_e2e:
         log("[bench] e2e")
         out["e2e"] = e2e_run(B, torch, n, args.steps, flags)

@@ -28,7 +28,8 @@
  *   cell index  n = x + nx*(y + ny*z), N = nx*ny*nz;
  *   populations f[q*N + n], fp32, absolute values, the natural (pre-collision) state f(x, t);
  *   flags       uint8 per cell: LBM_FLUID, LBM_SOLID (bounce-back), LBM_INLET (reservoir held at
- *               f_eq(rho_in, u_in), never updated);
+ *               f_eq(rho_in, u_in), never updated), LBM_MOVING_WALL (bounce-back off a wall moving
+ *               at u_w);
  *   rho[n], u[a*N + n] (a = 0,1,2), fp32.
  *
  * The step.  Per time step every FLUID cell x collides (BGK, relaxation omega = 1/tau,
@@ -36,7 +37,9 @@
  * Guo forcing: F = rho g, u = j/rho + g/2, source (1 - omega/2) w [3 (c - u).F + 9 (c.u)(c.F)])
  * and then receives population q from s = x - c_q, wrapped on PERIODIC axes and clamped onto the
  * last layer on OPEN axes (zero-gradient): FLUID s gives its post-collision f*_q(s); SOLID s
- * reflects x's own f*_opposite(q)(x) (halfway bounce-back); INLET s gives f_eq,q(rho_in, u_in).
+ * reflects x's own f*_opposite(q)(x) (halfway bounce-back); INLET s gives f_eq,q(rho_in, u_in);
+ * MOVING_WALL s reflects f*_opposite(q)(x) + 2 w_q (c_q.u_w)/c_s^2 ([Blog] §4.2, the mirror method,
+ * at the reference density 1).
  *
  * Ownership and threading.  The caller owns every array it passes; the library keeps no caller
  * pointer after a call returns.  Array arguments may be device pointers or host pointers (pinned
@@ -84,7 +87,7 @@ enum {
     LBM_ENOTFINITE = -5  /* lbm_check_finite found a NaN or infinity                         */
 };
 
-enum { LBM_FLUID = 0, LBM_SOLID = 1, LBM_INLET = 2 };
+enum { LBM_FLUID = 0, LBM_SOLID = 1, LBM_INLET = 2, LBM_MOVING_WALL = 3 };
 enum { LBM_PERIODIC = 0, LBM_OPEN = 1 };
 
 /* Create a context on the current CUDA device.  nx, ny, nz >= 1, nz <= 65535, N <= 2^31 - 1,
@@ -102,8 +105,9 @@ const char* lbm_last_error(void);
  * work of this context.  Work already enqueued on the previous stream is synchronised first. */
 int lbm_set_stream(lbm_ctx* ctx, void* cuda_stream);
 
-/* Cell flags, N bytes, LBM_FLUID / LBM_SOLID / LBM_INLET ([PortLBM] §3.1 boundary treatment;
- * [Layout]: the per-link rules are driven by the cell type).  Any other value -> LBM_EINVAL.
+/* Cell flags, N bytes, LBM_FLUID / LBM_SOLID / LBM_INLET / LBM_MOVING_WALL ([PortLBM] §3.1
+ * boundary treatment; [Blog] §4.2 moving walls; [Layout]: the per-link rules are driven by the
+ * cell type).  Any other value -> LBM_EINVAL.
  * Changing flags does not touch the populations.  Synchronous. */
 int lbm_set_flags(lbm_ctx* ctx, const uint8_t* flags);
 
@@ -114,6 +118,10 @@ int lbm_set_faces(lbm_ctx* ctx, int face_x, int face_y, int face_z);
 
 /* State held by every INLET cell: f = f_eq(rho, (ux, uy, uz)).  rho > 0 and finite. */
 int lbm_set_inlet(lbm_ctx* ctx, float rho, float ux, float uy, float uz);
+
+/* Velocity u_w of every LBM_MOVING_WALL cell ([Blog] §4.2).  Finite; 0 (the initial value) makes
+ * moving walls behave as solid ones. */
+int lbm_set_wall_velocity(lbm_ctx* ctx, float ux, float uy, float uz);
 
 /* Body acceleration g (force density F = rho g), applied with Guo forcing.  0 disables it. */
 int lbm_set_body_force(lbm_ctx* ctx, float gx, float gy, float gz);
@@ -129,7 +137,8 @@ int lbm_set_equilibrium(lbm_ctx* ctx, const float* rho, const float* u);
 
 /* Read the natural state f(x, t) into f[19*N] (canonical, absolute fp32), whatever the AA parity
  * or A-B buffer state: after an odd AA step count the streaming half of the next step is applied
- * on the fly.  SOLID cells read 0, INLET cells f_eq(rho_in, u_in).  Synchronous. */
+ * on the fly.  SOLID and MOVING_WALL cells read 0, INLET cells f_eq(rho_in, u_in).
+ * Synchronous. */
 int lbm_get_populations(lbm_ctx* ctx, float* f);
 
 /* Enqueue n >= 0 time steps ([PortLBM] Eq. 1 with the per-link rules above) on the context
@@ -137,8 +146,8 @@ int lbm_get_populations(lbm_ctx* ctx, float* f);
  * post-collision state (read with lbm_force_momentum_exchange).  Asynchronous; n = 0 is a no-op
  * that leaves the last force unchanged.  With graph launch on (the default) the steps are
  * replayed from CUDA graphs of up to 32 steps, captured on a private stream on first use and
- * cached per (length, buffer state); the setters of flags, faces, inlet and body force drop the
- * cache.  Results are identical with graph launch on or off. */
+ * cached per (length, buffer state); the setters of flags, faces, inlet, wall velocity and body
+ * force drop the cache.  Results are identical with graph launch on or off. */
 int lbm_step(lbm_ctx* ctx, int n);
 
 /* Turn graph replay of lbm_step on (enable != 0, the default) or off (one launch per kernel).
@@ -146,14 +155,16 @@ int lbm_step(lbm_ctx* ctx, int n);
 int lbm_set_graph_launch(lbm_ctx* ctx, int enable);
 
 /* Density and velocity of the natural state: rho[N], u[3*N] (fp32).  FLUID: rho = sum f,
- * u = j/rho + g/2 (Guo's half-force shift).  SOLID: 0, 0.  INLET: rho_in, u_in.  Synchronous. */
+ * u = j/rho + g/2 (Guo's half-force shift).  SOLID: 0, 0.  INLET: rho_in, u_in.  MOVING_WALL:
+ * 1, u_w.  Synchronous. */
 int lbm_macroscopic(lbm_ctx* ctx, float* rho, float* u);
 
-/* Force on all SOLID cells (one body) from the last step of the last lbm_step call
- * ([Layout]: the momentum exchange is taken in the step whose forces are read back): the sum
- * over every bounce-back link of a FLUID cell of 2 c_q f*_q, accumulated in fp32 within each warp
- * of 32 cells and in fp64 across warps, in a fixed order.  F[3] in lattice units.  LBM_ESTATE before the first step
- * or after the state was reloaded.  Synchronous. */
+/* Force on all SOLID and MOVING_WALL cells (one body) from the last step of the last lbm_step
+ * call ([Layout]: the momentum exchange is taken in the step whose forces are read back): the sum
+ * over every bounce-back link of a FLUID cell of 2 c_q f*_q (on a MOVING_WALL link
+ * c_q (2 f*_q - 6 w_q (c_q.u_w)), what the fluid gives up there), accumulated in fp32 within each
+ * warp of 32 cells and in fp64 across warps, in a fixed order.  F[3] in lattice units.
+ * LBM_ESTATE before the first step or after the state was reloaded.  Synchronous. */
 int lbm_force_momentum_exchange(lbm_ctx* ctx, double F[3]);
 
 /* LBM_OK if every population of every FLUID cell is finite, LBM_ENOTFINITE otherwise.

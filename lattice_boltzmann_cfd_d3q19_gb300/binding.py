@@ -18,7 +18,7 @@ from . import build as _build
 LAYOUT_STREAM, LAYOUT_BUNDLE, LAYOUT_COLLISION = 0, 1, 2
 STREAMING_AUTO, STREAMING_AA, STREAMING_AB, STREAMING_AB2 = 0, 1, 2, 3
 OK, EINVAL, ENOMEM, ECUDA, ESTATE, ENOTFINITE = 0, -1, -2, -3, -4, -5
-FLUID, SOLID, INLET = 0, 1, 2
+FLUID, SOLID, INLET, MOVING_WALL = 0, 1, 2, 3
 PERIODIC, OPEN = 0, 1
 # profiling kinds of lbm_profile_read
 K_AA_EVEN, K_AA_ODD, K_AB_PULL, K_AB_COLLIDE, K_STREAM, K_PREGATHER, K_FORCE, K_BOUNDARY = range(8)
@@ -33,6 +33,7 @@ SIGNATURES = {
     "lbm_set_faces": (_I, [_P, _I, _I, _I]),
     "lbm_set_inlet": (_I, [_P, _F, _F, _F, _F]),
     "lbm_set_body_force": (_I, [_P, _F, _F, _F]),
+    "lbm_set_wall_velocity": (_I, [_P, _F, _F, _F]),
     "lbm_set_populations": (_I, [_P, _P]),
     "lbm_set_equilibrium": (_I, [_P, _P, _P]),
     "lbm_get_populations": (_I, [_P, _P]),
@@ -151,6 +152,10 @@ def lbm_set_inlet(ctx: int, rho: float, ux: float, uy: float, uz: float) -> None
 
 def lbm_set_body_force(ctx: int, gx: float, gy: float, gz: float) -> None:
     _check(load().lbm_set_body_force(ctx, float(gx), float(gy), float(gz)))
+
+
+def lbm_set_wall_velocity(ctx: int, ux: float, uy: float, uz: float) -> None:
+    _check(load().lbm_set_wall_velocity(ctx, float(ux), float(uy), float(uz)))
 
 
 def lbm_set_populations(ctx: int, f) -> None:

@@ -108,8 +108,10 @@ struct lbm_ctx {
     uint32_t* mask = nullptr;
     uint32_t* special = nullptr;  // sorted indices of the special FLUID cells
     uint32_t n_special = 0;
-    uint32_t* count_dev = nullptr;  // 2 counters: special cells, cells with a SOLID link
+    uint32_t* count_dev = nullptr;  // counters: special cells, SOLID links, MOVING_WALL links
     int any_solid_link = 0;
+    int any_moving = 0;
+    float uw[3] = {0.f, 0.f, 0.f};
     float* scratch = nullptr;
     size_t face_base[3][2] = {};
     double* partial = nullptr;    // nblocks main-kernel partials, then the boundary kernels'
@@ -151,6 +153,13 @@ struct lbm_ctx {
         p.flags = flags;
         p.mask = mask;
         p.any_solid_link = any_solid_link;
+        p.any_moving = any_moving;
+        for (int a = 0; a < 3; ++a) p.uw[a] = uw[a];
+        for (int q = 0; q < 19; ++q) {
+            const double w = q == 0 ? 1.0 / 3.0 : q <= 6 ? 1.0 / 18.0 : 1.0 / 36.0;
+            p.wterm[q] = (float)(6.0 * w * (cx(q) * (double)uw[0] + cy(q) * (double)uw[1] +
+                                            cz(q) * (double)uw[2]));
+        }
         p.special = special;
         p.n_special = n_special;
         p.scratch = scratch;
@@ -261,12 +270,12 @@ size_t partial_triples(size_t main_blocks, uint32_t n_special) {
 // faces.  Synchronous.
 int classify(lbm_ctx* c) {
     Params p = c->params(nullptr, nullptr);
-    LBM_CUDA(cudaMemsetAsync(c->count_dev, 0, 2 * sizeof(uint32_t), c->stream), "classify");
+    LBM_CUDA(cudaMemsetAsync(c->count_dev, 0, 3 * sizeof(uint32_t), c->stream), "classify");
     LBM_CUDA(launch_classify(p, c->types, c->flags, c->mask, c->count_dev, c->grid, c->block,
                              c->stream), "classify flags");
     ++c->launches;
-    uint32_t counts[2] = {0, 0};
-    LBM_CUDA(cudaMemcpyAsync(counts, c->count_dev, 2 * sizeof(uint32_t), cudaMemcpyDeviceToHost,
+    uint32_t counts[3] = {0, 0, 0};
+    LBM_CUDA(cudaMemcpyAsync(counts, c->count_dev, 3 * sizeof(uint32_t), cudaMemcpyDeviceToHost,
                              c->stream), "classify");
     LBM_CUDA(cudaStreamSynchronize(c->stream), "classify");
     const uint32_t count = counts[0];
@@ -310,6 +319,7 @@ int classify(lbm_ctx* c) {
     c->special = dev_list;
     c->n_special = count;
     c->any_solid_link = counts[1] > 0;
+    c->any_moving = counts[2] > 0;
     return LBM_OK;
 }
 
@@ -539,7 +549,7 @@ lbm_ctx* lbm_create(int nx, int ny, int nz, float tau, int layout, int streaming
     if ((e = cudaMalloc(&c->types, N)) != cudaSuccess) return bad(e, "lbm_create: cell types");
     if ((e = cudaMalloc(&c->flags, N)) != cudaSuccess) return bad(e, "lbm_create: cell flags");
     if ((e = cudaMalloc(&c->mask, N * sizeof(uint32_t))) != cudaSuccess) return bad(e, "lbm_create: link masks");
-    if ((e = cudaMalloc(&c->count_dev, 2 * sizeof(uint32_t))) != cudaSuccess) return bad(e, "lbm_create: counter");
+    if ((e = cudaMalloc(&c->count_dev, 3 * sizeof(uint32_t))) != cudaSuccess) return bad(e, "lbm_create: counter");
     if ((e = cudaMalloc(&c->stage, 3 * kForceStage * sizeof(double))) != cudaSuccess)
         return bad(e, "lbm_create: force stage");
     if ((e = cudaMalloc(&c->force_dev, 3 * sizeof(double))) != cudaSuccess) return bad(e, "lbm_create: force");
@@ -580,7 +590,8 @@ int lbm_set_flags(lbm_ctx* c, const uint8_t* flags) {
     if (e != cudaSuccess) {
         rc = cuda_fail(e, "lbm_set_flags");
     } else if (*c->err_host) {
-        rc = fail(LBM_EINVAL, "lbm_set_flags: flag values must be 0 (FLUID), 1 (SOLID) or 2 (INLET)");
+        rc = fail(LBM_EINVAL, "lbm_set_flags: flag values must be 0 (FLUID), 1 (SOLID), 2 (INLET) "
+                              "or 3 (MOVING_WALL)");
     } else {
         ++c->launches;
         c->drop_graphs();
@@ -640,6 +651,17 @@ int lbm_set_inlet(lbm_ctx* c, float rho, float ux, float uy, float uz) {
     c->inlet[3] = uz;
     const double u[3] = {ux, uy, uz};
     shifted_equilibrium(rho, u, c->heq_in);
+    return LBM_OK;
+}
+
+int lbm_set_wall_velocity(lbm_ctx* c, float ux, float uy, float uz) {
+    if (!c) return fail(LBM_EINVAL, "lbm_set_wall_velocity: NULL context");
+    if (!std::isfinite(ux) || !std::isfinite(uy) || !std::isfinite(uz))
+        return fail(LBM_EINVAL, "lbm_set_wall_velocity: u_w must be finite");
+    c->drop_graphs();
+    c->uw[0] = ux;
+    c->uw[1] = uy;
+    c->uw[2] = uz;
     return LBM_OK;
 }
 

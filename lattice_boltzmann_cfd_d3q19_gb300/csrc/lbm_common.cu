@@ -7,13 +7,14 @@ namespace {
 
 __global__ void __launch_bounds__(256) k_validate_types(const uint8_t* types, size_t N, int* bad) {
     const size_t n = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (n < N && types[n] > T_INLET) *bad = 1;
+    if (n < N && types[n] > T_MOVING) *bad = 1;
 }
 
 // Internal flags and solid-link masks.  For a FLUID cell: mask bit q when x + c_q (wrapped, or
-// clamped at an OPEN face) is SOLID; F_SPECIAL when some x + c_q is INLET or lies beyond an OPEN
-// face; F_BULK when no link rule applies at all.
-// count[0]: special cells; count[1]: FLUID cells with a SOLID link (not special)
+// clamped at an OPEN face) is SOLID; F_SPECIAL when some x + c_q is INLET or MOVING_WALL or lies
+// beyond an OPEN face; F_BULK when no link rule applies at all.
+// count[0]: special cells; count[1]: FLUID cells with a SOLID link; count[2]: FLUID cells with a
+// MOVING_WALL link
 __global__ void __launch_bounds__(256) k_classify(Params p, const uint8_t* types, uint8_t* flags,
                                                   uint32_t* mask, uint32_t* count) {
     const int x = blockIdx.x * blockDim.x + threadIdx.x;
@@ -25,13 +26,15 @@ __global__ void __launch_bounds__(256) k_classify(Params p, const uint8_t* types
     uint8_t out = t;
     uint32_t m = 0;
     if (t == T_FLUID) {
-        bool special = false;
+        bool special = false, moving = false;
         for (int q = 1; q < 19; ++q) {
             const Link s = link_cell(p, x, y, z, cx(q), cy(q), cz(q));
             const uint8_t ts = types[s.cell];
-            if (s.face >= 0 || ts == T_INLET) special = true;
+            if (s.face >= 0 || ts == T_INLET || ts == T_MOVING) special = true;
+            if (ts == T_MOVING) moving = true;
             if (ts == T_SOLID) m |= 1u << q;
         }
+        if (moving) atomicAdd(count + 2, 1u);
         if (special) {
             out |= F_SPECIAL;
             atomicAdd(count, 1u);

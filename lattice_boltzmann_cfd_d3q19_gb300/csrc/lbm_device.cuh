@@ -15,14 +15,14 @@ namespace lbm {
 enum : int { LAYOUT_STREAM = 0, LAYOUT_BUNDLE = 1, LAYOUT_COLLISION = 2 };
 
 // internal flag byte: bits 0-1 cell type; for FLUID cells
-//  bit 6 "special": a neighbour x + c_q is INLET or lies beyond an OPEN face -- the cell takes the
-//        general per-link path in the boundary kernels;
+//  bit 6 "special": a neighbour x + c_q is INLET or MOVING_WALL or lies beyond an OPEN face -- the
+//        cell takes the general per-link path in the boundary kernels;
 //  bit 7 "bulk": all 18 neighbours exist inside the domain (wrapped on periodic axes) and are
 //        FLUID -- no link rule applies.
 // FLUID cells that are neither have SOLID neighbours only; their links are described by the
 // per-cell solid-link mask (bit q set when x + c_q, wrapped or clamped, is SOLID).
-enum : uint8_t { T_FLUID = 0, T_SOLID = 1, T_INLET = 2, TYPE_MASK = 3, F_SPECIAL = 0x40,
-                 F_BULK = 0x80 };
+enum : uint8_t { T_FLUID = 0, T_SOLID = 1, T_INLET = 2, T_MOVING = 3, TYPE_MASK = 3,
+                 F_SPECIAL = 0x40, F_BULK = 0x80 };
 
 // what the population buffer holds between steps
 enum : int {
@@ -98,6 +98,7 @@ struct Params {
     const uint8_t* flags;  // internal flag bytes
     const uint32_t* mask;  // per-cell solid-link mask (0 for bulk cells)
     int any_solid_link;    // some FLUID cell has a SOLID neighbour (else every mask is 0)
+    int any_moving;        // some FLUID cell has a MOVING_WALL neighbour
     const uint32_t* special;  // indices of the special FLUID cells
     uint32_t n_special;
     float* scratch;        // open-face pre-gathered values (AA odd step)
@@ -112,6 +113,8 @@ struct Params {
     float tau_g[3];        // tau g: equilibrium velocity shift of the Guo forcing
     float wk[19];          // -omega (tau - 1/2)^2 w_q (4.5 (c_q.g)^2 - 1.5 g.g)
     float heq_in[19];      // shifted inlet state f_eq(rho_in, u_in) - w
+    float uw[3];           // velocity of the MOVING_WALL cells
+    float wterm[19];       // 6 w_q (c_q . u_w): the moving-wall term of a population q leaving the wall
     // hot-path addressing: population q of cell n is pa[q][n * cell_stride(q)] in A and
     // pb[q][n * cell_stride(q)] in B; pdiff[q] = pa[q] - pa[opposite(q)] in elements
     float* pa[19];

@@ -8,7 +8,9 @@
 // performance", paragraph after the layout bullets): population q of FLUID cell x comes from
 // s = x - c_q (wrapped on periodic axes, clamped onto the last layer beyond an OPEN face):
 // FLUID s streams its post-collision value, SOLID s reflects x's own post-collision population
-// opposite(q) (halfway bounce-back, PortLBM §3.1), INLET s supplies f_eq(rho_in, u_in).
+// opposite(q) (halfway bounce-back, PortLBM §3.1), INLET s supplies f_eq(rho_in, u_in), a
+// MOVING_WALL s reflects like SOLID plus 2 w_q (c_q.u_w) / c_s^2 (the mirror method of
+// "GPU加速LBM流体仿真" §4.2, at the reference density 1).
 #pragma once
 
 #include <type_traits>
@@ -97,6 +99,21 @@ __device__ __forceinline__ void mask_forces(uint32_t m, const float (&h)[19], fl
     if constexpr (Q < 18) mask_forces<Q + 1>(m, h, fx, fy, fz);
 }
 
+// Momentum exchange of the MOVING_WALL links of a special cell: what the fluid gives up on link q
+// is c_q (f*_q + f_back), f_back = f*_q + 6 w (c_opp(q).u_w), i.e. c_q (2 f*_q - 6 w_q (c_q.u_w)).
+template <int Q = 1>
+__device__ __forceinline__ void moving_forces(const Params& p, const float (&h)[19], int x, int y,
+                                              int z, float& fx, float& fy, float& fz) {
+    const Link d = link_cell(p, x, y, z, cx(Q), cy(Q), cz(Q));
+    if ((p.flags[d.cell] & TYPE_MASK) == T_MOVING) {
+        const float t = 2.0f * (h[Q] + wq(Q)) - p.wterm[Q];
+        if (cx(Q) > 0) fx += t; else if (cx(Q) < 0) fx -= t;
+        if (cy(Q) > 0) fy += t; else if (cy(Q) < 0) fy -= t;
+        if (cz(Q) > 0) fz += t; else if (cz(Q) < 0) fz -= t;
+    }
+    if constexpr (Q < 18) moving_forces<Q + 1>(p, h, x, y, z, fx, fy, fz);
+}
+
 template <int Q>
 __device__ __forceinline__ bool solid_link(uint32_t m) { return (m >> Q) & 1u; }
 
@@ -149,7 +166,10 @@ __global__ void __launch_bounds__(256) k_aa_even(Params p) {
             asm volatile("" : "+r"(ns) : "f"(h[0]), "f"(h[18]));
 #pragma unroll
             for (int q = 0; q < 19; ++q) p.pa[opp(q)][cell_off<L, I>(q, ns)] = h[q];
-            if (FORCE && !(fl & F_BULK)) mask_forces(p.mask[c.n], h, fx, fy, fz);
+            if (FORCE && !(fl & F_BULK)) {
+                mask_forces(p.mask[c.n], h, fx, fy, fz);
+                if (p.any_moving && (fl & F_SPECIAL)) moving_forces(p, h, c.x, c.y, c.z, fx, fy, fz);
+            }
         }
     }
     if (FORCE) warp_force(fx, fy, fz, p.partial);
@@ -237,6 +257,7 @@ __device__ __forceinline__ float aa_odd_gather(const Params& p, uint32_t n, int 
     const Link s = link_cell(p, x, y, z, -cx(Q), -cy(Q), -cz(Q));
     const int t = p.flags[s.cell] & TYPE_MASK;
     if (t == T_SOLID) return p.A[idx<L>(Q, n, p.N)];           // f*_opp(q)(x) sits at (q, x)
+    if (t == T_MOVING) return p.A[idx<L>(Q, n, p.N)] + p.wterm[Q];
     if (t == T_INLET) return p.heq_in[Q];
     if (s.face >= 0) return p.scratch[scratch_slot(p, s.face, Q, x, y, z)];
     return p.A[idx<L>(opp(Q), s.cell, p.N)];
@@ -279,6 +300,8 @@ __device__ __forceinline__ void aa_odd_scatter(const Params& p, float v, uint32_
     const int t = p.flags[d.cell] & TYPE_MASK;
     if (t == T_SOLID) {
         p.A[idx<L>(opp(Q), n, p.N)] = v;                          // bounces back into x
+    } else if (t == T_MOVING) {
+        p.A[idx<L>(opp(Q), n, p.N)] = v + p.wterm[opp(Q)];         // off the moving wall
     } else if (t == T_INLET) {
         p.A[idx<L>(opp(Q), n, p.N)] = p.heq_in[opp(Q)];            // the reservoir feeds x
     } else if (d.face < 0) {
@@ -310,7 +333,10 @@ __global__ void __launch_bounds__(256) k_aa_odd_special(Params p) {
         aa_odd_gather_all<L>(p, h, c.n, c.x, c.y, c.z);
         collide<BODY>(h, p);
         aa_odd_scatter_all<L>(p, h, c.n, c.x, c.y, c.z);
-        if (FORCE) mask_forces(p.mask[c.n], h, fx, fy, fz);
+        if (FORCE) {
+            mask_forces(p.mask[c.n], h, fx, fy, fz);
+            if (p.any_moving) moving_forces(p, h, c.x, c.y, c.z, fx, fy, fz);
+        }
     }
     if (FORCE) warp_force(fx, fy, fz, p.partial, p.part_special);
 }
@@ -366,6 +392,7 @@ __device__ __forceinline__ void ab_gather_all(const Params& p, float (&h)[19], u
     const Link s = link_cell(p, x, y, z, -cx(Q), -cy(Q), -cz(Q));
     const int t = p.flags[s.cell] & TYPE_MASK;
     if (t == T_SOLID) h[Q] = p.A[idx<L>(opp(Q), n, p.N)];
+    else if (t == T_MOVING) h[Q] = p.A[idx<L>(opp(Q), n, p.N)] + p.wterm[Q];
     else if (t == T_INLET) h[Q] = p.heq_in[Q];
     else h[Q] = p.A[idx<L>(Q, s.cell, p.N)];
     if constexpr (Q < 18) ab_gather_all<L, Q + 1>(p, h, n, x, y, z);
@@ -400,6 +427,8 @@ __global__ void __launch_bounds__(256, 6) k_ab(Params p) {
 #pragma unroll
             for (int q = 0; q < 19; ++q) p.pb[q][cell_off<L, I>(q, ns)] = h[q];
             if (FORCE && m) mask_forces(m, h, fx, fy, fz);
+            if (FORCE && FROM_NATURAL && p.any_moving && (fl & F_SPECIAL))
+                moving_forces(p, h, c.x, c.y, c.z, fx, fy, fz);
         } else if ((fl & TYPE_MASK) != T_FLUID && p.pb[0] != p.pa[0]) {
             // SOLID and INLET slots are never read; writing them keeps every 32-byte sector of
             // the destination fully written (no fill from DRAM for partly written sectors)
@@ -420,7 +449,10 @@ __global__ void __launch_bounds__(256) k_ab_special(Params p) {
         collide<BODY>(h, p);
 #pragma unroll
         for (int q = 0; q < 19; ++q) p.B[idx<L>(q, c.n, p.N)] = h[q];
-        if (FORCE) mask_forces(p.mask[c.n], h, fx, fy, fz);
+        if (FORCE) {
+            mask_forces(p.mask[c.n], h, fx, fy, fz);
+            if (p.any_moving) moving_forces(p, h, c.x, c.y, c.z, fx, fy, fz);
+        }
     }
     if (FORCE) warp_force(fx, fy, fz, p.partial, p.part_special);
 }
@@ -466,11 +498,12 @@ __device__ __forceinline__ float natural_h(const Params& p, int state, int q, ui
     const Link s = link_cell(p, x, y, z, -cx(q), -cy(q), -cz(q));
     const int t = p.flags[s.cell] & TYPE_MASK;
     if (t == T_INLET) return p.heq_in[q];
+    const float wall = t == T_MOVING ? p.wterm[q] : 0.0f;
     if (state == ST_POST_AA) {
-        if (t == T_SOLID) return p.A[idx_rt<L>(q, n, p.N)];
+        if (t == T_SOLID || t == T_MOVING) return p.A[idx_rt<L>(q, n, p.N)] + wall;
         return p.A[idx_rt<L>(opp(q), s.cell, p.N)];
     }
-    if (t == T_SOLID) return p.A[idx_rt<L>(opp(q), n, p.N)];
+    if (t == T_SOLID || t == T_MOVING) return p.A[idx_rt<L>(opp(q), n, p.N)] + wall;
     return p.A[idx_rt<L>(q, s.cell, p.N)];
 }
 
@@ -488,7 +521,7 @@ __global__ void __launch_bounds__(256) k_unpack(Params p, int state, float* out,
     const int z = (int)(n / ((uint32_t)p.nx * (uint32_t)p.ny));
     const int t = p.flags[n] & TYPE_MASK;
     float v;
-    if (t == T_SOLID) v = 0.0f;
+    if (t == T_SOLID || t == T_MOVING) v = 0.0f;
     else if (t == T_INLET) v = p.heq_in[q] + wq(q);
     else v = natural_h<L>(p, state, q, n, x, y, z) + wq(q);
     out[k] = v;
@@ -534,6 +567,7 @@ __global__ void __launch_bounds__(256) k_macro(Params p, int state, float rho_in
     const uint32_t n = n0 + k;
     const int t = p.flags[n] & TYPE_MASK;
     if (t == T_SOLID) { rho[k] = 0.f; u0[k] = u1[k] = u2[k] = 0.f; return; }
+    if (t == T_MOVING) { rho[k] = 1.f; u0[k] = p.uw[0]; u1[k] = p.uw[1]; u2[k] = p.uw[2]; return; }
     if (t == T_INLET) { rho[k] = rho_in; u0[k] = ux_in; u1[k] = uy_in; u2[k] = uz_in; return; }
     const int x = (int)(n % (uint32_t)p.nx);
     const int y = (int)((n / (uint32_t)p.nx) % (uint32_t)p.ny);

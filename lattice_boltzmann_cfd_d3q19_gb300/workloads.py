@@ -3,7 +3,8 @@
 This module holds no lattice Boltzmann arithmetic (no equilibrium, collision or streaming): it
 only builds density / velocity fields and geometry, with numpy's PCG64 generator, so that the GPU
 library and the CPU oracle are fed identical inputs.  Cell index n = x + nx*(y + ny*z); fields are
-returned flat (rho[N], u[3, N]) in float64; flags are uint8 (0 fluid, 1 solid, 2 inlet).
+returned flat (rho[N], u[3, N]) in float64; flags are uint8 (0 fluid, 1 solid, 2 inlet,
+3 moving wall).
 
 Workloads (sizes as named by their callers):
   * Taylor-Green vortex (the validation case PortLBM lists beside Hagen-Poiseuille and Karman
@@ -13,6 +14,7 @@ Workloads (sizes as named by their callers):
   * sphere: SOLID where (x-cx)^2 + (y-cy)^2 + (z-cz)^2 <= r^2, optional INLET layer at x = 0.
   * porous medium: 3x3x3 solid blobs at uniformly drawn corners (periodic wrap), drawn in order
     until the solid fraction first reaches the target.
+  * lid-driven cavity: resting walls on five faces, a moving lid (MOVING_WALL) on the sixth.
 """
 from __future__ import annotations
 
@@ -108,6 +110,16 @@ def porous_flags(nx: int, ny: int, nz: int, solid_fraction: float = 0.30, blob: 
     K = int(np.partition(first_cover, target - 1)[target - 1]) + 1
     flags = np.zeros(N, np.uint8)
     flags[first_cover < K] = SOLID
+    return flags
+
+
+def cavity_flags(nx: int, ny: int, nz: int) -> np.ndarray:
+    """Lid-driven cavity: resting walls on the x, z and lower y faces, a MOVING_WALL lid on the
+    layer y = ny - 1 (it covers the lid's edges)."""
+    x, y, z = coords(nx, ny, nz)
+    flags = np.zeros(x.size, np.uint8)
+    flags[(x == 0) | (x == nx - 1) | (y == 0) | (z == 0) | (z == nz - 1)] = SOLID
+    flags[y == ny - 1] = MOVING_WALL
     return flags
 
 

@@ -19,7 +19,7 @@ class Case:
     """One problem: grid, tau, flags, faces, inlet, body force and initial natural state f0."""
 
     def __init__(self, nx, ny, nz, tau, f0, flags=None, faces=(0, 0, 0),
-                 inlet=(1.0, 0.0, 0.0, 0.0), g=(0.0, 0.0, 0.0)):
+                 inlet=(1.0, 0.0, 0.0, 0.0), g=(0.0, 0.0, 0.0), wall=(0.0, 0.0, 0.0)):
         self.nx, self.ny, self.nz = nx, ny, nz
         self.N = nx * ny * nz
         self.tau = tau
@@ -27,6 +27,7 @@ class Case:
         self.faces = tuple(faces)
         self.inlet = tuple(float(v) for v in inlet)
         self.g = tuple(float(v) for v in g)
+        self.wall = tuple(float(v) for v in wall)
         # the input both sides start from, exactly representable in fp32
         if isinstance(f0, np.ndarray) and f0.dtype == np.float32:
             self.f0_32 = np.ascontiguousarray(f0.reshape(19, self.N))
@@ -40,7 +41,8 @@ class Case:
 
     def oracle_problem(self, threads=0):
         return oracle.Problem(self.nx, self.ny, self.nz, self.tau, flags=self.flags,
-                              faces=self.faces, inlet=self.inlet, g=self.g, threads=threads)
+                              faces=self.faces, inlet=self.inlet, g=self.g, threads=threads,
+                              wall=self.wall)
 
     def run_oracle(self, steps, want_force=False):
         return self.oracle_problem().step_ab(self.f0_32.astype(np.float64), steps, want_force)
@@ -53,6 +55,7 @@ class Case:
             B.lbm_set_faces(ctx, *self.faces)
             B.lbm_set_inlet(ctx, *self.inlet)
             B.lbm_set_body_force(ctx, *self.g)
+            B.lbm_set_wall_velocity(ctx, *self.wall)
             if device_input:
                 B.lbm_set_populations(ctx, torch.from_numpy(self.f0_32.copy()).cuda())
             else:
@@ -104,6 +107,6 @@ def window(case, center, half, f):
     idx = (xs[None, None, :] + nx * (ys[None, :, None] + ny * zs[:, None, None])).reshape(-1)
     m = 2 * half + 1
     sub = Case(m, m, m, case.tau, f.reshape(19, -1)[:, idx], flags=case.flags[idx],
-               inlet=case.inlet, g=case.g)
+               inlet=case.inlet, g=case.g, wall=case.wall)
     centre_index = half + m * (half + m * half)
     return sub, centre_index, idx

@@ -20,15 +20,18 @@ if not torch.cuda.is_available():
 
 
 def mixed_case(nx, ny, nz, faces, seed, solid=0.15, inlet_layer=True, g=(2e-5, -1e-5, 1e-5),
-               tau=0.62):
+               tau=0.62, moving=0.0):
+    """Random solids (a fraction `moving` of them moving walls), an optional inlet layer."""
     r = np.random.default_rng(seed)
     N = nx * ny * nz
     flags = (r.uniform(size=N) < solid).astype(np.uint8)
+    if moving:
+        flags[(flags == wl.SOLID) & (r.uniform(size=N) < moving)] = wl.MOVING_WALL
     if inlet_layer:
         x, _, _ = wl.coords(nx, ny, nz)
         flags[x == 0] = wl.INLET
     return Case(nx, ny, nz, tau, random_state(N, seed + 1), flags=flags, faces=faces,
-                inlet=(1.01, 0.04, -0.01, 0.02), g=g)
+                inlet=(1.01, 0.04, -0.01, 0.02), g=g, wall=(0.03, -0.02, 0.01))
 
 
 # ---- small cases: every scheme x layout, all link types, ragged grids, even and odd counts -------
@@ -56,6 +59,104 @@ def test_small_cases_match_oracle(ci, layout, scheme):
         assert max_fluid_diff(case, fg, fo) <= TOL_F, (steps, max_fluid_diff(case, fg, fo))
         scale = max(1.0, float(np.abs(Fo).max()))
         assert np.abs(Fg - Fo).max() <= 1e-4 * scale, (Fg, Fo)
+
+
+MOVING = [
+    # nx, ny, nz, faces, solid fraction, inlet layer
+    (37, 23, 19, (0, 0, 0), 0.2, False),
+    (33, 17, 9, (1, 0, 0), 0.15, True),
+]
+
+
+@pytest.mark.parametrize("scheme", ["AA", "AB", "AB2"])
+@pytest.mark.parametrize("layout", ["stream", "bundle", "collision"])
+@pytest.mark.parametrize("ci", range(len(MOVING)))
+def test_moving_walls_match_oracle(ci, layout, scheme):
+    nx, ny, nz, faces, solid, inlet = MOVING[ci]
+    case = mixed_case(nx, ny, nz, faces, 700 + ci, solid=solid, inlet_layer=inlet, moving=0.5)
+    assert (case.flags == wl.MOVING_WALL).any()
+    for steps in (1, 4, 7):
+        fo, Fo = case.run_oracle(steps, want_force=True)
+        fg, Fg = case.run_gpu(steps, layout, scheme, want_force=True)
+        assert max_fluid_diff(case, fg, fo) <= TOL_F, (steps, max_fluid_diff(case, fg, fo))
+        scale = max(1.0, float(np.abs(Fo).max()))
+        assert np.abs(Fg - Fo).max() <= 1e-4 * scale, (Fg, Fo)
+
+
+def test_couette_matches_oracle_and_is_linear():
+    """Plane Couette flow (resting wall y = 0, lid y = ny - 1 moving at U along x), 16 x 18 x 16
+    on the GPU against the oracle's 1 x 18 x 1 column (x/z invariance), 30000 steps."""
+    ny, tau, U, steps = 18, 0.9, 0.02, 30000
+    H = ny - 2
+    def flags_for(nx, nz):
+        _, y, _ = wl.coords(nx, ny, nz)
+        fl = np.zeros(nx * ny * nz, np.uint8)
+        fl[y == 0] = wl.SOLID
+        fl[y == ny - 1] = wl.MOVING_WALL
+        return fl
+    col = Case(1, ny, 1, tau, oracle.equilibrium_field(*wl.uniform_fields(ny)),
+               flags=flags_for(1, 1), wall=(U, 0, 0))
+    fo, _ = col.run_oracle(steps)
+    full = Case(16, ny, 16, tau, oracle.equilibrium_field(*wl.uniform_fields(16 * ny * 16)),
+                flags=flags_for(16, 16), wall=(U, 0, 0))
+    for scheme in ("AA", "AB"):
+        fg, Fg = full.run_gpu(steps, "stream", scheme, want_force=True)
+        fo_full = np.broadcast_to(fo.reshape(19, 1, ny, 1), (19, 16, ny, 16)).reshape(19, -1)
+        assert max_fluid_diff(full, fg, fo_full) <= TOL_F
+        F4 = fg.reshape(19, 16, ny, 16)
+        with np.errstate(invalid="ignore"):  # wall cells hold 0
+            ux = (F4 * oracle.tables()[0][:, 0, None, None, None]).sum(axis=0) / F4.sum(axis=0)
+        y = np.arange(1, ny - 1)
+        assert np.abs(ux[:, 1:ny - 1, :] - (U * (y - 0.5) / H)[None, :, None]).max() < 1e-3 * U
+        # steady state: the shear forces on the two walls (rho nu U / H each, 16 x 16 cells)
+        # cancel
+        wall_force = (tau - 0.5) / 3 * U / H * 256
+        assert abs(Fg[0]) < 1e-2 * wall_force
+
+
+def test_lid_driven_cavity():
+    """Lid-driven cavity: full parity at 32^3 (300 steps), AA == A-B, mass conservation."""
+    n = 32
+    flags = wl.cavity_flags(n, n, n)
+    case = Case(n, n, n, 0.6, oracle.equilibrium_field(*wl.uniform_fields(n ** 3)), flags=flags,
+                wall=(0.05, 0.0, 0.0))
+    fo, Fo = case.run_oracle(300, want_force=True)
+    fa, Fa = case.run_gpu(300, "stream", "AA", want_force=True)
+    fb, Fb = case.run_gpu(300, "stream", "AB", want_force=True)
+    assert max_fluid_diff(case, fa, fo) <= TOL_F
+    assert max_fluid_diff(case, fb, fo) <= TOL_F
+    assert np.abs(Fa - Fo).max() <= 1e-4 * max(1.0, np.abs(Fo).max())
+    fl = case.fluid
+    assert abs(fa[:, fl].sum() / case.f0_32[:, fl].astype(np.float64).sum() - 1) < 1e-6
+
+
+@pytest.mark.slow
+def test_lid_driven_cavity_256_windows_and_mass():
+    n, k = 256, 3
+    flags = wl.cavity_flags(n, n, n)
+    r = np.random.default_rng(17).uniform(-1, 1, n ** 3).astype(np.float32)
+    _, w, _ = oracle.tables()
+    f0 = np.empty((19, n ** 3), np.float32)
+    for q in range(19):
+        f0[q] = np.float32(w[q]) * (1 + np.float32(0.01) * np.roll(r, 4099 * q))
+    case = Case(n, n, n, 0.6, f0, flags=flags, wall=(0.05, 0.0, 0.0))
+    fg, _ = case.run_gpu(k, "stream", "AA")
+    # windows away from the non-periodic faces see exactly the full problem's cells
+    for c in [(128, n - 2, 128), (1, n - 2, 1), (n - 2, 1, n - 2), (100, 200, 50), (5, 254, 250)]:
+        sub, ci, _ = window(case, c, k + 1, f0)
+        fo, _ = sub.run_oracle(k)
+        nn = c[0] + n * (c[1] + n * c[2])
+        assert np.abs(fg[:, nn] - fo[:, ci]).max() <= TOL_F, c
+    ctx = case.gpu_context()
+    try:
+        m0 = case.f0_32[:, case.fluid].astype(np.float64).sum()
+        B.lbm_step(ctx, 1000)
+        f = np.zeros((19, case.N), np.float32)
+        B.lbm_get_populations(ctx, f)
+        assert B.lbm_check_finite(ctx)
+    finally:
+        B.lbm_destroy(ctx)
+    assert abs(f[:, case.fluid].astype(np.float64).sum() / m0 - 1) < 1e-5
 
 
 def test_degenerate_grids():
