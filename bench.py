@@ -191,6 +191,18 @@ def whole_job_mlups(cells_per_step: int, steps: int, world: int, max_seconds: fl
     return world * cells_per_step * steps / max_seconds / 1e6
 
 
+def workload_config(n, tau, g, fluid_fraction):
+    """The `config` object of both arms: the porous workload and how it is timed."""
+    N = n ** 3
+    return {"workload": f"porous medium {n}^3, 30% solid in 3^3 blobs (seed 1005), periodic, "
+                        "Guo body force gx=1e-6, tau=0.7, AA in place, stream (SoA) layout",
+            "nx": n, "ny": n, "nz": n, "streaming": "AA", "layout": "stream",
+            "tau": tau, "g": list(g), "fluid_fraction": round(fluid_fraction, 4),
+            "lbm_steps_per_step": 2,
+            "l2": (f"inputs larger than L2 ({19 * 4 * N / 1e9:.1f} GB population buffer vs "
+                   "126 MB L2), no flush")}
+
+
 # ---- the GPU arm ---------------------------------------------------------------------------------------
 
 def make_porous_context(B, torch, n, tau, g, scheme="AA"):
@@ -386,15 +398,8 @@ def run_ours(args):
         "ms_per_step": round(max_s * 1e3 / args.steps, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": f"porous medium {n}^3, 30% solid in 3^3 blobs (seed 1005), "
-                               "periodic, Guo body force gx=1e-6, tau=0.7, AA in place, "
-                               "stream (SoA) layout",
-                   "nx": n, "ny": n, "nz": n, "streaming": "AA", "layout": "stream",
-                   "tau": tau, "g": list(g), "fluid_fraction": round(n_fluid / N, 4),
-                   "lbm_steps_per_step": 2,
-                   "l2": (f"inputs larger than L2 ({19 * 4 * N / 1e9:.1f} GB population "
-                          "buffer vs 126 MB L2), no flush"),
-                   "fluid_mlups": round(value * n_fluid / N, 1)},
+        "config": dict(workload_config(n, tau, g, n_fluid / N),
+                       fluid_mlups=round(value * n_fluid / N, 1)),
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_source": f"{peak_kind} hbm_gbs",
@@ -454,7 +459,9 @@ def run_reference(args):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt * 1e3 / args.steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "porous medium 512^3 (bounded slab sample), CPU oracle"},
+        "config": dict(workload_config(n, 0.7, (1e-6, 0.0, 0.0),
+                                       float((flags == wl.FLUID).mean())),
+                       sample=sample),
         "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": oracle.max_threads(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
