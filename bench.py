@@ -259,10 +259,12 @@ def timed_steps(B, torch, ctx, steps, warmup, per_step=2, profile=True, sampler=
     return ms, launches, prof, clocks
 
 
-def variant(B, torch, n, scheme, steps=10, warmup=3, cavity=False):
+def variant(B, torch, n, scheme, steps=10, warmup=3, cavity=False, fp16=False):
     """Periodic box without solids, g = 0, uniform flow: the clean roofline point.  With
-    cavity=True: a lid-driven cavity (resting walls, lid moving at 0.05 along x), fluid at rest."""
-    ctx = B.lbm_create(n, n, n, 0.6, B.LAYOUT_STREAM,
+    cavity=True: a lid-driven cavity (resting walls, lid moving at 0.05 along x), fluid at rest.
+    With fp16=True the populations are stored in half precision (76 population bytes per update
+    instead of 152; the roofline fraction uses those bytes)."""
+    ctx = B.lbm_create(n, n, n, 0.6, B.LAYOUT_STREAM_FP16 if fp16 else B.LAYOUT_STREAM,
                        B.STREAMING_AA if scheme == "AA" else B.STREAMING_AB)
     try:
         N = n ** 3
@@ -281,15 +283,17 @@ def variant(B, torch, n, scheme, steps=10, warmup=3, cavity=False):
         B.lbm_destroy(ctx)
     mlups = N * 2 * steps / (ms / 1e3) / 1e6
     peak, _ = measured_peaks()
+    per_cell = (POP_BYTES // 2 if fp16 else POP_BYTES) + FLAG_BYTES
     kernels = {}
     for name, (cnt, tot) in prof.items():
         if name == "force_reduce":
             continue
-        gbs = algorithmic_bytes(N) / (tot / cnt / 1e3) / 1e9
+        gbs = N * per_cell / (tot / cnt / 1e3) / 1e9
         kernels[name] = {"ms": round(tot / cnt, 4), "GB/s": round(gbs, 1),
                          "frac": round(gbs / peak, 4)}
     return {"mlups": round(mlups, 1), "ms_per_lbm_step": round(ms / (2 * steps), 4),
-            "frac_of_roofline": round(mlups * 1e6 * (POP_BYTES + FLAG_BYTES) / 1e9 / peak, 4),
+            "bytes_per_update": per_cell,
+            "frac_of_roofline": round(mlups * 1e6 * per_cell / 1e9 / peak, 4),
             "kernels": kernels}
 
 
@@ -421,6 +425,9 @@ def run_ours(args):
         out["variants"] = {f"{s}_{m}^3_periodic": variant(B, torch, m, s)
                            for m in (128, 512) for s in ("AA", "AB")}
         out["variants"]["AA_256^3_lid_driven_cavity"] = variant(B, torch, 256, "AA", cavity=True)
+        for s in ("AA", "AB"):
+            out["variants"][f"{s}_512^3_periodic_fp16_storage"] = variant(B, torch, 512, s,
+                                                                          fp16=True)
     if not args.no_e2e:
         log("[bench] e2e")
         out["e2e"] = e2e_run(B, torch, n, args.steps, flags)

@@ -20,7 +20,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "liblbm.so")
 
 SOURCES = ["lbm_abi.cu", "lbm_common.cu", "lbm_layout_stream.cu", "lbm_layout_bundle.cu",
-           "lbm_layout_collision.cu", "lbm_noalloc.cu"]
+           "lbm_layout_collision.cu", "lbm_layout_stream_fp16.cu", "lbm_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", INCLUDE, "-I", CSRC]

@@ -100,7 +100,7 @@ struct lbm_ctx {
     float g[3] = {0.f, 0.f, 0.f};
     float inlet[4] = {1.f, 0.f, 0.f, 0.f};
     float heq_in[19] = {};
-    float* buf[2] = {nullptr, nullptr};
+    void* buf[2] = {nullptr, nullptr};
     int cur = 0;
     int state = ST_NATURAL;
     uint8_t* types = nullptr;
@@ -146,7 +146,7 @@ struct lbm_ctx {
     std::vector<std::pair<cudaEvent_t, cudaEvent_t>> prof[K_NUM_KINDS];
     std::vector<cudaEvent_t> event_pool;
 
-    Params params(float* A, float* B) const {
+    Params params(void* A, void* B) const {
         Params p;
         p.A = A;
         p.B = B;
@@ -178,8 +178,9 @@ struct lbm_ctx {
         for (int q = 0; q < 19; ++q) p.heq_in[q] = heq_in[q];
         for (int q = 0; q < 19; ++q) {
             const size_t off = plane_offset(q), off_opp = plane_offset(opp(q));
-            p.pa[q] = A ? A + off : nullptr;
-            p.pb[q] = B ? B + off : nullptr;
+            const size_t bytes = off * elem_bytes_of();
+            p.pa[q] = A ? static_cast<char*>(A) + bytes : nullptr;
+            p.pb[q] = B ? static_cast<char*>(B) + bytes : nullptr;
             p.pdiff[q] = (long long)off - (long long)off_opp;
             p.plane32[q] = (uint32_t)off;  // used only while 19 N <= 2^32
         }
@@ -190,13 +191,15 @@ struct lbm_ctx {
         switch (layout) {
             case LBM_LAYOUT_BUNDLE: return idx<LAYOUT_BUNDLE>(q, 0, N);
             case LBM_LAYOUT_COLLISION: return idx<LAYOUT_COLLISION>(q, 0, N);
+            case LBM_LAYOUT_STREAM_FP16: return idx<LAYOUT_STREAM_FP16>(q, 0, N);
             default: return idx<LAYOUT_STREAM>(q, 0, N);
         }
     }
     bool body() const { return g[0] != 0.f || g[1] != 0.f || g[2] != 0.f; }
     bool any_open() const { return face[0] == LBM_OPEN || face[1] == LBM_OPEN || face[2] == LBM_OPEN; }
     // buffer holding the current state and its meaning
-    float* state_buffer() const { return streaming == LBM_STREAMING_AA ? buf[0] : buf[cur]; }
+    void* state_buffer() const { return streaming == LBM_STREAMING_AA ? buf[0] : buf[cur]; }
+    size_t elem_bytes_of() const { return layout == LBM_LAYOUT_STREAM_FP16 ? 2 : 4; }
 
     cudaEvent_t take_event() {
         cudaEvent_t e = nullptr;
@@ -250,6 +253,7 @@ const LayoutOps* ops_for(int layout) {
         case LBM_LAYOUT_STREAM: return &layout_ops_stream();
         case LBM_LAYOUT_BUNDLE: return &layout_ops_bundle();
         case LBM_LAYOUT_COLLISION: return &layout_ops_collision();
+        case LBM_LAYOUT_STREAM_FP16: return &layout_ops_stream_fp16();
     }
     return nullptr;
 }
@@ -541,7 +545,7 @@ lbm_ctx* lbm_create(int nx, int ny, int nz, float tau, int layout, int streaming
         return nullptr;
     };
     cudaError_t e;
-    const size_t pop_bytes = 19 * N * sizeof(float);
+    const size_t pop_bytes = 19 * N * c->elem_bytes_of();
     if ((e = cudaMalloc(&c->buf[0], pop_bytes)) != cudaSuccess) return bad(e, "lbm_create: population buffer");
     if (c->streaming != LBM_STREAMING_AA &&
         (e = cudaMalloc(&c->buf[1], pop_bytes)) != cudaSuccess)
@@ -684,7 +688,7 @@ static void reset_state(lbm_ctx* c) {
 
 int lbm_set_populations(lbm_ctx* c, const float* f) {
     if (!c || !f) return fail(LBM_EINVAL, "lbm_set_populations: NULL argument");
-    float* dst = c->state_buffer();
+    void* dst = c->state_buffer();
     const Params p = c->params(dst, dst);
     const size_t total = 19 * c->N;
     if (is_device_pointer(f)) {
@@ -706,7 +710,7 @@ int lbm_set_populations(lbm_ctx* c, const float* f) {
 
 int lbm_set_equilibrium(lbm_ctx* c, const float* rho, const float* u) {
     if (!c || !rho || !u) return fail(LBM_EINVAL, "lbm_set_equilibrium: NULL argument");
-    float* dst = c->state_buffer();
+    void* dst = c->state_buffer();
     const Params p = c->params(dst, dst);
     const size_t N = c->N;
     if (is_device_pointer(rho) && is_device_pointer(u)) {
@@ -734,7 +738,7 @@ int lbm_set_equilibrium(lbm_ctx* c, const float* rho, const float* u) {
 
 int lbm_get_populations(lbm_ctx* c, float* f) {
     if (!c || !f) return fail(LBM_EINVAL, "lbm_get_populations: NULL argument");
-    float* src = c->state_buffer();
+    void* src = c->state_buffer();
     const Params p = c->params(src, src);
     const size_t total = 19 * c->N;
     if (is_device_pointer(f)) {
@@ -775,7 +779,7 @@ int lbm_step(lbm_ctx* c, int n) {
 
 int lbm_macroscopic(lbm_ctx* c, float* rho, float* u) {
     if (!c || !rho || !u) return fail(LBM_EINVAL, "lbm_macroscopic: NULL argument");
-    float* src = c->state_buffer();
+    void* src = c->state_buffer();
     const Params p = c->params(src, src);
     const size_t N = c->N;
     if (is_device_pointer(rho) && is_device_pointer(u)) {
@@ -813,7 +817,7 @@ int lbm_force_momentum_exchange(lbm_ctx* c, double F[3]) {
 
 int lbm_check_finite(lbm_ctx* c) {
     if (!c) return fail(LBM_EINVAL, "lbm_check_finite: NULL context");
-    float* src = c->state_buffer();
+    void* src = c->state_buffer();
     LBM_CUDA(cudaMemsetAsync(c->err_dev, 0, sizeof(int), c->stream), "lbm_check_finite");
     LBM_CUDA(c->ops->check_finite(c->params(src, src), c->err_dev, c->grid, c->block, c->stream),
              "lbm_check_finite");

@@ -8,11 +8,16 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 namespace lbm {
 
-enum : int { LAYOUT_STREAM = 0, LAYOUT_BUNDLE = 1, LAYOUT_COLLISION = 2 };
+// LAYOUT_STREAM_FP16: the stream layout with the shifted populations stored as IEEE half
+// precision (arithmetic stays fp32); half the bytes per cell update.
+enum : int { LAYOUT_STREAM = 0, LAYOUT_BUNDLE = 1, LAYOUT_COLLISION = 2, LAYOUT_STREAM_FP16 = 3 };
+__host__ __device__ constexpr bool is_soa(int L) { return L == LAYOUT_STREAM || L == LAYOUT_STREAM_FP16; }
+__host__ __device__ constexpr size_t elem_bytes(int L) { return L == LAYOUT_STREAM_FP16 ? 2 : 4; }
 
 // internal flag byte: bits 0-1 cell type; for FLUID cells
 //  bit 6 "special": a neighbour x + c_q is INLET or MOVING_WALL or lies beyond an OPEN face -- the
@@ -64,7 +69,7 @@ __host__ __device__ constexpr int bundle_j(int q) { return bundle_size(q) == 3 ?
 // Element offset of population q of cell n.
 template <int L, typename I = size_t>
 __host__ __device__ __forceinline__ I idx(int q, uint32_t n, I N) {
-    if (L == LAYOUT_STREAM) return (I)q * N + (I)n;
+    if (is_soa(L)) return (I)q * N + (I)n;
     if (L == LAYOUT_COLLISION) return (I)n * (I)19 + (I)q;
     return (I)bundle_off(q) * N + (I)n * (I)bundle_size(q) + (I)bundle_j(q);
 }
@@ -72,12 +77,24 @@ __host__ __device__ __forceinline__ I idx(int q, uint32_t n, I N) {
 // plane(q) = idx(q, 0); opposite populations share their stride.
 template <int L>
 __host__ __device__ constexpr int cell_stride(int q) {
-    return L == LAYOUT_STREAM ? 1 : L == LAYOUT_COLLISION ? 19 : bundle_size(q);
+    return is_soa(L) ? 1 : L == LAYOUT_COLLISION ? 19 : bundle_size(q);
+}
+
+// Population storage access: element `off` of a buffer of layout L, as fp32.
+template <int L, typename Off>
+__device__ __forceinline__ float ld(const void* base, Off off) {
+    if constexpr (L == LAYOUT_STREAM_FP16) return __half2float(static_cast<const __half*>(base)[off]);
+    else return static_cast<const float*>(base)[off];
+}
+template <int L, typename Off>
+__device__ __forceinline__ void st(void* base, Off off, float v) {
+    if constexpr (L == LAYOUT_STREAM_FP16) static_cast<__half*>(base)[off] = __float2half_rn(v);
+    else static_cast<float*>(base)[off] = v;
 }
 // runtime-q variant (off the hot path)
 template <int L>
 __host__ __device__ __forceinline__ size_t idx_rt(int q, uint32_t n, size_t N) {
-    if (L == LAYOUT_STREAM) return (size_t)q * N + n;
+    if (is_soa(L)) return (size_t)q * N + n;
     if (L == LAYOUT_COLLISION) return (size_t)n * 19u + (size_t)q;
     int s = 0, o = 0, j = 0;
     switch (q) {
@@ -93,8 +110,8 @@ __host__ __device__ __forceinline__ size_t idx_rt(int q, uint32_t n, size_t N) {
 
 // ---- kernel parameters (passed by value) ---------------------------------------------------------
 struct Params {
-    float* A;              // buffer read (AA: the only buffer; A-B: source)
-    float* B;              // A-B destination (may equal A for the in-place collision)
+    void* A;               // buffer read (AA: the only buffer; A-B: source)
+    void* B;               // A-B destination (may equal A for the in-place collision)
     const uint8_t* flags;  // internal flag bytes
     const uint32_t* mask;  // per-cell solid-link mask (0 for bulk cells)
     int any_solid_link;    // some FLUID cell has a SOLID neighbour (else every mask is 0)
@@ -117,8 +134,8 @@ struct Params {
     float wterm[19];       // 6 w_q (c_q . u_w): the moving-wall term of a population q leaving the wall
     // hot-path addressing: population q of cell n is pa[q][n * cell_stride(q)] in A and
     // pb[q][n * cell_stride(q)] in B; pdiff[q] = pa[q] - pa[opposite(q)] in elements
-    float* pa[19];
-    float* pb[19];
+    void* pa[19];
+    void* pb[19];
     long long pdiff[19];
     // compact addressing while every element offset fits in 32 bits (19 N <= 2^32): population q
     // of cell n is A[plane32[q] + n * cell_stride(q)] (one base, one 32-bit offset per access)

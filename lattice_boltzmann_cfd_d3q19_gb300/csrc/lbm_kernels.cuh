@@ -159,13 +159,13 @@ __global__ void __launch_bounds__(256) k_aa_even(Params p) {
         if ((fl & TYPE_MASK) == T_FLUID) {
             float h[19];
 #pragma unroll
-            for (int q = 0; q < 19; ++q) h[q] = p.pa[q][cell_off<L, I>(q, c.n)];
+            for (int q = 0; q < 19; ++q) h[q] = ld<L>(p.pa[q], cell_off<L, I>(q, c.n));
             collide<BODY>(h, p);
             // store addresses formed after the collision, not kept from the loads
             uint32_t ns = c.n;
             asm volatile("" : "+r"(ns) : "f"(h[0]), "f"(h[18]));
 #pragma unroll
-            for (int q = 0; q < 19; ++q) p.pa[opp(q)][cell_off<L, I>(q, ns)] = h[q];
+            for (int q = 0; q < 19; ++q) st<L>(p.pa[opp(q)], cell_off<L, I>(q, ns), h[q]);
             if (FORCE && !(fl & F_BULK)) {
                 mask_forces(p.mask[c.n], h, fx, fy, fz);
                 if (p.any_moving && (fl & F_SPECIAL)) moving_forces(p, h, c.x, c.y, c.z, fx, fy, fz);
@@ -194,11 +194,11 @@ __device__ __forceinline__ void aa_odd_load(const Params& p, const Nbr& nb, uint
         // own slot (q, x); neighbour slot (opp q, x - c_q)
         const uint32_t own = p.plane32[Q] + n * S;
         const uint32_t far = p.plane32[opp(Q)] + nb.template at<Q, -1>(n) * S;
-        h[Q] = p.A[solid_link<opp(Q)>(m) ? own : far];
+        h[Q] = ld<L>(p.A, solid_link<opp(Q)>(m) ? own : far);
     } else {
         const I own = (I)p.pdiff[Q] + cell_off<L, I>(Q, n);
         const I far = cell_off<L, I>(Q, nb.template at<Q, -1>(n));
-        h[Q] = p.pa[opp(Q)][solid_link<opp(Q)>(m) ? own : far];
+        h[Q] = ld<L>(p.pa[opp(Q)], solid_link<opp(Q)>(m) ? own : far);
     }
     if constexpr (Q < 18) aa_odd_load<L, I, Q + 1>(p, nb, n, m, h);
 }
@@ -214,11 +214,11 @@ __device__ __forceinline__ void aa_odd_store(const Params& p, const Nbr& nb, uin
     if constexpr (std::is_same<I, uint32_t>::value) {
         const uint32_t own = p.plane32[opp(Q)] + n * S;
         const uint32_t far = p.plane32[Q] + nb.template at<Q, 1>(n) * S;
-        p.A[bounce ? own : far] = h[Q];
+        st<L>(p.A, bounce ? own : far, h[Q]);
     } else {
         const I own = cell_off<L, I>(Q, n) - (I)p.pdiff[Q];
         const I far = cell_off<L, I>(Q, nb.template at<Q, 1>(n));
-        p.pa[Q][bounce ? own : far] = h[Q];
+        st<L>(p.pa[Q], bounce ? own : far, h[Q]);
     }
     if (FORCE && Q > 0 && bounce) accumulate_force<Q>(h[Q], fx, fy, fz);
     if constexpr (Q < 18) aa_odd_store<L, I, FORCE, Q + 1>(p, nb, n, m, h, fx, fy, fz);
@@ -256,11 +256,11 @@ template <int L, int Q>
 __device__ __forceinline__ float aa_odd_gather(const Params& p, uint32_t n, int x, int y, int z) {
     const Link s = link_cell(p, x, y, z, -cx(Q), -cy(Q), -cz(Q));
     const int t = p.flags[s.cell] & TYPE_MASK;
-    if (t == T_SOLID) return p.A[idx<L>(Q, n, p.N)];           // f*_opp(q)(x) sits at (q, x)
-    if (t == T_MOVING) return p.A[idx<L>(Q, n, p.N)] + p.wterm[Q];
+    if (t == T_SOLID) return ld<L>(p.A, idx<L>(Q, n, p.N));           // f*_opp(q)(x) sits at (q, x)
+    if (t == T_MOVING) return ld<L>(p.A, idx<L>(Q, n, p.N)) + p.wterm[Q];
     if (t == T_INLET) return p.heq_in[Q];
     if (s.face >= 0) return p.scratch[scratch_slot(p, s.face, Q, x, y, z)];
-    return p.A[idx<L>(opp(Q), s.cell, p.N)];
+    return ld<L>(p.A, idx<L>(opp(Q), s.cell, p.N));
 }
 
 template <int L, int Q>
@@ -289,7 +289,7 @@ __device__ __forceinline__ void aa_odd_face_copies(const Params& p, float v, int
         }
         if (!valid) continue;
         const uint32_t rc = (uint32_t)r[0] + (uint32_t)p.nx * ((uint32_t)r[1] + (uint32_t)p.ny * r[2]);
-        if ((p.flags[rc] & TYPE_MASK) == T_FLUID) p.A[idx<L>(Q, rc, p.N)] = v;
+        if ((p.flags[rc] & TYPE_MASK) == T_FLUID) st<L>(p.A, idx<L>(Q, rc, p.N), v);
     }
 }
 
@@ -299,13 +299,13 @@ __device__ __forceinline__ void aa_odd_scatter(const Params& p, float v, uint32_
     const Link d = link_cell(p, x, y, z, cx(Q), cy(Q), cz(Q));
     const int t = p.flags[d.cell] & TYPE_MASK;
     if (t == T_SOLID) {
-        p.A[idx<L>(opp(Q), n, p.N)] = v;                          // bounces back into x
+        st<L>(p.A, idx<L>(opp(Q), n, p.N), v);                          // bounces back into x
     } else if (t == T_MOVING) {
-        p.A[idx<L>(opp(Q), n, p.N)] = v + p.wterm[opp(Q)];         // off the moving wall
+        st<L>(p.A, idx<L>(opp(Q), n, p.N), v + p.wterm[opp(Q)]);         // off the moving wall
     } else if (t == T_INLET) {
-        p.A[idx<L>(opp(Q), n, p.N)] = p.heq_in[opp(Q)];            // the reservoir feeds x
+        st<L>(p.A, idx<L>(opp(Q), n, p.N), p.heq_in[opp(Q)]);            // the reservoir feeds x
     } else if (d.face < 0) {
-        p.A[idx<L>(Q, d.cell, p.N)] = v;
+        st<L>(p.A, idx<L>(Q, d.cell, p.N), v);
     }
     if (p.open[0] | p.open[1] | p.open[2]) aa_odd_face_copies<L, Q>(p, v, x, y, z);
 }
@@ -361,7 +361,7 @@ __global__ void __launch_bounds__(256) k_pregather(Params p, int axis, int side)
     const Link s = link_cell(p, x, y, z, -cx(q), -cy(q), -cz(q));
     if (s.face != 2 * axis + side) return;
     if ((p.flags[s.cell] & TYPE_MASK) != T_FLUID) return;
-    p.scratch[p.face_base[axis][side] + (size_t)q * area + pos] = p.A[idx_rt<L>(opp(q), s.cell, p.N)];
+    p.scratch[p.face_base[axis][side] + (size_t)q * area + pos] = ld<L>(p.A, idx_rt<L>(opp(q), s.cell, p.N));
 }
 
 // ============================== two buffers (A-B) ===============================================
@@ -376,11 +376,11 @@ __device__ __forceinline__ void ab_load(const Params& p, const Nbr& nb, uint32_t
     if constexpr (std::is_same<I, uint32_t>::value) {
         const uint32_t own = p.plane32[opp(Q)] + n * S;
         const uint32_t far = p.plane32[Q] + nb.template at<Q, -1>(n) * S;
-        h[Q] = p.A[solid_link<opp(Q)>(m) ? own : far];
+        h[Q] = ld<L>(p.A, solid_link<opp(Q)>(m) ? own : far);
     } else {
         const I own = cell_off<L, I>(Q, n) - (I)p.pdiff[Q];
         const I far = cell_off<L, I>(Q, nb.template at<Q, -1>(n));
-        h[Q] = p.pa[Q][solid_link<opp(Q)>(m) ? own : far];
+        h[Q] = ld<L>(p.pa[Q], solid_link<opp(Q)>(m) ? own : far);
     }
     if constexpr (Q < 18) ab_load<L, I, Q + 1>(p, nb, n, m, h);
 }
@@ -391,10 +391,10 @@ __device__ __forceinline__ void ab_gather_all(const Params& p, float (&h)[19], u
                                               int y, int z) {
     const Link s = link_cell(p, x, y, z, -cx(Q), -cy(Q), -cz(Q));
     const int t = p.flags[s.cell] & TYPE_MASK;
-    if (t == T_SOLID) h[Q] = p.A[idx<L>(opp(Q), n, p.N)];
-    else if (t == T_MOVING) h[Q] = p.A[idx<L>(opp(Q), n, p.N)] + p.wterm[Q];
+    if (t == T_SOLID) h[Q] = ld<L>(p.A, idx<L>(opp(Q), n, p.N));
+    else if (t == T_MOVING) h[Q] = ld<L>(p.A, idx<L>(opp(Q), n, p.N)) + p.wterm[Q];
     else if (t == T_INLET) h[Q] = p.heq_in[Q];
-    else h[Q] = p.A[idx<L>(Q, s.cell, p.N)];
+    else h[Q] = ld<L>(p.A, idx<L>(Q, s.cell, p.N));
     if constexpr (Q < 18) ab_gather_all<L, Q + 1>(p, h, n, x, y, z);
 }
 
@@ -416,7 +416,7 @@ __global__ void __launch_bounds__(256, 6) k_ab(Params p) {
             float h[19];
             if (FROM_NATURAL) {
 #pragma unroll
-                for (int q = 0; q < 19; ++q) h[q] = p.pa[q][cell_off<L, I>(q, c.n)];
+                for (int q = 0; q < 19; ++q) h[q] = ld<L>(p.pa[q], cell_off<L, I>(q, c.n));
             } else {
                 const Nbr nb(p, c.x, c.y, c.z);
                 ab_load<L, I>(p, nb, c.n, m, h);
@@ -425,7 +425,7 @@ __global__ void __launch_bounds__(256, 6) k_ab(Params p) {
             uint32_t ns = c.n;
             asm volatile("" : "+r"(ns) : "f"(h[0]), "f"(h[18]));
 #pragma unroll
-            for (int q = 0; q < 19; ++q) p.pb[q][cell_off<L, I>(q, ns)] = h[q];
+            for (int q = 0; q < 19; ++q) st<L>(p.pb[q], cell_off<L, I>(q, ns), h[q]);
             if (FORCE && m) mask_forces(m, h, fx, fy, fz);
             if (FORCE && FROM_NATURAL && p.any_moving && (fl & F_SPECIAL))
                 moving_forces(p, h, c.x, c.y, c.z, fx, fy, fz);
@@ -433,7 +433,7 @@ __global__ void __launch_bounds__(256, 6) k_ab(Params p) {
             // SOLID and INLET slots are never read; writing them keeps every 32-byte sector of
             // the destination fully written (no fill from DRAM for partly written sectors)
 #pragma unroll
-            for (int q = 0; q < 19; ++q) p.pb[q][cell_off<L, I>(q, c.n)] = 0.0f;
+            for (int q = 0; q < 19; ++q) st<L>(p.pb[q], cell_off<L, I>(q, c.n), 0.0f);
         }
     }
     if (FORCE) warp_force(fx, fy, fz, p.partial);
@@ -448,7 +448,7 @@ __global__ void __launch_bounds__(256) k_ab_special(Params p) {
         ab_gather_all<L>(p, h, c.n, c.x, c.y, c.z);
         collide<BODY>(h, p);
 #pragma unroll
-        for (int q = 0; q < 19; ++q) p.B[idx<L>(q, c.n, p.N)] = h[q];
+        for (int q = 0; q < 19; ++q) st<L>(p.B, idx<L>(q, c.n, p.N), h[q]);
         if (FORCE) {
             mask_forces(p.mask[c.n], h, fx, fy, fz);
             if (p.any_moving) moving_forces(p, h, c.x, c.y, c.z, fx, fy, fz);
@@ -468,7 +468,7 @@ __global__ void __launch_bounds__(256) k_stream(Params p) {
     if ((fl & TYPE_MASK) != T_FLUID) {
         // never-read SOLID / INLET slots written to keep the destination's sectors whole
 #pragma unroll
-        for (int q = 0; q < 19; ++q) p.pb[q][cell_off<L, I>(q, c.n)] = 0.0f;
+        for (int q = 0; q < 19; ++q) st<L>(p.pb[q], cell_off<L, I>(q, c.n), 0.0f);
         return;
     }
     if (fl & F_SPECIAL) return;
@@ -476,7 +476,7 @@ __global__ void __launch_bounds__(256) k_stream(Params p) {
     float h[19];
     ab_load<L, I>(p, nb, c.n, m, h);
 #pragma unroll
-    for (int q = 0; q < 19; ++q) p.pb[q][cell_off<L, I>(q, c.n)] = h[q];
+    for (int q = 0; q < 19; ++q) st<L>(p.pb[q], cell_off<L, I>(q, c.n), h[q]);
 }
 
 template <int L>
@@ -486,7 +486,7 @@ __global__ void __launch_bounds__(256) k_stream_special(Params p) {
     float h[19];
     ab_gather_all<L>(p, h, c.n, c.x, c.y, c.z);
 #pragma unroll
-    for (int q = 0; q < 19; ++q) p.B[idx<L>(q, c.n, p.N)] = h[q];
+    for (int q = 0; q < 19; ++q) st<L>(p.B, idx<L>(q, c.n, p.N), h[q]);
 }
 
 // ============================== state access off the step path ==================================
@@ -494,17 +494,17 @@ __global__ void __launch_bounds__(256) k_stream_special(Params p) {
 template <int L>
 __device__ __forceinline__ float natural_h(const Params& p, int state, int q, uint32_t n, int x,
                                            int y, int z) {
-    if (state == ST_NATURAL) return p.A[idx_rt<L>(q, n, p.N)];
+    if (state == ST_NATURAL) return ld<L>(p.A, idx_rt<L>(q, n, p.N));
     const Link s = link_cell(p, x, y, z, -cx(q), -cy(q), -cz(q));
     const int t = p.flags[s.cell] & TYPE_MASK;
     if (t == T_INLET) return p.heq_in[q];
     const float wall = t == T_MOVING ? p.wterm[q] : 0.0f;
     if (state == ST_POST_AA) {
-        if (t == T_SOLID || t == T_MOVING) return p.A[idx_rt<L>(q, n, p.N)] + wall;
-        return p.A[idx_rt<L>(opp(q), s.cell, p.N)];
+        if (t == T_SOLID || t == T_MOVING) return ld<L>(p.A, idx_rt<L>(q, n, p.N)) + wall;
+        return ld<L>(p.A, idx_rt<L>(opp(q), s.cell, p.N));
     }
-    if (t == T_SOLID || t == T_MOVING) return p.A[idx_rt<L>(opp(q), n, p.N)] + wall;
-    return p.A[idx_rt<L>(q, s.cell, p.N)];
+    if (t == T_SOLID || t == T_MOVING) return ld<L>(p.A, idx_rt<L>(opp(q), n, p.N)) + wall;
+    return ld<L>(p.A, idx_rt<L>(q, s.cell, p.N));
 }
 
 // Canonical absolute f[q*N + n] for flat indices [i0, i0 + count) into out[0, count).
@@ -535,7 +535,7 @@ __global__ void __launch_bounds__(256) k_pack(Params p, const float* in, size_t 
     const size_t i = i0 + k;
     const int q = (int)(i / p.N);
     const uint32_t n = (uint32_t)(i - (size_t)q * p.N);
-    p.A[idx_rt<L>(q, n, p.N)] = in[k] - wq(q);
+    st<L>(p.A, idx_rt<L>(q, n, p.N), in[k] - wq(q));
 }
 
 // Natural shifted state f_eq(rho, u) - w for cells [n0, n0 + count).
@@ -553,7 +553,7 @@ __global__ void __launch_bounds__(256) k_equilibrium(Params p, const float* rho,
     for (int q = 0; q < 19; ++q) {
         const float cu = (float)cx(q) * ux + (float)cy(q) * uy + (float)cz(q) * uz;
         const float poly = fmaf(cu, fmaf(4.5f, cu, 3.0f), -uu15);
-        p.A[idx<L>(q, n, p.N)] = wq(q) * fmaf(r, poly, drho);
+        st<L>(p.A, idx<L>(q, n, p.N), wq(q) * fmaf(r, poly, drho));
     }
 }
 
@@ -599,7 +599,7 @@ __global__ void __launch_bounds__(256) k_check_finite(Params p, int* bad) {
     if ((p.flags[n] & TYPE_MASK) != T_FLUID) return;
     bool ok = true;
 #pragma unroll
-    for (int q = 0; q < 19; ++q) ok &= isfinite(p.A[idx<L>(q, n, p.N)]);
+    for (int q = 0; q < 19; ++q) ok &= isfinite(ld<L>(p.A, idx<L>(q, n, p.N)));
     if (!ok) *bad = 1;
 }
 

@@ -43,6 +43,7 @@ struct LayoutOps {
 const LayoutOps& layout_ops_stream();
 const LayoutOps& layout_ops_bundle();
 const LayoutOps& layout_ops_collision();
+const LayoutOps& layout_ops_stream_fp16();
 
 // layout-independent kernels
 cudaError_t launch_validate_types(const uint8_t* types, size_t N, int* bad, cudaStream_t s);

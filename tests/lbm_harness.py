@@ -12,6 +12,20 @@ from lattice_boltzmann_cfd_d3q19_gb300 import workloads as wl
 TOL_F = 1e-5
 
 LAYOUTS = {"stream": B.LAYOUT_STREAM, "bundle": B.LAYOUT_BUNDLE, "collision": B.LAYOUT_COLLISION}
+# half-precision storage of the stream layout (its own tolerance, see fp16_tolerance)
+FP16 = {"stream_fp16": B.LAYOUT_STREAM_FP16}
+
+
+def fp16_tolerance(f0, steps, w=None):
+    """Bound on |f_fp16 - f_fp32| after `steps` steps: every stored population is rounded to 11
+    significant bits (relative error <= 2^-11) once when loaded and once per step; the collision
+    mixes populations with weights of at most ~1, so the errors add at most linearly.  Twice that
+    bound, on the largest shifted population |f - w| of the initial state."""
+    import oracle
+    if w is None:
+        _, w, _ = oracle.tables()
+    H = float(np.abs(np.asarray(f0, np.float64).reshape(19, -1) - w[:, None]).max())
+    return 2.0 * (steps + 1) * H * 2.0 ** -11
 SCHEMES = {"AA": B.STREAMING_AA, "AB": B.STREAMING_AB, "AB2": B.STREAMING_AB2}
 
 
@@ -49,7 +63,8 @@ class Case:
 
     def gpu_context(self, layout="stream", scheme="AA", device_input=True):
         import torch
-        ctx = B.lbm_create(self.nx, self.ny, self.nz, self.tau, LAYOUTS[layout], SCHEMES[scheme])
+        ctx = B.lbm_create(self.nx, self.ny, self.nz, self.tau, {**LAYOUTS, **FP16}[layout],
+                           SCHEMES[scheme])
         try:
             B.lbm_set_flags(ctx, self.flags)
             B.lbm_set_faces(ctx, *self.faces)

@@ -47,7 +47,7 @@ def test_library_symbols_with_nm():
     ((4, 4, 4, 0.5, 0, 0), "tau"),
     ((4, 4, 4, float("nan"), 0, 0), "tau"),
     ((4, 4, 4, float("inf"), 0, 0), "tau"),
-    ((4, 4, 4, 0.6, 3, 0), "layout"),
+    ((4, 4, 4, 0.6, 4, 0), "layout"),
     ((4, 4, 4, 0.6, 0, 4), "streaming"),
     ((4, 70000, 4, 0.6, 0, 0), "65535"),
     ((2048, 2048, 1024, 0.6, 0, 0), "2^31"),

@@ -570,3 +570,31 @@ def test_graph_replay_equals_direct_launches(scheme):
     assert np.array_equal(out[0][0], out[1][0])
     for a, b in zip(out[0][1], out[1][1]):
         assert np.array_equal(a, b)
+
+
+# ---- half-precision storage (LBM_LAYOUT_STREAM_FP16) ---------------------------------------------
+
+from lbm_harness import fp16_tolerance  # noqa: E402
+
+
+@pytest.mark.parametrize("scheme", ["AA", "AB", "AB2"])
+@pytest.mark.parametrize("ci", range(len(SMALL)))
+def test_fp16_storage_equals_fp32_within_rounding(ci, scheme):
+    """Same kernels, populations stored in half precision: equal to the fp32 layout within the
+    fp16 rounding bound (an indexing error would show as O(1e-2) differences)."""
+    nx, ny, nz, faces, solid, inlet = SMALL[ci]
+    case = mixed_case(nx, ny, nz, faces, 300 + ci, solid=solid, inlet_layer=inlet)
+    for steps in (1, 4, 7):
+        f32, F32 = case.run_gpu(steps, "stream", scheme, want_force=True)
+        f16, F16 = case.run_gpu(steps, "stream_fp16", scheme, want_force=True)
+        tol = fp16_tolerance(case.f0_32, steps)
+        assert max_fluid_diff(case, f16, f32) <= tol, (steps, max_fluid_diff(case, f16, f32), tol)
+
+
+def test_fp16_taylor_green_against_oracle():
+    rho, u = wl.taylor_green(32, 32, 32, 0.02, noise=1e-4, seed=wl.SEED_TG32)
+    case = Case(32, 32, 32, 0.6, oracle.equilibrium_field(rho, u))
+    fo, _ = case.run_oracle(100)
+    for scheme in ("AA", "AB"):
+        fg, _ = case.run_gpu(100, "stream_fp16", scheme)
+        assert max_fluid_diff(case, fg, fo) <= fp16_tolerance(case.f0_32, 100)
