@@ -39,6 +39,7 @@ SIGNATURES = {
     "lbm_get_populations": (_I, [_P, _P]),
     "lbm_step": (_I, [_P, _I]),
     "lbm_set_graph_launch": (_I, [_P, _I]),
+    "lbm_set_cell_pairs": (_I, [_P, _I]),
     "lbm_macroscopic": (_I, [_P, _P, _P]),
     "lbm_force_momentum_exchange": (_I, [_P, _P]),
     "lbm_check_finite": (_I, [_P]),
@@ -176,6 +177,14 @@ def lbm_step(ctx: int, n: int) -> None:
 
 def lbm_set_graph_launch(ctx: int, enable: bool) -> None:
     _check(load().lbm_set_graph_launch(ctx, 1 if enable else 0))
+
+
+def lbm_set_cell_pairs(ctx: int, enable: bool) -> bool:
+    """Allow or forbid the two-cell step kernels; True when they will run."""
+    rc = load().lbm_set_cell_pairs(ctx, 1 if enable else 0)
+    if rc < 0:
+        raise LbmError(rc, _err())
+    return rc == 1
 
 
 def lbm_macroscopic(ctx: int, rho, u) -> None:

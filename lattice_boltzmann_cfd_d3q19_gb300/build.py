@@ -22,7 +22,9 @@ LIB = os.path.join(PKG, "liblbm.so")
 SOURCES = ["lbm_abi.cu", "lbm_common.cu", "lbm_layout_stream.cu", "lbm_layout_bundle.cu",
            "lbm_layout_collision.cu", "lbm_layout_stream_fp16.cu", "lbm_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
+# -fmad=false: no multiply-add is fused unless the source asks for it (the kernels spell out
+# their fused multiply-adds, so the one-cell and two-cell forms round identically)
+FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-fmad=false", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", INCLUDE, "-I", CSRC]
 
 

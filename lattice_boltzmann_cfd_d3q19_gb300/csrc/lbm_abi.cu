@@ -117,6 +117,10 @@ struct lbm_ctx {
     double* partial = nullptr;    // nblocks main-kernel partials, then the boundary kernels'
     size_t partial_cap = 0;       // triples allocated
     size_t nblocks = 0;
+    // two-cell kernels: launch geometry over cell pairs, and whether the caller allows them
+    dim3 grid2, block2;
+    size_t nblocks2 = 0;
+    bool pairs_allowed = true;
     size_t force_triples = 0;     // partial triples written by the step that computes the force
     double* stage = nullptr;
     double* force_dev = nullptr;
@@ -164,7 +168,7 @@ struct lbm_ctx {
         p.n_special = n_special;
         p.scratch = scratch;
         p.partial = partial;
-        p.part_special = nblocks * kWarpsPerBlock;
+        p.part_special = main_blocks() * kWarpsPerBlock;
         p.nx = n[0];
         p.ny = n[1];
         p.nz = n[2];
@@ -195,6 +199,12 @@ struct lbm_ctx {
             default: return idx<LAYOUT_STREAM>(q, 0, N);
         }
     }
+    // the hot step kernels run two cells per thread: stream layouts, even nx, 32-bit offsets
+    bool pairs() const {
+        return pairs_allowed && is_soa(layout) && n[0] % 2 == 0 && 19 * N <= (size_t(1) << 32);
+    }
+    // blocks of the step kernels that write force partials
+    size_t main_blocks() const { return pairs() ? nblocks2 : nblocks; }
     bool body() const { return g[0] != 0.f || g[1] != 0.f || g[2] != 0.f; }
     bool any_open() const { return face[0] == LBM_OPEN || face[1] == LBM_OPEN || face[2] == LBM_OPEN; }
     // buffer holding the current state and its meaning
@@ -307,7 +317,7 @@ int classify(lbm_ctx* c) {
             return cuda_fail(e, "classify: special-cell list");
         }
     }
-    const size_t need = partial_triples(c->nblocks, count);
+    const size_t need = partial_triples(std::max(c->nblocks, c->nblocks2), count);
     if (need > c->partial_cap) {
         double* np_ = nullptr;
         cudaError_t e = cudaMalloc(&np_, 3 * need * sizeof(double));
@@ -351,11 +361,13 @@ int launch_kind(lbm_ctx* c, int kind, const Params& p, bool force, int main_kind
     } else if (kind == K_BOUNDARY) {
         e = c->ops->special(main_kind, p, force, c->body(), c->stream);
         ++c->launches;
-        if (force) c->force_triples = partial_triples(c->nblocks, c->n_special);
+        if (force) c->force_triples = partial_triples(c->main_blocks(), c->n_special);
     } else {
-        e = c->ops->cells(kind, p, force, c->body(), c->grid, c->block, c->stream);
+        const bool two = c->pairs() && kind != K_STREAM;
+        e = two ? c->ops->cells2(kind, p, force, c->body(), c->grid2, c->block2, c->stream)
+                : c->ops->cells(kind, p, force, c->body(), c->grid, c->block, c->stream);
         ++c->launches;
-        if (force) c->force_triples = partial_triples(c->nblocks, 0);
+        if (force) c->force_triples = partial_triples(c->main_blocks(), 0);
     }
     if (c->profiling && e0 && e1) {
         cudaEventRecord(e1, c->stream);
@@ -537,6 +549,13 @@ lbm_ctx* lbm_create(int nx, int ny, int nz, float tau, int layout, int streaming
     c->grid = dim3((unsigned)((nx + bx - 1) / bx), (unsigned)((ny + c->block.y - 1) / c->block.y),
                    (unsigned)nz);
     c->nblocks = (size_t)c->grid.x * c->grid.y * c->grid.z;
+    const unsigned npairs = (unsigned)((nx + 1) / 2);
+    unsigned bp = 32;
+    while (bp < npairs && bp < 256) bp *= 2;
+    c->block2 = dim3(bp, 256 / bp, 1);
+    c->grid2 = dim3((npairs + bp - 1) / bp, (unsigned)((ny + c->block2.y - 1) / c->block2.y),
+                    (unsigned)nz);
+    c->nblocks2 = (size_t)c->grid2.x * c->grid2.y * c->grid2.z;
 
     auto bad = [&](cudaError_t e, const char* what) {
         cuda_fail(e, what);
@@ -854,6 +873,15 @@ int lbm_profile_read(lbm_ctx* c, int kind, int64_t* launches, double* total_ms) 
     *launches = (int64_t)c->prof[kind].size();
     *total_ms = ms;
     return LBM_OK;
+}
+
+int lbm_set_cell_pairs(lbm_ctx* c, int enable) {
+    if (!c) return fail(LBM_EINVAL, "lbm_set_cell_pairs: NULL context");
+    if (c->pairs_allowed != (enable != 0)) {
+        c->drop_graphs();
+        c->pairs_allowed = enable != 0;
+    }
+    return c->pairs() ? 1 : 0;
 }
 
 int lbm_set_graph_launch(lbm_ctx* c, int enable) {

@@ -161,44 +161,144 @@ __device__ __forceinline__ int clampwrap(int v, int n, int open, bool& beyond) {
 // BGK with the second-order equilibrium (c_s^2 = 1/3) on shifted populations, plus Guo forcing
 // when BODY: u = j/rho + g/2, F = rho g, source (1 - omega/2) w [3 (c - u).F + 9 (c.u)(c.F)].
 // h[] holds h_q on entry and h*_q on exit.
-template <bool BODY>
-__device__ __forceinline__ void collide(float (&h)[19], const Params& p) {
-    float drho = 0.f, jx = 0.f, jy = 0.f, jz = 0.f;
-#pragma unroll
-    for (int q = 0; q < 19; ++q) {
-        drho += h[q];
-        if (cx(q) > 0) jx += h[q]; else if (cx(q) < 0) jx -= h[q];
-        if (cy(q) > 0) jy += h[q]; else if (cy(q) < 0) jy -= h[q];
-        if (cz(q) > 0) jz += h[q]; else if (cz(q) < 0) jz -= h[q];
+//
+// One cell (V = float) or two cells at once (V = float2, packed fp32x2 arithmetic: one
+// instruction updates both cells).  Every operation is an explicit round-to-nearest add, multiply
+// or fused multiply-add in a fixed order, so the two-cell form gives bit for bit the results of
+// the one-cell form.
+struct Arith1 {
+    using V = float;
+    static __device__ __forceinline__ V splat(float s) { return s; }
+    static __device__ __forceinline__ V add(V a, V b) { return __fadd_rn(a, b); }
+    static __device__ __forceinline__ V sub(V a, V b) { return __fsub_rn(a, b); }
+    static __device__ __forceinline__ V mul(V a, V b) { return __fmul_rn(a, b); }
+    static __device__ __forceinline__ V fma(V a, V b, V c) { return __fmaf_rn(a, b, c); }
+    static __device__ __forceinline__ V neg(V a) { return -a; }
+    // correctly rounded reciprocal, kept an opaque value: the compiler may otherwise evaluate a
+    // product by it as a quotient
+    static __device__ __forceinline__ V recip(V a) {
+        float r = __frcp_rn(a);
+        asm("" : "+f"(r));
+        return r;
     }
-    const float rho = 1.0f + drho;
-    const float inv = 1.0f / rho;
-    float ux = jx * inv, uy = jy * inv, uz = jz * inv;
+};
+// Packed fp32x2 operations written as PTX with an explicit .rn rounding: like the scalar
+// __fadd_rn / __fmul_rn they are never contracted into a fused multiply-add.
+struct Arith2 {
+    using V = float2;
+    static __device__ __forceinline__ unsigned long long pk(V a) {
+        unsigned long long r;
+        asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a.x), "f"(a.y));
+        return r;
+    }
+    static __device__ __forceinline__ V up(unsigned long long r) {
+        V a;
+        asm("mov.b64 {%0, %1}, %2;" : "=f"(a.x), "=f"(a.y) : "l"(r));
+        return a;
+    }
+    static __device__ __forceinline__ V splat(float s) { return make_float2(s, s); }
+    static __device__ __forceinline__ V add(V a, V b) {
+        unsigned long long d;
+        asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(pk(a)), "l"(pk(b)));
+        return up(d);
+    }
+    static __device__ __forceinline__ V sub(V a, V b) {
+        unsigned long long d;
+        asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(pk(a)), "l"(pk(b)));
+        return up(d);
+    }
+    static __device__ __forceinline__ V mul(V a, V b) {
+        unsigned long long d;
+        asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(pk(a)), "l"(pk(b)));
+        return up(d);
+    }
+    static __device__ __forceinline__ V fma(V a, V b, V c) {
+        unsigned long long d;
+        asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(pk(a)), "l"(pk(b)), "l"(pk(c)));
+        return up(d);
+    }
+    static __device__ __forceinline__ V neg(V a) { return make_float2(-a.x, -a.y); }
+    static __device__ __forceinline__ V recip(V a) {
+        float rx = __frcp_rn(a.x), ry = __frcp_rn(a.y);
+        asm("" : "+f"(rx), "+f"(ry));
+        return make_float2(rx, ry);
+    }
+};
+
+// sum over the populations whose velocity component along `axis` is `sign`, in q order
+template <typename A, int axis, int sign, int Q = 1, bool FIRST = true>
+__device__ __forceinline__ typename A::V side_sum(const typename A::V (&h)[19], typename A::V acc) {
+    if constexpr (Q > 18) {
+        return acc;
+    } else {
+        constexpr int c = axis == 0 ? cx(Q) : axis == 1 ? cy(Q) : cz(Q);
+        if constexpr (c == sign) {
+            typename A::V next;
+            if constexpr (FIRST) next = h[Q];
+            else next = A::add(acc, h[Q]);
+            return side_sum<A, axis, sign, Q + 1, false>(h, next);
+        } else {
+            return side_sum<A, axis, sign, Q + 1, FIRST>(h, acc);
+        }
+    }
+}
+template <typename A, int axis>
+__device__ __forceinline__ typename A::V momentum(const typename A::V (&h)[19]) {
+    return A::sub(side_sum<A, axis, 1>(h, A::splat(0.f)), side_sum<A, axis, -1>(h, A::splat(0.f)));
+}
+
+template <typename A, bool BODY>
+__device__ __forceinline__ void collide_t(typename A::V (&h)[19], const Params& p) {
+    using V = typename A::V;
+    V drho = h[0];
+#pragma unroll
+    for (int q = 1; q < 19; ++q) drho = A::add(drho, h[q]);
+    const V jx = momentum<A, 0>(h), jy = momentum<A, 1>(h), jz = momentum<A, 2>(h);
+    const V rho = A::add(A::splat(1.0f), drho);
+    const V inv = A::recip(rho);
     // Guo forcing, F = rho g, u = j/rho + g/2, source S_q = (1 - omega/2) d f_eq,q/du . g.
     // Because f_eq is quadratic in u, omega f_eq(u) + (1 - omega/2) d f_eq/du . g equals
     // omega f_eq(u + a g) - omega a^2 w rho (4.5 (c.g)^2 - 1.5 g.g) with a = tau - 1/2 exactly:
     // relax toward the equilibrium at j/rho + tau g and add rho wk_q, wk_q = -omega a^2 w_q
     // (4.5 (c_q.g)^2 - 1.5 g.g) (launch constants).
+    V ux, uy, uz;
     if (BODY) {
-        ux += p.tau_g[0];
-        uy += p.tau_g[1];
-        uz += p.tau_g[2];
+        ux = A::fma(jx, inv, A::splat(p.tau_g[0]));
+        uy = A::fma(jy, inv, A::splat(p.tau_g[1]));
+        uz = A::fma(jz, inv, A::splat(p.tau_g[2]));
+    } else {
+        ux = A::mul(jx, inv);
+        uy = A::mul(jy, inv);
+        uz = A::mul(jz, inv);
     }
-    const float uu15 = 1.5f * (ux * ux + uy * uy + uz * uz);
-    const float om = p.omega;
+    const V nuu15 = A::mul(A::splat(-1.5f), A::fma(ux, ux, A::fma(uy, uy, A::mul(uz, uz))));
+    const V nux = A::neg(ux), nuy = A::neg(uy), nuz = A::neg(uz);
+    const V nom = A::splat(-p.omega);
 #pragma unroll
     for (int q = 0; q < 19; ++q) {
-        float cu = 0.f;
-        if (cx(q) > 0) cu += ux; else if (cx(q) < 0) cu -= ux;
-        if (cy(q) > 0) cu += uy; else if (cy(q) < 0) cu -= uy;
-        if (cz(q) > 0) cu += uz; else if (cz(q) < 0) cu -= uz;
+        // c_q . u: the signed velocity components, summed x, y, z
+        V cu = A::splat(0.f);
+        bool have = false;
+        if (cx(q) != 0) { cu = cx(q) > 0 ? ux : nux; have = true; }
+        if (cy(q) != 0) { const V t = cy(q) > 0 ? uy : nuy; cu = have ? A::add(cu, t) : t; have = true; }
+        if (cz(q) != 0) { const V t = cz(q) > 0 ? uz : nuz; cu = have ? A::add(cu, t) : t; }
         // f_eq - w = w (rho - 1 + rho (3 cu + 4.5 cu^2 - 1.5 u.u))
-        const float poly = fmaf(cu, fmaf(4.5f, cu, 3.0f), -uu15);
-        const float heq = wq(q) * fmaf(rho, poly, drho);
-        float hn = fmaf(-om, h[q] - heq, h[q]);
-        if (BODY) hn = fmaf(rho, p.wk[q], hn);
+        const V poly = q == 0 ? nuu15 : A::fma(cu, A::fma(A::splat(4.5f), cu, A::splat(3.0f)), nuu15);
+        // h - (f_eq - w), then the relaxation h + (-omega) (h - h_eq)
+        const V d = A::fma(A::splat(-wq(q)), A::fma(rho, poly, drho), h[q]);
+        V hn = A::fma(nom, d, h[q]);
+        if (BODY) hn = A::fma(rho, A::splat(p.wk[q]), hn);
         h[q] = hn;
     }
+}
+
+template <bool BODY>
+__device__ __forceinline__ void collide(float (&h)[19], const Params& p) {
+    collide_t<Arith1, BODY>(h, p);
+}
+template <bool BODY>
+__device__ __forceinline__ void collide2(float2 (&h)[19], const Params& p) {
+    collide_t<Arith2, BODY>(h, p);
 }
 
 // ---- momentum-exchange warp reduction ----------------------------------------------------------------

@@ -92,21 +92,31 @@ __device__ __forceinline__ void accumulate_force(float h_post, float& fx, float&
     if (cz(Q) > 0) fz += t; else if (cz(Q) < 0) fz -= t;
 }
 
-template <int Q = 1>
-__device__ __forceinline__ void mask_forces(uint32_t m, const float (&h)[19], float& fx, float& fy,
-                                            float& fz) {
-    if ((m >> Q) & 1u) accumulate_force<Q>(h[Q], fx, fy, fz);
+// Post-collision population Q of one cell: from a one-cell array, or from lane LANE (0: the even
+// cell, 1: the odd cell) of a two-cell array.
+template <int Q>
+__device__ __forceinline__ float pop(const float (&h)[19]) { return h[Q]; }
+template <int LANE>
+struct PairLane {
+    const float2 (&h)[19];
+};
+template <int Q, int LANE>
+__device__ __forceinline__ float pop(const PairLane<LANE>& l) { return LANE ? l.h[Q].y : l.h[Q].x; }
+
+template <int Q = 1, typename H>
+__device__ __forceinline__ void mask_forces(uint32_t m, const H& h, float& fx, float& fy, float& fz) {
+    if ((m >> Q) & 1u) accumulate_force<Q>(pop<Q>(h), fx, fy, fz);
     if constexpr (Q < 18) mask_forces<Q + 1>(m, h, fx, fy, fz);
 }
 
 // Momentum exchange of the MOVING_WALL links of a special cell: what the fluid gives up on link q
 // is c_q (f*_q + f_back), f_back = f*_q + 6 w (c_opp(q).u_w), i.e. c_q (2 f*_q - 6 w_q (c_q.u_w)).
-template <int Q = 1>
-__device__ __forceinline__ void moving_forces(const Params& p, const float (&h)[19], int x, int y,
-                                              int z, float& fx, float& fy, float& fz) {
+template <int Q = 1, typename H>
+__device__ __forceinline__ void moving_forces(const Params& p, const H& h, int x, int y, int z,
+                                              float& fx, float& fy, float& fz) {
     const Link d = link_cell(p, x, y, z, cx(Q), cy(Q), cz(Q));
     if ((p.flags[d.cell] & TYPE_MASK) == T_MOVING) {
-        const float t = 2.0f * (h[Q] + wq(Q)) - p.wterm[Q];
+        const float t = 2.0f * (pop<Q>(h) + wq(Q)) - p.wterm[Q];
         if (cx(Q) > 0) fx += t; else if (cx(Q) < 0) fx -= t;
         if (cy(Q) > 0) fy += t; else if (cy(Q) < 0) fy -= t;
         if (cz(Q) > 0) fz += t; else if (cz(Q) < 0) fz -= t;

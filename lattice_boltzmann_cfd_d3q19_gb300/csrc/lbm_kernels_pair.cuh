@@ -1,0 +1,352 @@
+// Two-cell kernels of the hot steps, for the stream layouts (fp32 and fp16 storage) on grids with
+// an even nx and 19 N <= 2^32.  A thread owns the x-adjacent cells a = (x, y, z), x even, and
+// b = (x + 1, y, z); a is the even element of every population plane, so the pair's own slots,
+// and every slot reached along a velocity with c_x = 0, are one aligned two-element word.  The
+// collision of both cells runs in packed fp32x2 arithmetic (collide2) with bit-for-bit the
+// results of the one-cell kernels, and each address computation serves both cells, which halves
+// the instructions per cell update of the one-cell kernels (they are issue-bound in fp16 storage
+// and in porous media).
+//
+// Same steps and per-link rules as the one-cell kernels ("GPU lattice Boltzmann: streaming layout
+// and performance", "In place" and "Two buffers"), with one difference in which slots a launch
+// touches, confined to slots that nothing reads: the even AA step and the A-B steps store both
+// cells of a pair, so a non-FLUID cell beside a FLUID one gets its (never-read) slots overwritten,
+// and in the A-B pull a special cell's destination slots are written before its boundary kernel
+// overwrites them.  The odd AA step stores per cell (a SOLID or special cell's stores would land
+// in slots other cells read).
+#pragma once
+
+#include <type_traits>
+
+#include "lbm_kernels.cuh"
+
+namespace lbm {
+
+template <int L>
+using Elem = typename std::conditional<L == LAYOUT_STREAM_FP16, __half, float>::type;
+
+// one element / two adjacent elements (the first at an even offset) of a population buffer
+template <int L>
+__device__ __forceinline__ float ld1(const Elem<L>* e) {
+    if constexpr (L == LAYOUT_STREAM_FP16) return __half2float(*e);
+    else return *e;
+}
+template <int L>
+__device__ __forceinline__ void st1(Elem<L>* e, float v) {
+    if constexpr (L == LAYOUT_STREAM_FP16) *e = __float2half_rn(v);
+    else *e = v;
+}
+template <int L>
+__device__ __forceinline__ float2 ld2(const Elem<L>* e) {
+    if constexpr (L == LAYOUT_STREAM_FP16) return __half22float2(*reinterpret_cast<const __half2*>(e));
+    else return *reinterpret_cast<const float2*>(e);
+}
+template <int L>
+__device__ __forceinline__ void st2(Elem<L>* e, float2 v) {
+    if constexpr (L == LAYOUT_STREAM_FP16) *reinterpret_cast<__half2*>(e) = __float22half2_rn(v);
+    else *reinterpret_cast<float2*>(e) = v;
+}
+
+// Thread -> cell pair of the 3D launch (threads along x own pairs); false for the ragged tail.
+struct PairCoord {
+    int x, y, z;  // coordinates of the even cell a
+    uint32_t n;   // index of a (even)
+};
+__device__ __forceinline__ bool grid_pair(const Params& p, PairCoord& c) {
+    c.x = 2 * (int)(blockIdx.x * blockDim.x + threadIdx.x);
+    c.y = blockIdx.y * blockDim.y + threadIdx.y;
+    c.z = blockIdx.z;
+    c.n = (uint32_t)c.x + (uint32_t)p.nx * ((uint32_t)c.y + (uint32_t)p.ny * c.z);
+    return c.x < p.nx && c.y < p.ny;
+}
+
+// Neighbour geometry of a pair: the y and z parts of n + s c_q (wrapped) are shared by both cells;
+// along x, a - 1 and b + 1 may wrap, a + 1 = b and b - 1 = a never do.  The wrapped offsets are
+// taken on every axis (the cells whose links cross an OPEN face are special and store nothing
+// here; their loads only need to stay inside the buffer).
+struct NbrPair {
+    int dy[3], dz[3];  // y and z deltas for c = -1, 0, +1
+    int wa;            // (a - 1) - a along x, wrapped
+    int wb;            // (b + 1) - a along x, wrapped
+    __device__ __forceinline__ NbrPair(const Params& p, int x, int y, int z) {
+        const int sy = p.nx, sz = p.nx * p.ny;
+        dy[0] = y == 0 ? (p.ny - 1) * sy : -sy;
+        dy[1] = 0;
+        dy[2] = y == p.ny - 1 ? -(p.ny - 1) * sy : sy;
+        dz[0] = z == 0 ? (p.nz - 1) * sz : -sz;
+        dz[1] = 0;
+        dz[2] = z == p.nz - 1 ? -(p.nz - 1) * sz : sz;
+        wa = x == 0 ? p.nx - 1 : -1;
+        wb = x + 2 == p.nx ? 2 - p.nx : 2;
+    }
+    // a + (0, s cy(Q), s cz(Q)), before the x part
+    template <int Q, int S>
+    __device__ __forceinline__ uint32_t yz(uint32_t n) const {
+        return n + (uint32_t)(dy[S * cy(Q) + 1] + dz[S * cz(Q) + 1]);
+    }
+    // element offsets (from the one of a + yz part) of the cells a + S c_Q and b + S c_Q
+    template <int Q, int S>
+    __device__ __forceinline__ int xa() const {
+        constexpr int sx = S * cx(Q);
+        return sx == 0 ? 0 : sx < 0 ? wa : 1;
+    }
+    template <int Q, int S>
+    __device__ __forceinline__ int xb() const {
+        constexpr int sx = S * cx(Q);
+        return sx == 0 ? 1 : sx < 0 ? 0 : wb;
+    }
+    // the two cells a + S c_Q, b + S c_Q: element e of the plane holding (a + yz part) -> values
+    template <int L, int Q, int S>
+    __device__ __forceinline__ float2 load(const Elem<L>* e) const {
+        constexpr int sx = S * cx(Q);
+        if constexpr (sx == 0) return ld2<L>(e);
+        else if constexpr (sx < 0) return make_float2(ld1<L>(e + wa), ld1<L>(e));
+        else return make_float2(ld1<L>(e + 1), ld1<L>(e + wb));
+    }
+    template <int L, int Q, int S, bool BOTH>
+    __device__ __forceinline__ void store(Elem<L>* e, float2 v, bool act_a, bool act_b) const {
+        constexpr int sx = S * cx(Q);
+        if constexpr (sx == 0) {
+            if (BOTH) {
+                st2<L>(e, v);
+            } else {
+                if (act_a) st1<L>(e, v.x);
+                if (act_b) st1<L>(e + 1, v.y);
+            }
+        } else if constexpr (sx < 0) {
+            if (BOTH || act_a) st1<L>(e + wa, v.x);
+            if (BOTH || act_b) st1<L>(e, v.y);
+        } else {
+            if (BOTH || act_a) st1<L>(e + 1, v.x);
+            if (BOTH || act_b) st1<L>(e + wb, v.y);
+        }
+    }
+};
+
+// flag bytes and solid-link masks of a pair (both at an even index: one aligned load each)
+struct PairFlags {
+    uint8_t fa, fb;
+    uint32_t ma, mb;
+};
+__device__ __forceinline__ PairFlags pair_flags(const Params& p, uint32_t n, bool want_mask) {
+    PairFlags f;
+    const uint16_t fl = *reinterpret_cast<const uint16_t*>(p.flags + n);
+    f.fa = (uint8_t)(fl & 0xffu);
+    f.fb = (uint8_t)(fl >> 8);
+    if (want_mask) {
+        const uint2 m = *reinterpret_cast<const uint2*>(p.mask + n);
+        f.ma = m.x;
+        f.mb = m.y;
+    } else {
+        f.ma = f.mb = 0u;
+    }
+    return f;
+}
+
+// Momentum exchange of a pair, packed: the sum over the links q whose bit is set in the cell's
+// mask of c_q f*_q, f* = h* + w (per cell, one lane each); twice that is the force the fluid
+// gives up (bounce-back returns 2 c_q f*_q), so the factor 2 is applied once, in pair_force.
+struct PairForce {
+    float2 x = make_float2(0.f, 0.f), y = make_float2(0.f, 0.f), z = make_float2(0.f, 0.f);
+    template <int Q>
+    __device__ __forceinline__ void link(float2 h_post, bool ba, bool bb) {
+        const float2 hw = Arith2::add(h_post, Arith2::splat(wq(Q)));
+        const float2 t = make_float2(ba ? hw.x : 0.f, bb ? hw.y : 0.f);
+        if (cx(Q) > 0) x = Arith2::add(x, t); else if (cx(Q) < 0) x = Arith2::sub(x, t);
+        if (cy(Q) > 0) y = Arith2::add(y, t); else if (cy(Q) < 0) y = Arith2::sub(y, t);
+        if (cz(Q) > 0) z = Arith2::add(z, t); else if (cz(Q) < 0) z = Arith2::sub(z, t);
+    }
+    template <int Q = 1>
+    __device__ __forceinline__ void masks(uint32_t ma, uint32_t mb, const float2 (&h)[19]) {
+        link<Q>(h[Q], solid_link<Q>(ma), solid_link<Q>(mb));
+        if constexpr (Q < 18) masks<Q + 1>(ma, mb, h);
+    }
+    // add to the thread's (one-cell convention) accumulators
+    __device__ __forceinline__ void into(float& fx, float& fy, float& fz) const {
+        fx += 2.0f * (x.x + x.y);
+        fy += 2.0f * (y.x + y.y);
+        fz += 2.0f * (z.x + z.y);
+    }
+};
+
+// Gather of a pull (AA odd: FAR_OPP, population q from (opposite(q), x - c_q); A-B: from
+// (q, x - c_q)).  WALL: a cell whose link opposite(q) is a solid link takes its own mirrored slot
+// instead, (q, x) in AA and (opposite(q), x) in A-B; each cell then selects its address and
+// loads one element (no branches: all 38 loads are independent).  Without WALL the pair's
+// elements are loaded together where they are adjacent and aligned.
+template <int L, bool FAR_OPP, bool WALL, int Q = 0>
+__device__ __forceinline__ void pair_gather(const Params& p, const NbrPair& nb, uint32_t n,
+                                            uint32_t ma, uint32_t mb, float2 (&h)[19]) {
+    const Elem<L>* A = static_cast<const Elem<L>*>(p.A);
+    constexpr int far_plane = FAR_OPP ? opp(Q) : Q;
+    constexpr int own_plane = FAR_OPP ? Q : opp(Q);
+    const uint32_t far = p.plane32[far_plane] + nb.template yz<Q, -1>(n);
+    if constexpr (WALL && Q > 0) {
+        const uint32_t own = p.plane32[own_plane] + n;
+        const uint32_t oa = solid_link<opp(Q)>(ma) ? own : far + (uint32_t)nb.template xa<Q, -1>();
+        const uint32_t ob = solid_link<opp(Q)>(mb) ? own + 1u : far + (uint32_t)nb.template xb<Q, -1>();
+        h[Q] = make_float2(ld1<L>(A + oa), ld1<L>(A + ob));
+    } else {
+        h[Q] = nb.template load<L, Q, -1>(A + far);
+    }
+    if constexpr (Q < 18) pair_gather<L, FAR_OPP, WALL, Q + 1>(p, nb, n, ma, mb, h);
+}
+
+// ============================== AA pattern, even step, two cells ================================
+// Every FLUID cell; the pair's slots are read and written as aligned words.
+template <int L, bool FORCE, bool BODY>
+__global__ void __launch_bounds__(256) k_aa_even2(Params p) {
+    PairCoord c;
+    float fx = 0.f, fy = 0.f, fz = 0.f;
+    if (grid_pair(p, c)) {
+        const PairFlags f = pair_flags(p, c.n, false);
+        const bool act_a = (f.fa & TYPE_MASK) == T_FLUID, act_b = (f.fb & TYPE_MASK) == T_FLUID;
+        if (act_a || act_b) {
+            Elem<L>* A = static_cast<Elem<L>*>(p.A);
+            float2 h[19];
+#pragma unroll
+            for (int q = 0; q < 19; ++q) h[q] = ld2<L>(A + (p.plane32[q] + c.n));
+            collide2<BODY>(h, p);
+            uint32_t ns = c.n;
+            asm volatile("" : "+r"(ns) : "f"(h[0].x), "f"(h[18].y));
+#pragma unroll
+            for (int q = 0; q < 19; ++q) st2<L>(A + (p.plane32[opp(q)] + ns), h[q]);
+            if (FORCE) {
+                const bool wa_ = act_a && !(f.fa & F_BULK), wb_ = act_b && !(f.fb & F_BULK);
+                if (wa_ || wb_) {
+                    const uint2 m = *reinterpret_cast<const uint2*>(p.mask + c.n);
+                    PairForce pf;
+                    pf.masks(wa_ ? m.x : 0u, wb_ ? m.y : 0u, h);
+                    pf.into(fx, fy, fz);
+                    if (p.any_moving) {
+                        if (wa_ && (f.fa & F_SPECIAL))
+                            moving_forces(p, PairLane<0>{h}, c.x, c.y, c.z, fx, fy, fz);
+                        if (wb_ && (f.fb & F_SPECIAL))
+                            moving_forces(p, PairLane<1>{h}, c.x + 1, c.y, c.z, fx, fy, fz);
+                    }
+                }
+            }
+        }
+    }
+    if (FORCE) warp_force(fx, fy, fz, p.partial);
+}
+
+// ============================== AA pattern, odd step, two cells =================================
+// FLUID cells that are not special.  Population q goes to (q, x + c_q); on a solid link also to
+// the own mirrored slot (opposite(q), x), which is the one the next even step reads.
+// ma, mb: solid-link masks, zero for a cell that is not updated here.
+template <int L, bool WALL, bool BOTH, bool FORCE, int Q = 0>
+__device__ __forceinline__ void odd2_scatter(const Params& p, const NbrPair& nb, uint32_t n,
+                                             uint32_t ma, uint32_t mb, bool act_a, bool act_b,
+                                             const float2 (&h)[19], PairForce& pf) {
+    Elem<L>* A = static_cast<Elem<L>*>(p.A);
+    const uint32_t far = p.plane32[Q] + nb.template yz<Q, 1>(n);
+    if constexpr (WALL && Q > 0) {
+        // each cell: neighbour slot, or its own mirrored slot on a solid link
+        const bool ba = solid_link<Q>(ma), bb = solid_link<Q>(mb);
+        const uint32_t own = p.plane32[opp(Q)] + n;
+        const uint32_t oa = ba ? own : far + (uint32_t)nb.template xa<Q, 1>();
+        const uint32_t ob = bb ? own + 1u : far + (uint32_t)nb.template xb<Q, 1>();
+        if (BOTH || act_a) st1<L>(A + oa, h[Q].x);
+        if (BOTH || act_b) st1<L>(A + ob, h[Q].y);
+        if (FORCE) pf.template link<Q>(h[Q], ba, bb);
+    } else {
+        nb.template store<L, Q, 1, BOTH>(A + far, h[Q], act_a, act_b);
+    }
+    if constexpr (Q < 18) odd2_scatter<L, WALL, BOTH, FORCE, Q + 1>(p, nb, n, ma, mb, act_a, act_b, h, pf);
+}
+
+template <int L, bool FORCE, bool BODY>
+__global__ void __launch_bounds__(256, 4) k_aa_odd2(Params p) {
+    PairCoord c;
+    float fx = 0.f, fy = 0.f, fz = 0.f;
+    const bool in = grid_pair(p, c);
+    PairFlags f{0, 0, 0u, 0u};
+    if (in) f = pair_flags(p, c.n, p.any_solid_link != 0);
+    const bool act_a = in && (f.fa & (TYPE_MASK | F_SPECIAL)) == T_FLUID;
+    const bool act_b = in && (f.fb & (TYPE_MASK | F_SPECIAL)) == T_FLUID;
+    if (!act_a) f.ma = 0u;
+    if (!act_b) f.mb = 0u;
+    // warp-uniform code paths: any solid link in the warp; every working thread owns two
+    // working cells
+    const bool wall = __any_sync(0xffffffffu, (f.ma | f.mb) != 0u);
+    const bool both = __all_sync(0xffffffffu, act_a == act_b);
+    if (act_a || act_b) {
+        float2 h[19];
+        {
+            const NbrPair nb(p, c.x, c.y, c.z);
+            if (wall) pair_gather<L, true, true>(p, nb, c.n, f.ma, f.mb, h);
+            else pair_gather<L, true, false>(p, nb, c.n, f.ma, f.mb, h);
+        }
+        collide2<BODY>(h, p);
+        // the scatter's geometry is formed after the collision (not held in registers across it)
+        uint32_t ns = c.n, mas = f.ma, mbs = f.mb;
+        int xs = c.x, ys = c.y, zs = c.z;
+        asm volatile("" : "+r"(ns), "+r"(mas), "+r"(mbs), "+r"(xs), "+r"(ys), "+r"(zs)
+                     : "f"(h[0].x), "f"(h[18].y));
+        const NbrPair nb(p, xs, ys, zs);
+        PairForce pf;
+        if (wall) {
+            if (both) odd2_scatter<L, true, true, FORCE>(p, nb, ns, mas, mbs, act_a, act_b, h, pf);
+            else odd2_scatter<L, true, false, FORCE>(p, nb, ns, mas, mbs, act_a, act_b, h, pf);
+            if (FORCE) pf.into(fx, fy, fz);
+        } else {
+            if (both) odd2_scatter<L, false, true, FORCE>(p, nb, ns, mas, mbs, act_a, act_b, h, pf);
+            else odd2_scatter<L, false, false, FORCE>(p, nb, ns, mas, mbs, act_a, act_b, h, pf);
+        }
+    }
+    if (FORCE) warp_force(fx, fy, fz, p.partial);
+}
+
+// ============================== two buffers (A-B), two cells ====================================
+// FROM_NATURAL: collide the natural state of every FLUID cell (B may equal A).  Otherwise pull-
+// collide the FLUID cells that are not special.  Results go to (q, x) of B as aligned words.
+template <int L, bool FORCE, bool BODY, bool FROM_NATURAL>
+__global__ void __launch_bounds__(256, 4) k_ab2(Params p) {
+    PairCoord c;
+    float fx = 0.f, fy = 0.f, fz = 0.f;
+    const bool in = grid_pair(p, c);
+    PairFlags f{0, 0, 0u, 0u};
+    if (in) f = pair_flags(p, c.n, p.any_solid_link != 0 && (FORCE || !FROM_NATURAL));
+    const uint8_t want = FROM_NATURAL ? TYPE_MASK : (TYPE_MASK | F_SPECIAL);
+    const bool act_a = in && (f.fa & want) == T_FLUID;
+    const bool act_b = in && (f.fb & want) == T_FLUID;
+    const bool wall = !FROM_NATURAL && __any_sync(0xffffffffu, (act_a || act_b) && (f.ma | f.mb) != 0u);
+    Elem<L>* B = static_cast<Elem<L>*>(p.B);
+    if (act_a || act_b) {
+        float2 h[19];
+        if (FROM_NATURAL) {
+            const Elem<L>* A = static_cast<const Elem<L>*>(p.A);
+#pragma unroll
+            for (int q = 0; q < 19; ++q) h[q] = ld2<L>(A + (p.plane32[q] + c.n));
+        } else {
+            const NbrPair nb(p, c.x, c.y, c.z);
+            if (wall) pair_gather<L, false, true>(p, nb, c.n, f.ma, f.mb, h);
+            else pair_gather<L, false, false>(p, nb, c.n, f.ma, f.mb, h);
+        }
+        collide2<BODY>(h, p);
+        uint32_t ns = c.n;
+        asm volatile("" : "+r"(ns) : "f"(h[0].x), "f"(h[18].y));
+#pragma unroll
+        for (int q = 0; q < 19; ++q) st2<L>(B + (p.plane32[q] + ns), h[q]);
+        if (FORCE) {
+            if ((act_a && f.ma) || (act_b && f.mb)) {
+                PairForce pf;
+                pf.masks(act_a ? f.ma : 0u, act_b ? f.mb : 0u, h);
+                pf.into(fx, fy, fz);
+            }
+            if (FROM_NATURAL && p.any_moving) {
+                if (act_a && (f.fa & F_SPECIAL)) moving_forces(p, PairLane<0>{h}, c.x, c.y, c.z, fx, fy, fz);
+                if (act_b && (f.fb & F_SPECIAL)) moving_forces(p, PairLane<1>{h}, c.x + 1, c.y, c.z, fx, fy, fz);
+            }
+        }
+    } else if (in && p.B != p.A) {
+        // no working cell: SOLID / INLET / MOVING_WALL slots are never read and special cells'
+        // are rewritten by the boundary kernel; zeros keep every sector of B fully written
+#pragma unroll
+        for (int q = 0; q < 19; ++q) st2<L>(B + (p.plane32[q] + c.n), make_float2(0.f, 0.f));
+    }
+    if (FORCE) warp_force(fx, fy, fz, p.partial);
+}
+
+}  // namespace lbm

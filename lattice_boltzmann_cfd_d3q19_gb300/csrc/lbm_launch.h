@@ -27,6 +27,11 @@ struct LayoutOps {
     // step kernels: K_AA_EVEN, K_AA_ODD, K_AB_PULL, K_AB_COLLIDE, K_STREAM
     cudaError_t (*cells)(int kind, const Params& p, bool force, bool body, dim3 grid, dim3 block,
                          cudaStream_t s);
+    // two-cell step kernels (K_AA_EVEN, K_AA_ODD, K_AB_PULL, K_AB_COLLIDE) for the stream layouts
+    // on grids with an even nx and 19 N <= 2^32, launched over cell pairs; cudaErrorNotSupported
+    // for the other layouts
+    cudaError_t (*cells2)(int kind, const Params& p, bool force, bool body, dim3 grid, dim3 block,
+                          cudaStream_t s);
     // boundary kernel over the special-cell list for main kind K_AA_ODD, K_AB_PULL or K_STREAM
     cudaError_t (*special)(int kind, const Params& p, bool force, bool body, cudaStream_t s);
     cudaError_t (*pregather)(const Params& p, int axis, int side, cudaStream_t s);

@@ -2,6 +2,7 @@
 #pragma once
 
 #include "lbm_kernels.cuh"
+#include "lbm_kernels_pair.cuh"
 #include "lbm_launch.h"
 
 namespace lbm {
@@ -52,6 +53,41 @@ cudaError_t cells(int kind, const Params& p, bool force, bool body, dim3 grid, d
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
+}
+
+// Two-cell kernels (stream layouts only; the caller checks an even nx and 19 N <= 2^32).
+template <int LL, bool F, bool B>
+void launch_pair(int kind, const Params& p, dim3 grid, dim3 block, cudaStream_t s) {
+    switch (kind) {
+        case K_AA_EVEN: k_aa_even2<LL, F, B><<<grid, block, 0, s>>>(p); break;
+        case K_AA_ODD: k_aa_odd2<LL, F, B><<<grid, block, 0, s>>>(p); break;
+        case K_AB_PULL: k_ab2<LL, F, B, false><<<grid, block, 0, s>>>(p); break;
+        case K_AB_COLLIDE: k_ab2<LL, F, B, true><<<grid, block, 0, s>>>(p); break;
+    }
+}
+
+template <int LL>
+cudaError_t cells2_impl(int kind, const Params& p, bool force, bool body, dim3 grid, dim3 block,
+                        cudaStream_t s) {
+    if constexpr (!is_soa(LL)) {
+        return cudaErrorNotSupported;
+    } else {
+        if (kind != K_AA_EVEN && kind != K_AA_ODD && kind != K_AB_PULL && kind != K_AB_COLLIDE)
+            return cudaErrorInvalidValue;
+        if (force) {
+            if (body) launch_pair<LL, true, true>(kind, p, grid, block, s);
+            else launch_pair<LL, true, false>(kind, p, grid, block, s);
+        } else {
+            if (body) launch_pair<LL, false, true>(kind, p, grid, block, s);
+            else launch_pair<LL, false, false>(kind, p, grid, block, s);
+        }
+        return cudaGetLastError();
+    }
+}
+
+cudaError_t cells2(int kind, const Params& p, bool force, bool body, dim3 grid, dim3 block,
+                   cudaStream_t s) {
+    return cells2_impl<L>(kind, p, force, body, grid, block, s);
 }
 
 unsigned blocks_for(size_t count) { return (unsigned)((count + 255) / 256); }
@@ -120,7 +156,7 @@ cudaError_t check_finite(const Params& p, int* bad, dim3 grid, dim3 block, cudaS
     return cudaGetLastError();
 }
 
-const LayoutOps kOps = {cells, special, pregather, pack, unpack, equilibrium, macro, check_finite};
+const LayoutOps kOps = {cells, cells2, special, pregather, pack, unpack, equilibrium, macro, check_finite};
 
 }  // namespace
 }  // namespace lbm

@@ -598,3 +598,80 @@ def test_fp16_taylor_green_against_oracle():
     for scheme in ("AA", "AB"):
         fg, _ = case.run_gpu(100, "stream_fp16", scheme)
         assert max_fluid_diff(case, fg, fo) <= fp16_tolerance(case.f0_32, 100)
+
+
+# ---- two-cell kernels (lbm_set_cell_pairs) ---------------------------------------------------------
+
+PAIR_CASES = [
+    # nx even; nx, ny, nz, faces, solid fraction, inlet layer, moving fraction of the solids
+    (38, 23, 19, (0, 0, 0), 0.0, False, 0.0),
+    (38, 23, 19, (0, 0, 0), 0.25, False, 0.0),
+    (34, 17, 9, (1, 0, 0), 0.15, True, 0.0),
+    (20, 19, 11, (1, 1, 0), 0.15, True, 0.3),
+    (14, 14, 15, (1, 1, 1), 0.1, False, 0.0),
+    (16, 12, 10, (0, 0, 0), 0.2, False, 0.5),
+    (2, 5, 3, (0, 0, 0), 0.2, False, 0.0),
+    (4, 3, 2, (1, 0, 0), 0.1, True, 0.0),
+    (300, 3, 2, (1, 0, 1), 0.1, True, 0.0),
+]
+
+
+@pytest.mark.parametrize("scheme", ["AA", "AB", "AB2"])
+@pytest.mark.parametrize("layout", ["stream", "stream_fp16"])
+@pytest.mark.parametrize("ci", range(len(PAIR_CASES)))
+def test_cell_pairs_bit_identical_to_one_cell_kernels(ci, layout, scheme):
+    """The two-cell kernels do the same arithmetic in the same order as the one-cell kernels:
+    identical populations after every number of steps; the force (partial sums grouped per
+    thread) within 1e-5 relative."""
+    nx, ny, nz, faces, solid, inlet, moving = PAIR_CASES[ci]
+    case = mixed_case(nx, ny, nz, faces, 700 + ci, solid=solid, inlet_layer=inlet, moving=moving)
+    for steps in (1, 2, 5):
+        f2, F2 = case.run_gpu(steps, layout, scheme, want_force=True, pairs=True)
+        f1, F1 = case.run_gpu(steps, layout, scheme, want_force=True, pairs=False)
+        fl = case.fluid
+        assert np.array_equal(f2[:, fl], f1[:, fl]), (steps, np.abs(f2[:, fl] - f1[:, fl]).max())
+        scale = max(1.0, float(np.abs(F1).max()))
+        assert np.abs(F2 - F1).max() <= 1e-5 * scale, (steps, F2, F1)
+
+
+@pytest.mark.parametrize("scheme", ["AA", "AB", "AB2"])
+@pytest.mark.parametrize("ci", range(len(PAIR_CASES)))
+def test_cell_pairs_match_oracle(ci, scheme):
+    nx, ny, nz, faces, solid, inlet, moving = PAIR_CASES[ci]
+    case = mixed_case(nx, ny, nz, faces, 800 + ci, solid=solid, inlet_layer=inlet, moving=moving)
+    fo, Fo = case.run_oracle(7, want_force=True)
+    fg, Fg = case.run_gpu(7, "stream", scheme, want_force=True, pairs=True)
+    assert max_fluid_diff(case, fg, fo) <= TOL_F
+    assert np.abs(Fg - Fo).max() <= 1e-4 * max(1.0, float(np.abs(Fo).max()))
+
+
+def test_cell_pairs_eligibility():
+    def state(nx, layout, allow=True):
+        ctx = B.lbm_create(nx, 6, 4, 0.6, layout, B.STREAMING_AA)
+        try:
+            return B.lbm_set_cell_pairs(ctx, allow)
+        finally:
+            B.lbm_destroy(ctx)
+    assert state(8, B.LAYOUT_STREAM) is True
+    assert state(8, B.LAYOUT_STREAM_FP16) is True
+    assert state(8, B.LAYOUT_STREAM, allow=False) is False
+    assert state(7, B.LAYOUT_STREAM) is False
+    assert state(8, B.LAYOUT_BUNDLE) is False
+    assert state(8, B.LAYOUT_COLLISION) is False
+
+
+def test_cell_pairs_with_graphs_and_chunks():
+    """Toggling the kernel family between lbm_step calls (graphs dropped and recaptured) and
+    splitting the steps leaves the result unchanged."""
+    case = mixed_case(24, 10, 8, (0, 0, 0), 901, solid=0.2, inlet_layer=False, moving=0.3)
+    ref, _ = case.run_gpu(40, "stream", "AA", pairs=False)
+    ctx = case.gpu_context("stream", "AA")
+    try:
+        for i, n in enumerate((3, 32, 5)):
+            B.lbm_set_cell_pairs(ctx, i != 1)
+            B.lbm_step(ctx, n)
+        f = np.zeros((19, case.N), np.float32)
+        B.lbm_get_populations(ctx, f)
+    finally:
+        B.lbm_destroy(ctx)
+    assert np.array_equal(f.astype(np.float64)[:, case.fluid], ref[:, case.fluid])
