@@ -12,8 +12,9 @@
 // touches, confined to slots that nothing reads: the even AA step and the A-B steps store both
 // cells of a pair, so a non-FLUID cell beside a FLUID one gets its (never-read) slots overwritten,
 // and in the A-B pull a special cell's destination slots are written before its boundary kernel
-// overwrites them.  The odd AA step stores per cell (a SOLID or special cell's stores would land
-// in slots other cells read).
+// overwrites them; the odd AA step also writes a bounced population to its neighbour slot, which
+// belongs to the SOLID cell it bounced from and is read by nobody.  Otherwise the odd AA step
+// stores per cell (a SOLID or special cell's stores would land in slots other cells read).
 #pragma once
 
 #include <type_traits>
@@ -243,12 +244,14 @@ __device__ __forceinline__ void odd2_scatter(const Params& p, const NbrPair& nb,
     const uint32_t far = p.plane32[Q] + nb.template yz<Q, 1>(n);
     if constexpr (WALL && Q > 0) {
         // each cell: neighbour slot, or its own mirrored slot on a solid link
+        // every working cell writes its neighbour slot -- on a solid link that slot is the SOLID
+        // cell's, read by nobody, and writing it keeps the sectors of the plane whole -- and on a
+        // solid link also its own mirrored slot, the one the next even step reads
         const bool ba = solid_link<Q>(ma), bb = solid_link<Q>(mb);
-        const uint32_t own = p.plane32[opp(Q)] + n;
-        const uint32_t oa = ba ? own : far + (uint32_t)nb.template xa<Q, 1>();
-        const uint32_t ob = bb ? own + 1u : far + (uint32_t)nb.template xb<Q, 1>();
-        if (BOTH || act_a) st1<L>(A + oa, h[Q].x);
-        if (BOTH || act_b) st1<L>(A + ob, h[Q].y);
+        nb.template store<L, Q, 1, BOTH>(A + far, h[Q], act_a, act_b);
+        Elem<L>* own = A + (p.plane32[opp(Q)] + n);
+        if (ba) st1<L>(own, h[Q].x);
+        if (bb) st1<L>(own + 1, h[Q].y);
         if (FORCE) pf.template link<Q>(h[Q], ba, bb);
     } else {
         nb.template store<L, Q, 1, BOTH>(A + far, h[Q], act_a, act_b);
