@@ -675,3 +675,43 @@ def test_cell_pairs_with_graphs_and_chunks():
     finally:
         B.lbm_destroy(ctx)
     assert np.array_equal(f.astype(np.float64)[:, case.fluid], ref[:, case.fluid])
+
+
+@pytest.mark.parametrize("graphs", [True, False])
+@pytest.mark.parametrize("pairs", [True, False])
+@pytest.mark.parametrize("geometry", ["periodic", "inlet_open_x"])
+def test_flags_changed_between_even_and_odd_step(geometry, pairs, graphs):
+    """AA: new SOLID cells set after an even step.  The odd step that follows bounces back from
+    them (the two-cell kernels first write the pre-bounced values the new flags need); the result
+    matches the oracle run the same way, flags1 for one step, flags2 after."""
+    nx, ny, nz, tau, g = 20, 14, 12, 0.63, (1e-5, -2e-5, 0.0)
+    N = nx * ny * nz
+    r = np.random.default_rng(950)
+    flags1 = (r.uniform(size=N) < 0.15).astype(np.uint8)
+    faces = (0, 0, 0)
+    if geometry == "inlet_open_x":
+        x, _, _ = wl.coords(nx, ny, nz)
+        flags1[x == 0] = wl.INLET
+        faces = (1, 0, 0)
+    flags2 = flags1.copy()
+    flags2[(flags1 == wl.FLUID) & (r.uniform(size=N) < 0.1)] = wl.SOLID
+    inlet = (1.01, 0.03, 0.0, 0.0)
+    f0 = random_state(N, 951)
+    P1 = oracle.Problem(nx, ny, nz, tau, flags=flags1, faces=faces, inlet=inlet, g=g)
+    P2 = oracle.Problem(nx, ny, nz, tau, flags=flags2, faces=faces, inlet=inlet, g=g)
+    A, _ = P1.step_aa(f0, 0, 1)
+    A, _ = P2.step_aa(A, 1, 5)          # steps 2..6: natural state after an even count
+    case = Case(nx, ny, nz, tau, f0, flags=flags1, faces=faces, inlet=inlet, g=g)
+    ctx = case.gpu_context("stream", "AA", pairs=pairs)
+    try:
+        B.lbm_set_graph_launch(ctx, graphs)
+        B.lbm_step(ctx, 1)
+        B.lbm_set_flags(ctx, flags2)
+        B.lbm_step(ctx, 1)
+        B.lbm_step(ctx, 4)
+        f = np.zeros((19, N), np.float32)
+        B.lbm_get_populations(ctx, f)
+    finally:
+        B.lbm_destroy(ctx)
+    fl = flags2 == wl.FLUID
+    assert np.abs(f.astype(np.float64)[:, fl] - A[:, fl]).max() <= TOL_F
