@@ -175,6 +175,20 @@ int lbm_set_graph_launch(lbm_ctx* ctx, int enable);
  * choice for the same update.) */
 int lbm_set_cell_pairs(lbm_ctx* ctx, int enable);
 
+/* Allow (enable != 0) or forbid (enable = 0, the default) the TMA-staged AA odd step: an
+ * alternative AA odd kernel, off by default because it measured slower than the register-addressed
+ * two-cell kernel on every workload tried (512^3: 12.5 vs 3.1 ms).  Persistent CTAs (one per
+ * SM) stage each tile's source rows -- every population plane, plus the tile's own rows, flags
+ * and solid-link masks when the domain has solid links -- in shared memory with TMA bulk copies,
+ * two tiles in flight, and compute from there.  It runs where the two-cell kernels run and nx is
+ * a multiple of 16 no larger than 512.  Results are bit-identical to the other AA kernels (the
+ * force up to the grouping of its partial sums).  Every wait of the kernel on its copies is
+ * bounded (2 s); a wait that runs out sets a sticky fault that the next synchronising call
+ * (getters, lbm_check_finite) reports as LBM_ECUDA.  Returns 1 when the staged kernel will run,
+ * 0 when not, LBM_EINVAL for a NULL context.  Drops the cached step graphs.  ([Layout]'s in-place
+ * step; the staging is a GB300 launch choice, not a page's design.) */
+int lbm_set_tma_gather(lbm_ctx* ctx, int enable);
+
 /* Density and velocity of the natural state: rho[N], u[3*N] (fp32).  FLUID: rho = sum f,
  * u = j/rho + g/2 (Guo's half-force shift).  SOLID: 0, 0.  INLET: rho_in, u_in.  MOVING_WALL:
  * 1, u_w.  Synchronous. */

@@ -40,6 +40,7 @@ SIGNATURES = {
     "lbm_step": (_I, [_P, _I]),
     "lbm_set_graph_launch": (_I, [_P, _I]),
     "lbm_set_cell_pairs": (_I, [_P, _I]),
+    "lbm_set_tma_gather": (_I, [_P, _I]),
     "lbm_macroscopic": (_I, [_P, _P, _P]),
     "lbm_force_momentum_exchange": (_I, [_P, _P]),
     "lbm_check_finite": (_I, [_P]),
@@ -182,6 +183,14 @@ def lbm_set_graph_launch(ctx: int, enable: bool) -> None:
 def lbm_set_cell_pairs(ctx: int, enable: bool) -> bool:
     """Allow or forbid the two-cell step kernels; True when they will run."""
     rc = load().lbm_set_cell_pairs(ctx, 1 if enable else 0)
+    if rc < 0:
+        raise LbmError(rc, _err())
+    return rc == 1
+
+
+def lbm_set_tma_gather(ctx: int, enable: bool) -> bool:
+    """Allow or forbid the TMA-staged AA odd step; True when it will run."""
+    rc = load().lbm_set_tma_gather(ctx, 1 if enable else 0)
     if rc < 0:
         raise LbmError(rc, _err())
     return rc == 1

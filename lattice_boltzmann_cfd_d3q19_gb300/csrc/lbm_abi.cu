@@ -121,6 +121,11 @@ struct lbm_ctx {
     dim3 grid2, block2;
     size_t nblocks2 = 0;
     bool pairs_allowed = true;
+    // TMA-staged AA odd kernel: persistent grid and whether the caller allows it
+    unsigned ntma = 0;
+    bool tma_allowed = false;  // opt-in: measured slower than the register kernels
+    int* fault_dev = nullptr;   // set by a kernel whose bounded wait ran out (sticky)
+    int* fault_host = nullptr;
     size_t force_triples = 0;     // partial triples written by the step that computes the force
     double* stage = nullptr;
     double* force_dev = nullptr;
@@ -168,6 +173,7 @@ struct lbm_ctx {
         p.n_special = n_special;
         p.scratch = scratch;
         p.partial = partial;
+        p.fault = fault_dev;
         p.part_special = main_blocks() * kWarpsPerBlock;
         p.nx = n[0];
         p.ny = n[1];
@@ -203,8 +209,13 @@ struct lbm_ctx {
     bool pairs() const {
         return pairs_allowed && is_soa(layout) && n[0] % 2 == 0 && 19 * N <= (size_t(1) << 32);
     }
+    // the AA odd step stages its gather through shared memory (TMA bulk copies of whole rows)
+    bool tma() const { return pairs() && tma_allowed && n[0] % 16 == 0 && n[0] <= 512 && ntma > 0; }
     // blocks of the step kernels that write force partials
     size_t main_blocks() const { return pairs() ? nblocks2 : nblocks; }
+    size_t main_blocks_for(int kind) const {
+        return kind == K_AA_ODD && tma() ? ntma : main_blocks();
+    }
     bool body() const { return g[0] != 0.f || g[1] != 0.f || g[2] != 0.f; }
     bool any_open() const { return face[0] == LBM_OPEN || face[1] == LBM_OPEN || face[2] == LBM_OPEN; }
     // buffer holding the current state and its meaning
@@ -253,6 +264,8 @@ struct lbm_ctx {
         cudaFree(staging);
         cudaFreeHost(force_host);
         cudaFreeHost(err_host);
+        cudaFree(fault_dev);
+        cudaFreeHost(fault_host);
     }
 };
 
@@ -317,7 +330,7 @@ int classify(lbm_ctx* c) {
             return cuda_fail(e, "classify: special-cell list");
         }
     }
-    const size_t need = partial_triples(std::max(c->nblocks, c->nblocks2), count);
+    const size_t need = partial_triples(std::max({c->nblocks, c->nblocks2, (size_t)c->ntma}), count);
     if (need > c->partial_cap) {
         double* np_ = nullptr;
         cudaError_t e = cudaMalloc(&np_, 3 * need * sizeof(double));
@@ -361,13 +374,17 @@ int launch_kind(lbm_ctx* c, int kind, const Params& p, bool force, int main_kind
     } else if (kind == K_BOUNDARY) {
         e = c->ops->special(main_kind, p, force, c->body(), c->stream);
         ++c->launches;
-        if (force) c->force_triples = partial_triples(c->main_blocks(), c->n_special);
+        if (force) c->force_triples = partial_triples(c->main_blocks_for(main_kind), c->n_special);
     } else {
         const bool two = c->pairs() && kind != K_STREAM;
-        e = two ? c->ops->cells2(kind, p, force, c->body(), c->grid2, c->block2, c->stream)
-                : c->ops->cells(kind, p, force, c->body(), c->grid, c->block, c->stream);
+        if (kind == K_AA_ODD && c->tma())
+            e = c->ops->odd_tma(p, force, c->body(), c->ntma, c->stream);
+        else if (two)
+            e = c->ops->cells2(kind, p, force, c->body(), c->grid2, c->block2, c->stream);
+        else
+            e = c->ops->cells(kind, p, force, c->body(), c->grid, c->block, c->stream);
         ++c->launches;
-        if (force) c->force_triples = partial_triples(c->main_blocks(), 0);
+        if (force) c->force_triples = partial_triples(c->main_blocks_for(kind), 0);
     }
     if (c->profiling && e0 && e1) {
         cudaEventRecord(e1, c->stream);
@@ -386,9 +403,11 @@ int step_once(lbm_ctx* c, bool last) {
             c->state = ST_POST_AA;
         } else {
             // open-face sources are copied before either odd kernel writes
-            if (c->any_open()) rc = launch_kind(c, K_PREGATHER, p, false);
-            if (rc == LBM_OK) rc = launch_kind(c, K_AA_ODD, p, last);
-            if (rc == LBM_OK) rc = launch_kind(c, K_BOUNDARY, p, last, K_AA_ODD);
+            Params po = p;
+            po.part_special = c->main_blocks_for(K_AA_ODD) * kWarpsPerBlock;
+            if (c->any_open()) rc = launch_kind(c, K_PREGATHER, po, false);
+            if (rc == LBM_OK) rc = launch_kind(c, K_AA_ODD, po, last);
+            if (rc == LBM_OK) rc = launch_kind(c, K_BOUNDARY, po, last, K_AA_ODD);
             c->state = ST_NATURAL;
         }
     } else if (c->streaming == LBM_STREAMING_AB) {
@@ -415,7 +434,12 @@ int step_once(lbm_ctx* c, bool last) {
 }
 
 int sync(lbm_ctx* c, const char* what) {
+    LBM_CUDA(cudaMemcpyAsync(c->fault_host, c->fault_dev, sizeof(int), cudaMemcpyDeviceToHost,
+                             c->stream), what);
     LBM_CUDA(cudaStreamSynchronize(c->stream), what);
+    if (*c->fault_host)
+        return fail(LBM_ECUDA, "%s: a staged-gather kernel gave up waiting for its copies (code %d); "
+                    "the state is not valid", what, *c->fault_host);
     return LBM_OK;
 }
 
@@ -556,6 +580,17 @@ lbm_ctx* lbm_create(int nx, int ny, int nz, float tau, int layout, int streaming
     c->grid2 = dim3((npairs + bp - 1) / bp, (unsigned)((ny + c->block2.y - 1) / c->block2.y),
                     (unsigned)nz);
     c->nblocks2 = (size_t)c->grid2.x * c->grid2.y * c->grid2.z;
+    if (nx % 16 == 0 && nx <= 512) {
+        // persistent grid of the TMA-staged odd kernel: one CTA per SM, at most one per tile
+        int dev = 0, sms = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && sms > 0) {
+            const long long tiles = ((long long)ny * nz + (512 / nx) - 1) / (512 / nx);
+            c->ntma = (unsigned)std::min<long long>(sms, tiles);
+        } else {
+            cudaGetLastError();
+        }
+    }
 
     auto bad = [&](cudaError_t e, const char* what) {
         cuda_fail(e, what);
@@ -579,11 +614,15 @@ lbm_ctx* lbm_create(int nx, int ny, int nz, float tau, int layout, int streaming
     if ((e = cudaMalloc(&c->err_dev, sizeof(int))) != cudaSuccess) return bad(e, "lbm_create: error word");
     if ((e = cudaMallocHost(&c->force_host, 3 * sizeof(double))) != cudaSuccess) return bad(e, "lbm_create: pinned force");
     if ((e = cudaMallocHost(&c->err_host, sizeof(int))) != cudaSuccess) return bad(e, "lbm_create: pinned error word");
+    if ((e = cudaMalloc(&c->fault_dev, sizeof(int))) != cudaSuccess) return bad(e, "lbm_create: fault word");
+    if ((e = cudaMallocHost(&c->fault_host, sizeof(int))) != cudaSuccess) return bad(e, "lbm_create: pinned fault word");
+    *c->fault_host = 0;
     // rest state: h = f - w = 0 everywhere; all cells FLUID
     if ((e = cudaMemsetAsync(c->buf[0], 0, pop_bytes, c->stream)) != cudaSuccess) return bad(e, "lbm_create: init");
     if (c->buf[1] && (e = cudaMemsetAsync(c->buf[1], 0, pop_bytes, c->stream)) != cudaSuccess)
         return bad(e, "lbm_create: init");
     if ((e = cudaMemsetAsync(c->types, 0, N, c->stream)) != cudaSuccess) return bad(e, "lbm_create: init");
+    if ((e = cudaMemsetAsync(c->fault_dev, 0, sizeof(int), c->stream)) != cudaSuccess) return bad(e, "lbm_create: init");
     if (classify(c) != LBM_OK) {
         c->free_all();
         delete c;
@@ -882,6 +921,15 @@ int lbm_set_cell_pairs(lbm_ctx* c, int enable) {
         c->pairs_allowed = enable != 0;
     }
     return c->pairs() ? 1 : 0;
+}
+
+int lbm_set_tma_gather(lbm_ctx* c, int enable) {
+    if (!c) return fail(LBM_EINVAL, "lbm_set_tma_gather: NULL context");
+    if (c->tma_allowed != (enable != 0)) {
+        c->drop_graphs();
+        c->tma_allowed = enable != 0;
+    }
+    return c->tma() ? 1 : 0;
 }
 
 int lbm_set_graph_launch(lbm_ctx* c, int enable) {

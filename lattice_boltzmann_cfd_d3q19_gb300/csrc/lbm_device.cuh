@@ -120,6 +120,7 @@ struct Params {
     uint32_t n_special;
     float* scratch;        // open-face pre-gathered values (AA odd step)
     double* partial;       // per-block momentum-exchange partial sums, 3 per block
+    int* fault;            // set by a kernel whose bounded wait ran out (read by the host)
     size_t part_special;   // first partial slot (triple) of the boundary kernels' warps
     int nx, ny, nz;
     int open[3];           // axis has OPEN faces

@@ -32,6 +32,9 @@ struct LayoutOps {
     // for the other layouts
     cudaError_t (*cells2)(int kind, const Params& p, bool force, bool body, dim3 grid, dim3 block,
                           cudaStream_t s);
+    // AA odd step with the gather staged by TMA bulk copies (stream layouts, 16 | nx <= 512,
+    // 19 N <= 2^32): `grid` persistent CTAs of 256 threads; cudaErrorNotSupported otherwise
+    cudaError_t (*odd_tma)(const Params& p, bool force, bool body, unsigned grid, cudaStream_t s);
     // boundary kernel over the special-cell list for main kind K_AA_ODD, K_AB_PULL or K_STREAM
     cudaError_t (*special)(int kind, const Params& p, bool force, bool body, cudaStream_t s);
     cudaError_t (*pregather)(const Params& p, int axis, int side, cudaStream_t s);

@@ -3,6 +3,7 @@
 
 #include "lbm_kernels.cuh"
 #include "lbm_kernels_pair.cuh"
+#include "lbm_kernels_tma.cuh"
 #include "lbm_launch.h"
 
 namespace lbm {
@@ -90,6 +91,40 @@ cudaError_t cells2(int kind, const Params& p, bool force, bool body, dim3 grid, 
     return cells2_impl<L>(kind, p, force, body, grid, block, s);
 }
 
+// TMA-staged AA odd kernel (stream layouts; the caller checks 16 | nx <= 512 and 19 N <= 2^32).
+// The dynamic shared-memory limit is raised once per device and instantiation.
+template <int LL, bool F, bool B>
+cudaError_t launch_tma(const Params& p, unsigned grid, cudaStream_t s) {
+    constexpr int kMaxDevices = 64;
+    static bool raised[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (!raised[dev]) {
+        e = cudaFuncSetAttribute(k_aa_odd_tma<LL, F, B>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)TmaStage<LL>::total);
+        if (e != cudaSuccess) return e;
+        raised[dev] = true;
+    }
+    k_aa_odd_tma<LL, F, B><<<grid, kTmaThreads, TmaStage<LL>::total, s>>>(p);
+    return cudaGetLastError();
+}
+
+template <int LL>
+cudaError_t odd_tma_impl(const Params& p, bool force, bool body, unsigned grid, cudaStream_t s) {
+    if constexpr (!is_soa(LL)) {
+        return cudaErrorNotSupported;
+    } else {
+        if (force) return body ? launch_tma<LL, true, true>(p, grid, s) : launch_tma<LL, true, false>(p, grid, s);
+        return body ? launch_tma<LL, false, true>(p, grid, s) : launch_tma<LL, false, false>(p, grid, s);
+    }
+}
+
+cudaError_t odd_tma(const Params& p, bool force, bool body, unsigned grid, cudaStream_t s) {
+    return odd_tma_impl<L>(p, force, body, grid, s);
+}
+
 unsigned blocks_for(size_t count) { return (unsigned)((count + 255) / 256); }
 
 #define LBM_LAUNCH_SPECIAL(KERNEL)                                                     \
@@ -156,7 +191,7 @@ cudaError_t check_finite(const Params& p, int* bad, dim3 grid, dim3 block, cudaS
     return cudaGetLastError();
 }
 
-const LayoutOps kOps = {cells, cells2, special, pregather, pack, unpack, equilibrium, macro, check_finite};
+const LayoutOps kOps = {cells, cells2, odd_tma, special, pregather, pack, unpack, equilibrium, macro, check_finite};
 
 }  // namespace
 }  // namespace lbm

@@ -715,3 +715,81 @@ def test_flags_changed_between_even_and_odd_step(geometry, pairs, graphs):
         B.lbm_destroy(ctx)
     fl = flags2 == wl.FLUID
     assert np.abs(f.astype(np.float64)[:, fl] - A[:, fl]).max() <= TOL_F
+
+
+# ---- TMA-staged AA odd step (lbm_set_tma_gather) --------------------------------------------------
+
+TMA_CASES = [
+    # 16 | nx <= 512; nx, ny, nz, faces, solid fraction, inlet layer, moving fraction
+    (32, 23, 19, (0, 0, 0), 0.0, False, 0.0),
+    (32, 23, 19, (0, 0, 0), 0.25, False, 0.0),
+    (48, 17, 9, (1, 0, 0), 0.15, True, 0.0),
+    (16, 19, 11, (1, 1, 0), 0.15, True, 0.3),
+    (64, 14, 15, (1, 1, 1), 0.1, False, 0.0),
+    (16, 12, 10, (0, 0, 0), 0.2, False, 0.5),
+    (16, 1, 1, (0, 0, 0), 0.0, False, 0.0),
+    (512, 3, 2, (1, 0, 1), 0.1, True, 0.0),
+    (96, 33, 5, (0, 1, 0), 0.3, False, 0.2),
+]
+
+
+@pytest.mark.parametrize("layout", ["stream", "stream_fp16"])
+@pytest.mark.parametrize("ci", range(len(TMA_CASES)))
+def test_tma_gather_bit_identical(ci, layout):
+    """The staged odd step reads the same slots as the register one: identical populations after
+    odd and even step counts; the force within 1e-5 relative (its partial sums are grouped by the
+    persistent CTAs)."""
+    nx, ny, nz, faces, solid, inlet, moving = TMA_CASES[ci]
+    case = mixed_case(nx, ny, nz, faces, 1100 + ci, solid=solid, inlet_layer=inlet, moving=moving)
+    for steps in (2, 5, 8):
+        f1, F1 = case.run_gpu(steps, layout, "AA", want_force=True, tma=True)
+        f0, F0 = case.run_gpu(steps, layout, "AA", want_force=True, tma=False)
+        fl = case.fluid
+        assert np.array_equal(f1[:, fl], f0[:, fl]), (steps, np.abs(f1[:, fl] - f0[:, fl]).max())
+        scale = max(1.0, float(np.abs(F0).max()))
+        assert np.abs(F1 - F0).max() <= 1e-5 * scale, (steps, F1, F0)
+
+
+@pytest.mark.parametrize("ci", [1, 3, 8])
+def test_tma_gather_matches_oracle(ci):
+    nx, ny, nz, faces, solid, inlet, moving = TMA_CASES[ci]
+    case = mixed_case(nx, ny, nz, faces, 1200 + ci, solid=solid, inlet_layer=inlet, moving=moving)
+    fo, Fo = case.run_oracle(9, want_force=True)
+    fg, Fg = case.run_gpu(9, "stream", "AA", want_force=True, tma=True)
+    assert max_fluid_diff(case, fg, fo) <= TOL_F
+    assert np.abs(Fg - Fo).max() <= 1e-4 * max(1.0, float(np.abs(Fo).max()))
+
+
+def test_tma_gather_eligibility():
+    def state(nx, layout=B.LAYOUT_STREAM, pairs=True, allow=True):
+        ctx = B.lbm_create(nx, 6, 4, 0.6, layout, B.STREAMING_AA)
+        try:
+            B.lbm_set_cell_pairs(ctx, pairs)
+            return B.lbm_set_tma_gather(ctx, allow)
+        finally:
+            B.lbm_destroy(ctx)
+    assert state(16) is True
+    assert state(512) is True
+    assert state(32, B.LAYOUT_STREAM_FP16) is True
+    assert state(32, allow=False) is False
+    assert state(32, pairs=False) is False
+    assert state(20) is False
+    assert state(8) is False
+    assert state(528) is False
+    assert state(32, B.LAYOUT_BUNDLE) is False
+
+
+def test_tma_gather_with_graphs_and_toggles():
+    case = mixed_case(64, 10, 8, (0, 0, 0), 1301, solid=0.2, inlet_layer=False, moving=0.3)
+    ref, _ = case.run_gpu(41, "stream", "AA", tma=False)
+    ctx = case.gpu_context("stream", "AA")
+    try:
+        for i, n in enumerate((3, 32, 6)):
+            B.lbm_set_tma_gather(ctx, i != 1)
+            B.lbm_step(ctx, n)
+        f = np.zeros((19, case.N), np.float32)
+        B.lbm_get_populations(ctx, f)
+        assert B.lbm_check_finite(ctx)
+    finally:
+        B.lbm_destroy(ctx)
+    assert np.array_equal(f.astype(np.float64)[:, case.fluid], ref[:, case.fluid])
