@@ -125,6 +125,9 @@ struct lbm_ctx {
     unsigned ntma = 0;
     bool tma_allowed = false;  // opt-in: measured slower than the register kernels
     int* fault_dev = nullptr;   // set by a kernel whose bounded wait ran out (sticky)
+    // test hook (LBM_TEST_STAGE_TIMEOUT=1 at lbm_create): the staged kernel announces 16 bytes
+    // more than it copies, so its first wait runs out; nothing faults
+    uint32_t extra_tx = 0;
     int* fault_host = nullptr;
     size_t force_triples = 0;     // partial triples written by the step that computes the force
     double* stage = nullptr;
@@ -174,6 +177,7 @@ struct lbm_ctx {
         p.scratch = scratch;
         p.partial = partial;
         p.fault = fault_dev;
+        p.extra_tx = extra_tx;
         p.part_special = main_blocks() * kWarpsPerBlock;
         p.nx = n[0];
         p.ny = n[1];
@@ -617,6 +621,8 @@ lbm_ctx* lbm_create(int nx, int ny, int nz, float tau, int layout, int streaming
     if ((e = cudaMalloc(&c->fault_dev, sizeof(int))) != cudaSuccess) return bad(e, "lbm_create: fault word");
     if ((e = cudaMallocHost(&c->fault_host, sizeof(int))) != cudaSuccess) return bad(e, "lbm_create: pinned fault word");
     *c->fault_host = 0;
+    if (const char* v = std::getenv("LBM_TEST_STAGE_TIMEOUT"); v && std::strcmp(v, "1") == 0)
+        c->extra_tx = 16;
     // rest state: h = f - w = 0 everywhere; all cells FLUID
     if ((e = cudaMemsetAsync(c->buf[0], 0, pop_bytes, c->stream)) != cudaSuccess) return bad(e, "lbm_create: init");
     if (c->buf[1] && (e = cudaMemsetAsync(c->buf[1], 0, pop_bytes, c->stream)) != cudaSuccess)

@@ -121,6 +121,7 @@ struct Params {
     float* scratch;        // open-face pre-gathered values (AA odd step)
     double* partial;       // per-block momentum-exchange partial sums, 3 per block
     int* fault;            // set by a kernel whose bounded wait ran out (read by the host)
+    uint32_t extra_tx;     // test hook: bytes a staged tile announces beyond its copies (normally 0)
     size_t part_special;   // first partial slot (triple) of the boundary kernels' warps
     int nx, ny, nz;
     int open[3];           // axis has OPEN faces

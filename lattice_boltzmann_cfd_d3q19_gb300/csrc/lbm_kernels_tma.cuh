@@ -113,7 +113,7 @@ __device__ __forceinline__ void tma_issue(const Params& p, const TmaTiles& tg, i
     // the stage was last read by every thread (a barrier precedes this call); order those
     // generic-proxy reads before the async-proxy writes
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    mbar_expect_tx(bar, bytes);
+    mbar_expect_tx(bar, bytes + p.extra_tx);
     E* far = reinterpret_cast<E*>(st);
     E* own = reinterpret_cast<E*>(st + TmaStage<L>::own_off);
     const uint32_t n0 = (uint32_t)r0 * (uint32_t)p.nx;

@@ -793,3 +793,31 @@ def test_tma_gather_with_graphs_and_toggles():
     finally:
         B.lbm_destroy(ctx)
     assert np.array_equal(f.astype(np.float64)[:, case.fluid], ref[:, case.fluid])
+
+
+def test_tma_gather_wait_timeout_is_reported(monkeypatch):
+    """Failure detection without a GPU fault: with the test hook the staged odd step announces 16
+    bytes more than it copies, so its wait can never complete.  The wait gives up after its 2 s
+    bound, the kernel drains its own copies and returns, and the next synchronising call reports
+    LBM_ECUDA.  The device stays usable."""
+    import time
+    monkeypatch.setenv("LBM_TEST_STAGE_TIMEOUT", "1")
+    case = Case(32, 4, 2, 0.7, random_state(32 * 4 * 2, 1500))
+    ctx = case.gpu_context("stream", "AA", tma=True)
+    try:
+        assert B.lbm_set_tma_gather(ctx, True)
+        B.lbm_set_graph_launch(ctx, False)
+        t0 = time.time()
+        B.lbm_step(ctx, 2)
+        f = np.zeros((19, case.N), np.float32)
+        with pytest.raises(B.LbmError) as ei:
+            B.lbm_get_populations(ctx, f)
+        assert ei.value.code == B.ECUDA
+        assert "gave up waiting" in str(ei.value)
+        assert time.time() - t0 < 60
+    finally:
+        B.lbm_destroy(ctx)
+    monkeypatch.delenv("LBM_TEST_STAGE_TIMEOUT")
+    fg, _ = case.run_gpu(2, "stream", "AA", tma=True)
+    fo, _ = case.run_oracle(2)
+    assert max_fluid_diff(case, fg, fo) <= TOL_F
