@@ -177,6 +177,7 @@ struct lbm_ctx {
         p.scratch = scratch;
         p.partial = partial;
         p.fault = fault_dev;
+        p.zrev = 0;
         p.extra_tx = extra_tx;
         p.part_special = main_blocks() * kWarpsPerBlock;
         p.nx = n[0];
@@ -356,7 +357,20 @@ int classify(lbm_ctx* c) {
 
 // Launch a step kernel (or, for K_BOUNDARY, the boundary kernel of step kind `main_kind`), timed
 // when profiling is on.
-int launch_kind(lbm_ctx* c, int kind, const Params& p, bool force, int main_kind = -1) {
+// Sweep direction of a step kernel: each step walks the z planes opposite to the step before, so
+// it starts on the planes the previous step wrote last (still in L2 on grids near its size).
+int z_reversed(const lbm_ctx* c, int kind) {
+    switch (kind) {
+        case K_AA_ODD: return 1;
+        case K_AB_PULL: return c->cur;
+        case K_STREAM: return 1;
+        default: return 0;  // AA even step, A-B / AB2 collision from the natural state
+    }
+}
+
+int launch_kind(lbm_ctx* c, int kind, const Params& p_in, bool force, int main_kind = -1) {
+    Params p = p_in;
+    p.zrev = z_reversed(c, kind);
     if (kind == K_BOUNDARY && c->n_special == 0) return LBM_OK;
     cudaEvent_t e0 = nullptr, e1 = nullptr;
     if (c->profiling) {

@@ -124,6 +124,7 @@ struct Params {
     uint32_t extra_tx;     // test hook: bytes a staged tile announces beyond its copies (normally 0)
     size_t part_special;   // first partial slot (triple) of the boundary kernels' warps
     int nx, ny, nz;
+    int zrev;              // step kernels walk the z planes from nz - 1 down (alternated per step)
     int open[3];           // axis has OPEN faces
     size_t N;
     size_t face_base[3][2];  // scratch offset of face (axis, side); 19 * area values each

@@ -135,7 +135,7 @@ struct CellCoord {
 __device__ __forceinline__ bool grid_cell(const Params& p, CellCoord& c) {
     c.x = blockIdx.x * blockDim.x + threadIdx.x;
     c.y = blockIdx.y * blockDim.y + threadIdx.y;
-    c.z = blockIdx.z;
+    c.z = p.zrev ? p.nz - 1 - (int)blockIdx.z : (int)blockIdx.z;
     c.n = (uint32_t)c.x + (uint32_t)p.nx * ((uint32_t)c.y + (uint32_t)p.ny * c.z);
     return c.x < p.nx && c.y < p.ny;
 }
