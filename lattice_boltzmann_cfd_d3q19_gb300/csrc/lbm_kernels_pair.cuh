@@ -195,8 +195,10 @@ __device__ __forceinline__ void pair_gather(const Params& p, const NbrPair& nb, 
 
 // ============================== AA pattern, even step, two cells ================================
 // Every FLUID cell; the pair's slots are read and written as aligned words.
+// 4 resident blocks per SM (64 registers): with 66 registers the fp16 kernel fell to 3 blocks
+// and lost 9% (measured)
 template <int L, bool FORCE, bool BODY>
-__global__ void __launch_bounds__(256) k_aa_even2(Params p) {
+__global__ void __launch_bounds__(256, 4) k_aa_even2(Params p) {
     PairCoord c;
     float fx = 0.f, fy = 0.f, fz = 0.f;
     if (grid_pair(p, c)) {
