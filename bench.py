@@ -251,6 +251,7 @@ def timed_steps(B, torch, ctx, steps, warmup, per_step=2, profile=True, sampler=
     if profile:
         for kind, name in ((B.K_AA_EVEN, "aa_even"), (B.K_AA_ODD, "aa_odd"),
                            (B.K_AB_PULL, "ab_pull"), (B.K_AB_COLLIDE, "ab_collide"),
+                           (B.K_BOUNDARY, "boundary"), (B.K_PREGATHER, "pregather"),
                            (B.K_FORCE, "force_reduce")):
             cnt, tot = B.lbm_profile_read(ctx, kind)
             if cnt:
@@ -259,21 +260,34 @@ def timed_steps(B, torch, ctx, steps, warmup, per_step=2, profile=True, sampler=
     return ms, launches, prof, clocks
 
 
-def variant(B, torch, n, scheme, steps=10, warmup=3, cavity=False, fp16=False):
+def variant(B, torch, n, scheme, steps=10, warmup=3, cavity=False, fp16=False, layout="stream",
+            sphere=False):
     """Periodic box without solids, g = 0, uniform flow: the clean roofline point.  With
     cavity=True: a lid-driven cavity (resting walls, lid moving at 0.05 along x), fluid at rest.
-    With fp16=True the populations are stored in half precision (76 population bytes per update
-    instead of 152; the roofline fraction uses those bytes)."""
-    ctx = B.lbm_create(n, n, n, 0.6, B.LAYOUT_STREAM_FP16 if fp16 else B.LAYOUT_STREAM,
+    With sphere=True: the sphere workload (r = n/8 at (0.3125 n, n/2, n/2), equilibrium inlet
+    u = (0.05, 0, 0) on x = 0, zero-gradient outlet, y/z periodic, tau 0.56, fluid at the inlet
+    state).  With fp16=True the populations are stored in half precision (76 population bytes per
+    update instead of 152; the roofline fraction uses those bytes).  `layout`: stream, bundle or
+    collision (fp32)."""
+    lay = {"stream": B.LAYOUT_STREAM, "bundle": B.LAYOUT_BUNDLE,
+           "collision": B.LAYOUT_COLLISION}[layout]
+    tau = 0.56 if sphere else 0.6
+    ctx = B.lbm_create(n, n, n, tau, B.LAYOUT_STREAM_FP16 if fp16 else lay,
                        B.STREAMING_AA if scheme == "AA" else B.STREAMING_AB)
     try:
         N = n ** 3
         if cavity:
             B.lbm_set_flags(ctx, wl.cavity_flags(n, n, n))
             B.lbm_set_wall_velocity(ctx, 0.05, 0.0, 0.0)
+        if sphere:
+            B.lbm_set_flags(ctx, wl.sphere_flags(n, n, n, (5 * n // 16, n // 2, n // 2), n / 8))
+            B.lbm_set_faces(ctx, B.OPEN, B.PERIODIC, B.PERIODIC)
+            B.lbm_set_inlet(ctx, 1.0, 0.05, 0.0, 0.0)
         rho = torch.ones(N, dtype=torch.float32, device="cuda")
         u = torch.zeros(3 * N, dtype=torch.float32, device="cuda")
-        if not cavity:
+        if sphere:
+            u[:N] = 0.05
+        elif not cavity:
             u[:N] = 0.02
         B.lbm_set_equilibrium(ctx, rho, u)
         # throughput with graph replay (no per-kernel events), then per-kernel event timing
@@ -287,6 +301,10 @@ def variant(B, torch, n, scheme, steps=10, warmup=3, cavity=False, fp16=False):
     kernels = {}
     for name, (cnt, tot) in prof.items():
         if name == "force_reduce":
+            continue
+        if name in ("boundary", "pregather"):
+            # small kernels over the special cells / open faces: time only
+            kernels[name] = {"ms": round(tot / cnt, 4)}
             continue
         gbs = N * per_cell / (tot / cnt / 1e3) / 1e9
         kernels[name] = {"ms": round(tot / cnt, 4), "GB/s": round(gbs, 1),
@@ -313,10 +331,22 @@ def cpu_baseline(n=512, ny_sample=16, target_s=15.0):
     t0 = time.perf_counter()
     P.step_ab(f, steps)
     dt = time.perf_counter() - t0
-    return {"value": round(Ns * steps / dt / 1e6, 3), "unit": UNIT, "cores": oracle.max_threads(),
+    cores = oracle.max_threads()  # before the one-thread run below sets the thread count
+    # one thread, on a thinner slab of the same flags (a few seconds)
+    ny1 = 2
+    sub1 = np.ascontiguousarray(flags[:, :ny1, :]).reshape(-1)
+    N1 = n * ny1 * n
+    P1 = oracle.Problem(n, ny1, n, 0.7, flags=sub1, g=(1e-6, 0, 0), threads=1)
+    f1 = oracle.equilibrium_field(*wl.uniform_fields(N1))
+    t0 = time.perf_counter()
+    P1.step_ab(f1, 4)
+    dt1 = time.perf_counter() - t0
+    return {"value": round(Ns * steps / dt / 1e6, 3), "unit": UNIT, "cores": cores,
             "kind": "oracle",
             "sample": f"{n}x{ny_sample}x{n} slab of the porous 512^3 flags, periodic, {steps} steps "
-                      f"({dt:.1f} s), fp64 two-lattice oracle"}
+                      f"({dt:.1f} s), fp64 two-lattice oracle",
+            "single_thread": {"value": round(N1 * 4 / dt1 / 1e6, 3), "unit": UNIT, "cores": 1,
+                              "sample": f"{n}x{ny1}x{n} slab, 4 steps ({dt1:.1f} s)"}}
 
 
 def e2e_run(B, torch, n, steps, flags):
@@ -424,6 +454,13 @@ def run_ours(args):
         log("[bench] variants")
         out["variants"] = {f"{s}_{m}^3_periodic": variant(B, torch, m, s)
                            for m in (128, 512) for s in ("AA", "AB")}
+        for lay in ("bundle", "collision"):
+            for s in ("AA", "AB"):
+                out["variants"][f"{s}_128^3_periodic_{lay}_layout"] = variant(B, torch, 128, s,
+                                                                              layout=lay)
+        for s in ("AA", "AB"):
+            out["variants"][f"{s}_128^3_sphere_inlet_outlet"] = variant(B, torch, 128, s,
+                                                                        sphere=True)
         out["variants"]["AA_256^3_lid_driven_cavity"] = variant(B, torch, 256, "AA", cavity=True)
         for s in ("AA", "AB"):
             out["variants"][f"{s}_512^3_periodic_fp16_storage"] = variant(B, torch, 512, s,

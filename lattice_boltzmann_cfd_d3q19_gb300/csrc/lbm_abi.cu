@@ -291,7 +291,8 @@ int ensure_staging(lbm_ctx* c) {
     return LBM_OK;
 }
 
-unsigned special_blocks(uint32_t n_special) { return (n_special + 255) / 256; }
+// blocks of the boundary kernels that write force partials: one warp per special cell
+unsigned special_blocks(uint32_t n_special) { return (n_special + 7) / 8; }
 
 // one fp64 partial triple per warp of the step kernels and of the boundary kernels
 size_t partial_triples(size_t main_blocks, uint32_t n_special) {
@@ -380,12 +381,8 @@ int launch_kind(lbm_ctx* c, int kind, const Params& p_in, bool force, int main_k
     }
     cudaError_t e = cudaSuccess;
     if (kind == K_PREGATHER) {
-        for (int a = 0; a < 3 && e == cudaSuccess; ++a)
-            if (c->face[a] == LBM_OPEN)
-                for (int s = 0; s < 2 && e == cudaSuccess; ++s) {
-                    e = c->ops->pregather(p, a, s, c->stream);
-                    ++c->launches;
-                }
+        e = c->ops->pregather(p, c->stream);
+        ++c->launches;
     } else if (kind == K_FORCE) {
         e = launch_force_finalize(c->partial, c->force_triples, c->stage, c->force_dev, c->stream);
         c->launches += 2;

@@ -49,9 +49,27 @@ __host__ __device__ constexpr int cx(int q) { return vcode(q) % 3 - 1; }
 __host__ __device__ constexpr int cy(int q) { return (vcode(q) / 3) % 3 - 1; }
 __host__ __device__ constexpr int cz(int q) { return vcode(q) / 9 - 1; }
 __host__ __device__ constexpr int opp(int q) { return q == 0 ? 0 : (q & 1) ? q + 1 : q - 1; }
+// the same for a q known only at run time (one thread or lane per population)
+__device__ __forceinline__ int c_rt(unsigned pos, unsigned neg, int q) {
+    return (int)((pos >> q) & 1u) - (int)((neg >> q) & 1u);
+}
+__device__ __forceinline__ int cx_rt(int q) {
+    return c_rt((1u << 1) | (1u << 7) | (1u << 9) | (1u << 13) | (1u << 15),
+                (1u << 2) | (1u << 8) | (1u << 10) | (1u << 14) | (1u << 16), q);
+}
+__device__ __forceinline__ int cy_rt(int q) {
+    return c_rt((1u << 3) | (1u << 7) | (1u << 11) | (1u << 14) | (1u << 17),
+                (1u << 4) | (1u << 8) | (1u << 12) | (1u << 13) | (1u << 18), q);
+}
+__device__ __forceinline__ int cz_rt(int q) {
+    return c_rt((1u << 5) | (1u << 9) | (1u << 11) | (1u << 16) | (1u << 18),
+                (1u << 6) | (1u << 10) | (1u << 12) | (1u << 15) | (1u << 17), q);
+}
+__device__ __forceinline__ int opp_rt(int q) { return q == 0 ? 0 : (q & 1) ? q + 1 : q - 1; }
 __host__ __device__ constexpr float wq(int q) {
     return q == 0 ? 1.0f / 3.0f : q <= 6 ? 1.0f / 18.0f : 1.0f / 36.0f;
 }
+__device__ __forceinline__ float wq_rt(int q) { return wq(q); }
 
 // ---- layout addressing ------------------------------------------------------------------------
 // STREAM (SoA): q*N + n.  COLLISION (AoS): n*19 + q.  BUNDLE (SoAoS): the populations sharing

@@ -257,118 +257,45 @@ __global__ void __launch_bounds__(256) k_aa_odd(Params p) {
     if (FORCE) warp_force(fx, fy, fz, p.partial);
 }
 
-// Boundary kernel of the odd step: special cells (an INLET neighbour or a link across an OPEN
-// face), general per-link rules.  Populations whose source lies beyond an OPEN face were copied
-// to scratch by k_pregather before both kernels (gather before scatter), and the post-collision
-// values of cells on an OPEN face layer are also written to the neighbours that take them as their
-// clamped (zero-gradient) source.
-template <int L, int Q>
-__device__ __forceinline__ float aa_odd_gather(const Params& p, uint32_t n, int x, int y, int z) {
-    const Link s = link_cell(p, x, y, z, -cx(Q), -cy(Q), -cz(Q));
-    const int t = p.flags[s.cell] & TYPE_MASK;
-    if (t == T_SOLID) return ld<L>(p.A, idx<L>(Q, n, p.N));           // f*_opp(q)(x) sits at (q, x)
-    if (t == T_MOVING) return ld<L>(p.A, idx<L>(Q, n, p.N)) + p.wterm[Q];
-    if (t == T_INLET) return p.heq_in[Q];
-    if (s.face >= 0) return p.scratch[scratch_slot(p, s.face, Q, x, y, z)];
-    return ld<L>(p.A, idx<L>(opp(Q), s.cell, p.N));
-}
-
-template <int L, int Q>
-__device__ __forceinline__ void aa_odd_face_copies(const Params& p, float v, int x, int y, int z) {
-    // axes on which x sits on the layer where c_q points into the domain from an OPEN face
-    int M = 0;
-    if (cx(Q) != 0 && p.open[0] && ((cx(Q) > 0 && x == 0) || (cx(Q) < 0 && x == p.nx - 1))) M |= 1;
-    if (cy(Q) != 0 && p.open[1] && ((cy(Q) > 0 && y == 0) || (cy(Q) < 0 && y == p.ny - 1))) M |= 2;
-    if (cz(Q) != 0 && p.open[2] && ((cz(Q) > 0 && z == 0) || (cz(Q) < 0 && z == p.nz - 1))) M |= 4;
-    if (M == 0) return;
-    for (int S = 1; S < 8; ++S) {
-        if ((S & M) != S) continue;
-        // receiver r: on axes in S it shares x's coordinate (its source clamps back onto x)
-        int r[3] = {x, y, z};
-        const int c[3] = {cx(Q), cy(Q), cz(Q)};
-        const int nn[3] = {p.nx, p.ny, p.nz};
-        bool valid = true;
-        for (int a = 0; a < 3; ++a) {
-            if (S & (1 << a)) continue;
-            int v2 = r[a] + c[a];
-            if (v2 < 0 || v2 >= nn[a]) {
-                if (p.open[a]) valid = false;
-                else v2 = v2 < 0 ? v2 + nn[a] : v2 - nn[a];
-            }
-            r[a] = v2;
-        }
-        if (!valid) continue;
-        const uint32_t rc = (uint32_t)r[0] + (uint32_t)p.nx * ((uint32_t)r[1] + (uint32_t)p.ny * r[2]);
-        if ((p.flags[rc] & TYPE_MASK) == T_FLUID) st<L>(p.A, idx<L>(Q, rc, p.N), v);
-    }
-}
-
-template <int L, int Q>
-__device__ __forceinline__ void aa_odd_scatter(const Params& p, float v, uint32_t n, int x, int y,
-                                               int z) {
-    const Link d = link_cell(p, x, y, z, cx(Q), cy(Q), cz(Q));
-    const int t = p.flags[d.cell] & TYPE_MASK;
-    if (t == T_SOLID) {
-        st<L>(p.A, idx<L>(opp(Q), n, p.N), v);                          // bounces back into x
-    } else if (t == T_MOVING) {
-        st<L>(p.A, idx<L>(opp(Q), n, p.N), v + p.wterm[opp(Q)]);         // off the moving wall
-    } else if (t == T_INLET) {
-        st<L>(p.A, idx<L>(opp(Q), n, p.N), p.heq_in[opp(Q)]);            // the reservoir feeds x
-    } else if (d.face < 0) {
-        st<L>(p.A, idx<L>(Q, d.cell, p.N), v);
-    }
-    if (p.open[0] | p.open[1] | p.open[2]) aa_odd_face_copies<L, Q>(p, v, x, y, z);
-}
-
-template <int L, int Q = 0>
-__device__ __forceinline__ void aa_odd_gather_all(const Params& p, float (&h)[19], uint32_t n,
-                                                  int x, int y, int z) {
-    h[Q] = aa_odd_gather<L, Q>(p, n, x, y, z);
-    if constexpr (Q < 18) aa_odd_gather_all<L, Q + 1>(p, h, n, x, y, z);
-}
-
-template <int L, int Q = 0>
-__device__ __forceinline__ void aa_odd_scatter_all(const Params& p, const float (&h)[19],
-                                                   uint32_t n, int x, int y, int z) {
-    aa_odd_scatter<L, Q>(p, h[Q], n, x, y, z);
-    if constexpr (Q < 18) aa_odd_scatter_all<L, Q + 1>(p, h, n, x, y, z);
-}
-
-template <int L, bool FORCE, bool BODY>
-__global__ void __launch_bounds__(256) k_aa_odd_special(Params p) {
-    CellCoord c;
-    float fx = 0.f, fy = 0.f, fz = 0.f;
-    if (special_cell(p, c)) {
-        float h[19];
-        aa_odd_gather_all<L>(p, h, c.n, c.x, c.y, c.z);
-        collide<BODY>(h, p);
-        aa_odd_scatter_all<L>(p, h, c.n, c.x, c.y, c.z);
-        if (FORCE) {
-            mask_forces(p.mask[c.n], h, fx, fy, fz);
-            if (p.any_moving) moving_forces(p, h, c.x, c.y, c.z, fx, fy, fz);
-        }
-    }
-    if (FORCE) warp_force(fx, fy, fz, p.partial, p.part_special);
-}
+// The boundary kernels of the AA odd and A-B pull steps (special cells, general per-link rules)
+// are in lbm_kernels_boundary.cuh.
 
 // Open-face pre-gather for the AA odd step: for every FLUID cell x on face layer (axis, side) and
 // every q whose source x - c_q lies beyond that face first, copy the clamped source's
 // post-collision population q -- at (opposite(q), s) -- into scratch, before the odd kernels
-// overwrite that slot.
+// overwrite that slot.  Only the 5 velocities with c_axis pointing into the domain from that face
+// (+1 on the low side, -1 on the high side) can have such a source: one thread per (k, face cell),
+// k-th of those velocities.
+__device__ __forceinline__ int face_velocity(int axis, int sgn, int k) {
+    int cnt = 0;
+    for (int q = 1; q < 19; ++q) {
+        const int c = axis == 0 ? cx_rt(q) : axis == 1 ? cy_rt(q) : cz_rt(q);
+        if (c == sgn) {
+            if (cnt == k) return q;
+            ++cnt;
+        }
+    }
+    return 0;
+}
+
+// One launch for every open face: blockIdx.y = 2 * axis + side.
 template <int L>
-__global__ void __launch_bounds__(256) k_pregather(Params p, int axis, int side) {
+__global__ void __launch_bounds__(256) k_pregather(Params p) {
+    const int axis = (int)blockIdx.y >> 1, side = (int)blockIdx.y & 1;
+    if (!p.open[axis]) return;
     const size_t area = face_area(p, axis);
     const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= 19 * area) return;
-    const int q = (int)(i / area);
-    const size_t pos = i - (size_t)q * area;
+    if (i >= 5 * area) return;
+    const int k = (int)(i / area);
+    const size_t pos = i - (size_t)k * area;
+    const int q = face_velocity(axis, side ? -1 : 1, k);
     int x, y, z;
     if (axis == 0) { x = side ? p.nx - 1 : 0; y = (int)(pos % p.ny); z = (int)(pos / p.ny); }
     else if (axis == 1) { y = side ? p.ny - 1 : 0; x = (int)(pos % p.nx); z = (int)(pos / p.nx); }
     else { z = side ? p.nz - 1 : 0; x = (int)(pos % p.nx); y = (int)(pos / p.nx); }
     const uint32_t n = (uint32_t)x + (uint32_t)p.nx * ((uint32_t)y + (uint32_t)p.ny * z);
     if ((p.flags[n] & TYPE_MASK) != T_FLUID) return;
-    const Link s = link_cell(p, x, y, z, -cx(q), -cy(q), -cz(q));
+    const Link s = link_cell(p, x, y, z, -cx_rt(q), -cy_rt(q), -cz_rt(q));
     if (s.face != 2 * axis + side) return;
     if ((p.flags[s.cell] & TYPE_MASK) != T_FLUID) return;
     p.scratch[p.face_base[axis][side] + (size_t)q * area + pos] = ld<L>(p.A, idx_rt<L>(opp(q), s.cell, p.N));
@@ -447,24 +374,6 @@ __global__ void __launch_bounds__(256, 6) k_ab(Params p) {
         }
     }
     if (FORCE) warp_force(fx, fy, fz, p.partial);
-}
-
-template <int L, bool FORCE, bool BODY>
-__global__ void __launch_bounds__(256) k_ab_special(Params p) {
-    CellCoord c;
-    float fx = 0.f, fy = 0.f, fz = 0.f;
-    if (special_cell(p, c)) {
-        float h[19];
-        ab_gather_all<L>(p, h, c.n, c.x, c.y, c.z);
-        collide<BODY>(h, p);
-#pragma unroll
-        for (int q = 0; q < 19; ++q) st<L>(p.B, idx<L>(q, c.n, p.N), h[q]);
-        if (FORCE) {
-            mask_forces(p.mask[c.n], h, fx, fy, fz);
-            if (p.any_moving) moving_forces(p, h, c.x, c.y, c.z, fx, fy, fz);
-        }
-    }
-    if (FORCE) warp_force(fx, fy, fz, p.partial, p.part_special);
 }
 
 // Streaming only: natural state into B from the post-collision state in A (second pass of the

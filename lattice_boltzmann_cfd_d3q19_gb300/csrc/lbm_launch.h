@@ -37,7 +37,8 @@ struct LayoutOps {
     cudaError_t (*odd_tma)(const Params& p, bool force, bool body, unsigned grid, cudaStream_t s);
     // boundary kernel over the special-cell list for main kind K_AA_ODD, K_AB_PULL or K_STREAM
     cudaError_t (*special)(int kind, const Params& p, bool force, bool body, cudaStream_t s);
-    cudaError_t (*pregather)(const Params& p, int axis, int side, cudaStream_t s);
+    // open-face pre-gather of the AA odd step, every open face in one launch
+    cudaError_t (*pregather)(const Params& p, cudaStream_t s);
     cudaError_t (*pack)(const Params& p, const float* in, size_t i0, size_t count, cudaStream_t s);
     cudaError_t (*unpack)(const Params& p, int state, float* out, size_t i0, size_t count,
                           cudaStream_t s);

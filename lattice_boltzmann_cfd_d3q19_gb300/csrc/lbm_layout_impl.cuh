@@ -1,9 +1,12 @@
 // Instantiates the kernels for one population layout (LBM_LAYOUT) and fills its LayoutOps.
 #pragma once
 
+#include <algorithm>
+
 #include "lbm_kernels.cuh"
 #include "lbm_kernels_pair.cuh"
 #include "lbm_kernels_tma.cuh"
+#include "lbm_kernels_boundary.cuh"
 #include "lbm_launch.h"
 
 namespace lbm {
@@ -140,21 +143,25 @@ unsigned blocks_for(size_t count) { return (unsigned)((count + 255) / 256); }
 
 cudaError_t special(int kind, const Params& p, bool force, bool body, cudaStream_t s) {
     if (p.n_special == 0) return cudaSuccess;
-    const unsigned grid = blocks_for(p.n_special);
+    // one warp per special cell (8 per block) for the collision kernels
+    const unsigned grid = (p.n_special + kSpecialCellsPerBlock - 1) / kSpecialCellsPerBlock;
     switch (kind) {
         case K_AA_ODD: LBM_LAUNCH_SPECIAL(k_aa_odd_special); break;
         case K_AB_PULL: LBM_LAUNCH_SPECIAL(k_ab_special); break;
-        case K_STREAM: k_stream_special<L><<<grid, 256, 0, s>>>(p); break;
+        case K_STREAM: k_stream_special<L><<<blocks_for(p.n_special), 256, 0, s>>>(p); break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
 }
 #undef LBM_LAUNCH_SPECIAL
 
-cudaError_t pregather(const Params& p, int axis, int side, cudaStream_t s) {
-    const size_t area = axis == 0 ? (size_t)p.ny * p.nz
-                      : axis == 1 ? (size_t)p.nx * p.nz : (size_t)p.nx * p.ny;
-    k_pregather<L><<<blocks_for(19 * area), 256, 0, s>>>(p, axis, side);
+cudaError_t pregather(const Params& p, cudaStream_t s) {
+    size_t area = 0;
+    if (p.open[0]) area = std::max(area, (size_t)p.ny * p.nz);
+    if (p.open[1]) area = std::max(area, (size_t)p.nx * p.nz);
+    if (p.open[2]) area = std::max(area, (size_t)p.nx * p.ny);
+    if (area == 0) return cudaSuccess;
+    k_pregather<L><<<dim3(blocks_for(5 * area), 6), 256, 0, s>>>(p);
     return cudaGetLastError();
 }
 

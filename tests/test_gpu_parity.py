@@ -450,8 +450,9 @@ def test_stream_profile_and_launch_counts():
         B.lbm_step(ctx, 4)
         s.synchronize()
         launched = B.lbm_kernel_launches(ctx) - before
-        # 2 even + 2 odd + 2 boundary-cell odd + 2 x 2 open-face pre-gathers + 2 force-sum stages
-        assert launched == 2 + 2 + 2 + 4 + 2
+        # 2 even + 2 odd + 2 boundary-cell odd + 2 open-face pre-gathers (both x faces in one
+        # launch) + 2 force-sum stages
+        assert launched == 2 + 2 + 2 + 2 + 2
         n_even, ms_even = B.lbm_profile_read(ctx, B.K_AA_EVEN)
         n_odd, ms_odd = B.lbm_profile_read(ctx, B.K_AA_ODD)
         assert n_even == 2 and n_odd == 2 and ms_even > 0 and ms_odd > 0
