@@ -136,6 +136,12 @@ struct lbm_ctx {
     int* err_dev = nullptr;
     int* err_host = nullptr;
     float* staging = nullptr;
+    // double-buffered host transfers: the copy of one half of the staging buffer (on the private
+    // copy stream) overlaps the kernel on the other half (on the context stream)
+    cudaStream_t copy_stream = nullptr;
+    cudaEvent_t stage_full[2] = {nullptr, nullptr};  // a half holds data for its consumer
+    cudaEvent_t stage_free[2] = {nullptr, nullptr};  // a half's consumer is done with it
+    cudaEvent_t stage_mark = nullptr;                // start / end marker between the streams
     cudaStream_t stream = nullptr;
     int64_t steps = 0;
     bool force_valid = false;
@@ -267,6 +273,12 @@ struct lbm_ctx {
         cudaFree(force_dev);
         cudaFree(err_dev);
         cudaFree(staging);
+        for (int h = 0; h < 2; ++h) {
+            if (stage_full[h]) cudaEventDestroy(stage_full[h]);
+            if (stage_free[h]) cudaEventDestroy(stage_free[h]);
+        }
+        if (stage_mark) cudaEventDestroy(stage_mark);
+        if (copy_stream) cudaStreamDestroy(copy_stream);
         cudaFreeHost(force_host);
         cudaFreeHost(err_host);
         cudaFree(fault_dev);
@@ -288,6 +300,65 @@ const LayoutOps* ops_for(int layout) {
 
 int ensure_staging(lbm_ctx* c) {
     if (!c->staging) LBM_CUDA(cudaMalloc(&c->staging, kStagingFloats * sizeof(float)), "staging buffer");
+    if (!c->copy_stream)
+        LBM_CUDA(cudaStreamCreateWithFlags(&c->copy_stream, cudaStreamNonBlocking), "copy stream");
+    for (int h = 0; h < 2; ++h) {
+        if (!c->stage_full[h])
+            LBM_CUDA(cudaEventCreateWithFlags(&c->stage_full[h], cudaEventDisableTiming), "staging events");
+        if (!c->stage_free[h])
+            LBM_CUDA(cudaEventCreateWithFlags(&c->stage_free[h], cudaEventDisableTiming), "staging events");
+    }
+    if (!c->stage_mark)
+        LBM_CUDA(cudaEventCreateWithFlags(&c->stage_mark, cudaEventDisableTiming), "staging events");
+    // the copy stream starts after the work already on the context stream
+    LBM_CUDA(cudaEventRecord(c->stage_mark, c->stream), "staging");
+    LBM_CUDA(cudaStreamWaitEvent(c->copy_stream, c->stage_mark, 0), "staging");
+    return LBM_OK;
+}
+
+constexpr size_t kStageHalf = kStagingFloats / 2;  // floats per staging half
+
+// host -> staging half h (copy stream), then `use` it on the context stream
+int stage_in(lbm_ctx* c, int h, float* dst_half, const float* src, size_t count) {
+    LBM_CUDA(cudaStreamWaitEvent(c->copy_stream, c->stage_free[h], 0), "staging");
+    LBM_CUDA(cudaMemcpyAsync(dst_half, src, count * sizeof(float), cudaMemcpyDefault, c->copy_stream),
+             "host copy");
+    return LBM_OK;
+}
+int stage_in_done(lbm_ctx* c, int h) {
+    LBM_CUDA(cudaEventRecord(c->stage_full[h], c->copy_stream), "staging");
+    LBM_CUDA(cudaStreamWaitEvent(c->stream, c->stage_full[h], 0), "staging");
+    return LBM_OK;
+}
+// after the context stream's kernel has read (upload) or written (read-back) half h
+int stage_used(lbm_ctx* c, int h) {
+    LBM_CUDA(cudaEventRecord(c->stage_free[h], c->stream), "staging");
+    return LBM_OK;
+}
+// read-back: the context stream wrote half h; copy it to the host on the copy stream
+int stage_out(lbm_ctx* c, int h, float* dst, const float* src_half, size_t count) {
+    LBM_CUDA(cudaMemcpyAsync(dst, src_half, count * sizeof(float), cudaMemcpyDefault, c->copy_stream),
+             "host copy");
+    return LBM_OK;
+}
+int stage_out_begin(lbm_ctx* c, int h) {
+    // the copy that last read half h is done before the kernel overwrites it
+    LBM_CUDA(cudaStreamWaitEvent(c->stream, c->stage_free[h], 0), "staging");
+    return LBM_OK;
+}
+int stage_out_ready(lbm_ctx* c, int h) {
+    LBM_CUDA(cudaEventRecord(c->stage_full[h], c->stream), "staging");
+    LBM_CUDA(cudaStreamWaitEvent(c->copy_stream, c->stage_full[h], 0), "staging");
+    return LBM_OK;
+}
+int stage_out_copied(lbm_ctx* c, int h) {
+    LBM_CUDA(cudaEventRecord(c->stage_free[h], c->copy_stream), "staging");
+    return LBM_OK;
+}
+// the context stream completes after every copy of the copy stream
+int stage_end(lbm_ctx* c) {
+    LBM_CUDA(cudaEventRecord(c->stage_mark, c->copy_stream), "staging");
+    LBM_CUDA(cudaStreamWaitEvent(c->stream, c->stage_mark, 0), "staging");
     return LBM_OK;
 }
 
@@ -771,13 +842,18 @@ int lbm_set_populations(lbm_ctx* c, const float* f) {
         ++c->launches;
     } else {
         if (int rc = ensure_staging(c)) return rc;
-        for (size_t i0 = 0; i0 < total; i0 += kStagingFloats) {
-            const size_t cnt = total - i0 < kStagingFloats ? total - i0 : kStagingFloats;
-            LBM_CUDA(cudaMemcpyAsync(c->staging, f + i0, cnt * sizeof(float), cudaMemcpyDefault,
-                                     c->stream), "lbm_set_populations: copy");
-            LBM_CUDA(c->ops->pack(p, c->staging, i0, cnt, c->stream), "lbm_set_populations: pack");
+        int k = 0;
+        for (size_t i0 = 0; i0 < total; i0 += kStageHalf, ++k) {
+            const size_t cnt = total - i0 < kStageHalf ? total - i0 : kStageHalf;
+            const int h = k & 1;
+            float* s = c->staging + h * kStageHalf;
+            if (int rc = stage_in(c, h, s, f + i0, cnt)) return rc;
+            if (int rc = stage_in_done(c, h)) return rc;
+            LBM_CUDA(c->ops->pack(p, s, i0, cnt, c->stream), "lbm_set_populations: pack");
             ++c->launches;
+            if (int rc = stage_used(c, h)) return rc;
         }
+        if (int rc = stage_end(c)) return rc;
     }
     reset_state(c);
     return sync(c, "lbm_set_populations");
@@ -794,18 +870,23 @@ int lbm_set_equilibrium(lbm_ctx* c, const float* rho, const float* u) {
         ++c->launches;
     } else {
         if (int rc = ensure_staging(c)) return rc;
-        const size_t chunk = kStagingFloats / 4;
-        for (size_t n0 = 0; n0 < N; n0 += chunk) {
+        const size_t chunk = kStageHalf / 4;
+        int k = 0;
+        for (size_t n0 = 0; n0 < N; n0 += chunk, ++k) {
             const size_t cnt = N - n0 < chunk ? N - n0 : chunk;
-            float* s = c->staging;
-            LBM_CUDA(cudaMemcpyAsync(s, rho + n0, cnt * 4, cudaMemcpyDefault, c->stream), "lbm_set_equilibrium: copy");
+            const int h = k & 1;
+            float* s = c->staging + h * kStageHalf;
+            if (int rc = stage_in(c, h, s, rho + n0, cnt)) return rc;
             for (int a = 0; a < 3; ++a)
                 LBM_CUDA(cudaMemcpyAsync(s + (a + 1) * chunk, u + a * N + n0, cnt * 4, cudaMemcpyDefault,
-                                         c->stream), "lbm_set_equilibrium: copy");
+                                         c->copy_stream), "lbm_set_equilibrium: copy");
+            if (int rc = stage_in_done(c, h)) return rc;
             LBM_CUDA(c->ops->equilibrium(p, s, s + chunk, s + 2 * chunk, s + 3 * chunk, (uint32_t)n0,
                                          (uint32_t)cnt, c->stream), "lbm_set_equilibrium");
             ++c->launches;
+            if (int rc = stage_used(c, h)) return rc;
         }
+        if (int rc = stage_end(c)) return rc;
     }
     reset_state(c);
     return sync(c, "lbm_set_equilibrium");
@@ -821,13 +902,19 @@ int lbm_get_populations(lbm_ctx* c, float* f) {
         ++c->launches;
     } else {
         if (int rc = ensure_staging(c)) return rc;
-        for (size_t i0 = 0; i0 < total; i0 += kStagingFloats) {
-            const size_t cnt = total - i0 < kStagingFloats ? total - i0 : kStagingFloats;
-            LBM_CUDA(c->ops->unpack(p, c->state, c->staging, i0, cnt, c->stream), "lbm_get_populations");
+        int k = 0;
+        for (size_t i0 = 0; i0 < total; i0 += kStageHalf, ++k) {
+            const size_t cnt = total - i0 < kStageHalf ? total - i0 : kStageHalf;
+            const int h = k & 1;
+            float* s = c->staging + h * kStageHalf;
+            if (int rc = stage_out_begin(c, h)) return rc;
+            LBM_CUDA(c->ops->unpack(p, c->state, s, i0, cnt, c->stream), "lbm_get_populations");
             ++c->launches;
-            LBM_CUDA(cudaMemcpyAsync(f + i0, c->staging, cnt * sizeof(float), cudaMemcpyDefault,
-                                     c->stream), "lbm_get_populations: copy");
+            if (int rc = stage_out_ready(c, h)) return rc;
+            if (int rc = stage_out(c, h, f + i0, s, cnt)) return rc;
+            if (int rc = stage_out_copied(c, h)) return rc;
         }
+        if (int rc = stage_end(c)) return rc;
     }
     return sync(c, "lbm_get_populations");
 }
@@ -863,18 +950,23 @@ int lbm_macroscopic(lbm_ctx* c, float* rho, float* u) {
         ++c->launches;
     } else {
         if (int rc = ensure_staging(c)) return rc;
-        const size_t chunk = kStagingFloats / 4;
-        float* s = c->staging;
-        for (size_t n0 = 0; n0 < N; n0 += chunk) {
+        const size_t chunk = kStageHalf / 4;
+        int k = 0;
+        for (size_t n0 = 0; n0 < N; n0 += chunk, ++k) {
             const size_t cnt = N - n0 < chunk ? N - n0 : chunk;
+            const int h = k & 1;
+            float* s = c->staging + h * kStageHalf;
+            if (int rc = stage_out_begin(c, h)) return rc;
             LBM_CUDA(c->ops->macro(p, c->state, c->inlet, s, s + chunk, s + 2 * chunk, s + 3 * chunk,
                                    (uint32_t)n0, (uint32_t)cnt, c->stream), "lbm_macroscopic");
             ++c->launches;
-            LBM_CUDA(cudaMemcpyAsync(rho + n0, s, cnt * 4, cudaMemcpyDefault, c->stream), "lbm_macroscopic: copy");
+            if (int rc = stage_out_ready(c, h)) return rc;
+            if (int rc = stage_out(c, h, rho + n0, s, cnt)) return rc;
             for (int a = 0; a < 3; ++a)
-                LBM_CUDA(cudaMemcpyAsync(u + a * N + n0, s + (a + 1) * chunk, cnt * 4, cudaMemcpyDefault,
-                                         c->stream), "lbm_macroscopic: copy");
+                if (int rc = stage_out(c, h, u + a * N + n0, s + (a + 1) * chunk, cnt)) return rc;
+            if (int rc = stage_out_copied(c, h)) return rc;
         }
+        if (int rc = stage_end(c)) return rc;
     }
     return sync(c, "lbm_macroscopic");
 }
