@@ -217,7 +217,8 @@ int64_t lbm_kernel_launches(lbm_ctx* ctx);
  * kernel kind `kind` (0 AA even, 1 AA odd, 2 A-B pull, 3 A-B collide, 4 stream, 5 open-face
  * gather, 6 force reduce, 7 boundary kernels of cells next to an inlet or an open face), the
  * number of launches and their summed milliseconds since profiling was enabled, and
- * synchronises the stream. */
+ * synchronises the stream.  The environment variable LBM_PROFILE=1 at lbm_create turns
+ * profiling on from the start.  While it is on, steps are launched one by one (no graphs). */
 int lbm_profile_enable(lbm_ctx* ctx, int enable);
 int lbm_profile_read(lbm_ctx* ctx, int kind, int64_t* launches, double* total_ms);
 

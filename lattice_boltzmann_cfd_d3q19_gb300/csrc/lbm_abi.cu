@@ -705,6 +705,9 @@ lbm_ctx* lbm_create(int nx, int ny, int nz, float tau, int layout, int streaming
     *c->fault_host = 0;
     if (const char* v = std::getenv("LBM_TEST_STAGE_TIMEOUT"); v && std::strcmp(v, "1") == 0)
         c->extra_tx = 16;
+    // LBM_PROFILE=1: per-kernel event timing from the start, as lbm_profile_enable(ctx, 1)
+    if (const char* v = std::getenv("LBM_PROFILE"); v && std::strcmp(v, "1") == 0)
+        c->profiling = true;
     // rest state: h = f - w = 0 everywhere; all cells FLUID
     if ((e = cudaMemsetAsync(c->buf[0], 0, pop_bytes, c->stream)) != cudaSuccess) return bad(e, "lbm_create: init");
     if (c->buf[1] && (e = cudaMemsetAsync(c->buf[1], 0, pop_bytes, c->stream)) != cudaSuccess)

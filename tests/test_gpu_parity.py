@@ -822,3 +822,58 @@ def test_tma_gather_wait_timeout_is_reported(monkeypatch):
     fg, _ = case.run_gpu(2, "stream", "AA", tma=True)
     fo, _ = case.run_oracle(2)
     assert max_fluid_diff(case, fg, fo) <= TOL_F
+
+
+# ---- neighbour indexing of the two-cell and staged kernels, checkpoint / resume, profiling env -----
+
+@pytest.mark.parametrize("tma", [False, True])
+@pytest.mark.parametrize("scheme", ["AA", "AB", "AB2"])
+@pytest.mark.parametrize("dims, faces", [((32, 10, 7), (0, 0, 0)), ((2, 5, 3), (0, 0, 0)),
+                                         ((22, 9, 4), (1, 1, 0)), ((48, 6, 5), (1, 0, 1))])
+def test_streaming_permutation_bit_exact_two_cell(dims, faces, scheme, tma):
+    """The permutation test on even nx (two cells per thread, x-wrap at both pair edges) and on nx
+    a multiple of 16 (the staged odd step when tma): every label lands where the oracle puts it."""
+    nx, ny, nz = dims
+    r = np.random.default_rng(43)
+    flags = (r.uniform(size=nx * ny * nz) < 0.2).astype(np.uint8)
+    case = Case(nx, ny, nz, 1e30, wl.labels(nx * ny * nz), flags=flags, faces=faces)
+    for steps in (1, 2, 5):
+        fo, _ = case.run_oracle(steps)
+        fg, _ = case.run_gpu(steps, "stream", scheme, tma=tma)
+        fl = case.fluid
+        assert np.array_equal(fg[:, fl], fo[:, fl]), steps
+
+
+@pytest.mark.parametrize("scheme", ["AA", "AB", "AB2"])
+def test_checkpoint_resume_across_parities(scheme):
+    """lbm_get_populations + lbm_set_populations form a full checkpoint: stopping after an odd or an
+    even number of steps (the AA buffer in either parity), restoring into a fresh context and
+    continuing matches the uninterrupted run (to the rounding of f = (f - w) + w at the restore)."""
+    case = mixed_case(24, 13, 9, (1, 0, 0), 1400, moving=0.3)
+    total = 9
+    full, _ = case.run_gpu(total, "stream", scheme)
+    for k in (3, 4):
+        ctx = case.gpu_context("stream", scheme)
+        try:
+            B.lbm_step(ctx, k)
+            f = np.zeros((19, case.N), np.float32)
+            B.lbm_get_populations(ctx, f)
+        finally:
+            B.lbm_destroy(ctx)
+        resumed = Case(case.nx, case.ny, case.nz, case.tau, f, flags=case.flags, faces=case.faces,
+                       inlet=case.inlet, g=case.g, wall=case.wall)
+        fr, _ = resumed.run_gpu(total - k, "stream", scheme)
+        assert max_fluid_diff(case, fr, full) <= 1e-6, k
+
+
+def test_profile_environment_variable(monkeypatch):
+    monkeypatch.setenv("LBM_PROFILE", "1")
+    case = mixed_case(16, 8, 6, (0, 0, 0), 1500, inlet_layer=False)
+    ctx = case.gpu_context("stream", "AA")
+    try:
+        B.lbm_step(ctx, 4)
+        n_even, ms_even = B.lbm_profile_read(ctx, B.K_AA_EVEN)
+        n_odd, _ = B.lbm_profile_read(ctx, B.K_AA_ODD)
+        assert n_even == 2 and n_odd == 2 and ms_even > 0
+    finally:
+        B.lbm_destroy(ctx)
