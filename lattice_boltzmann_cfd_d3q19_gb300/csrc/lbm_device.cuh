@@ -246,71 +246,104 @@ struct Arith2 {
     }
 };
 
+// Population source of the collision: a one- or two-cell array, or two cells' stored half-precision
+// values converted to fp32 where they are used (fewer registers held than an fp32 array).
+template <typename V>
+struct ArrayView {
+    const V (&a)[19];
+    __device__ __forceinline__ V operator()(int q) const { return a[q]; }
+};
+struct HalfPairView {
+    const __half2 (&a)[19];
+    __device__ __forceinline__ float2 operator()(int q) const { return __half22float2(a[q]); }
+};
+
 // sum over the populations whose velocity component along `axis` is `sign`, in q order
-template <typename A, int axis, int sign, int Q = 1, bool FIRST = true>
-__device__ __forceinline__ typename A::V side_sum(const typename A::V (&h)[19], typename A::V acc) {
+template <typename A, int axis, int sign, int Q = 1, bool FIRST = true, typename H>
+__device__ __forceinline__ typename A::V side_sum(const H& h, typename A::V acc) {
     if constexpr (Q > 18) {
         return acc;
     } else {
         constexpr int c = axis == 0 ? cx(Q) : axis == 1 ? cy(Q) : cz(Q);
         if constexpr (c == sign) {
             typename A::V next;
-            if constexpr (FIRST) next = h[Q];
-            else next = A::add(acc, h[Q]);
+            if constexpr (FIRST) next = h(Q);
+            else next = A::add(acc, h(Q));
             return side_sum<A, axis, sign, Q + 1, false>(h, next);
         } else {
             return side_sum<A, axis, sign, Q + 1, FIRST>(h, acc);
         }
     }
 }
-template <typename A, int axis>
-__device__ __forceinline__ typename A::V momentum(const typename A::V (&h)[19]) {
+template <typename A, int axis, typename H>
+__device__ __forceinline__ typename A::V momentum(const H& h) {
     return A::sub(side_sum<A, axis, 1>(h, A::splat(0.f)), side_sum<A, axis, -1>(h, A::splat(0.f)));
 }
 
-template <typename A, bool BODY>
-__device__ __forceinline__ void collide_t(typename A::V (&h)[19], const Params& p) {
+// What the relaxation of every population needs from the cell's moments.
+template <typename A>
+struct Moments {
+    typename A::V drho, rho, ux, uy, uz, nux, nuy, nuz, nuu15, nom;
+};
+
+template <typename A, bool BODY, typename H>
+__device__ __forceinline__ Moments<A> moments(const H& h, const Params& p) {
     using V = typename A::V;
-    V drho = h[0];
+    Moments<A> m;
+    V drho = h(0);
 #pragma unroll
-    for (int q = 1; q < 19; ++q) drho = A::add(drho, h[q]);
+    for (int q = 1; q < 19; ++q) drho = A::add(drho, h(q));
     const V jx = momentum<A, 0>(h), jy = momentum<A, 1>(h), jz = momentum<A, 2>(h);
-    const V rho = A::add(A::splat(1.0f), drho);
-    const V inv = A::recip(rho);
+    m.drho = drho;
+    m.rho = A::add(A::splat(1.0f), drho);
+    const V inv = A::recip(m.rho);
     // Guo forcing, F = rho g, u = j/rho + g/2, source S_q = (1 - omega/2) d f_eq,q/du . g.
     // Because f_eq is quadratic in u, omega f_eq(u) + (1 - omega/2) d f_eq/du . g equals
     // omega f_eq(u + a g) - omega a^2 w rho (4.5 (c.g)^2 - 1.5 g.g) with a = tau - 1/2 exactly:
     // relax toward the equilibrium at j/rho + tau g and add rho wk_q, wk_q = -omega a^2 w_q
     // (4.5 (c_q.g)^2 - 1.5 g.g) (launch constants).
-    V ux, uy, uz;
     if (BODY) {
-        ux = A::fma(jx, inv, A::splat(p.tau_g[0]));
-        uy = A::fma(jy, inv, A::splat(p.tau_g[1]));
-        uz = A::fma(jz, inv, A::splat(p.tau_g[2]));
+        m.ux = A::fma(jx, inv, A::splat(p.tau_g[0]));
+        m.uy = A::fma(jy, inv, A::splat(p.tau_g[1]));
+        m.uz = A::fma(jz, inv, A::splat(p.tau_g[2]));
     } else {
-        ux = A::mul(jx, inv);
-        uy = A::mul(jy, inv);
-        uz = A::mul(jz, inv);
+        m.ux = A::mul(jx, inv);
+        m.uy = A::mul(jy, inv);
+        m.uz = A::mul(jz, inv);
     }
-    const V nuu15 = A::mul(A::splat(-1.5f), A::fma(ux, ux, A::fma(uy, uy, A::mul(uz, uz))));
-    const V nux = A::neg(ux), nuy = A::neg(uy), nuz = A::neg(uz);
-    const V nom = A::splat(-p.omega);
+    m.nuu15 = A::mul(A::splat(-1.5f), A::fma(m.ux, m.ux, A::fma(m.uy, m.uy, A::mul(m.uz, m.uz))));
+    m.nux = A::neg(m.ux);
+    m.nuy = A::neg(m.uy);
+    m.nuz = A::neg(m.uz);
+    m.nom = A::splat(-p.omega);
+    return m;
+}
+
+// Post-collision value of population q (a constant after unrolling) with pre-collision value h.
+template <typename A, bool BODY>
+__device__ __forceinline__ typename A::V relax_q(const Moments<A>& m, int q, typename A::V h,
+                                                 const Params& p) {
+    using V = typename A::V;
+    // c_q . u: the signed velocity components, summed x, y, z
+    V cu = A::splat(0.f);
+    bool have = false;
+    if (cx(q) != 0) { cu = cx(q) > 0 ? m.ux : m.nux; have = true; }
+    if (cy(q) != 0) { const V t = cy(q) > 0 ? m.uy : m.nuy; cu = have ? A::add(cu, t) : t; have = true; }
+    if (cz(q) != 0) { const V t = cz(q) > 0 ? m.uz : m.nuz; cu = have ? A::add(cu, t) : t; }
+    // f_eq - w = w (rho - 1 + rho (3 cu + 4.5 cu^2 - 1.5 u.u))
+    const V poly = q == 0 ? m.nuu15 : A::fma(cu, A::fma(A::splat(4.5f), cu, A::splat(3.0f)), m.nuu15);
+    // h - (f_eq - w), then the relaxation h + (-omega) (h - h_eq)
+    const V d = A::fma(A::splat(-wq(q)), A::fma(m.rho, poly, m.drho), h);
+    V hn = A::fma(m.nom, d, h);
+    if (BODY) hn = A::fma(m.rho, A::splat(p.wk[q]), hn);
+    return hn;
+}
+
+template <typename A, bool BODY>
+__device__ __forceinline__ void collide_t(typename A::V (&h)[19], const Params& p) {
+    const Moments<A> m = moments<A, BODY>(ArrayView<typename A::V>{h}, p);
 #pragma unroll
-    for (int q = 0; q < 19; ++q) {
-        // c_q . u: the signed velocity components, summed x, y, z
-        V cu = A::splat(0.f);
-        bool have = false;
-        if (cx(q) != 0) { cu = cx(q) > 0 ? ux : nux; have = true; }
-        if (cy(q) != 0) { const V t = cy(q) > 0 ? uy : nuy; cu = have ? A::add(cu, t) : t; have = true; }
-        if (cz(q) != 0) { const V t = cz(q) > 0 ? uz : nuz; cu = have ? A::add(cu, t) : t; }
-        // f_eq - w = w (rho - 1 + rho (3 cu + 4.5 cu^2 - 1.5 u.u))
-        const V poly = q == 0 ? nuu15 : A::fma(cu, A::fma(A::splat(4.5f), cu, A::splat(3.0f)), nuu15);
-        // h - (f_eq - w), then the relaxation h + (-omega) (h - h_eq)
-        const V d = A::fma(A::splat(-wq(q)), A::fma(rho, poly, drho), h[q]);
-        V hn = A::fma(nom, d, h[q]);
-        if (BODY) hn = A::fma(rho, A::splat(p.wk[q]), hn);
-        h[q] = hn;
-    }
+    for (int q = 0; q < 19; ++q) h[q] = relax_q<A, BODY>(m, q, h[q], p);
 }
 
 template <bool BODY>

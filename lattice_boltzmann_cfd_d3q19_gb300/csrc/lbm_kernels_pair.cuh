@@ -48,6 +48,10 @@ __device__ __forceinline__ void st2(Elem<L>* e, float2 v) {
     else *reinterpret_cast<float2*>(e) = v;
 }
 
+// Half-precision storage: two cells' stored values kept as one packed register until used.
+__device__ __forceinline__ __half2 ld2h(const __half* e) { return *reinterpret_cast<const __half2*>(e); }
+__device__ __forceinline__ __half2 pack_h(__half a, __half b) { return __halves2half2(a, b); }
+
 // Thread -> cell pair of the 3D launch (threads along x own pairs); false for the ragged tail.
 struct PairCoord {
     int x, y, z;  // coordinates of the even cell a
@@ -103,6 +107,14 @@ struct NbrPair {
         if constexpr (sx == 0) return ld2<L>(e);
         else if constexpr (sx < 0) return make_float2(ld1<L>(e + wa), ld1<L>(e));
         else return make_float2(ld1<L>(e + 1), ld1<L>(e + wb));
+    }
+    // the same, half-precision storage, packed without conversion
+    template <int Q, int S>
+    __device__ __forceinline__ __half2 load_h(const __half* e) const {
+        constexpr int sx = S * cx(Q);
+        if constexpr (sx == 0) return ld2h(e);
+        else if constexpr (sx < 0) return pack_h(e[wa], e[0]);
+        else return pack_h(e[1], e[wb]);
     }
     template <int L, int Q, int S, bool BOTH>
     __device__ __forceinline__ void store(Elem<L>* e, float2 v, bool act_a, bool act_b) const {
@@ -193,18 +205,129 @@ __device__ __forceinline__ void pair_gather(const Params& p, const NbrPair& nb, 
     if constexpr (Q < 18) pair_gather<L, FAR_OPP, WALL, Q + 1>(p, nb, n, ma, mb, h);
 }
 
+// The gather in half-precision storage: the same addresses as pair_gather, the values kept packed.
+template <bool FAR_OPP, bool WALL, int Q = 0>
+__device__ __forceinline__ void pair_gather_h(const Params& p, const NbrPair& nb, uint32_t n,
+                                              uint32_t ma, uint32_t mb, __half2 (&hh)[19]) {
+    const __half* A = static_cast<const __half*>(p.A);
+    constexpr int far_plane = FAR_OPP ? opp(Q) : Q;
+    constexpr int own_plane = FAR_OPP ? Q : opp(Q);
+    const uint32_t far = p.plane32[far_plane] + nb.template yz<Q, -1>(n);
+    if constexpr (WALL && Q > 0) {
+        const uint32_t own = p.plane32[own_plane] + n;
+        const uint32_t oa = solid_link<opp(Q)>(ma) ? own : far + (uint32_t)nb.template xa<Q, -1>();
+        const uint32_t ob = solid_link<opp(Q)>(mb) ? own + 1u : far + (uint32_t)nb.template xb<Q, -1>();
+        hh[Q] = pack_h(A[oa], A[ob]);
+    } else {
+        hh[Q] = nb.template load_h<Q, -1>(A + far);
+    }
+    if constexpr (Q < 18) pair_gather_h<FAR_OPP, WALL, Q + 1>(p, nb, n, ma, mb, hh);
+}
+
+// Half-precision storage: which kernels keep the stored pairs packed (fewer registers, 6 blocks
+// per SM) and relax each population where it is stored.  Measured at 512^3: the even step gains
+// (1.72 -> 1.60 ms); the odd and A-B steps, which also hold neighbour geometry, spilled at 5-6
+// blocks and lost, and keep the fp32 arrays at 4 blocks.
+constexpr bool kPackedHalfEven = true;
+constexpr bool kPackedHalfOdd = false;
+constexpr bool kPackedHalfAB = false;
+template <int L>
+constexpr int pair_min_blocks(bool packed) { return L == LAYOUT_STREAM_FP16 && packed ? 6 : 4; }
+
+// Post-collision values of a pair, population by population: an array relaxed in place (fp32
+// storage), or the relaxation of the stored half-precision values, done where each is stored
+// (the fp32 values of all 19 populations are then never held at once).
+struct ArraySrc {
+    const float2 (&h)[19];
+    template <int Q>
+    __device__ __forceinline__ float2 get() const { return h[Q]; }
+};
+template <bool BODY>
+struct RelaxSrc {
+    const Moments<Arith2>& m;
+    const __half2 (&hh)[19];
+    const Params& p;
+    template <int Q>
+    __device__ __forceinline__ float2 get() const {
+        // a fresh conversion of the stored pair (opaque to the compiler, so the moments pass's
+        // fp32 values are not kept alive for it)
+        unsigned bits = *reinterpret_cast<const unsigned*>(&hh[Q]);
+        asm volatile("" : "+r"(bits));
+        return relax_q<Arith2, BODY>(m, Q, __half22float2(*reinterpret_cast<const __half2*>(&bits)), p);
+    }
+};
+
+// Momentum exchange of the MOVING_WALL links of cell (x, y, z), population Q with post-collision
+// value h: c_Q (2 f*_Q - 6 w_Q (c_Q.u_w)) when x + c_Q is a MOVING_WALL cell.
+template <int Q>
+__device__ __forceinline__ void moving_link(const Params& p, int x, int y, int z, float h, float& fx,
+                                            float& fy, float& fz) {
+    const Link d = link_cell(p, x, y, z, cx(Q), cy(Q), cz(Q));
+    if ((p.flags[d.cell] & TYPE_MASK) == T_MOVING) {
+        const float t = 2.0f * (h + wq(Q)) - p.wterm[Q];
+        if (cx(Q) > 0) fx += t; else if (cx(Q) < 0) fx -= t;
+        if (cy(Q) > 0) fy += t; else if (cy(Q) < 0) fy -= t;
+        if (cz(Q) > 0) fz += t; else if (cz(Q) < 0) fz -= t;
+    }
+}
+
+// Stores of a pair at its own slots (plane opposite(q) in the AA even step, plane q in the A-B
+// steps), with the momentum exchange of the solid links (masks ma, mb) and of the moving-wall links
+// (cells with mov_a / mov_b set).
+template <int L, bool OPP_PLANE, bool FORCE, int Q = 0, typename S>
+__device__ __forceinline__ void own_store(const Params& p, Elem<L>* base, uint32_t n, const S& src,
+                                          uint32_t ma, uint32_t mb, bool mov_a, bool mov_b, int x,
+                                          int y, int z, PairForce& pf, float& fx, float& fy,
+                                          float& fz) {
+    const float2 v = src.template get<Q>();
+    st2<L>(base + (p.plane32[OPP_PLANE ? opp(Q) : Q] + n), v);
+    if constexpr (FORCE && Q > 0) {
+        pf.template link<Q>(v, solid_link<Q>(ma), solid_link<Q>(mb));
+        if (mov_a) moving_link<Q>(p, x, y, z, v.x, fx, fy, fz);
+        if (mov_b) moving_link<Q>(p, x + 1, y, z, v.y, fx, fy, fz);
+    }
+    if constexpr (Q < 18)
+        own_store<L, OPP_PLANE, FORCE, Q + 1>(p, base, n, src, ma, mb, mov_a, mov_b, x, y, z, pf, fx, fy, fz);
+}
+
 // ============================== AA pattern, even step, two cells ================================
 // Every FLUID cell; the pair's slots are read and written as aligned words.
 // 4 resident blocks per SM (64 registers): with 66 registers the fp16 kernel fell to 3 blocks
 // and lost 9% (measured)
 template <int L, bool FORCE, bool BODY>
-__global__ void __launch_bounds__(256, 4) k_aa_even2(Params p) {
+__global__ void __launch_bounds__(256, pair_min_blocks<L>(kPackedHalfEven)) k_aa_even2(Params p) {
     PairCoord c;
     float fx = 0.f, fy = 0.f, fz = 0.f;
     if (grid_pair(p, c)) {
         const PairFlags f = pair_flags(p, c.n, false);
         const bool act_a = (f.fa & TYPE_MASK) == T_FLUID, act_b = (f.fb & TYPE_MASK) == T_FLUID;
-        if (act_a || act_b) {
+        if ((act_a || act_b) && L == LAYOUT_STREAM_FP16 && kPackedHalfEven) {
+            // half-precision storage: the stored pairs stay packed; each population is relaxed
+            // where it is stored
+            __half* A = static_cast<__half*>(p.A);
+            __half2 hh[19];
+#pragma unroll
+            for (int q = 0; q < 19; ++q) hh[q] = ld2h(A + (p.plane32[q] + c.n));
+            const Moments<Arith2> m = moments<Arith2, BODY>(HalfPairView{hh}, p);
+            uint32_t ns = c.n;
+            asm volatile("" : "+r"(ns) : "f"(m.rho.x), "f"(m.rho.y));
+            uint32_t ma = 0u, mb = 0u;
+            bool mov_a = false, mov_b = false;
+            if (FORCE) {
+                const bool wa_ = act_a && !(f.fa & F_BULK), wb_ = act_b && !(f.fb & F_BULK);
+                if (wa_ || wb_) {
+                    const uint2 mm = *reinterpret_cast<const uint2*>(p.mask + c.n);
+                    ma = wa_ ? mm.x : 0u;
+                    mb = wb_ ? mm.y : 0u;
+                }
+                mov_a = p.any_moving && wa_ && (f.fa & F_SPECIAL);
+                mov_b = p.any_moving && wb_ && (f.fb & F_SPECIAL);
+            }
+            PairForce pf;
+            own_store<L, true, FORCE>(p, reinterpret_cast<Elem<L>*>(A), ns, RelaxSrc<BODY>{m, hh, p},
+                                      ma, mb, mov_a, mov_b, c.x, c.y, c.z, pf, fx, fy, fz);
+            if (FORCE) pf.into(fx, fy, fz);
+        } else if (act_a || act_b) {
             Elem<L>* A = static_cast<Elem<L>*>(p.A);
             float2 h[19];
 #pragma unroll
@@ -238,31 +361,32 @@ __global__ void __launch_bounds__(256, 4) k_aa_even2(Params p) {
 // FLUID cells that are not special.  Population q goes to (q, x + c_q); on a solid link also to
 // the own mirrored slot (opposite(q), x), which is the one the next even step reads.
 // ma, mb: solid-link masks, zero for a cell that is not updated here.
-template <int L, bool WALL, bool BOTH, bool FORCE, int Q = 0>
+template <int L, bool WALL, bool BOTH, bool FORCE, int Q = 0, typename S>
 __device__ __forceinline__ void odd2_scatter(const Params& p, const NbrPair& nb, uint32_t n,
                                              uint32_t ma, uint32_t mb, bool act_a, bool act_b,
-                                             const float2 (&h)[19], PairForce& pf) {
+                                             const S& src, PairForce& pf) {
     Elem<L>* A = static_cast<Elem<L>*>(p.A);
     const uint32_t far = p.plane32[Q] + nb.template yz<Q, 1>(n);
+    const float2 v = src.template get<Q>();
     if constexpr (WALL && Q > 0) {
         // each cell: neighbour slot, or its own mirrored slot on a solid link
         // every working cell writes its neighbour slot -- on a solid link that slot is the SOLID
         // cell's, read by nobody, and writing it keeps the sectors of the plane whole -- and on a
         // solid link also its own mirrored slot, the one the next even step reads
         const bool ba = solid_link<Q>(ma), bb = solid_link<Q>(mb);
-        nb.template store<L, Q, 1, BOTH>(A + far, h[Q], act_a, act_b);
+        nb.template store<L, Q, 1, BOTH>(A + far, v, act_a, act_b);
         Elem<L>* own = A + (p.plane32[opp(Q)] + n);
-        if (ba) st1<L>(own, h[Q].x);
-        if (bb) st1<L>(own + 1, h[Q].y);
-        if (FORCE) pf.template link<Q>(h[Q], ba, bb);
+        if (ba) st1<L>(own, v.x);
+        if (bb) st1<L>(own + 1, v.y);
+        if (FORCE) pf.template link<Q>(v, ba, bb);
     } else {
-        nb.template store<L, Q, 1, BOTH>(A + far, h[Q], act_a, act_b);
+        nb.template store<L, Q, 1, BOTH>(A + far, v, act_a, act_b);
     }
-    if constexpr (Q < 18) odd2_scatter<L, WALL, BOTH, FORCE, Q + 1>(p, nb, n, ma, mb, act_a, act_b, h, pf);
+    if constexpr (Q < 18) odd2_scatter<L, WALL, BOTH, FORCE, Q + 1>(p, nb, n, ma, mb, act_a, act_b, src, pf);
 }
 
 template <int L, bool FORCE, bool BODY>
-__global__ void __launch_bounds__(256, 4) k_aa_odd2(Params p) {
+__global__ void __launch_bounds__(256, pair_min_blocks<L>(kPackedHalfOdd)) k_aa_odd2(Params p) {
     PairCoord c;
     float fx = 0.f, fy = 0.f, fz = 0.f;
     const bool in = grid_pair(p, c);
@@ -276,7 +400,32 @@ __global__ void __launch_bounds__(256, 4) k_aa_odd2(Params p) {
     // working cells
     const bool wall = __any_sync(0xffffffffu, (f.ma | f.mb) != 0u);
     const bool both = __all_sync(0xffffffffu, act_a == act_b);
-    if (act_a || act_b) {
+    if ((act_a || act_b) && L == LAYOUT_STREAM_FP16 && kPackedHalfOdd) {
+        // half-precision storage: the gathered pairs stay packed; each population is relaxed in
+        // the scatter
+        __half2 hh[19];
+        {
+            const NbrPair nb(p, c.x, c.y, c.z);
+            if (wall) pair_gather_h<true, true>(p, nb, c.n, f.ma, f.mb, hh);
+            else pair_gather_h<true, false>(p, nb, c.n, f.ma, f.mb, hh);
+        }
+        const Moments<Arith2> m = moments<Arith2, BODY>(HalfPairView{hh}, p);
+        uint32_t ns = c.n, mas = f.ma, mbs = f.mb;
+        int xs = c.x, ys = c.y, zs = c.z;
+        asm volatile("" : "+r"(ns), "+r"(mas), "+r"(mbs), "+r"(xs), "+r"(ys), "+r"(zs)
+                     : "f"(m.rho.x), "f"(m.rho.y));
+        const NbrPair nb(p, xs, ys, zs);
+        const RelaxSrc<BODY> src{m, hh, p};
+        PairForce pf;
+        if (wall) {
+            if (both) odd2_scatter<L, true, true, FORCE>(p, nb, ns, mas, mbs, act_a, act_b, src, pf);
+            else odd2_scatter<L, true, false, FORCE>(p, nb, ns, mas, mbs, act_a, act_b, src, pf);
+            if (FORCE) pf.into(fx, fy, fz);
+        } else {
+            if (both) odd2_scatter<L, false, true, FORCE>(p, nb, ns, mas, mbs, act_a, act_b, src, pf);
+            else odd2_scatter<L, false, false, FORCE>(p, nb, ns, mas, mbs, act_a, act_b, src, pf);
+        }
+    } else if (act_a || act_b) {
         float2 h[19];
         {
             const NbrPair nb(p, c.x, c.y, c.z);
@@ -290,14 +439,15 @@ __global__ void __launch_bounds__(256, 4) k_aa_odd2(Params p) {
         asm volatile("" : "+r"(ns), "+r"(mas), "+r"(mbs), "+r"(xs), "+r"(ys), "+r"(zs)
                      : "f"(h[0].x), "f"(h[18].y));
         const NbrPair nb(p, xs, ys, zs);
+        const ArraySrc src{h};
         PairForce pf;
         if (wall) {
-            if (both) odd2_scatter<L, true, true, FORCE>(p, nb, ns, mas, mbs, act_a, act_b, h, pf);
-            else odd2_scatter<L, true, false, FORCE>(p, nb, ns, mas, mbs, act_a, act_b, h, pf);
+            if (both) odd2_scatter<L, true, true, FORCE>(p, nb, ns, mas, mbs, act_a, act_b, src, pf);
+            else odd2_scatter<L, true, false, FORCE>(p, nb, ns, mas, mbs, act_a, act_b, src, pf);
             if (FORCE) pf.into(fx, fy, fz);
         } else {
-            if (both) odd2_scatter<L, false, true, FORCE>(p, nb, ns, mas, mbs, act_a, act_b, h, pf);
-            else odd2_scatter<L, false, false, FORCE>(p, nb, ns, mas, mbs, act_a, act_b, h, pf);
+            if (both) odd2_scatter<L, false, true, FORCE>(p, nb, ns, mas, mbs, act_a, act_b, src, pf);
+            else odd2_scatter<L, false, false, FORCE>(p, nb, ns, mas, mbs, act_a, act_b, src, pf);
         }
     }
     if (FORCE) warp_force(fx, fy, fz, p.partial);
@@ -307,7 +457,7 @@ __global__ void __launch_bounds__(256, 4) k_aa_odd2(Params p) {
 // FROM_NATURAL: collide the natural state of every FLUID cell (B may equal A).  Otherwise pull-
 // collide the FLUID cells that are not special.  Results go to (q, x) of B as aligned words.
 template <int L, bool FORCE, bool BODY, bool FROM_NATURAL>
-__global__ void __launch_bounds__(256, 4) k_ab2(Params p) {
+__global__ void __launch_bounds__(256, pair_min_blocks<L>(kPackedHalfAB)) k_ab2(Params p) {
     PairCoord c;
     float fx = 0.f, fy = 0.f, fz = 0.f;
     const bool in = grid_pair(p, c);
@@ -318,7 +468,29 @@ __global__ void __launch_bounds__(256, 4) k_ab2(Params p) {
     const bool act_b = in && (f.fb & want) == T_FLUID;
     const bool wall = !FROM_NATURAL && __any_sync(0xffffffffu, (act_a || act_b) && (f.ma | f.mb) != 0u);
     Elem<L>* B = static_cast<Elem<L>*>(p.B);
-    if (act_a || act_b) {
+    if ((act_a || act_b) && L == LAYOUT_STREAM_FP16 && kPackedHalfAB) {
+        // half-precision storage: the pairs stay packed; each population is relaxed where stored
+        __half2 hh[19];
+        if (FROM_NATURAL) {
+            const __half* A = static_cast<const __half*>(p.A);
+#pragma unroll
+            for (int q = 0; q < 19; ++q) hh[q] = ld2h(A + (p.plane32[q] + c.n));
+        } else {
+            const NbrPair nb(p, c.x, c.y, c.z);
+            if (wall) pair_gather_h<false, true>(p, nb, c.n, f.ma, f.mb, hh);
+            else pair_gather_h<false, false>(p, nb, c.n, f.ma, f.mb, hh);
+        }
+        const Moments<Arith2> m = moments<Arith2, BODY>(HalfPairView{hh}, p);
+        uint32_t ns = c.n;
+        asm volatile("" : "+r"(ns) : "f"(m.rho.x), "f"(m.rho.y));
+        const uint32_t ma = (FORCE && act_a) ? f.ma : 0u, mb = (FORCE && act_b) ? f.mb : 0u;
+        const bool mov_a = FORCE && FROM_NATURAL && p.any_moving && act_a && (f.fa & F_SPECIAL);
+        const bool mov_b = FORCE && FROM_NATURAL && p.any_moving && act_b && (f.fb & F_SPECIAL);
+        PairForce pf;
+        own_store<L, false, FORCE>(p, B, ns, RelaxSrc<BODY>{m, hh, p}, ma, mb, mov_a, mov_b, c.x,
+                                   c.y, c.z, pf, fx, fy, fz);
+        if (FORCE) pf.into(fx, fy, fz);
+    } else if (act_a || act_b) {
         float2 h[19];
         if (FROM_NATURAL) {
             const Elem<L>* A = static_cast<const Elem<L>*>(p.A);

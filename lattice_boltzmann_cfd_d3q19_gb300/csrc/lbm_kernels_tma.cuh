@@ -232,14 +232,15 @@ __global__ void __launch_bounds__(kTmaThreads, 1) k_aa_odd_tma(Params p) {
             tma_gather<L>(st, j, x, p.nx, ma, mb, p.any_solid_link != 0, h);
             collide2<BODY>(h, p);
             const NbrPair nb(p, x, r % p.ny, r / p.ny);
+            const ArraySrc src{h};
             PairForce pf;
             if (wall) {
-                if (both) odd2_scatter<L, true, true, FORCE>(p, nb, n, ma, mb, act_a, act_b, h, pf);
-                else odd2_scatter<L, true, false, FORCE>(p, nb, n, ma, mb, act_a, act_b, h, pf);
+                if (both) odd2_scatter<L, true, true, FORCE>(p, nb, n, ma, mb, act_a, act_b, src, pf);
+                else odd2_scatter<L, true, false, FORCE>(p, nb, n, ma, mb, act_a, act_b, src, pf);
                 if (FORCE) pf.into(fx, fy, fz);
             } else {
-                if (both) odd2_scatter<L, false, true, FORCE>(p, nb, n, ma, mb, act_a, act_b, h, pf);
-                else odd2_scatter<L, false, false, FORCE>(p, nb, n, ma, mb, act_a, act_b, h, pf);
+                if (both) odd2_scatter<L, false, true, FORCE>(p, nb, n, ma, mb, act_a, act_b, src, pf);
+                else odd2_scatter<L, false, false, FORCE>(p, nb, n, ma, mb, act_a, act_b, src, pf);
             }
         }
         // every thread is done with stage s before it is refilled
