@@ -163,21 +163,6 @@ struct Params {
     uint32_t plane32[19];
 };
 
-// ---- per-link geometry ----------------------------------------------------------------------------
-// Coordinate v + c along an axis of n cells: wrapped on a periodic axis; on an open axis a value
-// beyond the face is clamped onto the last layer and *beyond is set.
-__device__ __forceinline__ int clampwrap(int v, int n, int open, bool& beyond) {
-    if (v < 0) {
-        if (open) { beyond = true; return 0; }
-        return v + n;
-    }
-    if (v >= n) {
-        if (open) { beyond = true; return n - 1; }
-        return v - n;
-    }
-    return v;
-}
-
 // ---- collision -------------------------------------------------------------------------------------
 // BGK with the second-order equilibrium (c_s^2 = 1/3) on shifted populations, plus Guo forcing
 // when BODY: u = j/rho + g/2, F = rho g, source (1 - omega/2) w [3 (c - u).F + 9 (c.u)(c.F)].
