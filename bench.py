@@ -315,6 +315,25 @@ def variant(B, torch, n, scheme, steps=10, warmup=3, cavity=False, fp16=False, l
             "kernels": kernels}
 
 
+def cpu_description():
+    """Host CPU for the CPU baseline: architecture, model (x86 'model name', or the Arm
+    implementer/part codes) and logical CPU count."""
+    import platform
+    model = None
+    try:
+        info = {}
+        with open("/proc/cpuinfo") as fh:
+            for line in fh:
+                k, _, v = line.partition(":")
+                info.setdefault(k.strip(), v.strip())
+        model = info.get("model name") or (
+            f"implementer {info['CPU implementer']} part {info['CPU part']}"
+            if "CPU part" in info else None)
+    except OSError:
+        pass
+    return {"machine": platform.machine(), "model": model, "logical_cpus": os.cpu_count()}
+
+
 def cpu_baseline(n=512, ny_sample=16, target_s=15.0):
     """The CPU oracle, as it is, on a bounded sample of the porous workload: a 512 x ny_sample x
     512 slab of the same flags (periodic), same tau and body force."""
@@ -342,7 +361,7 @@ def cpu_baseline(n=512, ny_sample=16, target_s=15.0):
     P1.step_ab(f1, 4)
     dt1 = time.perf_counter() - t0
     return {"value": round(Ns * steps / dt / 1e6, 3), "unit": UNIT, "cores": cores,
-            "kind": "oracle",
+            "kind": "oracle", "cpu": cpu_description(),
             "sample": f"{n}x{ny_sample}x{n} slab of the porous 512^3 flags, periodic, {steps} steps "
                       f"({dt:.1f} s), fp64 two-lattice oracle",
             "single_thread": {"value": round(N1 * 4 / dt1 / 1e6, 3), "unit": UNIT, "cores": 1,
@@ -507,7 +526,7 @@ def run_reference(args):
                                        float((flags == wl.FLUID).mean())),
                        sample=sample),
         "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": oracle.max_threads(),
-                         "kind": "oracle", "sample": sample},
+                         "kind": "oracle", "cpu": cpu_description(), "sample": sample},
         "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }), flush=True)
