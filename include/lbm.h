@@ -189,6 +189,17 @@ int lbm_set_cell_pairs(lbm_ctx* ctx, int enable);
  * step; the staging is a GB300 launch choice, not a page's design.) */
 int lbm_set_tma_gather(lbm_ctx* ctx, int enable);
 
+/* Run each step's boundary kernel (the special cells: neighbours of INLET and MOVING_WALL cells,
+ * links across OPEN faces) beside the step's main kernel (enable != 0, the default) or after it
+ * (enable = 0).  Beside: the boundary kernel goes to a private stream of the highest priority,
+ * forked from the context stream after the open-face pre-gather and joined back before the next
+ * kernel, so lbm_step's ordering on the context stream is unchanged.  The two kernels store into
+ * disjoint slots, so the populations are bit-identical either way.  Steps run one after the
+ * other while per-kernel profiling is on.  Returns LBM_OK, LBM_EINVAL for a NULL context; drops
+ * the cached step graphs.  (A launch choice for the same update; the per-link rules are
+ * [Layout]'s.) */
+int lbm_set_boundary_overlap(lbm_ctx* ctx, int enable);
+
 /* Density and velocity of the natural state: rho[N], u[3*N] (fp32).  FLUID: rho = sum f,
  * u = j/rho + g/2 (Guo's half-force shift).  SOLID: 0, 0.  INLET: rho_in, u_in.  MOVING_WALL:
  * 1, u_w.  Synchronous. */

@@ -41,6 +41,7 @@ SIGNATURES = {
     "lbm_set_graph_launch": (_I, [_P, _I]),
     "lbm_set_cell_pairs": (_I, [_P, _I]),
     "lbm_set_tma_gather": (_I, [_P, _I]),
+    "lbm_set_boundary_overlap": (_I, [_P, _I]),
     "lbm_macroscopic": (_I, [_P, _P, _P]),
     "lbm_force_momentum_exchange": (_I, [_P, _P]),
     "lbm_check_finite": (_I, [_P]),
@@ -194,6 +195,11 @@ def lbm_set_tma_gather(ctx: int, enable: bool) -> bool:
     if rc < 0:
         raise LbmError(rc, _err())
     return rc == 1
+
+
+def lbm_set_boundary_overlap(ctx: int, enable: bool) -> None:
+    """Run each step's boundary kernel beside its main kernel (True) or after it (False)."""
+    _check(load().lbm_set_boundary_overlap(ctx, 1 if enable else 0))
 
 
 def lbm_macroscopic(ctx: int, rho, u) -> None:

@@ -143,6 +143,15 @@ struct lbm_ctx {
     cudaEvent_t stage_free[2] = {nullptr, nullptr};  // a half's consumer is done with it
     cudaEvent_t stage_mark = nullptr;                // start / end marker between the streams
     cudaStream_t stream = nullptr;
+    // The boundary kernel of a step runs beside the step's main kernel, on a second stream of the
+    // highest priority forked from `stream` and joined back into it: the two store into disjoint
+    // slots (each cell's own), and the special cells' latency-bound warps then overlap the main
+    // kernel's streaming instead of following it.  Serial while profiling (per-kernel times) or
+    // when the caller switches it off.
+    cudaStream_t side_stream = nullptr;
+    cudaEvent_t side_fork = nullptr, side_join = nullptr;
+    bool overlap_allowed = true;
+    bool overlap() const { return overlap_allowed && !profiling && n_special > 0; }
     int64_t steps = 0;
     bool force_valid = false;
     int64_t launches = 0;
@@ -279,6 +288,9 @@ struct lbm_ctx {
         }
         if (stage_mark) cudaEventDestroy(stage_mark);
         if (copy_stream) cudaStreamDestroy(copy_stream);
+        if (side_fork) cudaEventDestroy(side_fork);
+        if (side_join) cudaEventDestroy(side_join);
+        if (side_stream) cudaStreamDestroy(side_stream);
         cudaFreeHost(force_host);
         cudaFreeHost(err_host);
         cudaFree(fault_dev);
@@ -440,7 +452,8 @@ int z_reversed(const lbm_ctx* c, int kind) {
     }
 }
 
-int launch_kind(lbm_ctx* c, int kind, const Params& p_in, bool force, int main_kind = -1) {
+int launch_kind(lbm_ctx* c, int kind, const Params& p_in, bool force, int main_kind = -1,
+                cudaStream_t boundary_stream = nullptr) {
     Params p = p_in;
     p.zrev = z_reversed(c, kind);
     if (kind == K_BOUNDARY && c->n_special == 0) return LBM_OK;
@@ -458,7 +471,8 @@ int launch_kind(lbm_ctx* c, int kind, const Params& p_in, bool force, int main_k
         e = launch_force_finalize(c->partial, c->force_triples, c->stage, c->force_dev, c->stream);
         c->launches += 2;
     } else if (kind == K_BOUNDARY) {
-        e = c->ops->special(main_kind, p, force, c->body(), c->stream);
+        e = c->ops->special(main_kind, p, force, c->body(),
+                            boundary_stream ? boundary_stream : c->stream);
         ++c->launches;
         if (force) c->force_triples = partial_triples(c->main_blocks_for(main_kind), c->n_special);
     } else {
@@ -480,6 +494,29 @@ int launch_kind(lbm_ctx* c, int kind, const Params& p_in, bool force, int main_k
     return LBM_OK;
 }
 
+// The main kernel of step kind `kind` and its boundary kernel: side by side on two streams when
+// the context allows it, else one after the other on the context stream.
+int main_and_boundary(lbm_ctx* c, int kind, const Params& p, bool force) {
+    if (!c->overlap()) {
+        int rc = launch_kind(c, kind, p, force);
+        if (rc == LBM_OK) rc = launch_kind(c, K_BOUNDARY, p, force, kind);
+        return rc;
+    }
+    LBM_CUDA(cudaEventRecord(c->side_fork, c->stream), "lbm_step: fork");
+    LBM_CUDA(cudaStreamWaitEvent(c->side_stream, c->side_fork, 0), "lbm_step: fork");
+    // the boundary kernel first: its blocks are then dispatched ahead of the main kernel's
+    int rc = launch_kind(c, K_BOUNDARY, p, force, kind, c->side_stream);
+    if (rc == LBM_OK) rc = launch_kind(c, kind, p, force);
+    // joined even after a failed launch, so that a capture in progress ends joined
+    cudaError_t e = cudaEventRecord(c->side_join, c->side_stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(c->stream, c->side_join, 0);
+    if (rc != LBM_OK) return rc;
+    if (e != cudaSuccess) return cuda_fail(e, "lbm_step: join");
+    // both kernels' force partials (the main kernel's launch recorded only its own)
+    if (force) c->force_triples = partial_triples(c->main_blocks_for(kind), c->n_special);
+    return LBM_OK;
+}
+
 int step_once(lbm_ctx* c, bool last) {
     int rc = LBM_OK;
     if (c->streaming == LBM_STREAMING_AA) {
@@ -492,8 +529,7 @@ int step_once(lbm_ctx* c, bool last) {
             Params po = p;
             po.part_special = c->main_blocks_for(K_AA_ODD) * kWarpsPerBlock;
             if (c->any_open()) rc = launch_kind(c, K_PREGATHER, po, false);
-            if (rc == LBM_OK) rc = launch_kind(c, K_AA_ODD, po, last);
-            if (rc == LBM_OK) rc = launch_kind(c, K_BOUNDARY, po, last, K_AA_ODD);
+            if (rc == LBM_OK) rc = main_and_boundary(c, K_AA_ODD, po, last);
             c->state = ST_NATURAL;
         }
     } else if (c->streaming == LBM_STREAMING_AB) {
@@ -501,8 +537,7 @@ int step_once(lbm_ctx* c, bool last) {
         if (c->state == ST_NATURAL) {
             rc = launch_kind(c, K_AB_COLLIDE, p, last);
         } else {
-            rc = launch_kind(c, K_AB_PULL, p, last);
-            if (rc == LBM_OK) rc = launch_kind(c, K_BOUNDARY, p, last, K_AB_PULL);
+            rc = main_and_boundary(c, K_AB_PULL, p, last);
         }
         c->cur ^= 1;
         c->state = ST_POST_AB;
@@ -510,8 +545,7 @@ int step_once(lbm_ctx* c, bool last) {
         const Params pc = c->params(c->buf[c->cur], c->buf[c->cur]);
         rc = launch_kind(c, K_AB_COLLIDE, pc, last);
         const Params ps = c->params(c->buf[c->cur], c->buf[c->cur ^ 1]);
-        if (rc == LBM_OK) rc = launch_kind(c, K_STREAM, ps, false);
-        if (rc == LBM_OK) rc = launch_kind(c, K_BOUNDARY, ps, false, K_STREAM);
+        if (rc == LBM_OK) rc = main_and_boundary(c, K_STREAM, ps, false);
         c->cur ^= 1;
         c->state = ST_NATURAL;
     }
@@ -703,6 +737,14 @@ lbm_ctx* lbm_create(int nx, int ny, int nz, float tau, int layout, int streaming
     if ((e = cudaMalloc(&c->fault_dev, sizeof(int))) != cudaSuccess) return bad(e, "lbm_create: fault word");
     if ((e = cudaMallocHost(&c->fault_host, sizeof(int))) != cudaSuccess) return bad(e, "lbm_create: pinned fault word");
     *c->fault_host = 0;
+    int prio_least = 0, prio_greatest = 0;
+    if ((e = cudaDeviceGetStreamPriorityRange(&prio_least, &prio_greatest)) != cudaSuccess)
+        return bad(e, "lbm_create: stream priorities");
+    if ((e = cudaStreamCreateWithPriority(&c->side_stream, cudaStreamNonBlocking, prio_greatest)) != cudaSuccess)
+        return bad(e, "lbm_create: boundary stream");
+    if ((e = cudaEventCreateWithFlags(&c->side_fork, cudaEventDisableTiming)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&c->side_join, cudaEventDisableTiming)) != cudaSuccess)
+        return bad(e, "lbm_create: boundary stream events");
     if (const char* v = std::getenv("LBM_TEST_STAGE_TIMEOUT"); v && std::strcmp(v, "1") == 0)
         c->extra_tx = 16;
     // LBM_PROFILE=1: per-kernel event timing from the start, as lbm_profile_enable(ctx, 1)
@@ -1042,6 +1084,15 @@ int lbm_set_tma_gather(lbm_ctx* c, int enable) {
         c->tma_allowed = enable != 0;
     }
     return c->tma() ? 1 : 0;
+}
+
+int lbm_set_boundary_overlap(lbm_ctx* c, int enable) {
+    if (!c) return fail(LBM_EINVAL, "lbm_set_boundary_overlap: NULL context");
+    if (c->overlap_allowed != (enable != 0)) {
+        c->drop_graphs();
+        c->overlap_allowed = enable != 0;
+    }
+    return LBM_OK;
 }
 
 int lbm_set_graph_launch(lbm_ctx* c, int enable) {

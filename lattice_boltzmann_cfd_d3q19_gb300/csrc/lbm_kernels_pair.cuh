@@ -10,11 +10,11 @@
 // Same steps and per-link rules as the one-cell kernels ("GPU lattice Boltzmann: streaming layout
 // and performance", "In place" and "Two buffers"), with one difference in which slots a launch
 // touches, confined to slots that nothing reads: the even AA step and the A-B steps store both
-// cells of a pair, so a non-FLUID cell beside a FLUID one gets its (never-read) slots overwritten,
-// and in the A-B pull a special cell's destination slots are written before its boundary kernel
-// overwrites them; the odd AA step also writes a bounced population to its neighbour slot, which
-// belongs to the SOLID cell it bounced from and is read by nobody.  Otherwise the odd AA step
-// stores per cell (a SOLID or special cell's stores would land in slots other cells read).
+// cells of a pair, so a non-FLUID cell beside a FLUID one gets its (never-read) slots overwritten
+// (never a special cell's: its boundary kernel may run at the same time); the odd AA step also
+// writes a bounced population to its neighbour slot, which belongs to the SOLID cell it bounced
+// from and is read by nobody.  Otherwise the odd AA step stores per cell (a SOLID or special
+// cell's stores would land in slots other cells read).
 #pragma once
 
 #include <type_traits>
@@ -46,6 +46,22 @@ template <int L>
 __device__ __forceinline__ void st2(Elem<L>* e, float2 v) {
     if constexpr (L == LAYOUT_STREAM_FP16) *reinterpret_cast<__half2*>(e) = __float22half2_rn(v);
     else *reinterpret_cast<float2*>(e) = v;
+}
+
+// A pair's two elements, or only one of them: keep_a / keep_b (one conversion of the pair in
+// half precision, whose halves round as the single conversions do).
+template <int L>
+__device__ __forceinline__ void st2_keep(Elem<L>* e, float2 v, bool keep_a, bool keep_b) {
+    if constexpr (L == LAYOUT_STREAM_FP16) {
+        const __half2 hv = __float22half2_rn(v);
+        if (keep_a && keep_b) *reinterpret_cast<__half2*>(e) = hv;
+        else if (keep_a) e[0] = __low2half(hv);
+        else if (keep_b) e[1] = __high2half(hv);
+    } else {
+        if (keep_a && keep_b) *reinterpret_cast<float2*>(e) = v;
+        else if (keep_a) e[0] = v.x;
+        else if (keep_b) e[1] = v.y;
+    }
 }
 
 // Stores of the odd AA step, with the evict-first ("streaming") cache hint in fp32 storage: the
@@ -155,6 +171,9 @@ struct PairFlags {
     uint8_t fa, fb;
     uint32_t ma, mb;
 };
+__device__ __forceinline__ bool special_fluid(uint8_t fl) {
+    return (fl & (TYPE_MASK | F_SPECIAL)) == (T_FLUID | F_SPECIAL);
+}
 __device__ __forceinline__ PairFlags pair_flags(const Params& p, uint32_t n, bool want_mask) {
     PairFlags f;
     const uint16_t fl = *reinterpret_cast<const uint16_t*>(p.flags + n);
@@ -241,10 +260,9 @@ __device__ __forceinline__ void pair_gather_h(const Params& p, const NbrPair& nb
 // Half-precision storage: which kernels keep the stored pairs packed (fewer registers, 6 blocks
 // per SM) and relax each population where it is stored.  Measured at 512^3: the even step gains
 // (1.72 -> 1.60 ms); the odd and A-B steps, which also hold neighbour geometry, spilled at 5-6
-// blocks and lost, and keep the fp32 arrays at 4 blocks.
+// blocks and lost, and keep the fp32 arrays at 4 blocks (the A-B pull has no packed form).
 constexpr bool kPackedHalfEven = true;
 constexpr bool kPackedHalfOdd = false;
-constexpr bool kPackedHalfAB = false;
 template <int L>
 constexpr int pair_min_blocks(bool packed) { return L == LAYOUT_STREAM_FP16 && packed ? 6 : 4; }
 
@@ -469,9 +487,11 @@ __global__ void __launch_bounds__(256, pair_min_blocks<L>(kPackedHalfOdd)) k_aa_
 
 // ============================== two buffers (A-B), two cells ====================================
 // FROM_NATURAL: collide the natural state of every FLUID cell (B may equal A).  Otherwise pull-
-// collide the FLUID cells that are not special.  Results go to (q, x) of B as aligned words.
+// collide the FLUID cells that are not special.  Results go to (q, x) of B as aligned words.  The
+// pull stores nothing into a special cell's slots: the boundary kernel writes those, possibly at
+// the same time on another stream; a warp holding special cells stores element by element.
 template <int L, bool FORCE, bool BODY, bool FROM_NATURAL>
-__global__ void __launch_bounds__(256, pair_min_blocks<L>(kPackedHalfAB)) k_ab2(Params p) {
+__global__ void __launch_bounds__(256, 4) k_ab2(Params p) {
     PairCoord c;
     float fx = 0.f, fy = 0.f, fz = 0.f;
     const bool in = grid_pair(p, c);
@@ -480,31 +500,12 @@ __global__ void __launch_bounds__(256, pair_min_blocks<L>(kPackedHalfAB)) k_ab2(
     const uint8_t want = FROM_NATURAL ? TYPE_MASK : (TYPE_MASK | F_SPECIAL);
     const bool act_a = in && (f.fa & want) == T_FLUID;
     const bool act_b = in && (f.fb & want) == T_FLUID;
+    const bool spec_a = !FROM_NATURAL && in && special_fluid(f.fa);
+    const bool spec_b = !FROM_NATURAL && in && special_fluid(f.fb);
     const bool wall = !FROM_NATURAL && __any_sync(0xffffffffu, (act_a || act_b) && (f.ma | f.mb) != 0u);
+    const bool split = !FROM_NATURAL && __any_sync(0xffffffffu, spec_a || spec_b);
     Elem<L>* B = static_cast<Elem<L>*>(p.B);
-    if ((act_a || act_b) && L == LAYOUT_STREAM_FP16 && kPackedHalfAB) {
-        // half-precision storage: the pairs stay packed; each population is relaxed where stored
-        __half2 hh[19];
-        if (FROM_NATURAL) {
-            const __half* A = static_cast<const __half*>(p.A);
-#pragma unroll
-            for (int q = 0; q < 19; ++q) hh[q] = ld2h(A + (p.plane32[q] + c.n));
-        } else {
-            const NbrPair nb(p, c.x, c.y, c.z);
-            if (wall) pair_gather_h<false, true>(p, nb, c.n, f.ma, f.mb, hh);
-            else pair_gather_h<false, false>(p, nb, c.n, f.ma, f.mb, hh);
-        }
-        const Moments<Arith2> m = moments<Arith2, BODY>(HalfPairView{hh}, p);
-        uint32_t ns = c.n;
-        asm volatile("" : "+r"(ns) : "f"(m.rho.x), "f"(m.rho.y));
-        const uint32_t ma = (FORCE && act_a) ? f.ma : 0u, mb = (FORCE && act_b) ? f.mb : 0u;
-        const bool mov_a = FORCE && FROM_NATURAL && p.any_moving && act_a && (f.fa & F_SPECIAL);
-        const bool mov_b = FORCE && FROM_NATURAL && p.any_moving && act_b && (f.fb & F_SPECIAL);
-        PairForce pf;
-        own_store<L, false, FORCE>(p, B, ns, RelaxSrc<BODY>{m, hh, p}, ma, mb, mov_a, mov_b, c.x,
-                                   c.y, c.z, pf, fx, fy, fz);
-        if (FORCE) pf.into(fx, fy, fz);
-    } else if (act_a || act_b) {
+    if (act_a || act_b) {
         float2 h[19];
         if (FROM_NATURAL) {
             const Elem<L>* A = static_cast<const Elem<L>*>(p.A);
@@ -518,8 +519,16 @@ __global__ void __launch_bounds__(256, pair_min_blocks<L>(kPackedHalfAB)) k_ab2(
         collide2<BODY>(h, p);
         uint32_t ns = c.n;
         asm volatile("" : "+r"(ns) : "f"(h[0].x), "f"(h[18].y));
+        if (!split) {
 #pragma unroll
-        for (int q = 0; q < 19; ++q) st2<L>(B + (p.plane32[q] + ns), h[q]);
+            for (int q = 0; q < 19; ++q) st2<L>(B + (p.plane32[q] + ns), h[q]);
+        } else {
+            // the pair's flags again (not held across the collision)
+            const PairFlags g = pair_flags(p, ns, false);
+            const bool keep_a = !special_fluid(g.fa), keep_b = !special_fluid(g.fb);
+#pragma unroll
+            for (int q = 0; q < 19; ++q) st2_keep<L>(B + (p.plane32[q] + ns), h[q], keep_a, keep_b);
+        }
         if (FORCE) {
             if ((act_a && f.ma) || (act_b && f.mb)) {
                 PairForce pf;
@@ -532,10 +541,11 @@ __global__ void __launch_bounds__(256, pair_min_blocks<L>(kPackedHalfAB)) k_ab2(
             }
         }
     } else if (in && p.B != p.A) {
-        // no working cell: SOLID / INLET / MOVING_WALL slots are never read and special cells'
-        // are rewritten by the boundary kernel; zeros keep every sector of B fully written
+        // no working cell: SOLID / INLET / MOVING_WALL slots are never read; zeros keep every
+        // sector of B fully written
 #pragma unroll
-        for (int q = 0; q < 19; ++q) st2<L>(B + (p.plane32[q] + c.n), make_float2(0.f, 0.f));
+        for (int q = 0; q < 19; ++q)
+            st2_keep<L>(B + (p.plane32[q] + c.n), make_float2(0.f, 0.f), !spec_a, !spec_b);
     }
     if (FORCE) warp_force(fx, fy, fz, p.partial);
 }

@@ -61,13 +61,15 @@ class Case:
     def run_oracle(self, steps, want_force=False):
         return self.oracle_problem().step_ab(self.f0_32.astype(np.float64), steps, want_force)
 
-    def gpu_context(self, layout="stream", scheme="AA", device_input=True, pairs=True, tma=False):
+    def gpu_context(self, layout="stream", scheme="AA", device_input=True, pairs=True, tma=False,
+                    overlap=True):
         import torch
         ctx = B.lbm_create(self.nx, self.ny, self.nz, self.tau, {**LAYOUTS, **FP16}[layout],
                            SCHEMES[scheme])
         try:
             B.lbm_set_cell_pairs(ctx, pairs)
             B.lbm_set_tma_gather(ctx, tma)
+            B.lbm_set_boundary_overlap(ctx, overlap)
             B.lbm_set_flags(ctx, self.flags)
             B.lbm_set_faces(ctx, *self.faces)
             B.lbm_set_inlet(ctx, *self.inlet)
@@ -83,12 +85,14 @@ class Case:
         return ctx
 
     def run_gpu(self, steps, layout="stream", scheme="AA", want_force=False, chunks=None,
-                device_input=True, pairs=True, tma=False):
+                device_input=True, pairs=True, tma=False, overlap=True, graphs=True):
         """Returns (f[19, N] float64, force or None).  `chunks` splits the steps into several
         lbm_step calls (the force belongs to the last call).  pairs=False forbids the two-cell
-        kernels, tma=True allows the TMA-staged odd step."""
-        ctx = self.gpu_context(layout, scheme, device_input, pairs, tma)
+        kernels, tma=True allows the TMA-staged odd step, overlap=False runs each boundary kernel
+        after its main kernel, graphs=False launches kernel by kernel."""
+        ctx = self.gpu_context(layout, scheme, device_input, pairs, tma, overlap)
         try:
+            B.lbm_set_graph_launch(ctx, graphs)
             for n in (chunks or [steps]):
                 B.lbm_step(ctx, n)
             f = np.zeros((19, self.N), np.float32)

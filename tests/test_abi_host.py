@@ -68,6 +68,7 @@ def test_null_context_calls_fail_cleanly():
     assert lib.lbm_check_finite(None) == B.EINVAL
     assert lib.lbm_set_cell_pairs(None, 1) == B.EINVAL
     assert lib.lbm_set_tma_gather(None, 1) == B.EINVAL
+    assert lib.lbm_set_boundary_overlap(None, 1) == B.EINVAL
     assert lib.lbm_set_graph_launch(None, 1) == B.EINVAL
     assert lib.lbm_step_count(None) == -1
     assert lib.lbm_kernel_launches(None) == -1

@@ -646,6 +646,45 @@ def test_cell_pairs_match_oracle(ci, scheme):
     assert np.abs(Fg - Fo).max() <= 1e-4 * max(1.0, float(np.abs(Fo).max()))
 
 
+# ---- boundary kernel beside the main kernel (lbm_set_boundary_overlap) ------------------------------
+
+# cases with special cells (inlet layers, open faces, moving walls); the last one large enough
+# that the boundary and main kernels run at the same time on the device
+OVERLAP_CASES = [2, 3, 4, 5, 7, 8, (96, 48, 40, (1, 0, 0), 0.1, True, 0.2)]
+
+
+@pytest.mark.parametrize("graphs", [True, False])
+@pytest.mark.parametrize("pairs", [True, False])
+@pytest.mark.parametrize("scheme", ["AA", "AB", "AB2"])
+@pytest.mark.parametrize("layout", ["stream", "stream_fp16", "collision"])
+@pytest.mark.parametrize("ci", range(len(OVERLAP_CASES)))
+def test_boundary_overlap_bit_identical(ci, layout, scheme, pairs, graphs):
+    """The boundary kernel on its own stream beside the main kernel stores into slots the main
+    kernel leaves alone: populations and force are identical to the serial order."""
+    spec = OVERLAP_CASES[ci]
+    nx, ny, nz, faces, solid, inlet, moving = PAIR_CASES[spec] if isinstance(spec, int) else spec
+    case = mixed_case(nx, ny, nz, faces, 960 + ci, solid=solid, inlet_layer=inlet, moving=moving)
+    for steps in (3, 6):
+        fo, Fo = case.run_gpu(steps, layout, scheme, want_force=True, pairs=pairs, graphs=graphs,
+                              overlap=True)
+        fs, Fs = case.run_gpu(steps, layout, scheme, want_force=True, pairs=pairs, graphs=graphs,
+                              overlap=False)
+        fl = case.fluid
+        assert np.array_equal(fo[:, fl], fs[:, fl]), (steps, np.abs(fo[:, fl] - fs[:, fl]).max())
+        assert np.array_equal(Fo, Fs), (steps, Fo, Fs)
+
+
+def test_boundary_overlap_large_case_matches_oracle():
+    """The overlapped AA and A-B steps on the large overlap case against the oracle."""
+    nx, ny, nz, faces, solid, inlet, moving = OVERLAP_CASES[-1]
+    case = mixed_case(nx, ny, nz, faces, 990, solid=solid, inlet_layer=inlet, moving=moving)
+    fo, Fo = case.run_oracle(6, want_force=True)
+    for scheme in ("AA", "AB"):
+        fg, Fg = case.run_gpu(6, "stream", scheme, want_force=True)
+        assert max_fluid_diff(case, fg, fo) <= TOL_F, scheme
+        assert np.abs(Fg - Fo).max() <= 1e-4 * max(1.0, float(np.abs(Fo).max())), scheme
+
+
 def test_cell_pairs_eligibility():
     def state(nx, layout, allow=True):
         ctx = B.lbm_create(nx, 6, 4, 0.6, layout, B.STREAMING_AA)
