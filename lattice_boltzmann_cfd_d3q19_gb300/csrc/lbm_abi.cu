@@ -144,14 +144,19 @@ struct lbm_ctx {
     cudaEvent_t stage_mark = nullptr;                // start / end marker between the streams
     cudaStream_t stream = nullptr;
     // The boundary kernel of a step runs beside the step's main kernel, on a second stream of the
-    // highest priority forked from `stream` and joined back into it: the two store into disjoint
-    // slots (each cell's own), and the special cells' latency-bound warps then overlap the main
-    // kernel's streaming instead of following it.  Serial while profiling (per-kernel times) or
-    // when the caller switches it off.
+    // highest priority forked from `stream` and joined back into it, where the main kernel
+    // stores into no slot of a special cell (the AA odd kernels, the one-cell A-B pull and the
+    // streaming pass): the special cells' latency-bound warps then overlap the main kernel's
+    // streaming instead of following it.  The two-cell A-B pull writes special cells' slots with
+    // its whole-sector word stores and keeps the serial order.  Serial while profiling
+    // (per-kernel times) or when the caller switches it off.
     cudaStream_t side_stream = nullptr;
     cudaEvent_t side_fork = nullptr, side_join = nullptr;
     bool overlap_allowed = true;
-    bool overlap() const { return overlap_allowed && !profiling && n_special > 0; }
+    bool overlap(int kind) const {
+        if (!overlap_allowed || profiling || n_special == 0) return false;
+        return !(kind == K_AB_PULL && pairs());
+    }
     int64_t steps = 0;
     bool force_valid = false;
     int64_t launches = 0;
@@ -497,7 +502,7 @@ int launch_kind(lbm_ctx* c, int kind, const Params& p_in, bool force, int main_k
 // The main kernel of step kind `kind` and its boundary kernel: side by side on two streams when
 // the context allows it, else one after the other on the context stream.
 int main_and_boundary(lbm_ctx* c, int kind, const Params& p, bool force) {
-    if (!c->overlap()) {
+    if (!c->overlap(kind)) {
         int rc = launch_kind(c, kind, p, force);
         if (rc == LBM_OK) rc = launch_kind(c, K_BOUNDARY, p, force, kind);
         return rc;

@@ -10,11 +10,12 @@
 // Same steps and per-link rules as the one-cell kernels ("GPU lattice Boltzmann: streaming layout
 // and performance", "In place" and "Two buffers"), with one difference in which slots a launch
 // touches, confined to slots that nothing reads: the even AA step and the A-B steps store both
-// cells of a pair, so a non-FLUID cell beside a FLUID one gets its (never-read) slots overwritten
-// (never a special cell's: its boundary kernel may run at the same time); the odd AA step also
-// writes a bounced population to its neighbour slot, which belongs to the SOLID cell it bounced
-// from and is read by nobody.  Otherwise the odd AA step stores per cell (a SOLID or special
-// cell's stores would land in slots other cells read).
+// cells of a pair, so a non-FLUID cell beside a FLUID one gets its (never-read) slots overwritten,
+// and in the A-B pull a special cell's destination slots are written before its boundary kernel
+// overwrites them; the odd AA step also writes a bounced population to its neighbour slot, which
+// belongs to the SOLID cell it bounced from and is read by nobody.  Otherwise the odd AA step
+// stores per cell (a SOLID or special cell's stores would land in slots other cells read, and its
+// boundary kernel runs at the same time).
 #pragma once
 
 #include <type_traits>
@@ -46,22 +47,6 @@ template <int L>
 __device__ __forceinline__ void st2(Elem<L>* e, float2 v) {
     if constexpr (L == LAYOUT_STREAM_FP16) *reinterpret_cast<__half2*>(e) = __float22half2_rn(v);
     else *reinterpret_cast<float2*>(e) = v;
-}
-
-// A pair's two elements, or only one of them: keep_a / keep_b (one conversion of the pair in
-// half precision, whose halves round as the single conversions do).
-template <int L>
-__device__ __forceinline__ void st2_keep(Elem<L>* e, float2 v, bool keep_a, bool keep_b) {
-    if constexpr (L == LAYOUT_STREAM_FP16) {
-        const __half2 hv = __float22half2_rn(v);
-        if (keep_a && keep_b) *reinterpret_cast<__half2*>(e) = hv;
-        else if (keep_a) e[0] = __low2half(hv);
-        else if (keep_b) e[1] = __high2half(hv);
-    } else {
-        if (keep_a && keep_b) *reinterpret_cast<float2*>(e) = v;
-        else if (keep_a) e[0] = v.x;
-        else if (keep_b) e[1] = v.y;
-    }
 }
 
 // Stores of the odd AA step, with the evict-first ("streaming") cache hint in fp32 storage: the
@@ -171,9 +156,6 @@ struct PairFlags {
     uint8_t fa, fb;
     uint32_t ma, mb;
 };
-__device__ __forceinline__ bool special_fluid(uint8_t fl) {
-    return (fl & (TYPE_MASK | F_SPECIAL)) == (T_FLUID | F_SPECIAL);
-}
 __device__ __forceinline__ PairFlags pair_flags(const Params& p, uint32_t n, bool want_mask) {
     PairFlags f;
     const uint16_t fl = *reinterpret_cast<const uint16_t*>(p.flags + n);
@@ -487,9 +469,11 @@ __global__ void __launch_bounds__(256, pair_min_blocks<L>(kPackedHalfOdd)) k_aa_
 
 // ============================== two buffers (A-B), two cells ====================================
 // FROM_NATURAL: collide the natural state of every FLUID cell (B may equal A).  Otherwise pull-
-// collide the FLUID cells that are not special.  Results go to (q, x) of B as aligned words.  The
-// pull stores nothing into a special cell's slots: the boundary kernel writes those, possibly at
-// the same time on another stream; a warp holding special cells stores element by element.
+// collide the FLUID cells that are not special.  Results go to (q, x) of B as aligned words, a
+// special cell's slots included (its boundary kernel, launched after this one, overwrites them):
+// every sector of B is then written whole.  Leaving those slots out, so that the boundary kernel
+// could run at the same time, cost 8-13% on the sphere workload (partly written sectors filled
+// from DRAM) for a 1-3% gain from the overlap.
 template <int L, bool FORCE, bool BODY, bool FROM_NATURAL>
 __global__ void __launch_bounds__(256, 4) k_ab2(Params p) {
     PairCoord c;
@@ -500,10 +484,7 @@ __global__ void __launch_bounds__(256, 4) k_ab2(Params p) {
     const uint8_t want = FROM_NATURAL ? TYPE_MASK : (TYPE_MASK | F_SPECIAL);
     const bool act_a = in && (f.fa & want) == T_FLUID;
     const bool act_b = in && (f.fb & want) == T_FLUID;
-    const bool spec_a = !FROM_NATURAL && in && special_fluid(f.fa);
-    const bool spec_b = !FROM_NATURAL && in && special_fluid(f.fb);
     const bool wall = !FROM_NATURAL && __any_sync(0xffffffffu, (act_a || act_b) && (f.ma | f.mb) != 0u);
-    const bool split = !FROM_NATURAL && __any_sync(0xffffffffu, spec_a || spec_b);
     Elem<L>* B = static_cast<Elem<L>*>(p.B);
     if (act_a || act_b) {
         float2 h[19];
@@ -519,16 +500,8 @@ __global__ void __launch_bounds__(256, 4) k_ab2(Params p) {
         collide2<BODY>(h, p);
         uint32_t ns = c.n;
         asm volatile("" : "+r"(ns) : "f"(h[0].x), "f"(h[18].y));
-        if (!split) {
 #pragma unroll
-            for (int q = 0; q < 19; ++q) st2<L>(B + (p.plane32[q] + ns), h[q]);
-        } else {
-            // the pair's flags again (not held across the collision)
-            const PairFlags g = pair_flags(p, ns, false);
-            const bool keep_a = !special_fluid(g.fa), keep_b = !special_fluid(g.fb);
-#pragma unroll
-            for (int q = 0; q < 19; ++q) st2_keep<L>(B + (p.plane32[q] + ns), h[q], keep_a, keep_b);
-        }
+        for (int q = 0; q < 19; ++q) st2<L>(B + (p.plane32[q] + ns), h[q]);
         if (FORCE) {
             if ((act_a && f.ma) || (act_b && f.mb)) {
                 PairForce pf;
@@ -541,11 +514,10 @@ __global__ void __launch_bounds__(256, 4) k_ab2(Params p) {
             }
         }
     } else if (in && p.B != p.A) {
-        // no working cell: SOLID / INLET / MOVING_WALL slots are never read; zeros keep every
-        // sector of B fully written
+        // no working cell: SOLID / INLET / MOVING_WALL slots are never read and special cells'
+        // are rewritten by the boundary kernel; zeros keep every sector of B fully written
 #pragma unroll
-        for (int q = 0; q < 19; ++q)
-            st2_keep<L>(B + (p.plane32[q] + c.n), make_float2(0.f, 0.f), !spec_a, !spec_b);
+        for (int q = 0; q < 19; ++q) st2<L>(B + (p.plane32[q] + c.n), make_float2(0.f, 0.f));
     }
     if (FORCE) warp_force(fx, fy, fz, p.partial);
 }
