@@ -368,6 +368,39 @@ def cpu_baseline(n=512, ny_sample=16, target_s=15.0):
                               "sample": f"{n}x{ny1}x{n} slab, 4 steps ({dt1:.1f} s)"}}
 
 
+def variant_specs():
+    """The variant workloads of the JSON line: name -> (edge, scheme, options of variant())."""
+    specs = {}
+    for m in (128, 512):
+        for s in ("AA", "AB"):
+            specs[f"{s}_{m}^3_periodic"] = (m, s, {})
+    for lay in ("bundle", "collision"):
+        for s in ("AA", "AB"):
+            specs[f"{s}_128^3_periodic_{lay}_layout"] = (128, s, {"layout": lay})
+    for s in ("AA", "AB"):
+        specs[f"{s}_128^3_sphere_inlet_outlet"] = (128, s, {"sphere": True})
+    specs["AA_256^3_lid_driven_cavity"] = (256, "AA", {"cavity": True})
+    for s in ("AA", "AB"):
+        specs[f"{s}_512^3_periodic_fp16_storage"] = (512, s, {"fp16": True})
+    return specs
+
+
+def run_variants_only(args):
+    """--variant: the named variant workloads alone (a command for profiling captures), one JSON
+    line each; --variant-size replaces their edge."""
+    import torch
+    from lattice_boltzmann_cfd_d3q19_gb300 import binding as B
+    B.load()
+    specs = variant_specs()
+    for name in args.variant:
+        if name not in specs:
+            raise SystemExit(f"unknown variant {name!r}; known: {', '.join(specs)}")
+        m, s, kw = specs[name]
+        m = args.variant_size or m
+        res = variant(B, torch, m, s, steps=args.steps, warmup=args.warmup, **kw)
+        print(json.dumps({"variant": name, "edge": m, **res}), flush=True)
+
+
 def e2e_run(B, torch, n, steps, flags):
     """Through the public API with host buffers: load the state from pinned host memory, run the
     steps reading the drag force back after each, read rho and u back to pinned host memory."""
@@ -471,19 +504,8 @@ def run_ours(args):
     }
     if not args.no_variants:
         log("[bench] variants")
-        out["variants"] = {f"{s}_{m}^3_periodic": variant(B, torch, m, s)
-                           for m in (128, 512) for s in ("AA", "AB")}
-        for lay in ("bundle", "collision"):
-            for s in ("AA", "AB"):
-                out["variants"][f"{s}_128^3_periodic_{lay}_layout"] = variant(B, torch, 128, s,
-                                                                              layout=lay)
-        for s in ("AA", "AB"):
-            out["variants"][f"{s}_128^3_sphere_inlet_outlet"] = variant(B, torch, 128, s,
-                                                                        sphere=True)
-        out["variants"]["AA_256^3_lid_driven_cavity"] = variant(B, torch, 256, "AA", cavity=True)
-        for s in ("AA", "AB"):
-            out["variants"][f"{s}_512^3_periodic_fp16_storage"] = variant(B, torch, 512, s,
-                                                                          fp16=True)
+        out["variants"] = {name: variant(B, torch, m, s, **kw)
+                           for name, (m, s, kw) in variant_specs().items()}
     if not args.no_e2e:
         log("[bench] e2e")
         out["e2e"] = e2e_run(B, torch, n, args.steps, flags)
@@ -541,13 +563,20 @@ def main(argv=None):
     ap.add_argument("--no-variants", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--variant", action="append", default=[],
+                    help="run only this variant workload (repeatable; names as in the JSON "
+                         "line's 'variants'), one JSON line each: for profiling captures")
+    ap.add_argument("--variant-size", type=int, default=0,
+                    help="edge for --variant instead of the variant's own")
     ap.add_argument("--size", type=int, default=512,
                     help="edge of the porous workload (512 is the benchmark; smaller sizes are "
                          "for profiling captures)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.impl == "reference":
+    if args.variant:
+        run_variants_only(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
