@@ -388,13 +388,14 @@ def variant_specs():
 def run_variants_only(args):
     """--variant: the named variant workloads alone (a command for profiling captures), one JSON
     line each; --variant-size replaces their edge."""
-    import torch
-    from lattice_boltzmann_cfd_d3q19_gb300 import binding as B
-    B.load()
     specs = variant_specs()
     for name in args.variant:
         if name not in specs:
             raise SystemExit(f"unknown variant {name!r}; known: {', '.join(specs)}")
+    import torch
+    from lattice_boltzmann_cfd_d3q19_gb300 import binding as B
+    B.load()
+    for name in args.variant:
         m, s, kw = specs[name]
         m = args.variant_size or m
         res = variant(B, torch, m, s, steps=args.steps, warmup=args.warmup, **kw)

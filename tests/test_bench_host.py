@@ -77,3 +77,14 @@ def test_recorded_traffic_requires_matching_sources(tmp_path, monkeypatch):
     assert bench.recorded_traffic("aa_odd") == 150.0
     monkeypatch.setattr(bench, "kernel_source_hash", lambda: "changed")
     assert bench.recorded_traffic("aa_odd") is None
+
+
+def test_variant_table_and_unknown_name():
+    """The variant workloads of the JSON line come from one table (the --variant entry point
+    uses the same names); an unknown name stops before any library or GPU work."""
+    specs = bench.variant_specs()
+    assert "AA_512^3_periodic_fp16_storage" in specs
+    assert specs["AA_128^3_sphere_inlet_outlet"] == (128, "AA", {"sphere": True})
+    assert {s for (_, s, _) in specs.values()} == {"AA", "AB"}
+    with pytest.raises(SystemExit):
+        bench.main(["--variant", "no_such_workload"])
