@@ -234,18 +234,20 @@ def timed_steps(B, torch, ctx, steps, warmup, per_step=2, profile=True, sampler=
         dist.barrier()
     torch.cuda.synchronize()
     launches0 = B.lbm_kernel_launches(ctx)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
+    # one event between consecutive steps: the region's time and each step's
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    e0, e1 = ev[0], ev[-1]
     e0.record(stream)
-    for _ in range(steps):
+    for i in range(steps):
         B.lbm_step(ctx, per_step)
-    e1.record(stream)
+        ev[i + 1].record(stream)
     torch.cuda.synchronize()
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
     clocks = sampler.stop() if sampler else None
     ms = e0.elapsed_time(e1)
+    step_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
     launches = B.lbm_kernel_launches(ctx) - launches0
     prof = {}
     if profile:
@@ -257,7 +259,7 @@ def timed_steps(B, torch, ctx, steps, warmup, per_step=2, profile=True, sampler=
             if cnt:
                 prof[name] = (cnt, tot)
         B.lbm_profile_enable(ctx, False)
-    return ms, launches, prof, clocks
+    return ms, launches, prof, clocks, step_ms
 
 
 def variant(B, torch, n, scheme, steps=10, warmup=3, cavity=False, fp16=False, layout="stream",
@@ -291,8 +293,8 @@ def variant(B, torch, n, scheme, steps=10, warmup=3, cavity=False, fp16=False, l
             u[:N] = 0.02
         B.lbm_set_equilibrium(ctx, rho, u)
         # throughput with graph replay (no per-kernel events), then per-kernel event timing
-        ms, _, _, _ = timed_steps(B, torch, ctx, steps, warmup, profile=False)
-        _, _, prof, _ = timed_steps(B, torch, ctx, steps, warmup)
+        ms, _, _, _, _ = timed_steps(B, torch, ctx, steps, warmup, profile=False)
+        _, _, prof, _, _ = timed_steps(B, torch, ctx, steps, warmup)
     finally:
         B.lbm_destroy(ctx)
     mlups = N * 2 * steps / (ms / 1e3) / 1e6
@@ -455,8 +457,8 @@ def run_ours(args):
     n_fluid = int(np.count_nonzero(flags == wl.FLUID))
     sampler = ClockSampler(local) if rank == 0 else None
     try:
-        ms, launches, prof, clocks = timed_steps(B, torch, ctx, args.steps, args.warmup,
-                                                 sampler=sampler, world=world)
+        ms, launches, prof, clocks, step_ms = timed_steps(B, torch, ctx, args.steps, args.warmup,
+                                                          sampler=sampler, world=world)
     finally:
         B.lbm_destroy(ctx)
     max_s = reduce_max(ms / 1e3, world, device="cuda")
@@ -483,6 +485,10 @@ def run_ours(args):
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(max_s * 1e3 / args.steps, 4),
+        # each timed step alone (CUDA events between steps, rank 0): the median of the runs
+        # with their spread
+        "step_ms": {"median": round(statistics.median(step_ms), 4), "min": round(min(step_ms), 4),
+                    "max": round(max(step_ms), 4), "runs": len(step_ms)},
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
         "config": dict(workload_config(n, tau, g, n_fluid / N),
