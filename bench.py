@@ -77,13 +77,41 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def code_tokens(text: str) -> str:
+    """C / C++ / CUDA source without its comments, runs of white space reduced to one blank:
+    what the compiler sees, so that edits to comments leave it unchanged.  String and character
+    literals are kept as they are."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            while i < n and text[i] != "\n":
+                i += 1
+            out.append(" ")
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_hash() -> str:
+    """sha256 over the kernel sources' code (comments and layout of white space excluded)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "lattice_boltzmann_cfd_d3q19_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as fh:
+        with open(os.path.join(csrc, name), encoding="utf-8") as fh:
             h.update(name.encode())
-            h.update(fh.read())
+            h.update(code_tokens(fh.read()).encode())
     return h.hexdigest()
 
 

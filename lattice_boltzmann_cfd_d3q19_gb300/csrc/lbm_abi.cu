@@ -444,8 +444,6 @@ int classify(lbm_ctx* c) {
     return LBM_OK;
 }
 
-// Launch a step kernel (or, for K_BOUNDARY, the boundary kernel of step kind `main_kind`), timed
-// when profiling is on.
 // Sweep direction of a step kernel: each step walks the z planes opposite to the step before, so
 // it starts on the planes the previous step wrote last (still in L2 on grids near its size).
 int z_reversed(const lbm_ctx* c, int kind) {
@@ -457,6 +455,8 @@ int z_reversed(const lbm_ctx* c, int kind) {
     }
 }
 
+// Launch a step kernel (or, for K_BOUNDARY, the boundary kernel of step kind `main_kind`, on
+// `boundary_stream` when given), timed when profiling is on.
 int launch_kind(lbm_ctx* c, int kind, const Params& p_in, bool force, int main_kind = -1,
                 cudaStream_t boundary_stream = nullptr) {
     Params p = p_in;

@@ -153,8 +153,8 @@ __device__ __forceinline__ bool special_cell(const Params& p, CellCoord& c) {
 // ============================== AA pattern, even step ===========================================
 // "In place" bullet: read population q of x at (q, x); write the collided one at (opposite(q), x).
 // Purely local, so every FLUID cell (special ones included) is handled here.
-// Hot-path addressing: element offset, relative to a population's plane pointer, of cell n
-// (I = int when every offset of the launch fits, else long long).
+// Hot-path addressing: element offset of cell n relative to a population's plane pointer
+// (I = uint32_t when every element offset of the buffer fits in 32 bits, else long long).
 template <int L, typename I>
 __device__ __forceinline__ I cell_off(int q, uint32_t n) {
     return (I)n * (I)cell_stride<L>(q);

@@ -173,7 +173,7 @@ __device__ __forceinline__ PairFlags pair_flags(const Params& p, uint32_t n, boo
 
 // Momentum exchange of a pair, packed: the sum over the links q whose bit is set in the cell's
 // mask of c_q f*_q, f* = h* + w (per cell, one lane each); twice that is the force the fluid
-// gives up (bounce-back returns 2 c_q f*_q), so the factor 2 is applied once, in pair_force.
+// gives up (bounce-back returns 2 c_q f*_q), so the factor 2 is applied once, in into().
 struct PairForce {
     float2 x = make_float2(0.f, 0.f), y = make_float2(0.f, 0.f), z = make_float2(0.f, 0.f);
     template <int Q>
@@ -306,8 +306,8 @@ __device__ __forceinline__ void own_store(const Params& p, Elem<L>* base, uint32
 
 // ============================== AA pattern, even step, two cells ================================
 // Every FLUID cell; the pair's slots are read and written as aligned words.
-// 4 resident blocks per SM (64 registers): with 66 registers the fp16 kernel fell to 3 blocks
-// and lost 9% (measured)
+// Resident blocks per SM: 4 for fp32 storage (64 registers), 6 for the packed half-precision form
+// (40 registers); the fp16 kernel on fp32 arrays with 66 registers fell to 3 blocks and lost 9%.
 template <int L, bool FORCE, bool BODY>
 __global__ void __launch_bounds__(256, pair_min_blocks<L>(kPackedHalfEven)) k_aa_even2(Params p) {
     PairCoord c;

@@ -96,8 +96,8 @@ struct TmaTiles {
 };
 
 // Thread 0: issue the copies of tile t into stage `st` (its mbarrier `bar`).  One thread issues
-// every copy: the bulk-copy instruction is issued with warp-uniform operands, so copies are not
-// spread over the lanes of a warp.
+// every copy (a form that spread them over the lanes of a warp never saw all of its copies
+// arrive).
 template <int L>
 __device__ __forceinline__ void tma_issue(const Params& p, const TmaTiles& tg, int t,
                                          unsigned char* st, uint64_t* bar) {

@@ -24,12 +24,12 @@ void launch_main(int kind, const Params& p, dim3 grid, dim3 block, cudaStream_t 
     }
 }
 
-// The hot kernels address populations as plane pointer + 64-bit element offset (measured faster
-// than 32-bit offsets in the odd kernel, whose registers they keep lower).
+// Addressing of the one-cell kernels: the neighbour-addressing kernels (AA odd, A-B) take one
+// base pointer with 32-bit element offsets whenever all 19 N fit (fewer instructions per access);
+// the even kernel, which already streams at the copy bandwidth, and larger grids use per-population
+// plane pointers with 64-bit offsets.
 template <bool F, bool B>
 void launch_main_offsets(int kind, const Params& p, dim3 grid, dim3 block, cudaStream_t s) {
-    // the even kernel keeps plane pointers (it already streams at the copy bandwidth); the
-    // neighbour-addressing kernels take one base with 32-bit offsets whenever all 19 N fit
     const bool compact = 19 * p.N <= (size_t(1) << 32) && kind != K_AA_EVEN;
     if (compact) launch_main<F, B, uint32_t>(kind, p, grid, block, s);
     else launch_main<F, B, long long>(kind, p, grid, block, s);

@@ -88,3 +88,14 @@ def test_variant_table_and_unknown_name():
     assert {s for (_, s, _) in specs.values()} == {"AA", "AB"}
     with pytest.raises(SystemExit):
         bench.main(["--variant", "no_such_workload"])
+
+
+def test_code_tokens_ignore_comments_not_code():
+    """The kernel-source hash that guards the recorded DRAM traffic sees code only: comment and
+    white-space edits keep it, any code edit changes it (string literals are code)."""
+    a = "int a = 1; // one\n/* block\n comment */ float b = 2.0f;"
+    b = "int  a = 1;\n\n/* other words */ float b = 2.0f; // trailing"
+    assert bench.code_tokens(a) == bench.code_tokens(b) == "int a = 1; float b = 2.0f;"
+    assert bench.code_tokens(a) != bench.code_tokens(a.replace("2.0f", "3.0f"))
+    s = 'const char* u = "x // y /* z */"; char c = \'"\';'
+    assert bench.code_tokens(s) == s
