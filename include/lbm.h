@@ -101,7 +101,8 @@ enum { LBM_PERIODIC = 0, LBM_OPEN = 1 };
 
 /* Create a context on the current CUDA device.  nx, ny, nz >= 1, nz <= 65535, N <= 2^31 - 1,
  * tau > 1/2 and finite ([Blog] §5.1: omega = 1/tau must stay below 2).  Allocates the population
- * buffer(s) (AA: one, AB/AB2: two, 76 N bytes each) and the flag array.  Initial state: every cell
+ * buffer(s) (AA: one, AB/AB2: two, 76 N bytes each, 38 N in half-precision storage), the cell
+ * type and flag bytes and the solid-link masks (6 N bytes).  Initial state: every cell
  * FLUID, all faces PERIODIC, g = 0, inlet (1, 0, 0, 0), f = w_q (rest at rho = 1), step count 0,
  * stream 0 (the legacy default stream).  Returns NULL on error (see lbm_last_error). */
 lbm_ctx* lbm_create(int nx, int ny, int nz, float tau, int layout, int streaming);
