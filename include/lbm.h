@@ -93,7 +93,8 @@ enum {
     LBM_ENOMEM = -2,     /* device or host allocation failed                               */
     LBM_ECUDA = -3,      /* CUDA runtime error (message in lbm_last_error)                  */
     LBM_ESTATE = -4,     /* call not valid in the current state (e.g. force before a step)  */
-    LBM_ENOTFINITE = -5  /* lbm_check_finite found a NaN or infinity                         */
+    LBM_ENOTFINITE = -5, /* lbm_check_finite found a NaN or infinity                         */
+    LBM_ETIMEOUT = -6    /* a bounded wait inside a kernel ran out (state not valid)        */
 };
 
 enum { LBM_FLUID = 0, LBM_SOLID = 1, LBM_INLET = 2, LBM_MOVING_WALL = 3 };
@@ -185,7 +186,7 @@ int lbm_set_cell_pairs(lbm_ctx* ctx, int enable);
  * a multiple of 16 no larger than 512.  Results are bit-identical to the other AA kernels (the
  * force up to the grouping of its partial sums).  Every wait of the kernel on its copies is
  * bounded (2 s); a wait that runs out sets a sticky fault that the next synchronising call
- * (getters, lbm_check_finite) reports as LBM_ECUDA.  Returns 1 when the staged kernel will run,
+ * (getters, lbm_check_finite) reports as LBM_ETIMEOUT.  Returns 1 when the staged kernel will run,
  * 0 when not, LBM_EINVAL for a NULL context.  Drops the cached step graphs.  ([Layout]'s in-place
  * step; the staging is a GB300 launch choice, not a page's design.) */
 int lbm_set_tma_gather(lbm_ctx* ctx, int enable);

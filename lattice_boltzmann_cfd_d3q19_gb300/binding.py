@@ -17,7 +17,7 @@ from . import build as _build
 
 LAYOUT_STREAM, LAYOUT_BUNDLE, LAYOUT_COLLISION, LAYOUT_STREAM_FP16 = 0, 1, 2, 3
 STREAMING_AUTO, STREAMING_AA, STREAMING_AB, STREAMING_AB2 = 0, 1, 2, 3
-OK, EINVAL, ENOMEM, ECUDA, ESTATE, ENOTFINITE = 0, -1, -2, -3, -4, -5
+OK, EINVAL, ENOMEM, ECUDA, ESTATE, ENOTFINITE, ETIMEOUT = 0, -1, -2, -3, -4, -5, -6
 FLUID, SOLID, INLET, MOVING_WALL = 0, 1, 2, 3
 PERIODIC, OPEN = 0, 1
 # profiling kinds of lbm_profile_read

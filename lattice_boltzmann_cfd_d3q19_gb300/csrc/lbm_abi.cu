@@ -563,7 +563,7 @@ int sync(lbm_ctx* c, const char* what) {
                              c->stream), what);
     LBM_CUDA(cudaStreamSynchronize(c->stream), what);
     if (*c->fault_host)
-        return fail(LBM_ECUDA, "%s: a staged-gather kernel gave up waiting for its copies (code %d); "
+        return fail(LBM_ETIMEOUT, "%s: a staged-gather kernel gave up waiting for its copies (code %d); "
                     "the state is not valid", what, *c->fault_host);
     return LBM_OK;
 }

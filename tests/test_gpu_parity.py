@@ -839,7 +839,7 @@ def test_tma_gather_wait_timeout_is_reported(monkeypatch):
     """Failure detection without a GPU fault: with the test hook the staged odd step announces 16
     bytes more than it copies, so its wait can never complete.  The wait gives up after its 2 s
     bound, the kernel drains its own copies and returns, and the next synchronising call reports
-    LBM_ECUDA.  The device stays usable."""
+    LBM_ETIMEOUT.  The device stays usable."""
     import time
     monkeypatch.setenv("LBM_TEST_STAGE_TIMEOUT", "1")
     case = Case(32, 4, 2, 0.7, random_state(32 * 4 * 2, 1500))
@@ -852,7 +852,7 @@ def test_tma_gather_wait_timeout_is_reported(monkeypatch):
         f = np.zeros((19, case.N), np.float32)
         with pytest.raises(B.LbmError) as ei:
             B.lbm_get_populations(ctx, f)
-        assert ei.value.code == B.ECUDA
+        assert ei.value.code == B.ETIMEOUT
         assert "gave up waiting" in str(ei.value)
         assert time.time() - t0 < 60
     finally:
