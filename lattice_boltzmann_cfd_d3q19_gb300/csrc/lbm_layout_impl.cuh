@@ -30,6 +30,18 @@ void launch_main(int kind, const Params& p, dim3 grid, dim3 block, cudaStream_t 
 // plane pointers with 64-bit offsets.
 template <bool F, bool B>
 void launch_main_offsets(int kind, const Params& p, dim3 grid, dim3 block, cudaStream_t s) {
+    // the steps that touch only a cell's own populations stage the collision layout's records
+    // through shared memory (coalesced runs instead of elements 76 bytes apart)
+    if constexpr (L == LAYOUT_COLLISION) {
+        if (kind == K_AA_EVEN) {
+            k_own_staged<F, B, true><<<grid, block, 0, s>>>(p);
+            return;
+        }
+        if (kind == K_AB_COLLIDE) {
+            k_own_staged<F, B, false><<<grid, block, 0, s>>>(p);
+            return;
+        }
+    }
     const bool compact = 19 * p.N <= (size_t(1) << 32) && kind != K_AA_EVEN;
     if (compact) launch_main<F, B, uint32_t>(kind, p, grid, block, s);
     else launch_main<F, B, long long>(kind, p, grid, block, s);
