@@ -159,13 +159,21 @@ def test_lid_driven_cavity_256_windows_and_mass():
     assert abs(f[:, case.fluid].astype(np.float64).sum() / m0 - 1) < 1e-5
 
 
-def test_degenerate_grids():
+@pytest.mark.parametrize("layout", ["stream", "bundle", "collision"])
+def test_degenerate_grids(layout):
+    """Grids of one cell, one row, one plane (a warp holding one or a few cells), in every layout;
+    and a two-cell row between an inlet and an open face."""
     for (nx, ny, nz) in [(1, 1, 1), (2, 1, 1), (1, 3, 1), (2, 2, 2), (5, 1, 7)]:
         case = Case(nx, ny, nz, 0.7, random_state(nx * ny * nz, 7), g=(1e-4, 0, 0))
         fo, _ = case.run_oracle(5)
         for scheme in SCHEMES:
-            fg, _ = case.run_gpu(5, "stream", scheme)
-            assert max_fluid_diff(case, fg, fo) <= TOL_F
+            fg, _ = case.run_gpu(5, layout, scheme)
+            assert max_fluid_diff(case, fg, fo) <= TOL_F, ((nx, ny, nz), scheme)
+    case = mixed_case(3, 2, 1, (1, 0, 0), 8, solid=0.0, inlet_layer=True)
+    fo, _ = case.run_oracle(5)
+    for scheme in SCHEMES:
+        fg, _ = case.run_gpu(5, layout, scheme)
+        assert max_fluid_diff(case, fg, fo) <= TOL_F, scheme
 
 
 def test_zero_steps_is_identity_and_force_unavailable():
