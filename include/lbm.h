@@ -168,12 +168,14 @@ int lbm_set_graph_launch(lbm_ctx* ctx, int enable);
 /* Allow (enable != 0, the default) or forbid the two-cell step kernels: one thread updates the
  * x-adjacent cells (x, x+1), x even, loading and storing the pair's aligned slots as one word and
  * colliding both cells in packed fp32x2 arithmetic.  They serve the stream layouts (fp32 and
- * fp16 storage) when nx is even and 19 N <= 2^32; elsewhere one thread updates one cell.  The
+ * fp16 storage) when nx is even and 19 N <= 2^32, and on those grids the bundle layout's AA even
+ * step too (a pair's records of one bundle are one aligned run); elsewhere one thread updates one
+ * cell.  The
  * populations are bit-identical either way; the momentum-exchange force may differ in its last
  * bits (its partial sums are grouped by thread).  Populations of non-FLUID cells are not defined
  * under either kernel family: a cell turned FLUID by lbm_set_flags needs its populations set.
- * Returns 1 when the two-cell kernels will run, 0 when they will not, LBM_EINVAL for a NULL
- * context.  Drops the cached step graphs.  (No page prescribes this mapping; it is a launch
+ * Returns 1 when the stream layouts' two-cell kernels will run, 0 when they will not, LBM_EINVAL
+ * for a NULL context.  Drops the cached step graphs.  (No page prescribes this mapping; it is a launch
  * choice for the same update.) */
 int lbm_set_cell_pairs(lbm_ctx* ctx, int enable);
 

@@ -238,8 +238,19 @@ struct lbm_ctx {
     bool tma() const { return pairs() && tma_allowed && n[0] % 16 == 0 && n[0] <= 512 && ntma > 0; }
     // blocks of the step kernels that write force partials
     size_t main_blocks() const { return pairs() ? nblocks2 : nblocks; }
+    // the bundle layout's AA even step also runs two cells per thread (aligned pair runs)
+    bool bundle_pairs() const {
+        return pairs_allowed && layout == LBM_LAYOUT_BUNDLE && n[0] % 2 == 0 &&
+               19 * N <= (size_t(1) << 32);
+    }
+    // kernels launched over cell pairs for step kind `kind`
+    bool pairs_for(int kind) const {
+        if (kind == K_STREAM) return false;
+        return pairs() || (kind == K_AA_EVEN && bundle_pairs());
+    }
     size_t main_blocks_for(int kind) const {
-        return kind == K_AA_ODD && tma() ? ntma : main_blocks();
+        if (kind == K_AA_ODD && tma()) return ntma;
+        return pairs_for(kind) ? nblocks2 : nblocks;
     }
     bool body() const { return g[0] != 0.f || g[1] != 0.f || g[2] != 0.f; }
     bool any_open() const { return face[0] == LBM_OPEN || face[1] == LBM_OPEN || face[2] == LBM_OPEN; }
@@ -481,7 +492,7 @@ int launch_kind(lbm_ctx* c, int kind, const Params& p_in, bool force, int main_k
         ++c->launches;
         if (force) c->force_triples = partial_triples(c->main_blocks_for(main_kind), c->n_special);
     } else {
-        const bool two = c->pairs() && kind != K_STREAM;
+        const bool two = c->pairs_for(kind);
         if (kind == K_AA_ODD && c->tma())
             e = c->ops->odd_tma(p, force, c->body(), c->ntma, c->stream);
         else if (two)

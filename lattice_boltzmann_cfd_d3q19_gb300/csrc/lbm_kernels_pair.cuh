@@ -371,6 +371,94 @@ __global__ void __launch_bounds__(256, pair_min_blocks<L>(kPackedHalfEven)) k_aa
     if (FORCE) warp_force(fx, fy, fz, p.partial);
 }
 
+// ============================== AA pattern, even step, bundle layout, two cells =================
+// The bundle layout ([PortLBM] Fig. 2(c): the populations sharing (c_y, c_z) form a bundle, a
+// cell's members of one bundle stored together) on an even nx: a pair's records of one bundle are
+// one run of 2 m elements (m = 3 or 1 members) starting at an even element, so the 19 populations
+// of both cells load and store as 19 aligned two-element words, as in the stream layout (element
+// accesses at the bundle's stride touched 3 times the sectors per request).
+
+// member j (c_x = j - 1) of the bundle whose first member is q0; the only member of a 1-bundle
+__host__ __device__ constexpr int bundle_member(int q0, int j) {
+    for (int q = 0; q < 19; ++q)
+        if (cy(q) == cy(q0) && cz(q) == cz(q0) && (bundle_size(q0) == 1 || cx(q) == j - 1)) return q;
+    return -1;
+}
+
+// the pair's populations of the bundle that starts at Q (bundle_j(Q) == 0), then the next bundles
+template <int Q = 0>
+__device__ __forceinline__ void bundle_gather2(const float* A, uint32_t N, uint32_t a, float2 (&h)[19]) {
+    if constexpr (bundle_j(Q) == 0) {
+        const float* e = A + ((uint32_t)bundle_off(Q) * N + a * (uint32_t)bundle_size(Q));
+        if constexpr (bundle_size(Q) == 3) {
+            // [a0 a1 a2 b0 b1 b2] as three words
+            const float2 w0 = ld2<LAYOUT_BUNDLE>(e), w1 = ld2<LAYOUT_BUNDLE>(e + 2),
+                         w2 = ld2<LAYOUT_BUNDLE>(e + 4);
+            h[bundle_member(Q, 0)] = make_float2(w0.x, w1.y);
+            h[bundle_member(Q, 1)] = make_float2(w0.y, w2.x);
+            h[bundle_member(Q, 2)] = make_float2(w1.x, w2.y);
+        } else {
+            h[Q] = ld2<LAYOUT_BUNDLE>(e);
+        }
+    }
+    if constexpr (Q < 18) bundle_gather2<Q + 1>(A, N, a, h);
+}
+
+// AA even store: member p of a bundle receives the collided population opposite(p)
+template <int Q = 0>
+__device__ __forceinline__ void bundle_scatter2_opp(float* A, uint32_t N, uint32_t a,
+                                                    const float2 (&h)[19]) {
+    if constexpr (bundle_j(Q) == 0) {
+        float* e = A + ((uint32_t)bundle_off(Q) * N + a * (uint32_t)bundle_size(Q));
+        if constexpr (bundle_size(Q) == 3) {
+            const float2 v0 = h[opp(bundle_member(Q, 0))], v1 = h[opp(bundle_member(Q, 1))],
+                         v2 = h[opp(bundle_member(Q, 2))];
+            st2<LAYOUT_BUNDLE>(e, make_float2(v0.x, v1.x));
+            st2<LAYOUT_BUNDLE>(e + 2, make_float2(v2.x, v0.y));
+            st2<LAYOUT_BUNDLE>(e + 4, make_float2(v1.y, v2.y));
+        } else {
+            st2<LAYOUT_BUNDLE>(e, h[opp(Q)]);
+        }
+    }
+    if constexpr (Q < 18) bundle_scatter2_opp<Q + 1>(A, N, a, h);
+}
+
+template <bool FORCE, bool BODY>
+__global__ void __launch_bounds__(256, 4) k_aa_even2_bundle(Params p) {
+    PairCoord c;
+    float fx = 0.f, fy = 0.f, fz = 0.f;
+    if (grid_pair(p, c)) {
+        const PairFlags f = pair_flags(p, c.n, false);
+        const bool act_a = (f.fa & TYPE_MASK) == T_FLUID, act_b = (f.fb & TYPE_MASK) == T_FLUID;
+        if (act_a || act_b) {
+            float* A = static_cast<float*>(p.A);
+            const uint32_t N = (uint32_t)p.N;
+            float2 h[19];
+            bundle_gather2(A, N, c.n, h);
+            collide2<BODY>(h, p);
+            uint32_t ns = c.n;
+            asm volatile("" : "+r"(ns) : "f"(h[0].x), "f"(h[18].y));
+            bundle_scatter2_opp(A, N, ns, h);
+            if (FORCE) {
+                const bool wa_ = act_a && !(f.fa & F_BULK), wb_ = act_b && !(f.fb & F_BULK);
+                if (wa_ || wb_) {
+                    const uint2 m = *reinterpret_cast<const uint2*>(p.mask + c.n);
+                    PairForce pf;
+                    pf.masks(wa_ ? m.x : 0u, wb_ ? m.y : 0u, h);
+                    pf.into(fx, fy, fz);
+                    if (p.any_moving) {
+                        if (wa_ && (f.fa & F_SPECIAL))
+                            moving_forces(p, PairLane<0>{h}, c.x, c.y, c.z, fx, fy, fz);
+                        if (wb_ && (f.fb & F_SPECIAL))
+                            moving_forces(p, PairLane<1>{h}, c.x + 1, c.y, c.z, fx, fy, fz);
+                    }
+                }
+            }
+        }
+    }
+    if (FORCE) warp_force(fx, fy, fz, p.partial);
+}
+
 // ============================== AA pattern, odd step, two cells =================================
 // FLUID cells that are not special.  Population q goes to (q, x + c_q); on a solid link also to
 // the own mirrored slot (opposite(q), x), which is the one the next even step reads.

@@ -71,7 +71,8 @@ cudaError_t cells(int kind, const Params& p, bool force, bool body, dim3 grid, d
     return cudaGetLastError();
 }
 
-// Two-cell kernels (stream layouts only; the caller checks an even nx and 19 N <= 2^32).
+// Two-cell kernels (stream layouts; the bundle layout's even step; the caller checks an even nx and
+// 19 N <= 2^32).
 template <int LL, bool F, bool B>
 void launch_pair(int kind, const Params& p, dim3 grid, dim3 block, cudaStream_t s) {
     switch (kind) {
@@ -85,7 +86,18 @@ void launch_pair(int kind, const Params& p, dim3 grid, dim3 block, cudaStream_t 
 template <int LL>
 cudaError_t cells2_impl(int kind, const Params& p, bool force, bool body, dim3 grid, dim3 block,
                         cudaStream_t s) {
-    if constexpr (!is_soa(LL)) {
+    if constexpr (LL == LAYOUT_BUNDLE) {
+        // the bundle layout's even step (two cells per thread); its other steps are one-cell
+        if (kind != K_AA_EVEN) return cudaErrorNotSupported;
+        if (force) {
+            if (body) k_aa_even2_bundle<true, true><<<grid, block, 0, s>>>(p);
+            else k_aa_even2_bundle<true, false><<<grid, block, 0, s>>>(p);
+        } else {
+            if (body) k_aa_even2_bundle<false, true><<<grid, block, 0, s>>>(p);
+            else k_aa_even2_bundle<false, false><<<grid, block, 0, s>>>(p);
+        }
+        return cudaGetLastError();
+    } else if constexpr (!is_soa(LL)) {
         return cudaErrorNotSupported;
     } else {
         if (kind != K_AA_EVEN && kind != K_AA_ODD && kind != K_AB_PULL && kind != K_AB_COLLIDE)
