@@ -233,8 +233,18 @@ def workload_config(n, tau, g, fluid_fraction):
 
 # ---- the GPU arm ---------------------------------------------------------------------------------------
 
+_POROUS_FLAGS = {}
+
+
+def porous_flags(n):
+    """The benchmark's porous medium at edge n (generated once per run)."""
+    if n not in _POROUS_FLAGS:
+        _POROUS_FLAGS[n] = wl.porous_flags(n, n, n, 0.30, 3, seed=wl.SEED_POROUS512)
+    return _POROUS_FLAGS[n]
+
+
 def make_porous_context(B, torch, n, tau, g, scheme="AA"):
-    flags = wl.porous_flags(n, n, n, 0.30, 3, seed=wl.SEED_POROUS512)
+    flags = porous_flags(n)
     ctx = B.lbm_create(n, n, n, tau, B.LAYOUT_STREAM,
                        B.STREAMING_AA if scheme == "AA" else B.STREAMING_AB)
     B.lbm_set_flags(ctx, flags)
@@ -291,17 +301,18 @@ def timed_steps(B, torch, ctx, steps, warmup, per_step=2, profile=True, sampler=
 
 
 def variant(B, torch, n, scheme, steps=10, warmup=3, cavity=False, fp16=False, layout="stream",
-            sphere=False):
+            sphere=False, porous=False):
     """Periodic box without solids, g = 0, uniform flow: the clean roofline point.  With
     cavity=True: a lid-driven cavity (resting walls, lid moving at 0.05 along x), fluid at rest.
     With sphere=True: the sphere workload (r = n/8 at (0.3125 n, n/2, n/2), equilibrium inlet
     u = (0.05, 0, 0) on x = 0, zero-gradient outlet, y/z periodic, tau 0.56, fluid at the inlet
     state).  With fp16=True the populations are stored in half precision (76 population bytes per
     update instead of 152; the roofline fraction uses those bytes).  `layout`: stream, bundle or
-    collision (fp32)."""
+    collision (fp32).  With porous=True: the benchmark's porous medium (g = (1e-6, 0, 0), tau 0.7,
+    fluid at rest)."""
     lay = {"stream": B.LAYOUT_STREAM, "bundle": B.LAYOUT_BUNDLE,
            "collision": B.LAYOUT_COLLISION}[layout]
-    tau = 0.56 if sphere else 0.6
+    tau = 0.56 if sphere else 0.7 if porous else 0.6
     ctx = B.lbm_create(n, n, n, tau, B.LAYOUT_STREAM_FP16 if fp16 else lay,
                        B.STREAMING_AA if scheme == "AA" else B.STREAMING_AB)
     try:
@@ -309,6 +320,9 @@ def variant(B, torch, n, scheme, steps=10, warmup=3, cavity=False, fp16=False, l
         if cavity:
             B.lbm_set_flags(ctx, wl.cavity_flags(n, n, n))
             B.lbm_set_wall_velocity(ctx, 0.05, 0.0, 0.0)
+        if porous:
+            B.lbm_set_flags(ctx, porous_flags(n))
+            B.lbm_set_body_force(ctx, 1e-6, 0.0, 0.0)
         if sphere:
             B.lbm_set_flags(ctx, wl.sphere_flags(n, n, n, (5 * n // 16, n // 2, n // 2), n / 8))
             B.lbm_set_faces(ctx, B.OPEN, B.PERIODIC, B.PERIODIC)
@@ -317,7 +331,7 @@ def variant(B, torch, n, scheme, steps=10, warmup=3, cavity=False, fp16=False, l
         u = torch.zeros(3 * N, dtype=torch.float32, device="cuda")
         if sphere:
             u[:N] = 0.05
-        elif not cavity:
+        elif not cavity and not porous:
             u[:N] = 0.02
         B.lbm_set_equilibrium(ctx, rho, u)
         # throughput with graph replay (no per-kernel events), then per-kernel event timing
@@ -368,7 +382,7 @@ def cpu_baseline(n=512, ny_sample=16, target_s=15.0):
     """The CPU oracle, as it is, on a bounded sample of the porous workload: a 512 x ny_sample x
     512 slab of the same flags (periodic), same tau and body force."""
     import oracle
-    flags = wl.porous_flags(n, n, n, 0.30, 3, seed=wl.SEED_POROUS512).reshape(n, n, n)
+    flags = porous_flags(n).reshape(n, n, n)
     sub = np.ascontiguousarray(flags[:, :ny_sample, :]).reshape(-1)
     Ns = n * ny_sample * n
     P = oracle.Problem(n, ny_sample, n, 0.7, flags=sub, g=(1e-6, 0, 0))
@@ -412,6 +426,7 @@ def variant_specs():
     specs["AA_256^3_lid_driven_cavity"] = (256, "AA", {"cavity": True})
     for s in ("AA", "AB"):
         specs[f"{s}_512^3_periodic_fp16_storage"] = (512, s, {"fp16": True})
+    specs["AA_512^3_porous_fp16_storage"] = (512, "AA", {"fp16": True, "porous": True})
     return specs
 
 
