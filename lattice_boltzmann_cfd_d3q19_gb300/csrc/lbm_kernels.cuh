@@ -422,6 +422,44 @@ __global__ void __launch_bounds__(256, 6) k_ab(Params p) {
     if (FORCE) warp_force(fx, fy, fz, p.partial);
 }
 
+// A-B pull in the collision layout, with the stores staged: each lane gathers and collides its
+// cell as `k_ab` does (element loads from the neighbours' records), writes its record into the
+// warp's shared-memory tile, and the warp writes the 32 records to B as one coalesced run instead
+// of 19 stores 76 bytes apart.  Cells that are not pulled here (SOLID, INLET, MOVING_WALL,
+// special) get zeros, so every sector of B is written whole; the boundary kernel, launched after
+// this one, overwrites the special cells' records.
+template <bool FORCE, bool BODY, typename I>
+__global__ void __launch_bounds__(256) k_ab_pull_staged(Params p) {
+    constexpr int L = LAYOUT_COLLISION;
+    __shared__ float tile[kWarpsPerBlock][32 * 19];
+    CellCoord c;
+    const bool in = grid_cell(p, c);
+    const int lane = threadIdx.x & 31;
+    const int warp = (threadIdx.x + blockDim.x * threadIdx.y) >> 5;
+    const int cnt = __popc(__ballot_sync(0xffffffffu, in));
+    const uint32_t n0 = __shfl_sync(0xffffffffu, c.n, 0);
+    float* t = tile[warp];
+    float fx = 0.f, fy = 0.f, fz = 0.f;
+    const uint32_t m = (in && p.any_solid_link) ? p.mask[c.n] : 0u;
+    const uint8_t fl = in ? p.flags[c.n] : (uint8_t)T_SOLID;
+    if ((fl & (TYPE_MASK | F_SPECIAL)) == T_FLUID) {
+        const Nbr nb(p, c.x, c.y, c.z);
+        float h[19];
+        ab_load<L, I>(p, nb, c.n, m, h);
+        collide<BODY>(h, p);
+#pragma unroll
+        for (int q = 0; q < 19; ++q) t[idx<L, int>(q, (uint32_t)lane, 32)] = h[q];
+        if (FORCE && m) mask_forces(m, h, fx, fy, fz);
+    } else {
+#pragma unroll
+        for (int q = 0; q < 19; ++q) t[idx<L, int>(q, (uint32_t)lane, 32)] = 0.0f;
+    }
+    __syncwarp();
+    float* dst = static_cast<float*>(p.B) + (size_t)n0 * 19;
+    for (int k = lane; k < cnt * 19; k += 32) dst[k] = t[k];
+    if (FORCE) warp_force(fx, fy, fz, p.partial);
+}
+
 // Streaming only: natural state into B from the post-collision state in A (second pass of the
 // two-pass scheme).  Main kernel (non-special FLUID cells) and boundary kernel (special cells).
 template <int L, typename I>

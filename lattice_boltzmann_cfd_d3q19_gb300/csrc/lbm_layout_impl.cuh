@@ -41,6 +41,11 @@ void launch_main_offsets(int kind, const Params& p, dim3 grid, dim3 block, cudaS
             k_own_staged<F, B, false><<<grid, block, 0, s>>>(p);
             return;
         }
+        if (kind == K_AB_PULL) {
+            if (19 * p.N <= (size_t(1) << 32)) k_ab_pull_staged<F, B, uint32_t><<<grid, block, 0, s>>>(p);
+            else k_ab_pull_staged<F, B, long long><<<grid, block, 0, s>>>(p);
+            return;
+        }
     }
     const bool compact = 19 * p.N <= (size_t(1) << 32) && kind != K_AA_EVEN;
     if (compact) launch_main<F, B, uint32_t>(kind, p, grid, block, s);
