@@ -198,9 +198,9 @@ int lbm_set_tma_gather(lbm_ctx* ctx, int enable);
  * (enable = 0).  Beside: the boundary kernel goes to a private stream of the highest priority,
  * forked from the context stream after the open-face pre-gather and joined back before the next
  * kernel, so lbm_step's ordering on the context stream is unchanged.  It applies to the AA odd
- * step, the A-B pull of the one-cell kernels in the stream and bundle layouts and the AB2
- * streaming pass, whose main kernels store into no slot of a special cell, so the populations are
- * bit-identical either way; the two-cell A-B pull and the collision layout's A-B pull write those
+ * step, the A-B pull of the stream layout's one-cell kernels and the AB2 streaming pass, whose
+ * main kernels store into no slot of a special cell, so the populations are bit-identical either
+ * way; the two-cell A-B pull and the A-B pull of the bundle and collision layouts write those
  * slots (whole-sector stores that the boundary kernel then overwrites) and always run first.  Kernels run one after the other while per-kernel profiling is on.  Returns LBM_OK, LBM_EINVAL for a NULL context; drops
  * the cached step graphs.  (A launch choice for the same update; the per-link rules are
  * [Layout]'s.) */

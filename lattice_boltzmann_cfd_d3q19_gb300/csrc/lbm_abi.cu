@@ -147,16 +147,17 @@ struct lbm_ctx {
     // highest priority forked from `stream` and joined back into it, where the main kernel
     // stores into no slot of a special cell (the AA odd kernels, the one-cell A-B pull and the
     // streaming pass): the special cells' latency-bound warps then overlap the main kernel's
-    // streaming instead of following it.  The two-cell A-B pull and the collision layout's staged
-    // pull write special cells' slots with their whole-sector stores and keep the serial order.  Serial while profiling
+    // streaming instead of following it.  The two-cell A-B pull and the staged pull of the bundle
+    // and collision layouts write special cells' slots with their whole-sector stores and keep
+    // the serial order.  Serial while profiling
     // (per-kernel times) or when the caller switches it off.
     cudaStream_t side_stream = nullptr;
     cudaEvent_t side_fork = nullptr, side_join = nullptr;
     bool overlap_allowed = true;
     bool overlap(int kind) const {
         if (!overlap_allowed || profiling || n_special == 0) return false;
-        // the two-cell pull and the collision layout's staged pull write special cells' slots
-        return !(kind == K_AB_PULL && (pairs() || layout == LBM_LAYOUT_COLLISION));
+        // the two-cell pull and the staged pull of the non-SoA layouts write special cells' slots
+        return !(kind == K_AB_PULL && (pairs() || !is_soa(layout)));
     }
     int64_t steps = 0;
     bool force_valid = false;

@@ -422,15 +422,15 @@ __global__ void __launch_bounds__(256, 6) k_ab(Params p) {
     if (FORCE) warp_force(fx, fy, fz, p.partial);
 }
 
-// A-B pull in the collision layout, with the stores staged: each lane gathers and collides its
-// cell as `k_ab` does (element loads from the neighbours' records), writes its record into the
-// warp's shared-memory tile, and the warp writes the 32 records to B as one coalesced run instead
-// of 19 stores 76 bytes apart.  Cells that are not pulled here (SOLID, INLET, MOVING_WALL,
-// special) get zeros, so every sector of B is written whole; the boundary kernel, launched after
-// this one, overwrites the special cells' records.
-template <bool FORCE, bool BODY, typename I>
+// A-B pull in the collision and bundle layouts, with the stores staged: each lane gathers and
+// collides its cell as `k_ab` does (element loads from the neighbours' records), writes its
+// populations into the warp's shared-memory tile (the layout for N = 32), and the warp writes its
+// cells' records to B in coalesced runs -- one run (collision) or one per bundle -- instead of
+// element stores 76 or 12 bytes apart.  Cells that are not pulled here (SOLID, INLET,
+// MOVING_WALL, special) get zeros, so every sector of B is written whole; the boundary kernel,
+// launched after this one, overwrites the special cells' records.
+template <int L, bool FORCE, bool BODY, typename I>
 __global__ void __launch_bounds__(256) k_ab_pull_staged(Params p) {
-    constexpr int L = LAYOUT_COLLISION;
     __shared__ float tile[kWarpsPerBlock][32 * 19];
     CellCoord c;
     const bool in = grid_cell(p, c);
@@ -455,8 +455,18 @@ __global__ void __launch_bounds__(256) k_ab_pull_staged(Params p) {
         for (int q = 0; q < 19; ++q) t[idx<L, int>(q, (uint32_t)lane, 32)] = 0.0f;
     }
     __syncwarp();
-    float* dst = static_cast<float*>(p.B) + (size_t)n0 * 19;
-    for (int k = lane; k < cnt * 19; k += 32) dst[k] = t[k];
+    float* B = static_cast<float*>(p.B);
+#pragma unroll
+    for (int q = 0; q < 19; ++q) {
+        // one run per record group: the collision layout's records, or a bundle (from its first
+        // member q: bundle offset in units of N, members per cell)
+        if ((L == LAYOUT_COLLISION && q == 0) || (L != LAYOUT_COLLISION && bundle_j(q) == 0)) {
+            const int off = L == LAYOUT_COLLISION ? 0 : bundle_off(q);
+            const int m = L == LAYOUT_COLLISION ? 19 : bundle_size(q);
+            float* dst = B + (size_t)off * p.N + (size_t)n0 * m;
+            for (int k = lane; k < cnt * m; k += 32) dst[k] = t[32 * off + k];
+        }
+    }
     if (FORCE) warp_force(fx, fy, fz, p.partial);
 }
 

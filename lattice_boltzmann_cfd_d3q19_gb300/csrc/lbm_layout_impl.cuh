@@ -41,9 +41,11 @@ void launch_main_offsets(int kind, const Params& p, dim3 grid, dim3 block, cudaS
             k_own_staged<F, B, false><<<grid, block, 0, s>>>(p);
             return;
         }
+    }
+    if constexpr (!is_soa(L)) {
         if (kind == K_AB_PULL) {
-            if (19 * p.N <= (size_t(1) << 32)) k_ab_pull_staged<F, B, uint32_t><<<grid, block, 0, s>>>(p);
-            else k_ab_pull_staged<F, B, long long><<<grid, block, 0, s>>>(p);
+            if (19 * p.N <= (size_t(1) << 32)) k_ab_pull_staged<L, F, B, uint32_t><<<grid, block, 0, s>>>(p);
+            else k_ab_pull_staged<L, F, B, long long><<<grid, block, 0, s>>>(p);
             return;
         }
     }
