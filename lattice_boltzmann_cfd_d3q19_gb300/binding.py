@@ -62,6 +62,8 @@ class LbmError(RuntimeError):
 
 
 _lib = None
+# cells of every live context, so that array arguments can be checked against 19 N / 3 N / N
+_cells = {}
 
 
 def library_path() -> str:
@@ -130,7 +132,15 @@ def lbm_create(nx: int, ny: int, nz: int, tau: float, layout: int = LAYOUT_STREA
     h = load().lbm_create(int(nx), int(ny), int(nz), float(tau), int(layout), int(streaming))
     if not h:
         raise LbmError(EINVAL, _err())
+    _cells[h] = int(nx) * int(ny) * int(nz)
     return h
+
+
+def _n(ctx: int, per_cell: int = 1):
+    """Element count an array argument of this context must have (None for an unknown handle,
+    which the library rejects itself)."""
+    N = _cells.get(ctx)
+    return None if N is None else per_cell * N
 
 
 def lbm_last_error() -> str:
@@ -142,7 +152,8 @@ def lbm_set_stream(ctx: int, cuda_stream: int) -> None:
 
 
 def lbm_set_flags(ctx: int, flags) -> None:
-    _check(load().lbm_set_flags(ctx, _ptr(flags, np.uint8)))
+    p = _ptr(flags, np.uint8, _n(ctx))
+    _check(load().lbm_set_flags(ctx, p))
 
 
 def lbm_set_faces(ctx: int, fx: int, fy: int, fz: int) -> None:
@@ -162,15 +173,18 @@ def lbm_set_wall_velocity(ctx: int, ux: float, uy: float, uz: float) -> None:
 
 
 def lbm_set_populations(ctx: int, f) -> None:
-    _check(load().lbm_set_populations(ctx, _ptr(f, np.float32)))
+    p = _ptr(f, np.float32, _n(ctx, 19))
+    _check(load().lbm_set_populations(ctx, p))
 
 
 def lbm_set_equilibrium(ctx: int, rho, u) -> None:
-    _check(load().lbm_set_equilibrium(ctx, _ptr(rho, np.float32), _ptr(u, np.float32)))
+    pr, pu = _ptr(rho, np.float32, _n(ctx)), _ptr(u, np.float32, _n(ctx, 3))
+    _check(load().lbm_set_equilibrium(ctx, pr, pu))
 
 
 def lbm_get_populations(ctx: int, f) -> None:
-    _check(load().lbm_get_populations(ctx, _ptr(f, np.float32)))
+    p = _ptr(f, np.float32, _n(ctx, 19))
+    _check(load().lbm_get_populations(ctx, p))
 
 
 def lbm_step(ctx: int, n: int) -> None:
@@ -203,7 +217,8 @@ def lbm_set_boundary_overlap(ctx: int, enable: bool) -> None:
 
 
 def lbm_macroscopic(ctx: int, rho, u) -> None:
-    _check(load().lbm_macroscopic(ctx, _ptr(rho, np.float32), _ptr(u, np.float32)))
+    pr, pu = _ptr(rho, np.float32, _n(ctx)), _ptr(u, np.float32, _n(ctx, 3))
+    _check(load().lbm_macroscopic(ctx, pr, pu))
 
 
 def lbm_force_momentum_exchange(ctx: int) -> np.ndarray:
@@ -241,16 +256,21 @@ def lbm_profile_read(ctx: int, kind: int):
 
 def lbm_destroy(ctx: int) -> None:
     if ctx:
+        _cells.pop(ctx, None)
         load().lbm_destroy(ctx)
 
 
 def lbm_force_momentum_exchange_noalloc(f, flags, nx: int, ny: int, nz: int, faces=(0, 0, 0),
                                         tau: float = 0.6, g=(0.0, 0.0, 0.0),
                                         cuda_stream: int = 0) -> np.ndarray:
-    """Force of one collision of the device state f with no allocation (see include/lbm.h)."""
+    """Force of one collision of the device state f with no allocation (see include/lbm.h).
+    f must hold 19 nx ny nz floats and flags nx ny nz bytes: the C side cannot check array sizes,
+    so they are checked here before the call."""
+    N = int(nx) * int(ny) * int(nz)
+    pf = _ptr(f, np.float32, count=19 * N)
+    pflags = _ptr(flags, np.uint8, count=N)
     F = np.zeros(3, np.float64)
     _check(load().lbm_force_momentum_exchange_noalloc(
-        _ptr(f, np.float32), _ptr(flags, np.uint8), int(nx), int(ny), int(nz), int(faces[0]),
-        int(faces[1]), int(faces[2]), float(tau), float(g[0]), float(g[1]), float(g[2]),
-        F.ctypes.data, cuda_stream or None))
+        pf, pflags, int(nx), int(ny), int(nz), int(faces[0]), int(faces[1]), int(faces[2]),
+        float(tau), float(g[0]), float(g[1]), float(g[2]), F.ctypes.data, cuda_stream or None))
     return F

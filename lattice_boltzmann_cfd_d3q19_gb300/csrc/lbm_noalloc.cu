@@ -1,11 +1,11 @@
 // Momentum-exchange force of one collision of a caller-held state, computed without allocating
 // any device memory.
 //
-// Some callers cannot call cudaMalloc: code running while a CUDA graph is being captured on
-// their stream, plug-ins whose host application owns all device memory through its own pool,
-// or tools that must not grow the footprint of a process they are embedded in.  This entry point
-// serves them: the only working memory it uses is g_noalloc_scratch below, a fixed-size array
-// in the library's static device memory, which every GPU that loads the library holds until the
+// Some callers cannot call cudaMalloc: plug-ins whose host application owns all device memory
+// through its own pool (an allocation behind the pool's back can fail or break its accounting),
+// and tools that must not grow the footprint of a process they are embedded in.  This entry point
+// serves them: the only working memory it uses is g_noalloc_scratch below, a fixed-size array in
+// the library's static device memory, which every GPU that loads the library holds until the
 // process exits.  The caller passes the state, the flags and the output.
 #include <cmath>
 #include <cstdarg>
@@ -60,13 +60,15 @@ int lbm_noalloc_fail(int code, const char* fmt, ...) {
     return code;
 }
 
-bool is_device_memory(const void* p) {
+// True when p is device (or managed) memory of device `dev`.
+bool is_memory_of_device(const void* p, int dev) {
     cudaPointerAttributes a;
     if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
         cudaGetLastError();
         return false;
     }
-    return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+    if (a.type == cudaMemoryTypeManaged) return true;
+    return a.type == cudaMemoryTypeDevice && a.device == dev;
 }
 
 // One thread per cell: collide the natural state of a FLUID cell (shifted as the step kernels
@@ -126,10 +128,16 @@ extern "C" int lbm_force_momentum_exchange_noalloc(const float* f, const uint8_t
         return lbm_noalloc_fail(LBM_EINVAL, "lbm_force_momentum_exchange_noalloc: need a finite tau > 1/2");
     if (!std::isfinite(gx) || !std::isfinite(gy) || !std::isfinite(gz))
         return lbm_noalloc_fail(LBM_EINVAL, "lbm_force_momentum_exchange_noalloc: g must be finite");
-    if (!is_device_memory(f) || !is_device_memory(flags))
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return lbm_noalloc_fail(LBM_ECUDA, "lbm_force_momentum_exchange_noalloc: no current device");
+    }
+    if (!is_memory_of_device(f, dev) || !is_memory_of_device(flags, dev))
         return lbm_noalloc_fail(LBM_EINVAL,
                                 "lbm_force_momentum_exchange_noalloc: f and flags must be device "
-                                "memory (this entry point cannot stage host data)");
+                                "memory of the current device %d (this entry point cannot stage "
+                                "host data or reach another device's memory)", dev);
 
     double* scratch = nullptr;
     cudaError_t e = scratch_for_current_device(&scratch);

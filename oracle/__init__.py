@@ -126,9 +126,17 @@ class Problem:
         return (self.nx, self.ny, self.nz, self.tau, _ptr(self.flags), _ptr(self.faces),
                 _ptr(self.inlet), _ptr(self.g), _ptr(self.wall))
 
-    def step_ab(self, f, nsteps: int, want_force: bool = False):
-        """Two-lattice steps on a copy of natural f[19, N]; returns (f_new, force or None)."""
-        f = _f64(f).reshape(19, self.N).copy()
+    def step_ab(self, f, nsteps: int, want_force: bool = False, inplace: bool = False):
+        """Two-lattice steps on a copy of natural f[19, N]; returns (f_new, force or None).
+        inplace=True updates f itself (a C-contiguous float64 array of 19 N values), which keeps
+        the host memory of a large grid at two lattices instead of three."""
+        if inplace:
+            if not (isinstance(f, np.ndarray) and f.dtype == np.float64 and
+                    f.flags["C_CONTIGUOUS"] and f.size == 19 * self.N):
+                raise ValueError("inplace needs a C-contiguous float64 array of 19 N values")
+            f = f.reshape(19, self.N)
+        else:
+            f = _f64(f).reshape(19, self.N).copy()
         force = np.zeros(3, np.float64) if want_force else None
         rc = _load().oracle_step_ab(*self._args(), _ptr(f), int(nsteps), _ptr(force),
                                     self.threads)

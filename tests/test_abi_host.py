@@ -100,3 +100,33 @@ def test_shifted_storage_round_trips_integer_labels():
     for w in (np.float32(1 / 3), np.float32(1 / 18), np.float32(1 / 36)):
         h = (L - w).astype(np.float32)
         assert np.array_equal((h + w).astype(np.float32), L)
+
+
+def test_noalloc_binding_checks_array_sizes_before_the_call():
+    """The C side cannot see array sizes: the binding rejects a population array shorter than
+    19 nx ny nz floats or a flag array shorter than nx ny nz bytes before calling into the
+    library (a short array would otherwise be read past its end on the device)."""
+    with pytest.raises(ValueError):
+        B.lbm_force_momentum_exchange_noalloc(np.zeros(19 * 8 - 1, np.float32),
+                                              np.zeros(8, np.uint8), 2, 2, 2)
+    with pytest.raises(ValueError):
+        B.lbm_force_momentum_exchange_noalloc(np.zeros(19 * 8, np.float32),
+                                              np.zeros(7, np.uint8), 2, 2, 2)
+
+
+def test_context_binding_checks_array_sizes():
+    """Arrays passed with a context are checked against its cell count (19 N populations, N
+    flags or densities, 3 N velocities) before the call."""
+    ctx = 12345  # a handle the binding knows; no call reaches the library
+    B._cells[ctx] = 8
+    try:
+        for fn, args in ((B.lbm_set_populations, (np.zeros(19 * 8 + 1, np.float32),)),
+                         (B.lbm_get_populations, (np.zeros(19 * 7, np.float32),)),
+                         (B.lbm_set_flags, (np.zeros(9, np.uint8),)),
+                         (B.lbm_macroscopic, (np.zeros(8, np.float32), np.zeros(23, np.float32))),
+                         (B.lbm_set_equilibrium, (np.zeros(7, np.float32),
+                                                  np.zeros(24, np.float32)))):
+            with pytest.raises(ValueError):
+                fn(ctx, *args)
+    finally:
+        B._cells.pop(ctx, None)
