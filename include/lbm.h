@@ -47,6 +47,12 @@
  * host thread at a time.  Calls that only enqueue work (lbm_step) are asynchronous on the
  * context's stream; calls that return data to the caller synchronise that stream.
  *
+ * Changes between steps.  After an odd number of AA steps, and after any A-B step, the buffer holds
+ * post-collision values whose streaming (the second half of the last step) is still pending; a
+ * change of the flags, faces, inlet state or wall velocity made then acts on that streaming, as it
+ * does on every later step.  After an even number of AA steps and in the AB2 scheme the state is
+ * natural and a change acts from the next step on.
+ *
  * Errors.  Functions returning int give LBM_OK (0) or a negative LBM_E* code; lbm_create returns
  * NULL on failure.  The message for the calling thread's last failure is lbm_last_error().  A call
  * that fails argument validation changes nothing; a CUDA failure (LBM_ECUDA) leaves the context
@@ -109,36 +115,57 @@ enum { LBM_PERIODIC = 0, LBM_OPEN = 1 };
 lbm_ctx* lbm_create(int nx, int ny, int nz, float tau, int layout, int streaming);
 
 /* Message for the calling thread's most recent failure ("" if none).  Valid until that thread's
- * next call into the library. */
+ * next call into the library.  (No page defines an error interface; [PortLBM] §4 names only an
+ * abstract handler that initialises and controls a simulation.  Status codes with a per-thread
+ * message are this ABI's own convention.) */
 const char* lbm_last_error(void);
 
 /* Use `cuda_stream` (a cudaStream_t, e.g. torch.cuda.current_stream().cuda_stream) for all later
- * work of this context.  Work already enqueued on the previous stream is synchronised first. */
+ * work of this context.  Work already enqueued on the previous stream is synchronised first.
+ * ([Layout] submits a flow's steps as submissions to one device queue and reads the forces of a
+ * submission's last step; the CUDA stream is that queue here.  The stream belongs to the caller
+ * and must stay valid while the context uses it.) */
 int lbm_set_stream(lbm_ctx* ctx, void* cuda_stream);
 
 /* Cell flags, N bytes, LBM_FLUID / LBM_SOLID / LBM_INLET / LBM_MOVING_WALL ([PortLBM] §3.1
  * boundary treatment; [Blog] §4.2 moving walls; [Layout]: the per-link rules are driven by the
  * cell type).  Any other value -> LBM_EINVAL.
- * Changing flags does not touch the populations.  Synchronous. */
+ * Changing flags does not touch the FLUID cells' populations; INLET cells, which the step kernels
+ * run as producers of f_eq(rho_in, u_in), get their outgoing slots rewritten when streaming is
+ * pending (see "Changes between steps" above).  Synchronous. */
 int lbm_set_flags(lbm_ctx* ctx, const uint8_t* flags);
 
 /* Face type per axis: LBM_PERIODIC (wrap) or LBM_OPEN (zero-gradient: a population whose source
  * lies beyond the face comes from the source clamped onto the last layer).  An OPEN axis needs at
- * least 2 cells. */
+ * least 2 cells; any other value -> LBM_EINVAL, nothing changed.  ([PortLBM] §3.1, last
+ * paragraph: Neumann-type outlet; [Layout]: open-face rules are per-link rules.  Periodic wrap
+ * is the pages' periodic 128^3 case.) */
 int lbm_set_faces(lbm_ctx* ctx, int face_x, int face_y, int face_z);
 
-/* State held by every INLET cell: f = f_eq(rho, (ux, uy, uz)).  rho > 0 and finite. */
+/* State held by every INLET cell: f = f_eq(rho, (ux, uy, uz)).  rho > 0 and finite, u finite;
+ * otherwise LBM_EINVAL, nothing changed.  The step kernels run INLET cells as producers: their
+ * outgoing slots carry f_eq where a FLUID cell's post-collision values would be, so that their
+ * neighbours take the ordinary path.  When streaming is pending (see "Changes between steps"
+ * above) this call enqueues a small kernel on the context stream that rewrites those slots;
+ * asynchronous.  ([PortLBM] §3.1, last paragraph: the inlet imposes the equilibrium
+ * distribution.) */
 int lbm_set_inlet(lbm_ctx* ctx, float rho, float ux, float uy, float uz);
 
 /* Velocity u_w of every LBM_MOVING_WALL cell ([Blog] §4.2).  Finite; 0 (the initial value) makes
  * moving walls behave as solid ones. */
 int lbm_set_wall_velocity(lbm_ctx* ctx, float ux, float uy, float uz);
 
-/* Body acceleration g (force density F = rho g), applied with Guo forcing.  0 disables it. */
+/* Body acceleration g (force density F = rho g), applied with Guo forcing.  0 disables it; a
+ * non-finite component -> LBM_EINVAL, nothing changed.  (No page describes the forcing scheme:
+ * reading R4 of this library's design notes, Guo forcing with the half-force velocity shift
+ * u = j/rho + g/2 and the source (1 - omega/2) w [3 (c - u).F + 9 (c.u)(c.F)].) */
 int lbm_set_body_force(lbm_ctx* ctx, float gx, float gy, float gz);
 
 /* Load the natural state f(x, t) from f[19*N] (canonical, absolute fp32).  Values of SOLID and
- * INLET cells are ignored.  Resets the step count to 0 (AA even parity).  Synchronous. */
+ * INLET cells are ignored.  Resets the step count to 0 (AA even parity).  Synchronous.
+ * ([Layout] "In place": at an even step count the buffer holds population q of cell x at (q, x),
+ * so loading is a layout change plus the weight shift; in the two-buffer schemes it fills the
+ * source buffer.) */
 int lbm_set_populations(lbm_ctx* ctx, const float* f);
 
 /* Load f = f_eq(rho[n], u[.][n]) for every FLUID cell, computed on the device in fp32
@@ -149,7 +176,9 @@ int lbm_set_equilibrium(lbm_ctx* ctx, const float* rho, const float* u);
 /* Read the natural state f(x, t) into f[19*N] (canonical, absolute fp32), whatever the AA parity
  * or A-B buffer state: after an odd AA step count the streaming half of the next step is applied
  * on the fly.  SOLID and MOVING_WALL cells read 0, INLET cells f_eq(rho_in, u_in).
- * Synchronous. */
+ * Synchronous.  ([Layout] "In place": after an odd step the collided population q of cell x sits
+ * at (opposite(q), x) and reaches x + c_q only in the next step's read, which the decoder
+ * applies through the per-link rules.) */
 int lbm_get_populations(lbm_ctx* ctx, float* f);
 
 /* Enqueue n >= 0 time steps ([PortLBM] Eq. 1 with the per-link rules above) on the context
@@ -193,8 +222,9 @@ int lbm_set_cell_pairs(lbm_ctx* ctx, int enable);
  * step; the staging is a GB300 launch choice, not a page's design.) */
 int lbm_set_tma_gather(lbm_ctx* ctx, int enable);
 
-/* Run each step's boundary kernel (the special cells: neighbours of INLET and MOVING_WALL cells,
- * links across OPEN faces) beside the step's main kernel (enable != 0, the default) or after it
+/* Run each step's boundary kernel (the special cells: neighbours of MOVING_WALL cells and, in the
+ * AA scheme, cells with links across OPEN faces; the A-B pulls take those links, clamped, in their
+ * main kernels) beside the step's main kernel (enable != 0, the default) or after it
  * (enable = 0).  Beside: the boundary kernel goes to a private stream of the highest priority,
  * forked from the context stream after the open-face pre-gather and joined back before the next
  * kernel, so lbm_step's ordering on the context stream is unchanged.  It applies to the AA odd
@@ -208,7 +238,9 @@ int lbm_set_boundary_overlap(lbm_ctx* ctx, int enable);
 
 /* Density and velocity of the natural state: rho[N], u[3*N] (fp32).  FLUID: rho = sum f,
  * u = j/rho + g/2 (Guo's half-force shift).  SOLID: 0, 0.  INLET: rho_in, u_in.  MOVING_WALL:
- * 1, u_w.  Synchronous. */
+ * 1, u_w.  Synchronous.  ([PortLBM] §3.1: density and momentum are the zeroth and first moments
+ * of the populations, v = sum f c; §4: the handler gives access to these macroscopic
+ * observables.  The half-force shift is reading R4, as for lbm_set_body_force.) */
 int lbm_macroscopic(lbm_ctx* ctx, float* rho, float* u);
 
 /* Force on all SOLID and MOVING_WALL cells (one body) from the last step of the last lbm_step
@@ -239,28 +271,76 @@ int64_t lbm_kernel_launches(lbm_ctx* ctx);
 int lbm_profile_enable(lbm_ctx* ctx, int enable);
 int lbm_profile_read(lbm_ctx* ctx, int kind, int64_t* launches, double* total_ms);
 
-/* Release every resource of the context.  NULL-safe.  Synchronises its stream first. */
+/* Release every resource of the context.  NULL-safe.  Synchronises its stream first; the
+ * caller's stream itself is not destroyed.  (No page: the counterpart of lbm_create in this
+ * ABI's own lifetime convention.) */
 void lbm_destroy(lbm_ctx* ctx);
 
+/* ---- slab decomposition along z (several contexts, one per rank) ----------------------------------
+ * [Disaggregated] ("Disaggregated Design for GPU-Based Volumetric Data Structures", section
+ * "Improving LBM Scalability"): the domain is split into slabs along one axis, and each slab
+ * exchanges its boundary data with its two neighbours every time step.  A rank's context holds its
+ * owned planes plus one GHOST plane below (z = 0) and one above (z = nz - 1), copies of the
+ * neighbouring slabs' boundary planes.  After every lbm_step(ctx, 1) the rank packs what its
+ * neighbours need (lbm_halo_pack), the ranks swap those buffers, and each unpacks what it received
+ * into its ghost planes (lbm_halo_unpack).  Only the five populations that cross a slab face are
+ * exchanged: 10 nx ny values per slab and step.  The force of lbm_force_momentum_exchange then
+ * covers the owned cells only; the ranks add theirs.  The host side (partition, neighbours,
+ * message order, force reduction) is lattice_boltzmann_cfd_d3q19_gb300/slab.py. */
+
+/* enable != 0: planes z = 0 and z = nz - 1 of this context become ghost planes.  Their cells are
+ * stepped like the others, but their results are replaced by lbm_halo_unpack.  They have no links
+ * for the momentum exchange and are never special.  Needs the A-B scheme (LBM_STREAMING_AB),
+ * PERIODIC z faces and nz >= 3; LBM_EINVAL otherwise.  While enabled, lbm_step accepts n <= 1 only,
+ * and lbm_set_faces keeps z PERIODIC.  Flags, populations and fields of the ghost planes are set
+ * and read like any others: load them with the neighbours' boundary planes.  Synchronous; drops
+ * the cached step graphs. */
+int lbm_set_ghost_planes(lbm_ctx* ctx, int enable);
+
+/* Elements of one halo buffer: 5 nx ny (-1 for a NULL context). */
+int64_t lbm_halo_elements(lbm_ctx* ctx);
+/* Bytes of one halo element: the internal storage of the populations (4; 2 in half-precision
+ * storage).  Halo buffers are opaque: they hold stored values, meaningful only to lbm_halo_unpack
+ * of a context with the same layout. */
+int lbm_halo_element_bytes(lbm_ctx* ctx);
+
+/* After a step: the post-collision populations with c_z = -1 of the first owned plane (z = 1) into
+ * lo, and those with c_z = +1 of the last owned plane (z = nz - 2) into hi.  Each buffer holds
+ * lbm_halo_elements values, population-major in q order, cell x + nx y within a population.  lo
+ * goes to the slab below, hi to the slab above.  lo and hi are device memory of the current
+ * device (LBM_EINVAL otherwise).  LBM_ESTATE without ghost planes, or before the first step after
+ * a state load.  Asynchronous on the context stream. */
+int lbm_halo_pack(lbm_ctx* ctx, void* lo, void* hi);
+
+/* Write the neighbours' buffers into the ghost planes: from_below (the hi of the slab below) into
+ * the c_z = +1 populations of plane z = 0, and from_above (the lo of the slab above) into the
+ * c_z = -1 populations of plane z = nz - 1.  These are the only ghost values the next step's pull
+ * reads.  Same requirements and errors as lbm_halo_pack; asynchronous. */
+int lbm_halo_unpack(lbm_ctx* ctx, const void* from_below, const void* from_above);
+
 /* Momentum-exchange force of ONE collision of a caller-held state, without allocating any memory.
- * The source papers and pages describe no counterpart to this entry point; it exists for callers
- * that cannot call cudaMalloc (code running while a CUDA graph is captured on their stream,
- * plug-ins whose host application owns all device memory through its own pool, tools that must
- * not grow an embedding process's footprint).  It computes what lbm_force_momentum_exchange
- * reports after lbm_set_populations(f) and lbm_step(1) on a context with the same grid, tau,
- * flags, faces and body force: the sum over every bounce-back link of a FLUID cell of
- * 2 c_q f*_q, f* the post-collision state.
+ * The source papers and pages describe no counterpart to this entry point.  It exists for callers
+ * that cannot call cudaMalloc: plug-ins whose host application owns all device memory through its
+ * own pool (an allocation behind the pool's back can fail or break its accounting), and tools that
+ * must not grow the footprint of a process they are embedded in.  It computes what
+ * lbm_force_momentum_exchange reports after lbm_set_populations(f) and lbm_step(1) on a context
+ * with the same grid, tau, flags, faces and body force: the sum over every bounce-back link of a
+ * FLUID cell of 2 c_q f*_q, f* the post-collision state.
  *   f       device memory, canonical natural state f[q*N + n] (absolute fp32), 19*N floats;
- *   flags   device memory, N bytes, LBM_FLUID / LBM_SOLID / LBM_INLET (others -> LBM_EINVAL);
+ *   flags   device memory, N bytes, LBM_FLUID / LBM_SOLID / LBM_INLET (LBM_MOVING_WALL and other
+ *           values -> LBM_EINVAL, F unchanged);
  *   face_*  LBM_PERIODIC or LBM_OPEN per axis; tau > 1/2; g the body acceleration (Guo forcing);
  *   F       host memory, 3 doubles, written on success;
  *   cuda_stream  the stream to run on (NULL: the legacy default stream); synchronised on return.
+ * f, flags and the stream must belong to the CUDA device that is current on the calling thread;
+ * f or flags on another device -> LBM_EINVAL.
  * Working memory: one fixed array of about 1.5 MiB in the library's static device memory, held
  * by every GPU that loads the library until the process exits.  Grids of more than 16,777,216
  * cells (256^3) exceed it and are rejected with LBM_EINVAL before any CUDA call.  The first call
  * on each device looks the array's device address up (cudaGetSymbolAddress); make that first
- * call before any stream capture.  All calls share the array: calls that overlap on the GPU
- * (on different streams or host threads) race and give wrong results; serialise them. */
+ * call before any stream capture.  All calls share the array and each clears what it reads
+ * before writing it: calls that overlap on the GPU (on different streams or host threads) race
+ * and give wrong results; serialise them. */
 int lbm_force_momentum_exchange_noalloc(const float* f, const uint8_t* flags, int nx, int ny,
                                         int nz, int face_x, int face_y, int face_z, float tau,
                                         float gx, float gy, float gz, double F[3],

@@ -52,6 +52,11 @@ SIGNATURES = {
     "lbm_destroy": (None, [_P]),
     "lbm_force_momentum_exchange_noalloc": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _F, _F, _F, _F,
                                                  _P, _P]),
+    "lbm_set_ghost_planes": (_I, [_P, _I]),
+    "lbm_halo_elements": (_I64, [_P]),
+    "lbm_halo_element_bytes": (_I, [_P]),
+    "lbm_halo_pack": (_I, [_P, _P, _P]),
+    "lbm_halo_unpack": (_I, [_P, _P, _P]),
 }
 
 
@@ -258,6 +263,43 @@ def lbm_destroy(ctx: int) -> None:
     if ctx:
         _cells.pop(ctx, None)
         load().lbm_destroy(ctx)
+
+
+def lbm_set_ghost_planes(ctx: int, enable: bool) -> None:
+    _check(load().lbm_set_ghost_planes(ctx, 1 if enable else 0))
+
+
+def lbm_halo_elements(ctx: int) -> int:
+    return int(load().lbm_halo_elements(ctx))
+
+
+def lbm_halo_element_bytes(ctx: int) -> int:
+    rc = load().lbm_halo_element_bytes(ctx)
+    if rc < 0:
+        raise LbmError(rc, _err())
+    return int(rc)
+
+
+def _halo_ptr(ctx: int, t) -> int:
+    """A halo buffer: a contiguous CUDA tensor of lbm_halo_elements values of the stored width."""
+    import torch
+    width = lbm_halo_element_bytes(ctx)
+    want = torch.float16 if width == 2 else torch.float32
+    if not (hasattr(t, "data_ptr") and t.is_cuda and t.is_contiguous()):
+        raise ValueError("halo buffers are contiguous CUDA tensors")
+    if t.dtype != want or t.numel() != lbm_halo_elements(ctx):
+        raise ValueError(f"halo buffer must hold {lbm_halo_elements(ctx)} {want} values")
+    return t.data_ptr()
+
+
+def lbm_halo_pack(ctx: int, lo, hi) -> None:
+    pl, ph = _halo_ptr(ctx, lo), _halo_ptr(ctx, hi)
+    _check(load().lbm_halo_pack(ctx, pl, ph))
+
+
+def lbm_halo_unpack(ctx: int, from_below, from_above) -> None:
+    pb, pa = _halo_ptr(ctx, from_below), _halo_ptr(ctx, from_above)
+    _check(load().lbm_halo_unpack(ctx, pb, pa))
 
 
 def lbm_force_momentum_exchange_noalloc(f, flags, nx: int, ny: int, nz: int, faces=(0, 0, 0),

@@ -108,9 +108,10 @@ struct lbm_ctx {
     uint32_t* mask = nullptr;
     uint32_t* special = nullptr;  // sorted indices of the special FLUID cells
     uint32_t n_special = 0;
-    uint32_t* count_dev = nullptr;  // counters: special cells, SOLID links, MOVING_WALL links
+    uint32_t* count_dev = nullptr;  // counters: special cells, SOLID links, MOVING_WALL links, INLET cells
     int any_solid_link = 0;
     int any_moving = 0;
+    int any_inlet = 0;
     float uw[3] = {0.f, 0.f, 0.f};
     float* scratch = nullptr;
     size_t face_base[3][2] = {};
@@ -128,6 +129,7 @@ struct lbm_ctx {
     // test hook (LBM_TEST_STAGE_TIMEOUT=1 at lbm_create): the staged kernel announces 16 bytes
     // more than it copies, so its first wait runs out; nothing faults
     uint32_t extra_tx = 0;
+    bool ghost = false;           // z = 0 and z = nz - 1 are ghost planes of a slab decomposition
     int* fault_host = nullptr;
     size_t force_triples = 0;     // partial triples written by the step that computes the force
     double* stage = nullptr;
@@ -188,6 +190,9 @@ struct lbm_ctx {
         p.mask = mask;
         p.any_solid_link = any_solid_link;
         p.any_moving = any_moving;
+        p.any_inlet = any_inlet;
+        p.open_special = streaming == LBM_STREAMING_AA;
+        p.ghost_z = ghost ? 1 : 0;
         for (int a = 0; a < 3; ++a) p.uw[a] = uw[a];
         for (int q = 0; q < 19; ++q) {
             const double w = q == 0 ? 1.0 / 3.0 : q <= 6 ? 1.0 / 18.0 : 1.0 / 36.0;
@@ -404,12 +409,12 @@ size_t partial_triples(size_t main_blocks, uint32_t n_special) {
 // faces.  Synchronous.
 int classify(lbm_ctx* c) {
     Params p = c->params(nullptr, nullptr);
-    LBM_CUDA(cudaMemsetAsync(c->count_dev, 0, 3 * sizeof(uint32_t), c->stream), "classify");
+    LBM_CUDA(cudaMemsetAsync(c->count_dev, 0, 4 * sizeof(uint32_t), c->stream), "classify");
     LBM_CUDA(launch_classify(p, c->types, c->flags, c->mask, c->count_dev, c->grid, c->block,
                              c->stream), "classify flags");
     ++c->launches;
-    uint32_t counts[3] = {0, 0, 0};
-    LBM_CUDA(cudaMemcpyAsync(counts, c->count_dev, 3 * sizeof(uint32_t), cudaMemcpyDeviceToHost,
+    uint32_t counts[4] = {0, 0, 0, 0};
+    LBM_CUDA(cudaMemcpyAsync(counts, c->count_dev, 4 * sizeof(uint32_t), cudaMemcpyDeviceToHost,
                              c->stream), "classify");
     LBM_CUDA(cudaStreamSynchronize(c->stream), "classify");
     const uint32_t count = counts[0];
@@ -454,6 +459,7 @@ int classify(lbm_ctx* c) {
     c->n_special = count;
     c->any_solid_link = counts[1] > 0;
     c->any_moving = counts[2] > 0;
+    c->any_inlet = counts[3] > 0;
     return LBM_OK;
 }
 
@@ -578,6 +584,18 @@ int sync(lbm_ctx* c, const char* what) {
     if (*c->fault_host)
         return fail(LBM_ETIMEOUT, "%s: a staged-gather kernel gave up waiting for its copies (code %d); "
                     "the state is not valid", what, *c->fault_host);
+    return LBM_OK;
+}
+
+// INLET cells are producers in the step kernels: their post-collision slots carry the reservoir's
+// f_eq(rho_in, u_in) where the next step's pulls read them.  A change of the flags or of the inlet
+// state while the buffer holds a post-collision state rewrites those slots (enqueued on the
+// context stream); a natural state needs nothing (the next step's kernels write them).
+int refill_inlets(lbm_ctx* c, const char* what) {
+    if (!c->any_inlet || (c->state != ST_POST_AA && c->state != ST_POST_AB)) return LBM_OK;
+    void* buf = c->state_buffer();
+    LBM_CUDA(c->ops->fill_inlet(c->params(buf, buf), c->state, c->grid, c->block, c->stream), what);
+    ++c->launches;
     return LBM_OK;
 }
 
@@ -745,7 +763,7 @@ lbm_ctx* lbm_create(int nx, int ny, int nz, float tau, int layout, int streaming
     if ((e = cudaMalloc(&c->types, N)) != cudaSuccess) return bad(e, "lbm_create: cell types");
     if ((e = cudaMalloc(&c->flags, N)) != cudaSuccess) return bad(e, "lbm_create: cell flags");
     if ((e = cudaMalloc(&c->mask, N * sizeof(uint32_t))) != cudaSuccess) return bad(e, "lbm_create: link masks");
-    if ((e = cudaMalloc(&c->count_dev, 3 * sizeof(uint32_t))) != cudaSuccess) return bad(e, "lbm_create: counter");
+    if ((e = cudaMalloc(&c->count_dev, 4 * sizeof(uint32_t))) != cudaSuccess) return bad(e, "lbm_create: counter");
     if ((e = cudaMalloc(&c->stage, 3 * kForceStage * sizeof(double))) != cudaSuccess)
         return bad(e, "lbm_create: force stage");
     if ((e = cudaMalloc(&c->force_dev, 3 * sizeof(double))) != cudaSuccess) return bad(e, "lbm_create: force");
@@ -811,6 +829,7 @@ int lbm_set_flags(lbm_ctx* c, const uint8_t* flags) {
         e = cudaMemcpyAsync(c->types, tmp, c->N, cudaMemcpyDeviceToDevice, c->stream);
         if (e != cudaSuccess) rc = cuda_fail(e, "lbm_set_flags");
         if (rc == LBM_OK) rc = classify(c);
+        if (rc == LBM_OK) rc = refill_inlets(c, "lbm_set_flags");
         if (rc == LBM_OK) rc = sync(c, "lbm_set_flags");
     }
     cudaFree(tmp);
@@ -819,6 +838,8 @@ int lbm_set_flags(lbm_ctx* c, const uint8_t* flags) {
 
 int lbm_set_faces(lbm_ctx* c, int fx, int fy, int fz) {
     if (!c) return fail(LBM_EINVAL, "lbm_set_faces: NULL context");
+    if (c->ghost && fz != LBM_PERIODIC)
+        return fail(LBM_EINVAL, "lbm_set_faces: a context with ghost planes keeps its z faces PERIODIC");
     const int f[3] = {fx, fy, fz};
     for (int a = 0; a < 3; ++a) {
         if (f[a] != LBM_PERIODIC && f[a] != LBM_OPEN)
@@ -864,7 +885,7 @@ int lbm_set_inlet(lbm_ctx* c, float rho, float ux, float uy, float uz) {
     c->inlet[3] = uz;
     const double u[3] = {ux, uy, uz};
     shifted_equilibrium(rho, u, c->heq_in);
-    return LBM_OK;
+    return refill_inlets(c, "lbm_set_inlet");
 }
 
 int lbm_set_wall_velocity(lbm_ctx* c, float ux, float uy, float uz) {
@@ -985,6 +1006,9 @@ int lbm_get_populations(lbm_ctx* c, float* f) {
 int lbm_step(lbm_ctx* c, int n) {
     if (!c) return fail(LBM_EINVAL, "lbm_step: NULL context");
     if (n < 0) return fail(LBM_EINVAL, "lbm_step: n = %d < 0", n);
+    if (c->ghost && n > 1)
+        return fail(LBM_EINVAL, "lbm_step: with ghost planes, step once and exchange the halos "
+                                "between steps (n = %d)", n);
     if (c->use_graphs && !c->profiling) {
         for (int done = 0; done < n;) {
             const int len = n - done > kGraphChunk ? kGraphChunk : n - done;
@@ -1062,6 +1086,72 @@ int lbm_check_finite(lbm_ctx* c) {
 int64_t lbm_step_count(lbm_ctx* c) { return c ? c->steps : -1; }
 
 int64_t lbm_kernel_launches(lbm_ctx* c) { return c ? c->launches : -1; }
+
+int lbm_set_ghost_planes(lbm_ctx* c, int enable) {
+    if (!c) return fail(LBM_EINVAL, "lbm_set_ghost_planes: NULL context");
+    if (enable) {
+        if (c->streaming != LBM_STREAMING_AB)
+            return fail(LBM_EINVAL, "lbm_set_ghost_planes: needs the A-B scheme (LBM_STREAMING_AB)");
+        if (c->face[2] != LBM_PERIODIC)
+            return fail(LBM_EINVAL, "lbm_set_ghost_planes: the z faces must be PERIODIC");
+        if (c->n[2] < 3) return fail(LBM_EINVAL, "lbm_set_ghost_planes: needs nz >= 3");
+    }
+    const bool old = c->ghost;
+    c->ghost = enable != 0;
+    c->drop_graphs();
+    const int rc = classify(c);
+    if (rc != LBM_OK) c->ghost = old;
+    return rc;
+}
+
+int64_t lbm_halo_elements(lbm_ctx* c) {
+    return c ? 5 * (int64_t)c->n[0] * (int64_t)c->n[1] : -1;
+}
+
+int lbm_halo_element_bytes(lbm_ctx* c) {
+    if (!c) return fail(LBM_EINVAL, "lbm_halo_element_bytes: NULL context");
+    return (int)c->elem_bytes_of();
+}
+
+// Halo buffers are device memory of the context's device (they go to a communication library).
+static int check_halo(lbm_ctx* c, const void* a, const void* b, const char* what) {
+    if (!c || !a || !b) return fail(LBM_EINVAL, "%s: NULL argument", what);
+    if (!c->ghost) return fail(LBM_ESTATE, "%s: the context has no ghost planes", what);
+    if (c->state != ST_POST_AB)
+        return fail(LBM_ESTATE, "%s: no step taken since the state was loaded", what);
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(LBM_ECUDA, "%s: no current device", what);
+    }
+    for (const void* ptr : {a, b}) {
+        cudaPointerAttributes at;
+        if (cudaPointerGetAttributes(&at, ptr) != cudaSuccess) {
+            cudaGetLastError();
+            return fail(LBM_EINVAL, "%s: halo buffers must be device memory", what);
+        }
+        if (!(at.type == cudaMemoryTypeManaged || (at.type == cudaMemoryTypeDevice && at.device == dev)))
+            return fail(LBM_EINVAL, "%s: halo buffers must be device memory of the current device", what);
+    }
+    return LBM_OK;
+}
+
+int lbm_halo_pack(lbm_ctx* c, void* lo, void* hi) {
+    if (int rc = check_halo(c, lo, hi, "lbm_halo_pack")) return rc;
+    void* buf = c->buf[c->cur];
+    LBM_CUDA(c->ops->halo_pack(c->params(buf, buf), lo, hi, c->stream), "lbm_halo_pack");
+    ++c->launches;
+    return LBM_OK;
+}
+
+int lbm_halo_unpack(lbm_ctx* c, const void* from_below, const void* from_above) {
+    if (int rc = check_halo(c, from_below, from_above, "lbm_halo_unpack")) return rc;
+    void* buf = c->buf[c->cur];
+    LBM_CUDA(c->ops->halo_unpack(c->params(buf, buf), from_below, from_above, c->stream),
+             "lbm_halo_unpack");
+    ++c->launches;
+    return LBM_OK;
+}
 
 int lbm_profile_enable(lbm_ctx* c, int enable) {
     if (!c) return fail(LBM_EINVAL, "lbm_profile_enable: NULL context");

@@ -11,10 +11,13 @@ __global__ void __launch_bounds__(256) k_validate_types(const uint8_t* types, si
 }
 
 // Internal flags and solid-link masks.  For a FLUID cell: mask bit q when x + c_q (wrapped, or
-// clamped at an OPEN face) is SOLID; F_SPECIAL when some x + c_q is INLET or MOVING_WALL or lies
-// beyond an OPEN face; F_BULK when no link rule applies at all.
+// clamped at an OPEN face) is SOLID; F_SPECIAL when some x + c_q is MOVING_WALL or, in the AA
+// scheme (p.open_special), lies beyond an OPEN face; F_BULK when no link rule applies at all.
+// INLET neighbours need no special path: INLET cells are producers in the step kernels (their
+// slots carry f_eq(rho_in, u_in) where a FLUID neighbour's post-collision values would be), and
+// the A-B pulls clamp links across an OPEN face in their main kernels.
 // count[0]: special cells; count[1]: FLUID cells with a SOLID link; count[2]: FLUID cells with a
-// MOVING_WALL link
+// MOVING_WALL link; count[3]: INLET cells
 __global__ void __launch_bounds__(256) k_classify(Params p, const uint8_t* types, uint8_t* flags,
                                                   uint32_t* mask, uint32_t* count) {
     const int x = blockIdx.x * blockDim.x + threadIdx.x;
@@ -25,12 +28,17 @@ __global__ void __launch_bounds__(256) k_classify(Params p, const uint8_t* types
     const uint8_t t = types[n];
     uint8_t out = t;
     uint32_t m = 0;
-    if (t == T_FLUID) {
-        bool special = false, moving = false;
+    if (t == T_INLET) atomicAdd(count + 3, 1u);
+    // a ghost plane's cells are stepped like the others, but their results are replaced by the
+    // neighbouring slab's and they take no part in the momentum exchange: no links, never special
+    const bool ghost = p.ghost_z && (z == 0 || z == p.nz - 1);
+    if (t == T_FLUID && !ghost) {
+        bool special = false, moving = false, plain = true;
         for (int q = 1; q < 19; ++q) {
             const Link s = link_cell(p, x, y, z, cx(q), cy(q), cz(q));
             const uint8_t ts = types[s.cell];
-            if (s.face >= 0 || ts == T_INLET || ts == T_MOVING) special = true;
+            if ((s.face >= 0 && p.open_special) || ts == T_MOVING) special = true;
+            if (s.face >= 0 || ts != T_FLUID) plain = false;
             if (ts == T_MOVING) moving = true;
             if (ts == T_SOLID) m |= 1u << q;
         }
@@ -38,7 +46,7 @@ __global__ void __launch_bounds__(256) k_classify(Params p, const uint8_t* types
         if (special) {
             out |= F_SPECIAL;
             atomicAdd(count, 1u);
-        } else if (m == 0) {
+        } else if (plain) {
             out |= F_BULK;
         }
         if (m != 0) atomicAdd(count + 1, 1u);

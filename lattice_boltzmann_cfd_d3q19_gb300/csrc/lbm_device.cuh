@@ -134,6 +134,10 @@ struct Params {
     const uint32_t* mask;  // per-cell solid-link mask (0 for bulk cells)
     int any_solid_link;    // some FLUID cell has a SOLID neighbour (else every mask is 0)
     int any_moving;        // some FLUID cell has a MOVING_WALL neighbour
+    int any_inlet;         // some cell is INLET (the step kernels run INLET cells as producers)
+    int open_special;      // a link across an OPEN face makes a cell special (AA); the A-B pulls
+                           // clamp such links in their main kernels instead
+    int ghost_z;           // planes z = 0 and z = nz - 1 are ghost copies of neighbouring slabs
     const uint32_t* special;  // indices of the special FLUID cells
     uint32_t n_special;
     float* scratch;        // open-face pre-gathered values (AA odd step)

@@ -58,21 +58,26 @@ __device__ __forceinline__ size_t scratch_slot(const Params& p, int face, int q,
     return p.face_base[axis][face & 1] + (size_t)q * face_area(p, axis) + face_pos(p, axis, x, y, z);
 }
 
-// Neighbour cell indices of a cell whose 18 neighbours are inside the domain (wrapped on periodic
-// axes): n + d, with d the sum of one per-axis delta per velocity component.
+// Neighbour cell indices n + d, with d the sum of one per-axis delta per velocity component:
+// wrapped on PERIODIC axes, clamped onto the last layer on OPEN axes (the zero-gradient source of
+// a pull; the AA odd kernels never take a link across an OPEN face here -- such cells are special).
+__device__ __forceinline__ int edge_delta(int at, int n, int stride, bool open, int c) {
+    if (c < 0) return at == 0 ? (open ? 0 : (n - 1) * stride) : -stride;
+    return at == n - 1 ? (open ? 0 : -(n - 1) * stride) : stride;
+}
 struct Nbr {
     int dx[3], dy[3], dz[3];  // delta for c = -1, 0, +1 along each axis
     __device__ __forceinline__ Nbr(const Params& p, int x, int y, int z) {
         const int sx = 1, sy = p.nx, sz = p.nx * p.ny;
-        dx[0] = x == 0 ? (p.nx - 1) * sx : -sx;
+        dx[0] = edge_delta(x, p.nx, sx, p.open[0], -1);
         dx[1] = 0;
-        dx[2] = x == p.nx - 1 ? -(p.nx - 1) * sx : sx;
-        dy[0] = y == 0 ? (p.ny - 1) * sy : -sy;
+        dx[2] = edge_delta(x, p.nx, sx, p.open[0], 1);
+        dy[0] = edge_delta(y, p.ny, sy, p.open[1], -1);
         dy[1] = 0;
-        dy[2] = y == p.ny - 1 ? -(p.ny - 1) * sy : sy;
-        dz[0] = z == 0 ? (p.nz - 1) * sz : -sz;
+        dy[2] = edge_delta(y, p.ny, sy, p.open[1], 1);
+        dz[0] = edge_delta(z, p.nz, sz, p.open[2], -1);
         dz[1] = 0;
-        dz[2] = z == p.nz - 1 ? -(p.nz - 1) * sz : sz;
+        dz[2] = edge_delta(z, p.nz, sz, p.open[2], 1);
     }
     // cell n + s c_q, s = +1 or -1
     template <int Q, int S>
@@ -180,6 +185,10 @@ __global__ void __launch_bounds__(256) k_aa_even(Params p) {
                 mask_forces(p.mask[c.n], h, fx, fy, fz);
                 if (p.any_moving && (fl & F_SPECIAL)) moving_forces(p, h, c.x, c.y, c.z, fx, fy, fz);
             }
+        } else if (p.any_inlet && (fl & TYPE_MASK) == T_INLET) {
+            // an INLET cell's post-collision state is the reservoir's f_eq(rho_in, u_in)
+#pragma unroll
+            for (int q = 0; q < 19; ++q) st<L>(p.pa[opp(q)], cell_off<L, I>(q, c.n), p.heq_in[q]);
         }
     }
     if (FORCE) warp_force(fx, fy, fz, p.partial);
@@ -193,8 +202,8 @@ __global__ void __launch_bounds__(256) k_aa_even(Params p) {
 // bank conflicts); element loads strided by the 76-byte record touched 19 times as many sectors
 // per request (even step 0.173 -> 0.056 ms at 128^3).  The bundle layout's stride-3 element
 // accesses measured faster unstaged.  OPP: the AA even step (the collided population q goes to
-// opposite(q)); else the A-B collision (to q, in B, which may equal A).  A cell that is not FLUID
-// keeps what was loaded.
+// opposite(q)); else the A-B collision (to q, in B, which may equal A).  An INLET cell stores the
+// reservoir's f_eq(rho_in, u_in); any other cell that is not FLUID keeps what was loaded.
 template <bool FORCE, bool BODY, bool OPP>
 __global__ void __launch_bounds__(256) k_own_staged(Params p) {
     constexpr int L = LAYOUT_COLLISION;
@@ -225,6 +234,10 @@ __global__ void __launch_bounds__(256) k_own_staged(Params p) {
             mask_forces(p.mask[c.n], h, fx, fy, fz);
             if (p.any_moving && (fl & F_SPECIAL)) moving_forces(p, h, c.x, c.y, c.z, fx, fy, fz);
         }
+    } else if (p.any_inlet && (fl & TYPE_MASK) == T_INLET) {
+        // INLET producer: the reservoir's f_eq(rho_in, u_in) as its post-collision state
+#pragma unroll
+        for (int q = 0; q < 19; ++q) t[idx<L, int>(OPP ? opp(q) : q, (uint32_t)lane, 32)] = p.heq_in[q];
     }
     __syncwarp();
     for (int k = lane; k < cnt * 19; k += 32) dst[k] = t[k];
@@ -280,6 +293,30 @@ __device__ __forceinline__ void aa_odd_store(const Params& p, const Nbr& nb, uin
     if constexpr (Q < 18) aa_odd_store<L, I, FORCE, Q + 1>(p, nb, n, m, h, fx, fy, fz);
 }
 
+// INLET cells are producers in the AA odd step ("PortLBM", §3.1, last paragraph: the inlet imposes
+// the equilibrium): population q of the reservoir, f_eq,q(rho_in, u_in), goes to (q, s + c_q), the
+// slot in which a FLUID cell's scatter leaves its population q for the neighbour's next even step.
+// A link that leaves the domain through an OPEN face reaches nobody and is dropped (its wrapped
+// slot belongs to the zero-gradient copies of the boundary kernel).  The rest population stays.
+__device__ __forceinline__ bool leaves_open(const Params& p, int x, int y, int z, int c_x, int c_y,
+                                            int c_z) {
+    return (p.open[0] && ((c_x < 0 && x == 0) || (c_x > 0 && x == p.nx - 1))) ||
+           (p.open[1] && ((c_y < 0 && y == 0) || (c_y > 0 && y == p.ny - 1))) ||
+           (p.open[2] && ((c_z < 0 && z == 0) || (c_z > 0 && z == p.nz - 1)));
+}
+template <int L, typename I, int Q = 1>
+__device__ __forceinline__ void aa_odd_produce(const Params& p, const Nbr& nb, uint32_t n, int x,
+                                               int y, int z) {
+    constexpr uint32_t S = cell_stride<L>(Q);
+    if (!leaves_open(p, x, y, z, cx(Q), cy(Q), cz(Q))) {
+        if constexpr (std::is_same<I, uint32_t>::value)
+            st<L>(p.A, p.plane32[Q] + nb.template at<Q, 1>(n) * S, p.heq_in[Q]);
+        else
+            st<L>(p.pa[Q], cell_off<L, I>(Q, nb.template at<Q, 1>(n)), p.heq_in[Q]);
+    }
+    if constexpr (Q < 18) aa_odd_produce<L, I, Q + 1>(p, nb, n, x, y, z);
+}
+
 template <int L, bool FORCE, bool BODY, typename I>
 __global__ void __launch_bounds__(256) k_aa_odd(Params p) {
     CellCoord c;
@@ -298,6 +335,9 @@ __global__ void __launch_bounds__(256) k_aa_odd(Params p) {
             uint32_t ns = c.n, ms = m;
             asm volatile("" : "+r"(ns), "+r"(ms) : "f"(h[0]), "f"(h[18]));
             aa_odd_store<L, I, FORCE>(p, nb, ns, ms, h, fx, fy, fz);
+        } else if (p.any_inlet && (fl & TYPE_MASK) == T_INLET) {
+            const Nbr nb(p, c.x, c.y, c.z);
+            aa_odd_produce<L, I>(p, nb, c.n, c.x, c.y, c.z);
         }
     }
     if (FORCE) warp_force(fx, fy, fz, p.partial);
@@ -412,9 +452,14 @@ __global__ void __launch_bounds__(256, 6) k_ab(Params p) {
             if (FORCE && m) mask_forces(m, h, fx, fy, fz);
             if (FORCE && FROM_NATURAL && p.any_moving && (fl & F_SPECIAL))
                 moving_forces(p, h, c.x, c.y, c.z, fx, fy, fz);
+        } else if (p.any_inlet && (fl & TYPE_MASK) == T_INLET) {
+            // INLET producer: its post-collision state, where the pulls read it, is f_eq(rho_in,
+            // u_in) (written in place too: the two-pass scheme's streaming reads it there)
+#pragma unroll
+            for (int q = 0; q < 19; ++q) st<L>(p.pb[q], cell_off<L, I>(q, c.n), p.heq_in[q]);
         } else if ((fl & TYPE_MASK) != T_FLUID && p.pb[0] != p.pa[0]) {
-            // SOLID and INLET slots are never read; writing them keeps every 32-byte sector of
-            // the destination fully written (no fill from DRAM for partly written sectors)
+            // SOLID and MOVING_WALL slots are never read; writing them keeps every 32-byte sector
+            // of the destination fully written (no fill from DRAM for partly written sectors)
 #pragma unroll
             for (int q = 0; q < 19; ++q) st<L>(p.pb[q], cell_off<L, I>(q, c.n), 0.0f);
         }
@@ -426,9 +471,10 @@ __global__ void __launch_bounds__(256, 6) k_ab(Params p) {
 // collides its cell as `k_ab` does (element loads from the neighbours' records), writes its
 // populations into the warp's shared-memory tile (the layout for N = 32), and the warp writes its
 // cells' records to B in coalesced runs -- one run (collision) or one per bundle -- instead of
-// element stores 76 or 12 bytes apart.  Cells that are not pulled here (SOLID, INLET,
-// MOVING_WALL, special) get zeros, so every sector of B is written whole; the boundary kernel,
-// launched after this one, overwrites the special cells' records.
+// element stores 76 or 12 bytes apart.  INLET cells get the reservoir's f_eq(rho_in, u_in); the
+// other cells that are not pulled here (SOLID, MOVING_WALL, special) get zeros, so every sector of
+// B is written whole; the boundary kernel, launched after this one, overwrites the special cells'
+// records.
 template <int L, bool FORCE, bool BODY, typename I>
 __global__ void __launch_bounds__(256) k_ab_pull_staged(Params p) {
     __shared__ float tile[kWarpsPerBlock][32 * 19];
@@ -451,8 +497,10 @@ __global__ void __launch_bounds__(256) k_ab_pull_staged(Params p) {
         for (int q = 0; q < 19; ++q) t[idx<L, int>(q, (uint32_t)lane, 32)] = h[q];
         if (FORCE && m) mask_forces(m, h, fx, fy, fz);
     } else {
+        // INLET producer: f_eq(rho_in, u_in); zeros for the others
+        const bool inl = p.any_inlet && (fl & TYPE_MASK) == T_INLET;
 #pragma unroll
-        for (int q = 0; q < 19; ++q) t[idx<L, int>(q, (uint32_t)lane, 32)] = 0.0f;
+        for (int q = 0; q < 19; ++q) t[idx<L, int>(q, (uint32_t)lane, 32)] = inl ? p.heq_in[q] : 0.0f;
     }
     __syncwarp();
     float* B = static_cast<float*>(p.B);
@@ -479,7 +527,8 @@ __global__ void __launch_bounds__(256) k_stream(Params p) {
     const uint32_t m = p.any_solid_link ? p.mask[c.n] : 0u;
     const uint8_t fl = p.flags[c.n];
     if ((fl & TYPE_MASK) != T_FLUID) {
-        // never-read SOLID / INLET slots written to keep the destination's sectors whole
+        // SOLID / MOVING_WALL slots are never read; INLET slots are refilled by the next step's
+        // collision pass before any pull reads them: zeros keep the destination's sectors whole
 #pragma unroll
         for (int q = 0; q < 19; ++q) st<L>(p.pb[q], cell_off<L, I>(q, c.n), 0.0f);
         return;
@@ -599,6 +648,60 @@ __global__ void __launch_bounds__(256) k_macro(Params p, int state, float rho_in
     u0[k] = jx / r + 0.5f * p.g[0];
     u1[k] = jy / r + 0.5f * p.g[1];
     u2[k] = jz / r + 0.5f * p.g[2];
+}
+
+// The INLET cells' post-collision slots of a buffer in state `state` (ST_POST_AA: (opposite(q), s);
+// ST_POST_AB: (q, s)) refilled with the reservoir's f_eq(rho_in, u_in) -- after a change of the
+// flags or of the inlet state between steps, so that the next step's pulls read the new values
+// (every step kernel keeps them there afterwards).
+template <int L>
+__global__ void __launch_bounds__(256) k_fill_inlet(Params p, int state) {
+    const int x = blockIdx.x * blockDim.x + threadIdx.x;
+    const int y = blockIdx.y * blockDim.y + threadIdx.y;
+    const int z = blockIdx.z;
+    if (x >= p.nx || y >= p.ny) return;
+    const uint32_t n = (uint32_t)x + (uint32_t)p.nx * ((uint32_t)y + (uint32_t)p.ny * z);
+    if ((p.flags[n] & TYPE_MASK) != T_INLET) return;
+#pragma unroll
+    for (int q = 0; q < 19; ++q)
+        st<L>(p.A, idx<L>(state == ST_POST_AA ? opp(q) : q, n, p.N), p.heq_in[q]);
+}
+
+// ---- slab halos (A-B post-collision state, stored elements copied as they are) ------------------
+// The five populations with c_z = sgn, k-th in q order, of plane z: buf[k * nx ny + x + nx y].
+template <int L>
+using Stored = typename std::conditional<L == LAYOUT_STREAM_FP16, __half, float>::type;
+
+template <int L>
+__global__ void __launch_bounds__(256) k_halo_pack(Params p, int z_lo, int z_hi, Stored<L>* lo,
+                                                   Stored<L>* hi) {
+    const size_t area = (size_t)p.nx * p.ny;
+    const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= 10 * area) return;
+    const bool up = i >= 5 * area;
+    const size_t j = up ? i - 5 * area : i;
+    const int k = (int)(j / area);
+    const uint32_t xy = (uint32_t)(j - (size_t)k * area);
+    const int q = face_velocity(2, up ? 1 : -1, k);
+    const uint32_t n = xy + (uint32_t)area * (uint32_t)(up ? z_hi : z_lo);
+    const Stored<L>* A = static_cast<const Stored<L>*>(p.A);
+    (up ? hi : lo)[j] = A[idx_rt<L>(q, n, p.N)];
+}
+
+template <int L>
+__global__ void __launch_bounds__(256) k_halo_unpack(Params p, const Stored<L>* below,
+                                                     const Stored<L>* above) {
+    const size_t area = (size_t)p.nx * p.ny;
+    const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= 10 * area) return;
+    const bool top = i >= 5 * area;  // the upper ghost plane takes the slab above's c_z = -1 values
+    const size_t j = top ? i - 5 * area : i;
+    const int k = (int)(j / area);
+    const uint32_t xy = (uint32_t)(j - (size_t)k * area);
+    const int q = face_velocity(2, top ? -1 : 1, k);
+    const uint32_t n = xy + (uint32_t)area * (uint32_t)(top ? p.nz - 1 : 0);
+    Stored<L>* A = static_cast<Stored<L>*>(p.A);
+    A[idx_rt<L>(q, n, p.N)] = (top ? above : below)[j];
 }
 
 // Sets *bad when any stored population of a FLUID cell is not finite.

@@ -1,5 +1,5 @@
-// Boundary kernels of the AA odd and A-B pull steps: the special FLUID cells (a neighbour is an
-// INLET or a MOVING_WALL cell, or a link crosses an OPEN face), one warp per cell.  Lane q < 19
+// Boundary kernels of the AA odd and A-B pull steps: the special FLUID cells (a neighbour is a
+// MOVING_WALL cell, or -- AA odd step -- a link crosses an OPEN face), one warp per cell.  Lane q < 19
 // handles population q: it gathers it by the general per-link rules, the warp sums the moments,
 // every lane relaxes its own population, and lane q scatters it (with the open-face copies and
 // its link's momentum exchange).  A thread per cell walked the 19 links one after another, each
@@ -154,7 +154,9 @@ __global__ void __launch_bounds__(256) k_aa_odd_special(Params p) {
             } else if (t == T_MOVING) {
                 st<L>(p.A, idx_rt<L>(o, c.n, p.N), hn + p.wterm[o]);    // off the moving wall
             } else if (t == T_INLET) {
-                st<L>(p.A, idx_rt<L>(o, c.n, p.N), p.heq_in[o]);        // the reservoir feeds x
+                // the reservoir feeds x: a direct INLET neighbour writes (o, x) itself (it is a
+                // producer in the main kernel); one reached through an OPEN-face clamp does not
+                if (d.face >= 0) st<L>(p.A, idx_rt<L>(o, c.n, p.N), p.heq_in[o]);
             } else if (d.face < 0) {
                 st<L>(p.A, idx_rt<L>(q, d.cell, p.N), hn);
             }

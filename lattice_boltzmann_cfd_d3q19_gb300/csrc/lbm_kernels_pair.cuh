@@ -80,24 +80,25 @@ __device__ __forceinline__ bool grid_pair(const Params& p, PairCoord& c) {
     return c.x < p.nx && c.y < p.ny;
 }
 
-// Neighbour geometry of a pair: the y and z parts of n + s c_q (wrapped) are shared by both cells;
-// along x, a - 1 and b + 1 may wrap, a + 1 = b and b - 1 = a never do.  The wrapped offsets are
-// taken on every axis (the cells whose links cross an OPEN face are special and store nothing
-// here; their loads only need to stay inside the buffer).
+// Neighbour geometry of a pair: the y and z parts of n + s c_q are shared by both cells; along x,
+// a - 1 and b + 1 may leave the row, a + 1 = b and b - 1 = a never do.  Offsets wrap on PERIODIC
+// axes and clamp onto the last layer on OPEN axes (the zero-gradient source of the A-B pull; in
+// the AA odd step the cells whose links cross an OPEN face are special and store nothing here,
+// and an INLET producer drops such links).
 struct NbrPair {
     int dy[3], dz[3];  // y and z deltas for c = -1, 0, +1
-    int wa;            // (a - 1) - a along x, wrapped
-    int wb;            // (b + 1) - a along x, wrapped
+    int wa;            // (a - 1) - a along x
+    int wb;            // (b + 1) - a along x
     __device__ __forceinline__ NbrPair(const Params& p, int x, int y, int z) {
         const int sy = p.nx, sz = p.nx * p.ny;
-        dy[0] = y == 0 ? (p.ny - 1) * sy : -sy;
+        dy[0] = edge_delta(y, p.ny, sy, p.open[1], -1);
         dy[1] = 0;
-        dy[2] = y == p.ny - 1 ? -(p.ny - 1) * sy : sy;
-        dz[0] = z == 0 ? (p.nz - 1) * sz : -sz;
+        dy[2] = edge_delta(y, p.ny, sy, p.open[1], 1);
+        dz[0] = edge_delta(z, p.nz, sz, p.open[2], -1);
         dz[1] = 0;
-        dz[2] = z == p.nz - 1 ? -(p.nz - 1) * sz : sz;
-        wa = x == 0 ? p.nx - 1 : -1;
-        wb = x + 2 == p.nx ? 2 - p.nx : 2;
+        dz[2] = edge_delta(z, p.nz, sz, p.open[2], 1);
+        wa = x == 0 ? (p.open[0] ? 0 : p.nx - 1) : -1;
+        wb = x + 2 == p.nx ? (p.open[0] ? 1 : 2 - p.nx) : 2;
     }
     // a + (0, s cy(Q), s cz(Q)), before the x part
     template <int Q, int S>
@@ -169,6 +170,18 @@ __device__ __forceinline__ PairFlags pair_flags(const Params& p, uint32_t n, boo
         f.ma = f.mb = 0u;
     }
     return f;
+}
+
+// INLET cells as producers ("PortLBM", §3.1, last paragraph: the inlet imposes the equilibrium):
+// an INLET cell's post-collision state is the reservoir's f_eq(rho_in, u_in), stored by the step
+// kernels where a FLUID cell's would be, so that its neighbours read it through the ordinary
+// addressing.  In a pair, the INLET cell's lane of the collided array is replaced.
+__device__ __forceinline__ void inlet_lanes(const Params& p, bool ia, bool ib, float2 (&h)[19]) {
+#pragma unroll
+    for (int q = 0; q < 19; ++q) h[q] = make_float2(ia ? p.heq_in[q] : h[q].x, ib ? p.heq_in[q] : h[q].y);
+}
+__device__ __forceinline__ bool is_inlet(const Params& p, bool in, uint8_t f) {
+    return in && p.any_inlet && (f & TYPE_MASK) == T_INLET;
 }
 
 // Momentum exchange of a pair, packed: the sum over the links q whose bit is set in the cell's
@@ -315,7 +328,8 @@ __global__ void __launch_bounds__(256, pair_min_blocks<L>(kPackedHalfEven)) k_aa
     if (grid_pair(p, c)) {
         const PairFlags f = pair_flags(p, c.n, false);
         const bool act_a = (f.fa & TYPE_MASK) == T_FLUID, act_b = (f.fb & TYPE_MASK) == T_FLUID;
-        if ((act_a || act_b) && L == LAYOUT_STREAM_FP16 && kPackedHalfEven) {
+        const bool inl_a = is_inlet(p, true, f.fa), inl_b = is_inlet(p, true, f.fb);
+        if ((act_a || act_b) && !(inl_a || inl_b) && L == LAYOUT_STREAM_FP16 && kPackedHalfEven) {
             // half-precision storage: the stored pairs stay packed; each population is relaxed
             // where it is stored
             __half* A = static_cast<__half*>(p.A);
@@ -341,12 +355,13 @@ __global__ void __launch_bounds__(256, pair_min_blocks<L>(kPackedHalfEven)) k_aa
             own_store<L, true, FORCE>(p, reinterpret_cast<Elem<L>*>(A), ns, RelaxSrc<BODY>{m, hh, p},
                                       ma, mb, mov_a, mov_b, c.x, c.y, c.z, pf, fx, fy, fz);
             if (FORCE) pf.into(fx, fy, fz);
-        } else if (act_a || act_b) {
+        } else if (act_a || act_b || inl_a || inl_b) {
             Elem<L>* A = static_cast<Elem<L>*>(p.A);
             float2 h[19];
 #pragma unroll
             for (int q = 0; q < 19; ++q) h[q] = ld2<L>(A + (p.plane32[q] + c.n));
             collide2<BODY>(h, p);
+            if (inl_a || inl_b) inlet_lanes(p, inl_a, inl_b, h);
             uint32_t ns = c.n;
             asm volatile("" : "+r"(ns) : "f"(h[0].x), "f"(h[18].y));
 #pragma unroll
@@ -430,12 +445,14 @@ __global__ void __launch_bounds__(256, 4) k_aa_even2_bundle(Params p) {
     if (grid_pair(p, c)) {
         const PairFlags f = pair_flags(p, c.n, false);
         const bool act_a = (f.fa & TYPE_MASK) == T_FLUID, act_b = (f.fb & TYPE_MASK) == T_FLUID;
-        if (act_a || act_b) {
+        const bool inl_a = is_inlet(p, true, f.fa), inl_b = is_inlet(p, true, f.fb);
+        if (act_a || act_b || inl_a || inl_b) {
             float* A = static_cast<float*>(p.A);
             const uint32_t N = (uint32_t)p.N;
             float2 h[19];
             bundle_gather2(A, N, c.n, h);
             collide2<BODY>(h, p);
+            if (inl_a || inl_b) inlet_lanes(p, inl_a, inl_b, h);
             uint32_t ns = c.n;
             asm volatile("" : "+r"(ns) : "f"(h[0].x), "f"(h[18].y));
             bundle_scatter2_opp(A, N, ns, h);
@@ -485,6 +502,24 @@ __device__ __forceinline__ void odd2_scatter(const Params& p, const NbrPair& nb,
         nb.template store<L, Q, 1, BOTH>(A + far, v, act_a, act_b);
     }
     if constexpr (Q < 18) odd2_scatter<L, WALL, BOTH, FORCE, Q + 1>(p, nb, n, ma, mb, act_a, act_b, src, pf);
+}
+
+// AA odd step of INLET cells (producers): population q of the reservoir, f_eq,q(rho_in, u_in), to
+// (q, s + c_q) -- where a FLUID cell's scatter leaves its population q for the neighbour's next
+// even step -- for each INLET cell of the pair (ia, ib); a link leaving the domain through an OPEN
+// face is dropped (its wrapped slot belongs to the boundary kernel's zero-gradient copies).
+template <int L, int Q = 1>
+__device__ __forceinline__ void odd2_produce(const Params& p, const NbrPair& nb, uint32_t n, int x,
+                                             int y, int z, bool ia, bool ib) {
+    Elem<L>* A = static_cast<Elem<L>*>(p.A);
+    const uint32_t far = p.plane32[Q] + nb.template yz<Q, 1>(n);
+    const bool yz_out = (cy(Q) != 0 && p.open[1] && y == (cy(Q) > 0 ? p.ny - 1 : 0)) ||
+                        (cz(Q) != 0 && p.open[2] && z == (cz(Q) > 0 ? p.nz - 1 : 0));
+    const bool xa_out = cx(Q) < 0 && p.open[0] && x == 0;
+    const bool xb_out = cx(Q) > 0 && p.open[0] && x + 2 == p.nx;
+    if (ia && !yz_out && !xa_out) st1<L>(A + (far + (uint32_t)nb.template xa<Q, 1>()), p.heq_in[Q]);
+    if (ib && !yz_out && !xb_out) st1<L>(A + (far + (uint32_t)nb.template xb<Q, 1>()), p.heq_in[Q]);
+    if constexpr (Q < 18) odd2_produce<L, Q + 1>(p, nb, n, x, y, z, ia, ib);
 }
 
 template <int L, bool FORCE, bool BODY>
@@ -552,6 +587,11 @@ __global__ void __launch_bounds__(256, pair_min_blocks<L>(kPackedHalfOdd)) k_aa_
             else odd2_scatter<L, false, false, FORCE>(p, nb, ns, mas, mbs, act_a, act_b, src, pf);
         }
     }
+    const bool inl_a = is_inlet(p, in, f.fa), inl_b = is_inlet(p, in, f.fb);
+    if (inl_a || inl_b) {
+        const NbrPair nb(p, c.x, c.y, c.z);
+        odd2_produce<L>(p, nb, c.n, c.x, c.y, c.z, inl_a, inl_b);
+    }
     if (FORCE) warp_force(fx, fy, fz, p.partial);
 }
 
@@ -573,6 +613,7 @@ __global__ void __launch_bounds__(256, 4) k_ab2(Params p) {
     const bool act_a = in && (f.fa & want) == T_FLUID;
     const bool act_b = in && (f.fb & want) == T_FLUID;
     const bool wall = !FROM_NATURAL && __any_sync(0xffffffffu, (act_a || act_b) && (f.ma | f.mb) != 0u);
+    const bool inl_a = is_inlet(p, in, f.fa), inl_b = is_inlet(p, in, f.fb);
     Elem<L>* B = static_cast<Elem<L>*>(p.B);
     if (act_a || act_b) {
         float2 h[19];
@@ -586,6 +627,7 @@ __global__ void __launch_bounds__(256, 4) k_ab2(Params p) {
             else pair_gather<L, false, false>(p, nb, c.n, f.ma, f.mb, h);
         }
         collide2<BODY>(h, p);
+        if (inl_a || inl_b) inlet_lanes(p, inl_a, inl_b, h);
         uint32_t ns = c.n;
         asm volatile("" : "+r"(ns) : "f"(h[0].x), "f"(h[18].y));
 #pragma unroll
@@ -601,11 +643,13 @@ __global__ void __launch_bounds__(256, 4) k_ab2(Params p) {
                 if (act_b && (f.fb & F_SPECIAL)) moving_forces(p, PairLane<1>{h}, c.x + 1, c.y, c.z, fx, fy, fz);
             }
         }
-    } else if (in && p.B != p.A) {
-        // no working cell: SOLID / INLET / MOVING_WALL slots are never read and special cells'
-        // are rewritten by the boundary kernel; zeros keep every sector of B fully written
+    } else if (in && (p.B != p.A || inl_a || inl_b)) {
+        // no working cell: an INLET cell stores the reservoir's f_eq(rho_in, u_in); SOLID /
+        // MOVING_WALL slots are never read and special cells' are rewritten by the boundary
+        // kernel: zeros keep every sector of B fully written
 #pragma unroll
-        for (int q = 0; q < 19; ++q) st2<L>(B + (p.plane32[q] + c.n), make_float2(0.f, 0.f));
+        for (int q = 0; q < 19; ++q)
+            st2<L>(B + (p.plane32[q] + c.n), make_float2(inl_a ? p.heq_in[q] : 0.f, inl_b ? p.heq_in[q] : 0.f));
     }
     if (FORCE) warp_force(fx, fy, fz, p.partial);
 }

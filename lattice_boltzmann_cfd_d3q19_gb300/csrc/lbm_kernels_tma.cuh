@@ -243,6 +243,12 @@ __global__ void __launch_bounds__(kTmaThreads, 1) k_aa_odd_tma(Params p) {
                 else odd2_scatter<L, false, false, FORCE>(p, nb, n, ma, mb, act_a, act_b, src, pf);
             }
         }
+        // INLET cells of the tile: producers, as in the register kernel
+        const bool inl_a = is_inlet(p, in, fa), inl_b = is_inlet(p, in, fb);
+        if (inl_a || inl_b) {
+            const NbrPair nb(p, x, r % p.ny, r / p.ny);
+            odd2_produce<L>(p, nb, n, x, r % p.ny, r / p.ny, inl_a, inl_b);
+        }
         // every thread is done with stage s before it is refilled
         __syncthreads();
         const int t2 = t + 2 * (int)gridDim.x;

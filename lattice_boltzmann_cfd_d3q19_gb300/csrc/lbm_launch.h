@@ -47,6 +47,13 @@ struct LayoutOps {
     cudaError_t (*macro)(const Params& p, int state, const float inlet[4], float* rho, float* u0,
                          float* u1, float* u2, uint32_t n0, uint32_t count, cudaStream_t s);
     cudaError_t (*check_finite)(const Params& p, int* bad, dim3 grid, dim3 block, cudaStream_t s);
+    // the INLET cells' post-collision slots of a buffer in state ST_POST_AA or ST_POST_AB set to
+    // the reservoir's f_eq(rho_in, u_in)
+    cudaError_t (*fill_inlet)(const Params& p, int state, dim3 grid, dim3 block, cudaStream_t s);
+    // slab halos of the A-B post-collision state: the c_z = -1 populations of plane 1 into lo and
+    // the c_z = +1 ones of plane nz - 2 into hi; the reverse into the ghost planes 0 and nz - 1
+    cudaError_t (*halo_pack)(const Params& p, void* lo, void* hi, cudaStream_t s);
+    cudaError_t (*halo_unpack)(const Params& p, const void* below, const void* above, cudaStream_t s);
 };
 
 const LayoutOps& layout_ops_stream();

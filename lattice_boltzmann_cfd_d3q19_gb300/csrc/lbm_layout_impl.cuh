@@ -229,7 +229,25 @@ cudaError_t check_finite(const Params& p, int* bad, dim3 grid, dim3 block, cudaS
     return cudaGetLastError();
 }
 
-const LayoutOps kOps = {cells, cells2, odd_tma, special, pregather, pack, unpack, equilibrium, macro, check_finite};
+cudaError_t fill_inlet(const Params& p, int state, dim3 grid, dim3 block, cudaStream_t s) {
+    k_fill_inlet<L><<<grid, block, 0, s>>>(p, state);
+    return cudaGetLastError();
+}
+
+cudaError_t halo_pack(const Params& p, void* lo, void* hi, cudaStream_t s) {
+    k_halo_pack<L><<<blocks_for(10 * (size_t)p.nx * p.ny), 256, 0, s>>>(
+        p, 1, p.nz - 2, static_cast<Stored<L>*>(lo), static_cast<Stored<L>*>(hi));
+    return cudaGetLastError();
+}
+
+cudaError_t halo_unpack(const Params& p, const void* below, const void* above, cudaStream_t s) {
+    k_halo_unpack<L><<<blocks_for(10 * (size_t)p.nx * p.ny), 256, 0, s>>>(
+        p, static_cast<const Stored<L>*>(below), static_cast<const Stored<L>*>(above));
+    return cudaGetLastError();
+}
+
+const LayoutOps kOps = {cells, cells2, odd_tma, special, pregather, pack, unpack, equilibrium, macro, check_finite,
+                        fill_inlet, halo_pack, halo_unpack};
 
 }  // namespace
 }  // namespace lbm

@@ -246,7 +246,9 @@ def test_taylor_green_32_full(scheme):
     case = Case(32, 32, 32, 0.6, oracle.equilibrium_field(rho, u))
     fo, _ = case.run_oracle(100)
     fg, _ = case.run_gpu(100, "stream", scheme)
-    assert max_fluid_diff(case, fg, fo) <= TOL_F
+    d = max_fluid_diff(case, fg, fo)
+    print(f"\nfull-length parity taylor_green_32 {scheme} stream: all cells, max|df| {d:.3e}")
+    assert d <= TOL_F
 
 
 # ---- configuration 2: 64^3 channel, Guo forcing, 20000 steps -------------------------------------------
@@ -262,7 +264,10 @@ def test_channel_64_full_against_reduced_oracle():
                 flags=wl.channel_flags(n, n, n), g=(g, 0, 0))
     fg, Fg = full.run_gpu(steps, "stream", "AA", want_force=True)
     fo_full = np.broadcast_to(fo.reshape(19, 1, n, 1), (19, n, n, n)).reshape(19, -1)
-    assert max_fluid_diff(full, fg, fo_full) <= TOL_F
+    d = max_fluid_diff(full, fg, fo_full)
+    print(f"\nfull-length parity channel_64 AA stream: all cells, max|df| {d:.3e}, force x "
+          f"{Fg[0]:.6e} vs oracle {Fo[0] * n * n:.6e}")
+    assert d <= TOL_F
     assert abs(Fg[0] - Fo[0] * n * n) <= 1e-3 * abs(Fo[0] * n * n)
     # the profile: parabola with the startup transient (same bar as the oracle's own pin)
     ctx = full.gpu_context()
@@ -782,6 +787,54 @@ def test_flags_changed_between_even_and_odd_step(geometry, pairs, graphs):
         B.lbm_destroy(ctx)
     fl = flags2 == wl.FLUID
     assert np.abs(f.astype(np.float64)[:, fl] - A[:, fl]).max() <= TOL_F
+
+
+@pytest.mark.parametrize("pairs", [True, False])
+@pytest.mark.parametrize("scheme", ["AA", "AB", "AB2"])
+@pytest.mark.parametrize("k", [1, 2])
+@pytest.mark.parametrize("change", ["inlet_state", "new_inlet_cells"])
+def test_inlet_change_between_steps(change, k, scheme, pairs):
+    """INLET cells are producers: their post-collision slots carry f_eq(rho_in, u_in) for the next
+    step's pulls.  A change of the inlet state, or FLUID cells turned INLET, after k steps acts on
+    the streaming still pending: in a post-collision state (AA after an odd k, AB after any k) the
+    last step's streaming happens under the new problem.  The collision of a cell that stays FLUID
+    does not depend on the flags or the inlet, so the oracle reference is the old problem for k - 1
+    steps and the new one for the rest (k and the rest when no streaming is pending)."""
+    nx, ny, nz, tau, g = 18, 12, 10, 0.64, (1e-5, 0.0, -1e-5)
+    N = nx * ny * nz
+    r = np.random.default_rng(960 + k)
+    x, _, _ = wl.coords(nx, ny, nz)
+    flags1 = (r.uniform(size=N) < 0.1).astype(np.uint8)
+    flags1[x == 0] = wl.INLET
+    faces = (1, 0, 0)
+    inlet1 = (1.01, 0.03, 0.0, 0.0)
+    flags2, inlet2 = flags1.copy(), inlet1
+    if change == "inlet_state":
+        inlet2 = (0.99, 0.05, 0.01, -0.01)
+    else:
+        flags2[(flags1 == wl.FLUID) & (r.uniform(size=N) < 0.05)] = wl.INLET
+    f0 = random_state(N, 961)
+    P1 = oracle.Problem(nx, ny, nz, tau, flags=flags1, faces=faces, inlet=inlet1, g=g)
+    P2 = oracle.Problem(nx, ny, nz, tau, flags=flags2, faces=faces, inlet=inlet2, g=g)
+    pending = scheme == "AB" or (scheme == "AA" and k % 2 == 1)
+    k1 = k - 1 if pending else k
+    fo, _ = P1.step_ab(f0, k1)
+    fo, _ = P2.step_ab(fo, k + 5 - k1)
+    case = Case(nx, ny, nz, tau, f0, flags=flags1, faces=faces, inlet=inlet1, g=g)
+    ctx = case.gpu_context("stream", scheme, pairs=pairs)
+    try:
+        B.lbm_step(ctx, k)
+        if change == "inlet_state":
+            B.lbm_set_inlet(ctx, *inlet2)
+        else:
+            B.lbm_set_flags(ctx, flags2)
+        B.lbm_step(ctx, 5)
+        f = np.zeros((19, N), np.float32)
+        B.lbm_get_populations(ctx, f)
+    finally:
+        B.lbm_destroy(ctx)
+    fl = flags2 == wl.FLUID
+    assert np.abs(f.astype(np.float64)[:, fl] - fo[:, fl]).max() <= TOL_F
 
 
 # ---- TMA-staged AA odd step (lbm_set_tma_gather) --------------------------------------------------
