@@ -59,25 +59,27 @@ __device__ __forceinline__ size_t scratch_slot(const Params& p, int face, int q,
 }
 
 // Neighbour cell indices n + d, with d the sum of one per-axis delta per velocity component:
-// wrapped on PERIODIC axes, clamped onto the last layer on OPEN axes (the zero-gradient source of
-// a pull; the AA odd kernels never take a link across an OPEN face here -- such cells are special).
+// wrapped on PERIODIC axes; with `clamp` (the A-B pulls) clamped onto the last layer on OPEN axes,
+// the zero-gradient source of a pull.  The AA odd kernels wrap everywhere: a cell whose link
+// crosses an OPEN face is special there and takes no such link in the main kernel.  `clamp` is a
+// constant at every call site.
 __device__ __forceinline__ int edge_delta(int at, int n, int stride, bool open, int c) {
     if (c < 0) return at == 0 ? (open ? 0 : (n - 1) * stride) : -stride;
     return at == n - 1 ? (open ? 0 : -(n - 1) * stride) : stride;
 }
 struct Nbr {
     int dx[3], dy[3], dz[3];  // delta for c = -1, 0, +1 along each axis
-    __device__ __forceinline__ Nbr(const Params& p, int x, int y, int z) {
+    __device__ __forceinline__ Nbr(const Params& p, int x, int y, int z, bool clamp) {
         const int sx = 1, sy = p.nx, sz = p.nx * p.ny;
-        dx[0] = edge_delta(x, p.nx, sx, p.open[0], -1);
+        dx[0] = edge_delta(x, p.nx, sx, clamp && p.open[0], -1);
         dx[1] = 0;
-        dx[2] = edge_delta(x, p.nx, sx, p.open[0], 1);
-        dy[0] = edge_delta(y, p.ny, sy, p.open[1], -1);
+        dx[2] = edge_delta(x, p.nx, sx, clamp && p.open[0], 1);
+        dy[0] = edge_delta(y, p.ny, sy, clamp && p.open[1], -1);
         dy[1] = 0;
-        dy[2] = edge_delta(y, p.ny, sy, p.open[1], 1);
-        dz[0] = edge_delta(z, p.nz, sz, p.open[2], -1);
+        dy[2] = edge_delta(y, p.ny, sy, clamp && p.open[1], 1);
+        dz[0] = edge_delta(z, p.nz, sz, clamp && p.open[2], -1);
         dz[1] = 0;
-        dz[2] = edge_delta(z, p.nz, sz, p.open[2], 1);
+        dz[2] = edge_delta(z, p.nz, sz, clamp && p.open[2], 1);
     }
     // cell n + s c_q, s = +1 or -1
     template <int Q, int S>
@@ -326,7 +328,7 @@ __global__ void __launch_bounds__(256) k_aa_odd(Params p) {
         const uint32_t m = p.any_solid_link ? p.mask[c.n] : 0u;
         const uint8_t fl = p.flags[c.n];
         if ((fl & (TYPE_MASK | F_SPECIAL)) == T_FLUID) {
-            const Nbr nb(p, c.x, c.y, c.z);
+            const Nbr nb(p, c.x, c.y, c.z, false);
             float h[19];
             aa_odd_load<L, I>(p, nb, c.n, m, h);
             collide<BODY>(h, p);
@@ -336,7 +338,7 @@ __global__ void __launch_bounds__(256) k_aa_odd(Params p) {
             asm volatile("" : "+r"(ns), "+r"(ms) : "f"(h[0]), "f"(h[18]));
             aa_odd_store<L, I, FORCE>(p, nb, ns, ms, h, fx, fy, fz);
         } else if (p.any_inlet && (fl & TYPE_MASK) == T_INLET) {
-            const Nbr nb(p, c.x, c.y, c.z);
+            const Nbr nb(p, c.x, c.y, c.z, false);
             aa_odd_produce<L, I>(p, nb, c.n, c.x, c.y, c.z);
         }
     }
@@ -441,7 +443,7 @@ __global__ void __launch_bounds__(256, 6) k_ab(Params p) {
 #pragma unroll
                 for (int q = 0; q < 19; ++q) h[q] = ld<L>(p.pa[q], cell_off<L, I>(q, c.n));
             } else {
-                const Nbr nb(p, c.x, c.y, c.z);
+                const Nbr nb(p, c.x, c.y, c.z, true);
                 ab_load<L, I>(p, nb, c.n, m, h);
             }
             collide<BODY>(h, p);
@@ -489,7 +491,7 @@ __global__ void __launch_bounds__(256) k_ab_pull_staged(Params p) {
     const uint32_t m = (in && p.any_solid_link) ? p.mask[c.n] : 0u;
     const uint8_t fl = in ? p.flags[c.n] : (uint8_t)T_SOLID;
     if ((fl & (TYPE_MASK | F_SPECIAL)) == T_FLUID) {
-        const Nbr nb(p, c.x, c.y, c.z);
+        const Nbr nb(p, c.x, c.y, c.z, true);
         float h[19];
         ab_load<L, I>(p, nb, c.n, m, h);
         collide<BODY>(h, p);
@@ -534,7 +536,7 @@ __global__ void __launch_bounds__(256) k_stream(Params p) {
         return;
     }
     if (fl & F_SPECIAL) return;
-    const Nbr nb(p, c.x, c.y, c.z);
+    const Nbr nb(p, c.x, c.y, c.z, true);
     float h[19];
     ab_load<L, I>(p, nb, c.n, m, h);
 #pragma unroll

@@ -82,23 +82,24 @@ __device__ __forceinline__ bool grid_pair(const Params& p, PairCoord& c) {
 
 // Neighbour geometry of a pair: the y and z parts of n + s c_q are shared by both cells; along x,
 // a - 1 and b + 1 may leave the row, a + 1 = b and b - 1 = a never do.  Offsets wrap on PERIODIC
-// axes and clamp onto the last layer on OPEN axes (the zero-gradient source of the A-B pull; in
-// the AA odd step the cells whose links cross an OPEN face are special and store nothing here,
-// and an INLET producer drops such links).
+// axes; with `clamp` (the A-B pulls) they clamp onto the last layer on OPEN axes, the
+// zero-gradient source of a pull.  The AA odd kernels wrap everywhere: cells whose links cross an
+// OPEN face are special and store nothing there, and an INLET producer drops such links.  `clamp`
+// is a constant at every call site.
 struct NbrPair {
     int dy[3], dz[3];  // y and z deltas for c = -1, 0, +1
     int wa;            // (a - 1) - a along x
     int wb;            // (b + 1) - a along x
-    __device__ __forceinline__ NbrPair(const Params& p, int x, int y, int z) {
+    __device__ __forceinline__ NbrPair(const Params& p, int x, int y, int z, bool clamp) {
         const int sy = p.nx, sz = p.nx * p.ny;
-        dy[0] = edge_delta(y, p.ny, sy, p.open[1], -1);
+        dy[0] = edge_delta(y, p.ny, sy, clamp && p.open[1], -1);
         dy[1] = 0;
-        dy[2] = edge_delta(y, p.ny, sy, p.open[1], 1);
-        dz[0] = edge_delta(z, p.nz, sz, p.open[2], -1);
+        dy[2] = edge_delta(y, p.ny, sy, clamp && p.open[1], 1);
+        dz[0] = edge_delta(z, p.nz, sz, clamp && p.open[2], -1);
         dz[1] = 0;
-        dz[2] = edge_delta(z, p.nz, sz, p.open[2], 1);
-        wa = x == 0 ? (p.open[0] ? 0 : p.nx - 1) : -1;
-        wb = x + 2 == p.nx ? (p.open[0] ? 1 : 2 - p.nx) : 2;
+        dz[2] = edge_delta(z, p.nz, sz, clamp && p.open[2], 1);
+        wa = x == 0 ? (clamp && p.open[0] ? 0 : p.nx - 1) : -1;
+        wb = x + 2 == p.nx ? (clamp && p.open[0] ? 1 : 2 - p.nx) : 2;
     }
     // a + (0, s cy(Q), s cz(Q)), before the x part
     template <int Q, int S>
@@ -175,13 +176,32 @@ __device__ __forceinline__ PairFlags pair_flags(const Params& p, uint32_t n, boo
 // INLET cells as producers ("PortLBM", §3.1, last paragraph: the inlet imposes the equilibrium):
 // an INLET cell's post-collision state is the reservoir's f_eq(rho_in, u_in), stored by the step
 // kernels where a FLUID cell's would be, so that its neighbours read it through the ordinary
-// addressing.  In a pair, the INLET cell's lane of the collided array is replaced.
-__device__ __forceinline__ void inlet_lanes(const Params& p, bool ia, bool ib, float2 (&h)[19]) {
-#pragma unroll
-    for (int q = 0; q < 19; ++q) h[q] = make_float2(ia ? p.heq_in[q] : h[q].x, ib ? p.heq_in[q] : h[q].y);
-}
+// addressing.  The two-cell kernels do this in a tail pass after their main work, which re-reads
+// the pair's flag word and recomputes its coordinates: nothing about inlets is held in registers
+// through the collision and the scatter (the main path may have stored a value for the inlet cell
+// of a mixed pair first; the tail pass, in the same thread, overwrites it).
 __device__ __forceinline__ bool is_inlet(const Params& p, bool in, uint8_t f) {
     return in && p.any_inlet && (f & TYPE_MASK) == T_INLET;
+}
+__device__ __forceinline__ bool pair_inlets(const Params& p, PairCoord& c, bool& ia, bool& ib) {
+    if (!p.any_inlet || !grid_pair(p, c)) return false;
+    const uint16_t fl = *reinterpret_cast<const uint16_t*>(p.flags + c.n);
+    ia = (fl & TYPE_MASK) == T_INLET;
+    ib = ((fl >> 8) & TYPE_MASK) == T_INLET;
+    return ia || ib;
+}
+// f_eq - w of the reservoir into the pair's slots of plane (OPP ? opposite(q) : q) of buf (the
+// even AA step: opposite(q); the A-B steps: q of the destination)
+template <int L, bool OPP>
+__device__ __forceinline__ void pair_inlet_store(const Params& p, void* buf, uint32_t n, bool ia,
+                                                 bool ib) {
+    Elem<L>* B = static_cast<Elem<L>*>(buf);
+#pragma unroll
+    for (int q = 0; q < 19; ++q) {
+        Elem<L>* e = B + (p.plane32[OPP ? opp(q) : q] + n);
+        if (ia) st1<L>(e, p.heq_in[q]);
+        if (ib) st1<L>(e + 1, p.heq_in[q]);
+    }
 }
 
 // Momentum exchange of a pair, packed: the sum over the links q whose bit is set in the cell's
@@ -321,15 +341,16 @@ __device__ __forceinline__ void own_store(const Params& p, Elem<L>* base, uint32
 // Every FLUID cell; the pair's slots are read and written as aligned words.
 // Resident blocks per SM: 4 for fp32 storage (64 registers), 6 for the packed half-precision form
 // (40 registers); the fp16 kernel on fp32 arrays with 66 registers fell to 3 blocks and lost 9%.
-template <int L, bool FORCE, bool BODY>
+// INLETS: the kernel carries the INLET tail pass (off only for a domain without inlets, in the
+// half-precision instantiations: an issue-bound kernel pays for even a never-taken epilogue).
+template <int L, bool FORCE, bool BODY, bool INLETS>
 __global__ void __launch_bounds__(256, pair_min_blocks<L>(kPackedHalfEven)) k_aa_even2(Params p) {
     PairCoord c;
     float fx = 0.f, fy = 0.f, fz = 0.f;
     if (grid_pair(p, c)) {
         const PairFlags f = pair_flags(p, c.n, false);
         const bool act_a = (f.fa & TYPE_MASK) == T_FLUID, act_b = (f.fb & TYPE_MASK) == T_FLUID;
-        const bool inl_a = is_inlet(p, true, f.fa), inl_b = is_inlet(p, true, f.fb);
-        if ((act_a || act_b) && !(inl_a || inl_b) && L == LAYOUT_STREAM_FP16 && kPackedHalfEven) {
+        if ((act_a || act_b) && L == LAYOUT_STREAM_FP16 && kPackedHalfEven) {
             // half-precision storage: the stored pairs stay packed; each population is relaxed
             // where it is stored
             __half* A = static_cast<__half*>(p.A);
@@ -355,13 +376,12 @@ __global__ void __launch_bounds__(256, pair_min_blocks<L>(kPackedHalfEven)) k_aa
             own_store<L, true, FORCE>(p, reinterpret_cast<Elem<L>*>(A), ns, RelaxSrc<BODY>{m, hh, p},
                                       ma, mb, mov_a, mov_b, c.x, c.y, c.z, pf, fx, fy, fz);
             if (FORCE) pf.into(fx, fy, fz);
-        } else if (act_a || act_b || inl_a || inl_b) {
+        } else if (act_a || act_b) {
             Elem<L>* A = static_cast<Elem<L>*>(p.A);
             float2 h[19];
 #pragma unroll
             for (int q = 0; q < 19; ++q) h[q] = ld2<L>(A + (p.plane32[q] + c.n));
             collide2<BODY>(h, p);
-            if (inl_a || inl_b) inlet_lanes(p, inl_a, inl_b, h);
             uint32_t ns = c.n;
             asm volatile("" : "+r"(ns) : "f"(h[0].x), "f"(h[18].y));
 #pragma unroll
@@ -382,6 +402,11 @@ __global__ void __launch_bounds__(256, pair_min_blocks<L>(kPackedHalfEven)) k_aa
                 }
             }
         }
+    }
+    if constexpr (INLETS) {
+        PairCoord ci;
+        bool ia = false, ib = false;
+        if (pair_inlets(p, ci, ia, ib)) pair_inlet_store<L, true>(p, p.A, ci.n, ia, ib);
     }
     if (FORCE) warp_force(fx, fy, fz, p.partial);
 }
@@ -445,14 +470,12 @@ __global__ void __launch_bounds__(256, 4) k_aa_even2_bundle(Params p) {
     if (grid_pair(p, c)) {
         const PairFlags f = pair_flags(p, c.n, false);
         const bool act_a = (f.fa & TYPE_MASK) == T_FLUID, act_b = (f.fb & TYPE_MASK) == T_FLUID;
-        const bool inl_a = is_inlet(p, true, f.fa), inl_b = is_inlet(p, true, f.fb);
-        if (act_a || act_b || inl_a || inl_b) {
+        if (act_a || act_b) {
             float* A = static_cast<float*>(p.A);
             const uint32_t N = (uint32_t)p.N;
             float2 h[19];
             bundle_gather2(A, N, c.n, h);
             collide2<BODY>(h, p);
-            if (inl_a || inl_b) inlet_lanes(p, inl_a, inl_b, h);
             uint32_t ns = c.n;
             asm volatile("" : "+r"(ns) : "f"(h[0].x), "f"(h[18].y));
             bundle_scatter2_opp(A, N, ns, h);
@@ -470,6 +493,17 @@ __global__ void __launch_bounds__(256, 4) k_aa_even2_bundle(Params p) {
                             moving_forces(p, PairLane<1>{h}, c.x + 1, c.y, c.z, fx, fy, fz);
                     }
                 }
+            }
+        }
+    }
+    {
+        PairCoord ci;
+        bool ia = false, ib = false;
+        if (pair_inlets(p, ci, ia, ib)) {
+#pragma unroll
+            for (int q = 0; q < 19; ++q) {
+                if (ia) st<LAYOUT_BUNDLE>(p.A, idx<LAYOUT_BUNDLE, uint32_t>(opp(q), ci.n, (uint32_t)p.N), p.heq_in[q]);
+                if (ib) st<LAYOUT_BUNDLE>(p.A, idx<LAYOUT_BUNDLE, uint32_t>(opp(q), ci.n + 1, (uint32_t)p.N), p.heq_in[q]);
             }
         }
     }
@@ -522,7 +556,7 @@ __device__ __forceinline__ void odd2_produce(const Params& p, const NbrPair& nb,
     if constexpr (Q < 18) odd2_produce<L, Q + 1>(p, nb, n, x, y, z, ia, ib);
 }
 
-template <int L, bool FORCE, bool BODY>
+template <int L, bool FORCE, bool BODY, bool INLETS>
 __global__ void __launch_bounds__(256, pair_min_blocks<L>(kPackedHalfOdd)) k_aa_odd2(Params p) {
     PairCoord c;
     float fx = 0.f, fy = 0.f, fz = 0.f;
@@ -542,7 +576,7 @@ __global__ void __launch_bounds__(256, pair_min_blocks<L>(kPackedHalfOdd)) k_aa_
         // the scatter
         __half2 hh[19];
         {
-            const NbrPair nb(p, c.x, c.y, c.z);
+            const NbrPair nb(p, c.x, c.y, c.z, false);
             if (wall) pair_gather_h<true, true>(p, nb, c.n, f.ma, f.mb, hh);
             else pair_gather_h<true, false>(p, nb, c.n, f.ma, f.mb, hh);
         }
@@ -551,7 +585,7 @@ __global__ void __launch_bounds__(256, pair_min_blocks<L>(kPackedHalfOdd)) k_aa_
         int xs = c.x, ys = c.y, zs = c.z;
         asm volatile("" : "+r"(ns), "+r"(mas), "+r"(mbs), "+r"(xs), "+r"(ys), "+r"(zs)
                      : "f"(m.rho.x), "f"(m.rho.y));
-        const NbrPair nb(p, xs, ys, zs);
+        const NbrPair nb(p, xs, ys, zs, false);
         const RelaxSrc<BODY> src{m, hh, p};
         PairForce pf;
         if (wall) {
@@ -565,7 +599,7 @@ __global__ void __launch_bounds__(256, pair_min_blocks<L>(kPackedHalfOdd)) k_aa_
     } else if (act_a || act_b) {
         float2 h[19];
         {
-            const NbrPair nb(p, c.x, c.y, c.z);
+            const NbrPair nb(p, c.x, c.y, c.z, false);
             if (wall) pair_gather<L, true, true>(p, nb, c.n, f.ma, f.mb, h);
             else pair_gather<L, true, false>(p, nb, c.n, f.ma, f.mb, h);
         }
@@ -575,7 +609,7 @@ __global__ void __launch_bounds__(256, pair_min_blocks<L>(kPackedHalfOdd)) k_aa_
         int xs = c.x, ys = c.y, zs = c.z;
         asm volatile("" : "+r"(ns), "+r"(mas), "+r"(mbs), "+r"(xs), "+r"(ys), "+r"(zs)
                      : "f"(h[0].x), "f"(h[18].y));
-        const NbrPair nb(p, xs, ys, zs);
+        const NbrPair nb(p, xs, ys, zs, false);
         const ArraySrc src{h};
         PairForce pf;
         if (wall) {
@@ -587,10 +621,13 @@ __global__ void __launch_bounds__(256, pair_min_blocks<L>(kPackedHalfOdd)) k_aa_
             else odd2_scatter<L, false, false, FORCE>(p, nb, ns, mas, mbs, act_a, act_b, src, pf);
         }
     }
-    const bool inl_a = is_inlet(p, in, f.fa), inl_b = is_inlet(p, in, f.fb);
-    if (inl_a || inl_b) {
-        const NbrPair nb(p, c.x, c.y, c.z);
-        odd2_produce<L>(p, nb, c.n, c.x, c.y, c.z, inl_a, inl_b);
+    if constexpr (INLETS) {
+        PairCoord ci;
+        bool ia = false, ib = false;
+        if (pair_inlets(p, ci, ia, ib)) {
+            const NbrPair nb(p, ci.x, ci.y, ci.z, false);
+            odd2_produce<L>(p, nb, ci.n, ci.x, ci.y, ci.z, ia, ib);
+        }
     }
     if (FORCE) warp_force(fx, fy, fz, p.partial);
 }
@@ -602,7 +639,7 @@ __global__ void __launch_bounds__(256, pair_min_blocks<L>(kPackedHalfOdd)) k_aa_
 // every sector of B is then written whole.  Leaving those slots out, so that the boundary kernel
 // could run at the same time, cost 8-13% on the sphere workload (partly written sectors filled
 // from DRAM) for a 1-3% gain from the overlap.
-template <int L, bool FORCE, bool BODY, bool FROM_NATURAL>
+template <int L, bool FORCE, bool BODY, bool FROM_NATURAL, bool INLETS>
 __global__ void __launch_bounds__(256, 4) k_ab2(Params p) {
     PairCoord c;
     float fx = 0.f, fy = 0.f, fz = 0.f;
@@ -613,7 +650,6 @@ __global__ void __launch_bounds__(256, 4) k_ab2(Params p) {
     const bool act_a = in && (f.fa & want) == T_FLUID;
     const bool act_b = in && (f.fb & want) == T_FLUID;
     const bool wall = !FROM_NATURAL && __any_sync(0xffffffffu, (act_a || act_b) && (f.ma | f.mb) != 0u);
-    const bool inl_a = is_inlet(p, in, f.fa), inl_b = is_inlet(p, in, f.fb);
     Elem<L>* B = static_cast<Elem<L>*>(p.B);
     if (act_a || act_b) {
         float2 h[19];
@@ -622,12 +658,11 @@ __global__ void __launch_bounds__(256, 4) k_ab2(Params p) {
 #pragma unroll
             for (int q = 0; q < 19; ++q) h[q] = ld2<L>(A + (p.plane32[q] + c.n));
         } else {
-            const NbrPair nb(p, c.x, c.y, c.z);
+            const NbrPair nb(p, c.x, c.y, c.z, true);
             if (wall) pair_gather<L, false, true>(p, nb, c.n, f.ma, f.mb, h);
             else pair_gather<L, false, false>(p, nb, c.n, f.ma, f.mb, h);
         }
         collide2<BODY>(h, p);
-        if (inl_a || inl_b) inlet_lanes(p, inl_a, inl_b, h);
         uint32_t ns = c.n;
         asm volatile("" : "+r"(ns) : "f"(h[0].x), "f"(h[18].y));
 #pragma unroll
@@ -643,13 +678,17 @@ __global__ void __launch_bounds__(256, 4) k_ab2(Params p) {
                 if (act_b && (f.fb & F_SPECIAL)) moving_forces(p, PairLane<1>{h}, c.x + 1, c.y, c.z, fx, fy, fz);
             }
         }
-    } else if (in && (p.B != p.A || inl_a || inl_b)) {
-        // no working cell: an INLET cell stores the reservoir's f_eq(rho_in, u_in); SOLID /
-        // MOVING_WALL slots are never read and special cells' are rewritten by the boundary
-        // kernel: zeros keep every sector of B fully written
+    } else if (in && p.B != p.A) {
+        // no working cell: SOLID / MOVING_WALL slots are never read, special cells' are rewritten
+        // by the boundary kernel and INLET cells' by the tail pass: zeros keep every sector of B
+        // fully written
 #pragma unroll
-        for (int q = 0; q < 19; ++q)
-            st2<L>(B + (p.plane32[q] + c.n), make_float2(inl_a ? p.heq_in[q] : 0.f, inl_b ? p.heq_in[q] : 0.f));
+        for (int q = 0; q < 19; ++q) st2<L>(B + (p.plane32[q] + c.n), make_float2(0.f, 0.f));
+    }
+    if constexpr (INLETS) {
+        PairCoord ci;
+        bool ia = false, ib = false;
+        if (pair_inlets(p, ci, ia, ib)) pair_inlet_store<L, false>(p, p.B, ci.n, ia, ib);
     }
     if (FORCE) warp_force(fx, fy, fz, p.partial);
 }

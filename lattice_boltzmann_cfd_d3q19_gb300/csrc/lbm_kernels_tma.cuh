@@ -231,7 +231,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) k_aa_odd_tma(Params p) {
             float2 h[19];
             tma_gather<L>(st, j, x, p.nx, ma, mb, p.any_solid_link != 0, h);
             collide2<BODY>(h, p);
-            const NbrPair nb(p, x, r % p.ny, r / p.ny);
+            const NbrPair nb(p, x, r % p.ny, r / p.ny, false);
             const ArraySrc src{h};
             PairForce pf;
             if (wall) {
@@ -246,7 +246,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) k_aa_odd_tma(Params p) {
         // INLET cells of the tile: producers, as in the register kernel
         const bool inl_a = is_inlet(p, in, fa), inl_b = is_inlet(p, in, fb);
         if (inl_a || inl_b) {
-            const NbrPair nb(p, x, r % p.ny, r / p.ny);
+            const NbrPair nb(p, x, r % p.ny, r / p.ny, false);
             odd2_produce<L>(p, nb, n, x, r % p.ny, r / p.ny, inl_a, inl_b);
         }
         // every thread is done with stage s before it is refilled
