@@ -22,10 +22,16 @@ if not torch.cuda.is_available():
 TAU, G, INLET = 0.62, (2e-5, -1e-5, 1e-5), (1.0, 0.04, 0.0, 0.0)
 
 
-def global_problem(nx, ny, nz, seed):
+WALL = (0.03, -0.01, 0.02)
+
+
+def global_problem(nx, ny, nz, seed, moving):
+    """Random solids (a third of them moving walls when `moving`), an inlet layer on x = 0."""
     r = np.random.default_rng(seed)
     N = nx * ny * nz
     flags = (r.uniform(size=N) < 0.15).astype(np.uint8)
+    if moving:
+        flags[(flags == wl.SOLID) & (r.uniform(size=N) < 0.33)] = wl.MOVING_WALL
     x, _, _ = wl.coords(nx, ny, nz)
     flags[x == 0] = wl.INLET
     f0 = random_state(N, seed + 1).astype(np.float32)
@@ -39,15 +45,19 @@ def make_ctx(nx, ny, nz, layout, flags, pairs):
     B.lbm_set_faces(ctx, B.OPEN, B.PERIODIC, B.PERIODIC)
     B.lbm_set_inlet(ctx, *INLET)
     B.lbm_set_body_force(ctx, *G)
+    B.lbm_set_wall_velocity(ctx, *WALL)
     return ctx
 
 
+@pytest.mark.parametrize("moving", [False, True])
 @pytest.mark.parametrize("pairs", [True, False])
 @pytest.mark.parametrize("layout", ["stream", "collision", "stream_fp16"])
 @pytest.mark.parametrize("nz, world", [(12, 2), (13, 3)])
-def test_slabs_equal_the_unsliced_context(nz, world, layout, pairs):
+def test_slabs_equal_the_unsliced_context(nz, world, layout, pairs, moving):
+    """With moving walls the slabs also have special cells (boundary kernel), some of them next
+    to a ghost plane."""
     nx, ny, steps = 10, 8, 6
-    flags, f0 = global_problem(nx, ny, nz, 70 + nz)
+    flags, f0 = global_problem(nx, ny, nz, 70 + nz, moving)
     ref = make_ctx(nx, ny, nz, layout, flags, pairs)
     try:
         B.lbm_set_populations(ref, torch.from_numpy(f0.reshape(-1).copy()).cuda())
