@@ -359,6 +359,84 @@ def variant(B, torch, n, scheme, steps=10, warmup=3, cavity=False, fp16=False, l
             "kernels": kernels}
 
 
+def slab_variant(B, torch, n, world, steps=10, warmup=3):
+    """The porous n^3 medium (A-B scheme) as `world` z slabs of one context each, all on this GPU:
+    each slab holds its owned planes and two ghost planes, and the host moves the halo buffers
+    between the slabs with device copies.  Timed three ways, one LBM step per step: the unsliced
+    context (lbm_step), the slabs stepped then exchanged (lbm_step + lbm_halo_pack, copies,
+    lbm_halo_unpack), and the slabs with the exchange overlapped by the interior planes
+    (lbm_slab_step_begin, copies, lbm_slab_step_end).  On one GPU nothing crosses a link, so this
+    measures what the decomposition itself costs; MLUPS count the owned cells."""
+    from lattice_boltzmann_cfd_d3q19_gb300 import slab as S
+    flags = porous_flags(n)
+    N = n ** 3
+    stream = torch.cuda.current_stream()
+
+    def setup(ctx, nz, fl):
+        B.lbm_set_stream(ctx, stream.cuda_stream)
+        B.lbm_set_flags(ctx, fl)
+        B.lbm_set_body_force(ctx, 1e-6, 0.0, 0.0)
+        M = n * n * nz
+        B.lbm_set_equilibrium(ctx, torch.ones(M, dtype=torch.float32, device="cuda"),
+                              torch.zeros(3 * M, dtype=torch.float32, device="cuda"))
+
+    def timed(step):
+        for _ in range(warmup):
+            step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+
+    out = {"slabs": world, "halo_bytes_per_slab_and_step": 2 * 5 * n * n * 4}
+    ctx = B.lbm_create(n, n, n, 0.7, B.LAYOUT_STREAM, B.STREAMING_AB)
+    try:
+        setup(ctx, n, flags)
+        ms = timed(lambda: B.lbm_step(ctx, 1))
+    finally:
+        B.lbm_destroy(ctx)
+    out["unsliced"] = {"ms_per_lbm_step": round(ms, 4), "mlups": round(N / ms / 1e3, 1)}
+    slabs = [S.slab_of(n, r, world) for r in range(world)]
+    ctxs = []
+    try:
+        for sl in slabs:
+            c = B.lbm_create(n, n, sl.local_nz, 0.7, B.LAYOUT_STREAM, B.STREAMING_AB)
+            ctxs.append(c)
+            B.lbm_set_ghost_planes(c, True)
+            setup(c, sl.local_nz, S.local_slice(flags, sl, n, n))
+        eng = [S.LibraryEngine(c) for c in ctxs]
+        recv = [(e.halo_like(), e.halo_like()) for e in eng]  # (from below, from above)
+
+        def swap(packed):
+            for r, sl in enumerate(slabs):
+                recv[r][0].copy_(packed[sl.below][1])
+                recv[r][1].copy_(packed[sl.above][0])
+
+        def serial():
+            for e in eng:
+                e.step1()
+            swap([e.pack() for e in eng])
+            for e, (fb, fa) in zip(eng, recv):
+                e.unpack(fb, fa)
+
+        def overlapped():
+            swap([e.begin() for e in eng])
+            for e, (fb, fa) in zip(eng, recv):
+                e.end(fb, fa)
+
+        for name, fn in (("slabs_serial", serial), ("slabs_overlapped", overlapped)):
+            ms = timed(fn)
+            out[name] = {"ms_per_lbm_step": round(ms, 4), "mlups": round(N / ms / 1e3, 1)}
+    finally:
+        for c in ctxs:
+            B.lbm_destroy(c)
+    return out
+
+
 def cpu_description():
     """Host CPU for the CPU baseline: architecture, model (x86 'model name', or the Arm
     implementer/part codes) and logical CPU count."""
@@ -427,7 +505,14 @@ def variant_specs():
     for s in ("AA", "AB"):
         specs[f"{s}_512^3_periodic_fp16_storage"] = (512, s, {"fp16": True})
     specs["AA_512^3_porous_fp16_storage"] = (512, "AA", {"fp16": True, "porous": True})
+    specs["AB_512^3_porous_2_z_slabs_one_gpu"] = (512, "AB", {"slabs": 2})
     return specs
+
+
+def run_variant(B, torch, m, s, steps, warmup, **kw):
+    if "slabs" in kw:
+        return slab_variant(B, torch, m, kw["slabs"], steps=steps, warmup=warmup)
+    return variant(B, torch, m, s, steps=steps, warmup=warmup, **kw)
 
 
 def run_variants_only(args):
@@ -443,7 +528,7 @@ def run_variants_only(args):
     for name in args.variant:
         m, s, kw = specs[name]
         m = args.variant_size or m
-        res = variant(B, torch, m, s, steps=args.steps, warmup=args.warmup, **kw)
+        res = run_variant(B, torch, m, s, args.steps, args.warmup, **kw)
         print(json.dumps({"variant": name, "edge": m, **res}), flush=True)
 
 
@@ -554,7 +639,7 @@ def run_ours(args):
     }
     if not args.no_variants:
         log("[bench] variants")
-        out["variants"] = {name: variant(B, torch, m, s, **kw)
+        out["variants"] = {name: run_variant(B, torch, m, s, 10, 3, **kw)
                            for name, (m, s, kw) in variant_specs().items()}
     if not args.no_e2e:
         log("[bench] e2e")

@@ -318,6 +318,34 @@ int lbm_halo_pack(lbm_ctx* ctx, void* lo, void* hi);
  * reads.  Same requirements and errors as lbm_halo_pack; asynchronous. */
 int lbm_halo_unpack(lbm_ctx* ctx, const void* from_below, const void* from_above);
 
+/* One step of a slab with its halo exchange overlapped by the interior planes.  [Disaggregated],
+ * section "Disaggregation on a Dense Domain" (Overlapping Computation and Communication, OCC) and
+ * "Improving LBM Scalability", "Reference Implementation": a stencil step is split into the voxels
+ * that only need local data and the voxels that need the neighbours' data, so that the halo
+ * travels while the first kind is computed.  For a pull step the order is: the two boundary
+ * planes, whose results the neighbours need, then the interior while their halo travels.  A
+ * step = lbm_slab_step_begin, the exchange of lo / hi by the caller, then lbm_slab_step_end.
+ * Results are bit for bit those of lbm_step(ctx, 1) + lbm_halo_pack + exchange + lbm_halo_unpack.
+ * The force is summed in another order, so it agrees to rounding only.
+ *
+ * lbm_slab_step_begin: on the context stream, steps the owned boundary planes z = 1 and
+ * z = nz - 2 and their special cells, then packs their outgoing populations into lo and hi (as
+ * lbm_halo_pack).  It then launches the interior planes 2 .. nz - 3 and their special cells on the
+ * context's side stream, which waits for the pack.  A transfer the caller enqueues after this call,
+ * ordered after the context stream, therefore runs beside the interior.  The ghost planes are not
+ * stepped.  lo and hi are device memory of the current device (LBM_EINVAL otherwise).  LBM_ESTATE
+ * without ghost planes, or with a slab step already open.  Asynchronous. */
+int lbm_slab_step_begin(lbm_ctx* ctx, void* lo, void* hi);
+
+/* lbm_slab_step_end: the context stream waits for the interior planes, the step is completed (the
+ * momentum exchange of the owned cells, the buffer swap, the step count), and from_below /
+ * from_above are unpacked into the ghost planes (as lbm_halo_unpack).  The caller orders the
+ * receipt of the buffers before this call on the context stream (a communication library's wait
+ * on the stream).  LBM_ESTATE when no slab step is open.  Between begin and end, every other call
+ * on the context except lbm_halo_elements, lbm_halo_element_bytes, lbm_step_count,
+ * lbm_kernel_launches and lbm_destroy returns LBM_ESTATE.  Asynchronous. */
+int lbm_slab_step_end(lbm_ctx* ctx, const void* from_below, const void* from_above);
+
 /* Momentum-exchange force of ONE collision of a caller-held state, without allocating any memory.
  * The source papers and pages describe no counterpart to this entry point.  It exists for callers
  * that cannot call cudaMalloc: plug-ins whose host application owns all device memory through its

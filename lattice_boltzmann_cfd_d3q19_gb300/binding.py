@@ -57,6 +57,8 @@ SIGNATURES = {
     "lbm_halo_element_bytes": (_I, [_P]),
     "lbm_halo_pack": (_I, [_P, _P, _P]),
     "lbm_halo_unpack": (_I, [_P, _P, _P]),
+    "lbm_slab_step_begin": (_I, [_P, _P, _P]),
+    "lbm_slab_step_end": (_I, [_P, _P, _P]),
 }
 
 
@@ -300,6 +302,16 @@ def lbm_halo_pack(ctx: int, lo, hi) -> None:
 def lbm_halo_unpack(ctx: int, from_below, from_above) -> None:
     pb, pa = _halo_ptr(ctx, from_below), _halo_ptr(ctx, from_above)
     _check(load().lbm_halo_unpack(ctx, pb, pa))
+
+
+def lbm_slab_step_begin(ctx: int, lo, hi) -> None:
+    pl, ph = _halo_ptr(ctx, lo), _halo_ptr(ctx, hi)
+    _check(load().lbm_slab_step_begin(ctx, pl, ph))
+
+
+def lbm_slab_step_end(ctx: int, from_below, from_above) -> None:
+    pb, pa = _halo_ptr(ctx, from_below), _halo_ptr(ctx, from_above)
+    _check(load().lbm_slab_step_end(ctx, pb, pa))
 
 
 def lbm_force_momentum_exchange_noalloc(f, flags, nx: int, ny: int, nz: int, faces=(0, 0, 0),

@@ -108,6 +108,10 @@ struct lbm_ctx {
     uint32_t* mask = nullptr;
     uint32_t* special = nullptr;  // sorted indices of the special FLUID cells
     uint32_t n_special = 0;
+    // with ghost planes: the special cells of plane 1 are special[0, sp_lo_end), those of plane
+    // nz - 2 special[sp_hi_begin, n_special) (the list is sorted, ghost cells are never special)
+    uint32_t sp_lo_end = 0, sp_hi_begin = 0;
+    bool split = false;           // a slab step is open (lbm_slab_step_begin without its end)
     uint32_t* count_dev = nullptr;  // counters: special cells, SOLID links, MOVING_WALL links, INLET cells
     int any_solid_link = 0;
     int any_moving = 0;
@@ -205,6 +209,9 @@ struct lbm_ctx {
         p.partial = partial;
         p.fault = fault_dev;
         p.zrev = 0;
+        p.zbase = 0;
+        p.zstep = 1;
+        p.part_main = 0;
         p.extra_tx = extra_tx;
         p.part_special = main_blocks() * kWarpsPerBlock;
         p.nx = n[0];
@@ -457,6 +464,14 @@ int classify(lbm_ctx* c) {
     cudaFree(c->special);
     c->special = dev_list;
     c->n_special = count;
+    {
+        const uint32_t area = (uint32_t)c->n[0] * (uint32_t)c->n[1];
+        const uint32_t nz = (uint32_t)c->n[2];
+        c->sp_lo_end = (uint32_t)(std::lower_bound(list.begin(), list.end(), 2 * area) - list.begin());
+        c->sp_hi_begin = nz >= 3 ? (uint32_t)(std::lower_bound(list.begin(), list.end(), (nz - 2) * area) -
+                                             list.begin())
+                                 : count;
+    }
     c->any_solid_link = counts[1] > 0;
     c->any_moving = counts[2] > 0;
     c->any_inlet = counts[3] > 0;
@@ -480,6 +495,10 @@ int launch_kind(lbm_ctx* c, int kind, const Params& p_in, bool force, int main_k
                 cudaStream_t boundary_stream = nullptr) {
     Params p = p_in;
     p.zrev = z_reversed(c, kind);
+    if (p.zrev) {
+        p.zbase = c->n[2] - 1;
+        p.zstep = -1;
+    }
     if (kind == K_BOUNDARY && c->n_special == 0) return LBM_OK;
     cudaEvent_t e0 = nullptr, e1 = nullptr;
     if (c->profiling) {
@@ -672,6 +691,13 @@ int graph_steps(lbm_ctx* c, int len, bool force) {
 
 extern "C" {
 
+// every call that reads or changes the state, the buffers, the stream or the launch geometry
+// waits until an open slab step is ended
+static int split_open(const char* what) {
+    return fail(LBM_ESTATE, "%s: a slab step is open (lbm_slab_step_begin without lbm_slab_step_end)",
+                what);
+}
+
 const char* lbm_last_error(void) { return g_err.c_str(); }
 
 lbm_ctx* lbm_create(int nx, int ny, int nz, float tau, int layout, int streaming) {
@@ -803,6 +829,7 @@ lbm_ctx* lbm_create(int nx, int ny, int nz, float tau, int layout, int streaming
 
 int lbm_set_stream(lbm_ctx* c, void* cuda_stream) {
     if (!c) return fail(LBM_EINVAL, "lbm_set_stream: NULL context");
+    if (c->split) return split_open("lbm_set_stream");
     if (int rc = sync(c, "lbm_set_stream")) return rc;
     c->stream = (cudaStream_t)cuda_stream;
     return LBM_OK;
@@ -810,6 +837,7 @@ int lbm_set_stream(lbm_ctx* c, void* cuda_stream) {
 
 int lbm_set_flags(lbm_ctx* c, const uint8_t* flags) {
     if (!c || !flags) return fail(LBM_EINVAL, "lbm_set_flags: NULL argument");
+    if (c->split) return split_open("lbm_set_flags");
     uint8_t* tmp = nullptr;
     LBM_CUDA(cudaMalloc(&tmp, c->N), "lbm_set_flags: temporary");
     int rc = LBM_OK;
@@ -838,6 +866,7 @@ int lbm_set_flags(lbm_ctx* c, const uint8_t* flags) {
 
 int lbm_set_faces(lbm_ctx* c, int fx, int fy, int fz) {
     if (!c) return fail(LBM_EINVAL, "lbm_set_faces: NULL context");
+    if (c->split) return split_open("lbm_set_faces");
     if (c->ghost && fz != LBM_PERIODIC)
         return fail(LBM_EINVAL, "lbm_set_faces: a context with ghost planes keeps its z faces PERIODIC");
     const int f[3] = {fx, fy, fz};
@@ -875,6 +904,7 @@ int lbm_set_faces(lbm_ctx* c, int fx, int fy, int fz) {
 
 int lbm_set_inlet(lbm_ctx* c, float rho, float ux, float uy, float uz) {
     if (!c) return fail(LBM_EINVAL, "lbm_set_inlet: NULL context");
+    if (c->split) return split_open("lbm_set_inlet");
     if (!std::isfinite(rho) || !(rho > 0.f) || !std::isfinite(ux) || !std::isfinite(uy) ||
         !std::isfinite(uz))
         return fail(LBM_EINVAL, "lbm_set_inlet: need finite rho > 0 and finite u");
@@ -890,6 +920,7 @@ int lbm_set_inlet(lbm_ctx* c, float rho, float ux, float uy, float uz) {
 
 int lbm_set_wall_velocity(lbm_ctx* c, float ux, float uy, float uz) {
     if (!c) return fail(LBM_EINVAL, "lbm_set_wall_velocity: NULL context");
+    if (c->split) return split_open("lbm_set_wall_velocity");
     if (!std::isfinite(ux) || !std::isfinite(uy) || !std::isfinite(uz))
         return fail(LBM_EINVAL, "lbm_set_wall_velocity: u_w must be finite");
     c->drop_graphs();
@@ -901,6 +932,7 @@ int lbm_set_wall_velocity(lbm_ctx* c, float ux, float uy, float uz) {
 
 int lbm_set_body_force(lbm_ctx* c, float gx, float gy, float gz) {
     if (!c) return fail(LBM_EINVAL, "lbm_set_body_force: NULL context");
+    if (c->split) return split_open("lbm_set_body_force");
     if (!std::isfinite(gx) || !std::isfinite(gy) || !std::isfinite(gz))
         return fail(LBM_EINVAL, "lbm_set_body_force: g must be finite");
     c->drop_graphs();
@@ -918,6 +950,7 @@ static void reset_state(lbm_ctx* c) {
 
 int lbm_set_populations(lbm_ctx* c, const float* f) {
     if (!c || !f) return fail(LBM_EINVAL, "lbm_set_populations: NULL argument");
+    if (c->split) return split_open("lbm_set_populations");
     void* dst = c->state_buffer();
     const Params p = c->params(dst, dst);
     const size_t total = 19 * c->N;
@@ -945,6 +978,7 @@ int lbm_set_populations(lbm_ctx* c, const float* f) {
 
 int lbm_set_equilibrium(lbm_ctx* c, const float* rho, const float* u) {
     if (!c || !rho || !u) return fail(LBM_EINVAL, "lbm_set_equilibrium: NULL argument");
+    if (c->split) return split_open("lbm_set_equilibrium");
     void* dst = c->state_buffer();
     const Params p = c->params(dst, dst);
     const size_t N = c->N;
@@ -978,6 +1012,7 @@ int lbm_set_equilibrium(lbm_ctx* c, const float* rho, const float* u) {
 
 int lbm_get_populations(lbm_ctx* c, float* f) {
     if (!c || !f) return fail(LBM_EINVAL, "lbm_get_populations: NULL argument");
+    if (c->split) return split_open("lbm_get_populations");
     void* src = c->state_buffer();
     const Params p = c->params(src, src);
     const size_t total = 19 * c->N;
@@ -1005,6 +1040,7 @@ int lbm_get_populations(lbm_ctx* c, float* f) {
 
 int lbm_step(lbm_ctx* c, int n) {
     if (!c) return fail(LBM_EINVAL, "lbm_step: NULL context");
+    if (c->split) return split_open("lbm_step");
     if (n < 0) return fail(LBM_EINVAL, "lbm_step: n = %d < 0", n);
     if (c->ghost && n > 1)
         return fail(LBM_EINVAL, "lbm_step: with ghost planes, step once and exchange the halos "
@@ -1028,6 +1064,7 @@ int lbm_step(lbm_ctx* c, int n) {
 
 int lbm_macroscopic(lbm_ctx* c, float* rho, float* u) {
     if (!c || !rho || !u) return fail(LBM_EINVAL, "lbm_macroscopic: NULL argument");
+    if (c->split) return split_open("lbm_macroscopic");
     void* src = c->state_buffer();
     const Params p = c->params(src, src);
     const size_t N = c->N;
@@ -1060,6 +1097,7 @@ int lbm_macroscopic(lbm_ctx* c, float* rho, float* u) {
 
 int lbm_force_momentum_exchange(lbm_ctx* c, double F[3]) {
     if (!c || !F) return fail(LBM_EINVAL, "lbm_force_momentum_exchange: NULL argument");
+    if (c->split) return split_open("lbm_force_momentum_exchange");
     if (!c->force_valid)
         return fail(LBM_ESTATE, "lbm_force_momentum_exchange: no step since the state was loaded");
     LBM_CUDA(cudaMemcpyAsync(c->force_host, c->force_dev, 3 * sizeof(double), cudaMemcpyDeviceToHost,
@@ -1071,6 +1109,7 @@ int lbm_force_momentum_exchange(lbm_ctx* c, double F[3]) {
 
 int lbm_check_finite(lbm_ctx* c) {
     if (!c) return fail(LBM_EINVAL, "lbm_check_finite: NULL context");
+    if (c->split) return split_open("lbm_check_finite");
     void* src = c->state_buffer();
     LBM_CUDA(cudaMemsetAsync(c->err_dev, 0, sizeof(int), c->stream), "lbm_check_finite");
     LBM_CUDA(c->ops->check_finite(c->params(src, src), c->err_dev, c->grid, c->block, c->stream),
@@ -1089,6 +1128,7 @@ int64_t lbm_kernel_launches(lbm_ctx* c) { return c ? c->launches : -1; }
 
 int lbm_set_ghost_planes(lbm_ctx* c, int enable) {
     if (!c) return fail(LBM_EINVAL, "lbm_set_ghost_planes: NULL context");
+    if (c->split) return split_open("lbm_set_ghost_planes");
     if (enable) {
         if (c->streaming != LBM_STREAMING_AB)
             return fail(LBM_EINVAL, "lbm_set_ghost_planes: needs the A-B scheme (LBM_STREAMING_AB)");
@@ -1114,11 +1154,9 @@ int lbm_halo_element_bytes(lbm_ctx* c) {
 }
 
 // Halo buffers are device memory of the context's device (they go to a communication library).
-static int check_halo(lbm_ctx* c, const void* a, const void* b, const char* what) {
+static int check_halo_buffers(lbm_ctx* c, const void* a, const void* b, const char* what) {
     if (!c || !a || !b) return fail(LBM_EINVAL, "%s: NULL argument", what);
     if (!c->ghost) return fail(LBM_ESTATE, "%s: the context has no ghost planes", what);
-    if (c->state != ST_POST_AB)
-        return fail(LBM_ESTATE, "%s: no step taken since the state was loaded", what);
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) {
         cudaGetLastError();
@@ -1135,8 +1173,15 @@ static int check_halo(lbm_ctx* c, const void* a, const void* b, const char* what
     }
     return LBM_OK;
 }
+static int check_halo(lbm_ctx* c, const void* a, const void* b, const char* what) {
+    if (int rc = check_halo_buffers(c, a, b, what)) return rc;
+    if (c->state != ST_POST_AB)
+        return fail(LBM_ESTATE, "%s: no step taken since the state was loaded", what);
+    return LBM_OK;
+}
 
 int lbm_halo_pack(lbm_ctx* c, void* lo, void* hi) {
+    if (c && c->split) return split_open("lbm_halo_pack");
     if (int rc = check_halo(c, lo, hi, "lbm_halo_pack")) return rc;
     void* buf = c->buf[c->cur];
     LBM_CUDA(c->ops->halo_pack(c->params(buf, buf), lo, hi, c->stream), "lbm_halo_pack");
@@ -1145,6 +1190,7 @@ int lbm_halo_pack(lbm_ctx* c, void* lo, void* hi) {
 }
 
 int lbm_halo_unpack(lbm_ctx* c, const void* from_below, const void* from_above) {
+    if (c && c->split) return split_open("lbm_halo_unpack");
     if (int rc = check_halo(c, from_below, from_above, "lbm_halo_unpack")) return rc;
     void* buf = c->buf[c->cur];
     LBM_CUDA(c->ops->halo_unpack(c->params(buf, buf), from_below, from_above, c->stream),
@@ -1153,8 +1199,107 @@ int lbm_halo_unpack(lbm_ctx* c, const void* from_below, const void* from_above) 
     return LBM_OK;
 }
 
+// ---- slab step with the halo exchange overlapped ------------------------------------------------
+// The main kernel of step kind `kind` over `count` planes z = z0 + dz k (k < count), then the
+// boundary kernel over special[s0, s1), both on stream `s`, with the momentum exchange; their
+// force partials take the triples from `slot` on (advanced past them).
+static int launch_planes(lbm_ctx* c, int kind, const Params& p0, int z0, int dz, int count,
+                         uint32_t s0, uint32_t s1, size_t& slot, cudaStream_t s) {
+    if (count > 0) {
+        Params p = p0;
+        p.zbase = z0;
+        p.zstep = dz;
+        p.part_main = slot;
+        const bool two = c->pairs_for(kind);
+        dim3 grid = two ? c->grid2 : c->grid;
+        grid.z = (unsigned)count;
+        const cudaError_t e = two ? c->ops->cells2(kind, p, true, c->body(), grid, c->block2, s)
+                                  : c->ops->cells(kind, p, true, c->body(), grid, c->block, s);
+        ++c->launches;
+        if (e != cudaSuccess) return cuda_fail(e, "slab step: kernel launch");
+        slot += (size_t)grid.x * grid.y * grid.z * kWarpsPerBlock;
+    }
+    if (kind == K_AB_PULL && s1 > s0) {
+        Params p = p0;
+        p.special = c->special + s0;
+        p.n_special = s1 - s0;
+        p.part_special = slot;
+        const cudaError_t e = c->ops->special(K_AB_PULL, p, true, c->body(), s);
+        ++c->launches;
+        if (e != cudaSuccess) return cuda_fail(e, "slab step: boundary kernel launch");
+        slot += (size_t)special_blocks(s1 - s0) * kWarpsPerBlock;
+    }
+    return LBM_OK;
+}
+
+int lbm_slab_step_begin(lbm_ctx* c, void* lo, void* hi) {
+    if (c && c->split)
+        return fail(LBM_ESTATE, "lbm_slab_step_begin: the previous slab step is still open");
+    if (int rc = check_halo_buffers(c, lo, hi, "lbm_slab_step_begin")) return rc;
+    const int nz = c->n[2];
+    // a step from the loaded (natural) state is the collision alone, as in lbm_step
+    const int kind = c->state == ST_NATURAL ? K_AB_COLLIDE : K_AB_PULL;
+    void* dst = c->buf[c->cur ^ 1];
+    const Params p = c->params(c->buf[c->cur], dst);
+    // the edge planes 1 and nz - 2 (one plane when the slab owns one), their special cells, and
+    // the pack of their outgoing populations, on the context stream
+    const int edges = nz - 2 > 1 ? 2 : 1;
+    size_t slot = 0;
+    int rc = launch_planes(c, kind, p, 1, nz - 3, edges, 0, 0, slot, c->stream);
+    if (rc == LBM_OK) {
+        if (edges == 2) {
+            rc = launch_planes(c, kind, p, 0, 0, 0, 0, c->sp_lo_end, slot, c->stream);
+            if (rc == LBM_OK)
+                rc = launch_planes(c, kind, p, 0, 0, 0, c->sp_hi_begin, c->n_special, slot, c->stream);
+        } else {
+            rc = launch_planes(c, kind, p, 0, 0, 0, 0, c->n_special, slot, c->stream);
+        }
+    }
+    if (rc != LBM_OK) return rc;
+    LBM_CUDA(c->ops->halo_pack(c->params(dst, dst), lo, hi, c->stream), "lbm_slab_step_begin: pack");
+    ++c->launches;
+    // the interior planes 2 .. nz - 3 and their special cells on the side stream, forked after the
+    // pack: a transfer the caller orders after the context stream's work so far runs beside them
+    LBM_CUDA(cudaEventRecord(c->side_fork, c->stream), "lbm_slab_step_begin: fork");
+    LBM_CUDA(cudaStreamWaitEvent(c->side_stream, c->side_fork, 0), "lbm_slab_step_begin: fork");
+    if (edges == 2)
+        rc = launch_planes(c, kind, p, 2, 1, nz - 4, c->sp_lo_end, c->sp_hi_begin, slot, c->side_stream);
+    cudaError_t e = cudaEventRecord(c->side_join, c->side_stream);
+    if (rc != LBM_OK) {
+        if (e == cudaSuccess) cudaStreamWaitEvent(c->stream, c->side_join, 0);
+        return rc;
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "lbm_slab_step_begin: join");
+    if (slot > c->partial_cap)
+        return fail(LBM_ESTATE, "lbm_slab_step_begin: %zu force partials exceed the %zu allocated",
+                    slot, c->partial_cap);
+    c->force_triples = slot;
+    c->split = true;
+    return LBM_OK;
+}
+
+int lbm_slab_step_end(lbm_ctx* c, const void* from_below, const void* from_above) {
+    if (c && !c->split) return fail(LBM_ESTATE, "lbm_slab_step_end: no slab step is open");
+    if (int rc = check_halo_buffers(c, from_below, from_above, "lbm_slab_step_end")) return rc;
+    LBM_CUDA(cudaStreamWaitEvent(c->stream, c->side_join, 0), "lbm_slab_step_end: join");
+    c->split = false;
+    c->cur ^= 1;
+    c->state = ST_POST_AB;
+    c->steps += 1;
+    LBM_CUDA(launch_force_finalize(c->partial, c->force_triples, c->stage, c->force_dev, c->stream),
+             "lbm_slab_step_end: force");
+    c->launches += 2;
+    c->force_valid = true;
+    void* buf = c->buf[c->cur];
+    LBM_CUDA(c->ops->halo_unpack(c->params(buf, buf), from_below, from_above, c->stream),
+             "lbm_slab_step_end: unpack");
+    ++c->launches;
+    return LBM_OK;
+}
+
 int lbm_profile_enable(lbm_ctx* c, int enable) {
     if (!c) return fail(LBM_EINVAL, "lbm_profile_enable: NULL context");
+    if (c->split) return split_open("lbm_profile_enable");
     if (int rc = sync(c, "lbm_profile_enable")) return rc;
     c->release_profile();
     c->profiling = enable != 0;
@@ -1163,6 +1308,7 @@ int lbm_profile_enable(lbm_ctx* c, int enable) {
 
 int lbm_profile_read(lbm_ctx* c, int kind, int64_t* launches, double* total_ms) {
     if (!c || !launches || !total_ms) return fail(LBM_EINVAL, "lbm_profile_read: NULL argument");
+    if (c->split) return split_open("lbm_profile_read");
     if (kind < 0 || kind >= K_NUM_KINDS) return fail(LBM_EINVAL, "lbm_profile_read: kind %d", kind);
     if (int rc = sync(c, "lbm_profile_read")) return rc;
     double ms = 0.0;
@@ -1178,6 +1324,7 @@ int lbm_profile_read(lbm_ctx* c, int kind, int64_t* launches, double* total_ms) 
 
 int lbm_set_cell_pairs(lbm_ctx* c, int enable) {
     if (!c) return fail(LBM_EINVAL, "lbm_set_cell_pairs: NULL context");
+    if (c->split) return split_open("lbm_set_cell_pairs");
     if (c->pairs_allowed != (enable != 0)) {
         c->drop_graphs();
         c->pairs_allowed = enable != 0;
@@ -1187,6 +1334,7 @@ int lbm_set_cell_pairs(lbm_ctx* c, int enable) {
 
 int lbm_set_tma_gather(lbm_ctx* c, int enable) {
     if (!c) return fail(LBM_EINVAL, "lbm_set_tma_gather: NULL context");
+    if (c->split) return split_open("lbm_set_tma_gather");
     if (c->tma_allowed != (enable != 0)) {
         c->drop_graphs();
         c->tma_allowed = enable != 0;
@@ -1196,6 +1344,7 @@ int lbm_set_tma_gather(lbm_ctx* c, int enable) {
 
 int lbm_set_boundary_overlap(lbm_ctx* c, int enable) {
     if (!c) return fail(LBM_EINVAL, "lbm_set_boundary_overlap: NULL context");
+    if (c->split) return split_open("lbm_set_boundary_overlap");
     if (c->overlap_allowed != (enable != 0)) {
         c->drop_graphs();
         c->overlap_allowed = enable != 0;
@@ -1205,6 +1354,7 @@ int lbm_set_boundary_overlap(lbm_ctx* c, int enable) {
 
 int lbm_set_graph_launch(lbm_ctx* c, int enable) {
     if (!c) return fail(LBM_EINVAL, "lbm_set_graph_launch: NULL context");
+    if (c->split) return split_open("lbm_set_graph_launch");
     c->use_graphs = enable != 0;
     return LBM_OK;
 }

@@ -144,9 +144,14 @@ struct Params {
     double* partial;       // per-block momentum-exchange partial sums, 3 per block
     int* fault;            // set by a kernel whose bounded wait ran out (read by the host)
     uint32_t extra_tx;     // test hook: bytes a staged tile announces beyond its copies (normally 0)
+    size_t part_main;      // first partial slot (triple) of an A-B step kernel's warps
     size_t part_special;   // first partial slot (triple) of the boundary kernels' warps
     int nx, ny, nz;
     int zrev;              // step kernels walk the z planes from nz - 1 down (alternated per step)
+    // plane of an A-B step kernel's block (k_ab, k_ab2, k_ab_pull_staged, k_own_staged):
+    // z = zbase + zstep * blockIdx.z, the same sweep as zrev for a launch over all planes, other
+    // values for a launch over some planes (a slab's boundary or interior planes)
+    int zbase, zstep;
     int open[3];           // axis has OPEN faces
     size_t N;
     size_t face_base[3][2];  // scratch offset of face (axis, side); 19 * area values each

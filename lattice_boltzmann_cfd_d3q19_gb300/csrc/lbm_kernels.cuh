@@ -139,10 +139,13 @@ struct CellCoord {
     int x, y, z;
     uint32_t n;
 };
+// PLANES: the plane from zbase / zstep (the A-B step kernels, which also run over some planes)
+template <bool PLANES = false>
 __device__ __forceinline__ bool grid_cell(const Params& p, CellCoord& c) {
     c.x = blockIdx.x * blockDim.x + threadIdx.x;
     c.y = blockIdx.y * blockDim.y + threadIdx.y;
-    c.z = p.zrev ? p.nz - 1 - (int)blockIdx.z : (int)blockIdx.z;
+    if constexpr (PLANES) c.z = p.zbase + p.zstep * (int)blockIdx.z;
+    else c.z = p.zrev ? p.nz - 1 - (int)blockIdx.z : (int)blockIdx.z;
     c.n = (uint32_t)c.x + (uint32_t)p.nx * ((uint32_t)c.y + (uint32_t)p.ny * c.z);
     return c.x < p.nx && c.y < p.ny;
 }
@@ -211,7 +214,7 @@ __global__ void __launch_bounds__(256) k_own_staged(Params p) {
     constexpr int L = LAYOUT_COLLISION;
     __shared__ float tile[kWarpsPerBlock][32 * 19];
     CellCoord c;
-    const bool in = grid_cell(p, c);
+    const bool in = grid_cell<true>(p, c);
     const int lane = threadIdx.x & 31;
     const int warp = (threadIdx.x + blockDim.x * threadIdx.y) >> 5;
     // the warp's cells: lanes [0, cnt) of one row (blockDim.x is a multiple of 32), consecutive
@@ -243,7 +246,7 @@ __global__ void __launch_bounds__(256) k_own_staged(Params p) {
     }
     __syncwarp();
     for (int k = lane; k < cnt * 19; k += 32) dst[k] = t[k];
-    if (FORCE) warp_force(fx, fy, fz, p.partial);
+    if (FORCE) warp_force(fx, fy, fz, p.partial, p.part_main);
 }
 
 // ============================== AA pattern, odd step ============================================
@@ -431,7 +434,7 @@ template <int L, bool FORCE, bool BODY, bool FROM_NATURAL, typename I>
 __global__ void __launch_bounds__(256, 6) k_ab(Params p) {
     CellCoord c;
     float fx = 0.f, fy = 0.f, fz = 0.f;
-    if (grid_cell(p, c)) {
+    if (grid_cell<true>(p, c)) {
         // the natural-state collision needs the links only for the force; the mask is loaded
         // beside the flag byte, not after it
         const uint32_t m = (p.any_solid_link && (FORCE || !FROM_NATURAL)) ? p.mask[c.n] : 0u;
@@ -466,7 +469,7 @@ __global__ void __launch_bounds__(256, 6) k_ab(Params p) {
             for (int q = 0; q < 19; ++q) st<L>(p.pb[q], cell_off<L, I>(q, c.n), 0.0f);
         }
     }
-    if (FORCE) warp_force(fx, fy, fz, p.partial);
+    if (FORCE) warp_force(fx, fy, fz, p.partial, p.part_main);
 }
 
 // A-B pull in the collision and bundle layouts, with the stores staged: each lane gathers and
@@ -481,7 +484,7 @@ template <int L, bool FORCE, bool BODY, typename I>
 __global__ void __launch_bounds__(256) k_ab_pull_staged(Params p) {
     __shared__ float tile[kWarpsPerBlock][32 * 19];
     CellCoord c;
-    const bool in = grid_cell(p, c);
+    const bool in = grid_cell<true>(p, c);
     const int lane = threadIdx.x & 31;
     const int warp = (threadIdx.x + blockDim.x * threadIdx.y) >> 5;
     const int cnt = __popc(__ballot_sync(0xffffffffu, in));
@@ -517,7 +520,7 @@ __global__ void __launch_bounds__(256) k_ab_pull_staged(Params p) {
             for (int k = lane; k < cnt * m; k += 32) dst[k] = t[32 * off + k];
         }
     }
-    if (FORCE) warp_force(fx, fy, fz, p.partial);
+    if (FORCE) warp_force(fx, fy, fz, p.partial, p.part_main);
 }
 
 // Streaming only: natural state into B from the post-collision state in A (second pass of the

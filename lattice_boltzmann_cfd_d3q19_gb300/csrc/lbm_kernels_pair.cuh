@@ -72,10 +72,13 @@ struct PairCoord {
     int x, y, z;  // coordinates of the even cell a
     uint32_t n;   // index of a (even)
 };
+// PLANES: the plane from zbase / zstep (the A-B step kernel, which also runs over some planes)
+template <bool PLANES = false>
 __device__ __forceinline__ bool grid_pair(const Params& p, PairCoord& c) {
     c.x = 2 * (int)(blockIdx.x * blockDim.x + threadIdx.x);
     c.y = blockIdx.y * blockDim.y + threadIdx.y;
-    c.z = p.zrev ? p.nz - 1 - (int)blockIdx.z : (int)blockIdx.z;
+    if constexpr (PLANES) c.z = p.zbase + p.zstep * (int)blockIdx.z;
+    else c.z = p.zrev ? p.nz - 1 - (int)blockIdx.z : (int)blockIdx.z;
     c.n = (uint32_t)c.x + (uint32_t)p.nx * ((uint32_t)c.y + (uint32_t)p.ny * c.z);
     return c.x < p.nx && c.y < p.ny;
 }
@@ -183,8 +186,9 @@ __device__ __forceinline__ PairFlags pair_flags(const Params& p, uint32_t n, boo
 __device__ __forceinline__ bool is_inlet(const Params& p, bool in, uint8_t f) {
     return in && p.any_inlet && (f & TYPE_MASK) == T_INLET;
 }
+template <bool PLANES = false>
 __device__ __forceinline__ bool pair_inlets(const Params& p, PairCoord& c, bool& ia, bool& ib) {
-    if (!p.any_inlet || !grid_pair(p, c)) return false;
+    if (!p.any_inlet || !grid_pair<PLANES>(p, c)) return false;
     const uint16_t fl = *reinterpret_cast<const uint16_t*>(p.flags + c.n);
     ia = (fl & TYPE_MASK) == T_INLET;
     ib = ((fl >> 8) & TYPE_MASK) == T_INLET;
@@ -643,7 +647,7 @@ template <int L, bool FORCE, bool BODY, bool FROM_NATURAL, bool INLETS>
 __global__ void __launch_bounds__(256, 4) k_ab2(Params p) {
     PairCoord c;
     float fx = 0.f, fy = 0.f, fz = 0.f;
-    const bool in = grid_pair(p, c);
+    const bool in = grid_pair<true>(p, c);
     PairFlags f{0, 0, 0u, 0u};
     if (in) f = pair_flags(p, c.n, p.any_solid_link != 0 && (FORCE || !FROM_NATURAL));
     const uint8_t want = FROM_NATURAL ? TYPE_MASK : (TYPE_MASK | F_SPECIAL);
@@ -688,9 +692,9 @@ __global__ void __launch_bounds__(256, 4) k_ab2(Params p) {
     if constexpr (INLETS) {
         PairCoord ci;
         bool ia = false, ib = false;
-        if (pair_inlets(p, ci, ia, ib)) pair_inlet_store<L, false>(p, p.B, ci.n, ia, ib);
+        if (pair_inlets<true>(p, ci, ia, ib)) pair_inlet_store<L, false>(p, p.B, ci.n, ia, ib);
     }
-    if (FORCE) warp_force(fx, fy, fz, p.partial);
+    if (FORCE) warp_force(fx, fy, fz, p.partial, p.part_main);
 }
 
 }  // namespace lbm

@@ -15,6 +15,11 @@ boundary planes, in the library's internal storage, exchanged between device buf
 values per slab and step.  The momentum-exchange force of the owned cells is summed over ranks
 (three doubles, an all-reduce).
 
+An engine with begin() / end() overlaps the exchange with the interior planes ([Disaggregated],
+"Disaggregation on a Dense Domain", OCC): begin() steps the two boundary planes, packs their
+halos and starts the interior planes; the ranks swap the halos while the interior computes;
+end() completes the step and unpacks.  The runner uses that form unless told otherwise.
+
 This module holds no lattice Boltzmann arithmetic: the step, the packing and the unpacking run in
 the engine (for `LibraryEngine`, the library's CUDA kernels).
 """
@@ -83,11 +88,13 @@ class SlabRunner:
             empty tensor of a halo buffer's shape, dtype and device.
     dist:   torch.distributed (an initialised process group) or None for a single rank."""
 
-    def __init__(self, engine, slab: Slab, dist=None, group=None):
+    def __init__(self, engine, slab: Slab, dist=None, group=None, overlap: bool = True):
         self.engine = engine
         self.slab = slab
         self.dist = dist
         self.group = group
+        self.overlap = (overlap and callable(getattr(engine, "begin", None))
+                        and callable(getattr(engine, "end", None)))
         if slab.world > 1 and dist is None:
             raise ValueError("several ranks need torch.distributed")
         self.from_below = engine.halo_like()
@@ -95,6 +102,11 @@ class SlabRunner:
 
     def exchange(self) -> None:
         lo, hi = self.engine.pack()
+        self._swap(lo, hi)
+        self.engine.unpack(self.from_below, self.from_above)
+
+    def _swap(self, lo, hi) -> None:
+        """from_below <- the hi of the slab below, from_above <- the lo of the slab above."""
         s = self.slab
         if s.world == 1:
             # periodic in z on one rank: the slab is its own neighbour on both sides
@@ -112,12 +124,16 @@ class SlabRunner:
                    self.dist.P2POp(self.dist.irecv, self.from_above, s.above, self.group)]
             for r in self.dist.batch_isend_irecv(ops):
                 r.wait()
-        self.engine.unpack(self.from_below, self.from_above)
 
     def step(self, n: int) -> None:
         for _ in range(int(n)):
-            self.engine.step1()
-            self.exchange()
+            if self.overlap:
+                lo, hi = self.engine.begin()
+                self._swap(lo, hi)
+                self.engine.end(self.from_below, self.from_above)
+            else:
+                self.engine.step1()
+                self.exchange()
 
     def force(self):
         """Force on the solids of the whole domain: the owned cells' sums, added over ranks."""
@@ -163,6 +179,15 @@ class LibraryEngine:
 
     def unpack(self, from_below, from_above) -> None:
         self.B.lbm_halo_unpack(self.ctx, from_below, from_above)
+
+    def begin(self):
+        # the boundary planes and the pack on torch's current stream, the interior on the
+        # library's side stream: a send issued after this waits for the pack only
+        self.B.lbm_slab_step_begin(self.ctx, self._lo, self._hi)
+        return self._lo, self._hi
+
+    def end(self, from_below, from_above) -> None:
+        self.B.lbm_slab_step_end(self.ctx, from_below, from_above)
 
     def local_force(self):
         return self.B.lbm_force_momentum_exchange(self.ctx)

@@ -1,10 +1,12 @@
-"""The library's side of the z-slab decomposition on one GPU: ghost planes (lbm_set_ghost_planes)
-and the halo kernels (lbm_halo_pack / lbm_halo_unpack).  Several slab contexts live in one process
-and the host swaps their halo buffers between steps, in order (no kernel waits on another).  The
-slabs together must give the unsliced context's populations bit for bit (the same kernels on the
-same values) and its force up to the grouping of the fp64 sums ("Disaggregated Design for
-GPU-Based Volumetric Data Structures", "Improving LBM Scalability": each partition exchanges its
-boundary data with its neighbours every step)."""
+"""The library's side of the z-slab decomposition on one GPU: ghost planes (lbm_set_ghost_planes),
+the halo kernels (lbm_halo_pack / lbm_halo_unpack) and the step with the exchange overlapped by the
+interior planes (lbm_slab_step_begin / lbm_slab_step_end).  Several slab contexts live in one
+process and the host swaps their halo buffers between steps, in order (no kernel waits on
+another).  The slabs together must give the unsliced context's populations bit for bit (the same
+kernels on the same values) and its force up to the grouping of the fp64 sums ("Disaggregated
+Design for GPU-Based Volumetric Data Structures", "Improving LBM Scalability": each partition
+exchanges its boundary data with its neighbours every step; "Disaggregation on a Dense Domain":
+the exchange overlaps the voxels that need no neighbour data)."""
 import numpy as np
 import pytest
 
@@ -49,13 +51,15 @@ def make_ctx(nx, ny, nz, layout, flags, pairs):
     return ctx
 
 
+@pytest.mark.parametrize("overlap", [False, True])
 @pytest.mark.parametrize("moving", [False, True])
 @pytest.mark.parametrize("pairs", [True, False])
 @pytest.mark.parametrize("layout", ["stream", "collision", "stream_fp16"])
-@pytest.mark.parametrize("nz, world", [(12, 2), (13, 3)])
-def test_slabs_equal_the_unsliced_context(nz, world, layout, pairs, moving):
+@pytest.mark.parametrize("nz, world", [(12, 2), (13, 3), (4, 4), (6, 3)])
+def test_slabs_equal_the_unsliced_context(nz, world, layout, pairs, moving, overlap):
     """With moving walls the slabs also have special cells (boundary kernel), some of them next
-    to a ghost plane."""
+    to a ghost plane.  (4, 4): every slab owns one plane (no interior); (6, 3): two (both are
+    boundary planes)."""
     nx, ny, steps = 10, 8, 6
     flags, f0 = global_problem(nx, ny, nz, 70 + nz, moving)
     ref = make_ctx(nx, ny, nz, layout, flags, pairs)
@@ -77,12 +81,18 @@ def test_slabs_equal_the_unsliced_context(nz, world, layout, pairs, moving):
             B.lbm_set_populations(c, torch.from_numpy(S.local_slice(f0, s, nx, ny).reshape(-1)).cuda())
         eng = [S.LibraryEngine(c) for c in ctxs]
         for _ in range(steps):
-            for e in eng:
-                e.step1()
-            packed = [e.pack() for e in eng]  # (lo, hi) per slab
-            for r, e in enumerate(eng):
-                s = slabs[r]
-                e.unpack(packed[s.below][1], packed[s.above][0])
+            if overlap:
+                packed = [e.begin() for e in eng]  # (lo, hi) per slab; interiors still running
+                for r, e in enumerate(eng):
+                    s = slabs[r]
+                    e.end(packed[s.below][1], packed[s.above][0])
+            else:
+                for e in eng:
+                    e.step1()
+                packed = [e.pack() for e in eng]  # (lo, hi) per slab
+                for r, e in enumerate(eng):
+                    s = slabs[r]
+                    e.unpack(packed[s.below][1], packed[s.above][0])
         got, F = [], np.zeros(3)
         for s, c in zip(slabs, ctxs):
             loc = np.zeros((19, nx * ny * s.local_nz), np.float32)
@@ -126,5 +136,23 @@ def test_ghost_plane_rules():
         assert B.lbm_check_finite(ctx)
         with pytest.raises(ValueError):
             B.lbm_halo_pack(ctx, lo[:-1], hi)
+        # an open slab step admits no other call on the context until its end
+        with pytest.raises(B.LbmError) as ei:
+            B.lbm_slab_step_end(ctx, hi, lo)
+        assert ei.value.code == B.ESTATE
+        steps = B.lbm_step_count(ctx)
+        B.lbm_slab_step_begin(ctx, lo, hi)
+        for call in (lambda: B.lbm_slab_step_begin(ctx, lo, hi), lambda: B.lbm_step(ctx, 1),
+                     lambda: B.lbm_halo_pack(ctx, lo, hi),
+                     lambda: B.lbm_force_momentum_exchange(ctx),
+                     lambda: B.lbm_set_body_force(ctx, 0.0, 0.0, 0.0)):
+            with pytest.raises(B.LbmError) as ei:
+                call()
+            assert ei.value.code == B.ESTATE and "slab step" in str(ei.value)
+        assert B.lbm_halo_elements(ctx) == 5 * 8 * 6 and B.lbm_step_count(ctx) == steps
+        B.lbm_slab_step_end(ctx, hi, lo)
+        assert B.lbm_step_count(ctx) == steps + 1
+        assert B.lbm_check_finite(ctx)
+        B.lbm_step(ctx, 1)
     finally:
         B.lbm_destroy(ctx)
