@@ -260,7 +260,7 @@ struct lbm_ctx {
     // kernels launched over cell pairs for step kind `kind`
     bool pairs_for(int kind) const {
         if (kind == K_STREAM) return false;
-        return pairs() || (kind == K_AA_EVEN && bundle_pairs());
+        return pairs() || ((kind == K_AA_EVEN || kind == K_AA_ODD) && bundle_pairs());
     }
     size_t main_blocks_for(int kind) const {
         if (kind == K_AA_ODD && tma()) return ntma;

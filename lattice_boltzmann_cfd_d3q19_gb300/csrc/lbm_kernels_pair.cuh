@@ -514,6 +514,194 @@ __global__ void __launch_bounds__(256, 4) k_aa_even2_bundle(Params p) {
     if (FORCE) warp_force(fx, fy, fz, p.partial);
 }
 
+// ============================== AA pattern, odd step, bundle layout, two cells ===================
+// The AA odd step in the bundle layout on an even nx.  Population q, member m = c_x + 1 of bundle
+// (c_y, c_z), comes from member 2 - m of the opposite bundle in the record of x - c_q and goes to
+// member m of its own bundle in the record of x + c_q.  For a pair (a = x, b = x + 1) the six
+// elements one bundle of three members touches on one row lie in the records x - 1 .. x + 2: two
+// aligned words inside the pair's own two records (e .. e + 1 and e + 4 .. e + 5, e = 3 x
+// relative to the row) and one element on either side.  A bundle of one member is one aligned
+// word, as in the stream layout.  Element by element, each of those accesses touched a third of
+// the sectors of a request.  Warps with a solid link select each cell's own mirrored slot per
+// element, as the stream-layout kernel does.  3 blocks per SM (80 registers): at 4 (64 registers)
+// the kernel spilled and took 0.468 ms at 256^3 instead of 0.427.
+
+// element offset of population q of cell n in the bundle layout
+template <int Q>
+__device__ __forceinline__ uint32_t bidx(uint32_t N, uint32_t n) {
+    return idx<LAYOUT_BUNDLE, uint32_t>(Q, n, N);
+}
+// the solid-link select of the gather: own mirrored slot (q, x) when the link opposite(q) is solid
+template <int Q>
+__device__ __forceinline__ uint32_t bsel(uint32_t m, uint32_t own, uint32_t far) {
+    if constexpr (Q == 0) return far;
+    else return solid_link<opp(Q)>(m) ? own : far;
+}
+
+// the own mirrored slot (opposite(q), x) of a cell whose link q is solid, and the link's momentum
+// exchange
+template <int Q, bool FORCE>
+__device__ __forceinline__ void bundle_bounce(float* A, uint32_t N, uint32_t n, uint32_t ma,
+                                              uint32_t mb, float2 v, PairForce& pf) {
+    const bool ba = solid_link<Q>(ma), bb = solid_link<Q>(mb);
+    if (ba) st1s<LAYOUT_BUNDLE>(A + bidx<opp(Q)>(N, n), v.x);
+    if (bb) st1s<LAYOUT_BUNDLE>(A + bidx<opp(Q)>(N, n + 1), v.y);
+    if (FORCE) pf.template link<Q>(v, ba, bb);
+}
+
+template <bool WALL, int Q = 0>
+__device__ __forceinline__ void bundle_odd_gather2(const float* A, uint32_t N, const NbrPair& nb,
+                                                   uint32_t n, uint32_t ma, uint32_t mb,
+                                                   float2 (&h)[19]) {
+    if constexpr (bundle_j(Q) == 0) {
+        // the source: the opposite bundle on the row (y - c_y, z - c_z)
+        const uint32_t r = nb.template yz<Q, -1>(n);
+        if constexpr (bundle_size(Q) == 3) {
+            constexpr int m0 = bundle_member(Q, 0), m1 = bundle_member(Q, 1), m2 = bundle_member(Q, 2);
+            const uint32_t e = (uint32_t)bundle_off(opp(Q)) * N + 3u * r;
+            if constexpr (WALL) {
+                h[m2] = make_float2(A[bsel<m2>(ma, bidx<m2>(N, n), e + 3 * nb.wa)],
+                                    A[bsel<m2>(mb, bidx<m2>(N, n + 1), e)]);
+                h[m1] = make_float2(A[bsel<m1>(ma, bidx<m1>(N, n), e + 1)],
+                                    A[bsel<m1>(mb, bidx<m1>(N, n + 1), e + 4)]);
+                h[m0] = make_float2(A[bsel<m0>(ma, bidx<m0>(N, n), e + 5)],
+                                    A[bsel<m0>(mb, bidx<m0>(N, n + 1), e + 3 * nb.wb + 2)]);
+            } else {
+                const float2 w0 = ld2<LAYOUT_BUNDLE>(A + e), w1 = ld2<LAYOUT_BUNDLE>(A + e + 4);
+                h[m2] = make_float2(A[e + 3 * nb.wa], w0.x);
+                h[m1] = make_float2(w0.y, w1.x);
+                h[m0] = make_float2(w1.y, A[e + 3 * nb.wb + 2]);
+            }
+        } else {
+            const uint32_t e = (uint32_t)bundle_off(opp(Q)) * N + r;
+            if constexpr (WALL)
+                h[Q] = make_float2(A[bsel<Q>(ma, bidx<Q>(N, n), e)],
+                                   A[bsel<Q>(mb, bidx<Q>(N, n + 1), e + 1)]);
+            else
+                h[Q] = ld2<LAYOUT_BUNDLE>(A + e);
+        }
+    }
+    if constexpr (Q < 18) bundle_odd_gather2<WALL, Q + 1>(A, N, nb, n, ma, mb, h);
+}
+
+// the scatter: the pair's slots in the records of x + c_q (whole words when both cells work,
+// else per cell), and with WALL on each solid link also the own mirrored slot (opposite(q), x)
+// and the link's momentum exchange
+template <bool WALL, bool BOTH, bool FORCE, int Q = 0>
+__device__ __forceinline__ void bundle_odd_scatter2(float* A, uint32_t N, const NbrPair& nb,
+                                                    uint32_t n, uint32_t ma, uint32_t mb,
+                                                    bool act_a, bool act_b, const float2 (&h)[19],
+                                                    PairForce& pf) {
+    if constexpr (bundle_j(Q) == 0) {
+        // the destination: this bundle on the row (y + c_y, z + c_z)
+        const uint32_t r = nb.template yz<Q, 1>(n);
+        if constexpr (bundle_size(Q) == 3) {
+            constexpr int m0 = bundle_member(Q, 0), m1 = bundle_member(Q, 1), m2 = bundle_member(Q, 2);
+            const uint32_t e = (uint32_t)bundle_off(Q) * N + 3u * r;
+            const float2 v0 = h[m0], v1 = h[m1], v2 = h[m2];
+            if constexpr (BOTH) {
+                st2s<LAYOUT_BUNDLE>(A + e, make_float2(v0.y, v1.x));
+                st2s<LAYOUT_BUNDLE>(A + e + 4, make_float2(v1.y, v2.x));
+                st1s<LAYOUT_BUNDLE>(A + e + 3 * nb.wa, v0.x);
+                st1s<LAYOUT_BUNDLE>(A + e + 3 * nb.wb + 2, v2.y);
+            } else {
+                if (act_a) {
+                    st1s<LAYOUT_BUNDLE>(A + e + 3 * nb.wa, v0.x);
+                    st1s<LAYOUT_BUNDLE>(A + e + 1, v1.x);
+                    st1s<LAYOUT_BUNDLE>(A + e + 5, v2.x);
+                }
+                if (act_b) {
+                    st1s<LAYOUT_BUNDLE>(A + e, v0.y);
+                    st1s<LAYOUT_BUNDLE>(A + e + 4, v1.y);
+                    st1s<LAYOUT_BUNDLE>(A + e + 3 * nb.wb + 2, v2.y);
+                }
+            }
+            if constexpr (WALL) {
+                bundle_bounce<m0, FORCE>(A, N, n, ma, mb, v0, pf);
+                if constexpr (m1 != 0) bundle_bounce<m1, FORCE>(A, N, n, ma, mb, v1, pf);
+                bundle_bounce<m2, FORCE>(A, N, n, ma, mb, v2, pf);
+            }
+        } else {
+            const uint32_t e = (uint32_t)bundle_off(Q) * N + r;
+            if constexpr (BOTH) {
+                st2s<LAYOUT_BUNDLE>(A + e, h[Q]);
+            } else {
+                if (act_a) st1s<LAYOUT_BUNDLE>(A + e, h[Q].x);
+                if (act_b) st1s<LAYOUT_BUNDLE>(A + e + 1, h[Q].y);
+            }
+            if constexpr (WALL) bundle_bounce<Q, FORCE>(A, N, n, ma, mb, h[Q], pf);
+        }
+    }
+    if constexpr (Q < 18)
+        bundle_odd_scatter2<WALL, BOTH, FORCE, Q + 1>(A, N, nb, n, ma, mb, act_a, act_b, h, pf);
+}
+
+// INLET producers of the odd step in the bundle layout: f_eq,q of the reservoir to (q, s + c_q),
+// links leaving through an OPEN face dropped (as odd2_produce)
+template <int Q = 1>
+__device__ __forceinline__ void odd2_produce_bundle(const Params& p, const NbrPair& nb, uint32_t n,
+                                                    int x, int y, int z, bool ia, bool ib) {
+    float* A = static_cast<float*>(p.A);
+    const uint32_t N = (uint32_t)p.N;
+    const uint32_t r = nb.template yz<Q, 1>(n);
+    const bool yz_out = (cy(Q) != 0 && p.open[1] && y == (cy(Q) > 0 ? p.ny - 1 : 0)) ||
+                        (cz(Q) != 0 && p.open[2] && z == (cz(Q) > 0 ? p.nz - 1 : 0));
+    const bool xa_out = cx(Q) < 0 && p.open[0] && x == 0;
+    const bool xb_out = cx(Q) > 0 && p.open[0] && x + 2 == p.nx;
+    if (ia && !yz_out && !xa_out) A[bidx<Q>(N, r + (uint32_t)nb.template xa<Q, 1>())] = p.heq_in[Q];
+    if (ib && !yz_out && !xb_out) A[bidx<Q>(N, r + (uint32_t)nb.template xb<Q, 1>())] = p.heq_in[Q];
+    if constexpr (Q < 18) odd2_produce_bundle<Q + 1>(p, nb, n, x, y, z, ia, ib);
+}
+
+template <bool FORCE, bool BODY, bool INLETS>
+__global__ void __launch_bounds__(256, 3) k_aa_odd2_bundle(Params p) {
+    PairCoord c;
+    float fx = 0.f, fy = 0.f, fz = 0.f;
+    const bool in = grid_pair(p, c);
+    PairFlags f{0, 0, 0u, 0u};
+    if (in) f = pair_flags(p, c.n, p.any_solid_link != 0);
+    const bool act_a = in && (f.fa & (TYPE_MASK | F_SPECIAL)) == T_FLUID;
+    const bool act_b = in && (f.fb & (TYPE_MASK | F_SPECIAL)) == T_FLUID;
+    if (!act_a) f.ma = 0u;
+    if (!act_b) f.mb = 0u;
+    const bool wall = __any_sync(0xffffffffu, (f.ma | f.mb) != 0u);
+    const bool both = __all_sync(0xffffffffu, act_a == act_b);
+    if (act_a || act_b) {
+        float* A = static_cast<float*>(p.A);
+        const uint32_t N = (uint32_t)p.N;
+        float2 h[19];
+        {
+            const NbrPair nb(p, c.x, c.y, c.z, false);
+            if (wall) bundle_odd_gather2<true>(A, N, nb, c.n, f.ma, f.mb, h);
+            else bundle_odd_gather2<false>(A, N, nb, c.n, f.ma, f.mb, h);
+        }
+        collide2<BODY>(h, p);
+        uint32_t ns = c.n, mas = f.ma, mbs = f.mb;
+        int xs = c.x, ys = c.y, zs = c.z;
+        asm volatile("" : "+r"(ns), "+r"(mas), "+r"(mbs), "+r"(xs), "+r"(ys), "+r"(zs)
+                     : "f"(h[0].x), "f"(h[18].y));
+        const NbrPair nb(p, xs, ys, zs, false);
+        PairForce pf;
+        if (wall) {
+            if (both) bundle_odd_scatter2<true, true, FORCE>(A, N, nb, ns, mas, mbs, act_a, act_b, h, pf);
+            else bundle_odd_scatter2<true, false, FORCE>(A, N, nb, ns, mas, mbs, act_a, act_b, h, pf);
+            if (FORCE) pf.into(fx, fy, fz);
+        } else {
+            if (both) bundle_odd_scatter2<false, true, FORCE>(A, N, nb, ns, mas, mbs, act_a, act_b, h, pf);
+            else bundle_odd_scatter2<false, false, FORCE>(A, N, nb, ns, mas, mbs, act_a, act_b, h, pf);
+        }
+    }
+    if constexpr (INLETS) {
+        PairCoord ci;
+        bool ia = false, ib = false;
+        if (pair_inlets(p, ci, ia, ib)) {
+            const NbrPair nb(p, ci.x, ci.y, ci.z, false);
+            odd2_produce_bundle(p, nb, ci.n, ci.x, ci.y, ci.z, ia, ib);
+        }
+    }
+    if (FORCE) warp_force(fx, fy, fz, p.partial);
+}
+
 // ============================== AA pattern, odd step, two cells =================================
 // FLUID cells that are not special.  Population q goes to (q, x + c_q); on a solid link also to
 // the own mirrored slot (opposite(q), x), which is the one the next even step reads.

@@ -107,14 +107,25 @@ template <int LL>
 cudaError_t cells2_impl(int kind, const Params& p, bool force, bool body, dim3 grid, dim3 block,
                         cudaStream_t s) {
     if constexpr (LL == LAYOUT_BUNDLE) {
-        // the bundle layout's even step (two cells per thread); its other steps are one-cell
-        if (kind != K_AA_EVEN) return cudaErrorNotSupported;
-        if (force) {
-            if (body) k_aa_even2_bundle<true, true><<<grid, block, 0, s>>>(p);
-            else k_aa_even2_bundle<true, false><<<grid, block, 0, s>>>(p);
+        // the bundle layout's AA steps (two cells per thread); its A-B steps are one-cell
+        if (kind == K_AA_EVEN) {
+            if (force) {
+                if (body) k_aa_even2_bundle<true, true><<<grid, block, 0, s>>>(p);
+                else k_aa_even2_bundle<true, false><<<grid, block, 0, s>>>(p);
+            } else {
+                if (body) k_aa_even2_bundle<false, true><<<grid, block, 0, s>>>(p);
+                else k_aa_even2_bundle<false, false><<<grid, block, 0, s>>>(p);
+            }
+        } else if (kind == K_AA_ODD) {
+            if (force) {
+                if (body) k_aa_odd2_bundle<true, true, true><<<grid, block, 0, s>>>(p);
+                else k_aa_odd2_bundle<true, false, true><<<grid, block, 0, s>>>(p);
+            } else {
+                if (body) k_aa_odd2_bundle<false, true, true><<<grid, block, 0, s>>>(p);
+                else k_aa_odd2_bundle<false, false, true><<<grid, block, 0, s>>>(p);
+            }
         } else {
-            if (body) k_aa_even2_bundle<false, true><<<grid, block, 0, s>>>(p);
-            else k_aa_even2_bundle<false, false><<<grid, block, 0, s>>>(p);
+            return cudaErrorNotSupported;
         }
         return cudaGetLastError();
     } else if constexpr (!is_soa(LL)) {
