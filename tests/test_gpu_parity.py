@@ -650,12 +650,13 @@ PAIR_CASES = [
 
 
 @pytest.mark.parametrize("scheme", ["AA", "AB", "AB2"])
-@pytest.mark.parametrize("layout", ["stream", "stream_fp16"])
+@pytest.mark.parametrize("layout", ["stream", "stream_fp16", "bundle"])
 @pytest.mark.parametrize("ci", range(len(PAIR_CASES)))
 def test_cell_pairs_bit_identical_to_one_cell_kernels(ci, layout, scheme):
     """The two-cell kernels do the same arithmetic in the same order as the one-cell kernels:
     identical populations after every number of steps; the force (partial sums grouped per
-    thread) within 1e-5 relative."""
+    thread) within 1e-5 relative.  In the bundle layout the AA steps have two-cell kernels (the
+    A-B steps run one cell per thread either way)."""
     nx, ny, nz, faces, solid, inlet, moving = PAIR_CASES[ci]
     case = mixed_case(nx, ny, nz, faces, 700 + ci, solid=solid, inlet_layer=inlet, moving=moving)
     for steps in (1, 2, 5):
@@ -673,9 +674,10 @@ def test_cell_pairs_match_oracle(ci, scheme):
     nx, ny, nz, faces, solid, inlet, moving = PAIR_CASES[ci]
     case = mixed_case(nx, ny, nz, faces, 800 + ci, solid=solid, inlet_layer=inlet, moving=moving)
     fo, Fo = case.run_oracle(7, want_force=True)
-    fg, Fg = case.run_gpu(7, "stream", scheme, want_force=True, pairs=True)
-    assert max_fluid_diff(case, fg, fo) <= TOL_F
-    assert np.abs(Fg - Fo).max() <= 1e-4 * max(1.0, float(np.abs(Fo).max()))
+    for layout in (("stream", "bundle") if scheme == "AA" else ("stream",)):
+        fg, Fg = case.run_gpu(7, layout, scheme, want_force=True, pairs=True)
+        assert max_fluid_diff(case, fg, fo) <= TOL_F, layout
+        assert np.abs(Fg - Fo).max() <= 1e-4 * max(1.0, float(np.abs(Fo).max())), layout
 
 
 # ---- boundary kernel beside the main kernel (lbm_set_boundary_overlap) ------------------------------
@@ -688,7 +690,7 @@ OVERLAP_CASES = [2, 3, 4, 5, 7, 8, (96, 48, 40, (1, 0, 0), 0.1, True, 0.2)]
 @pytest.mark.parametrize("graphs", [True, False])
 @pytest.mark.parametrize("pairs", [True, False])
 @pytest.mark.parametrize("scheme", ["AA", "AB", "AB2"])
-@pytest.mark.parametrize("layout", ["stream", "stream_fp16", "collision"])
+@pytest.mark.parametrize("layout", ["stream", "stream_fp16", "bundle", "collision"])
 @pytest.mark.parametrize("ci", range(len(OVERLAP_CASES)))
 def test_boundary_overlap_bit_identical(ci, layout, scheme, pairs, graphs):
     """The boundary kernel on its own stream beside the main kernel stores into slots the main
