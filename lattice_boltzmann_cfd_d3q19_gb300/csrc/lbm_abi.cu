@@ -250,8 +250,8 @@ struct lbm_ctx {
     }
     // the AA odd step stages its gather through shared memory (TMA bulk copies of whole rows)
     bool tma() const { return pairs() && tma_allowed && n[0] % 16 == 0 && n[0] <= 512 && ntma > 0; }
-    // blocks of the step kernels that write force partials
-    size_t main_blocks() const { return pairs() ? nblocks2 : nblocks; }
+    // blocks of the step kernels that write force partials (the boundary kernels' partials follow)
+    size_t main_blocks() const { return pairs() || bundle_pairs() ? nblocks2 : nblocks; }
     // the bundle layout's AA even step also runs two cells per thread (aligned pair runs)
     bool bundle_pairs() const {
         return pairs_allowed && layout == LBM_LAYOUT_BUNDLE && n[0] % 2 == 0 &&
@@ -260,7 +260,7 @@ struct lbm_ctx {
     // kernels launched over cell pairs for step kind `kind`
     bool pairs_for(int kind) const {
         if (kind == K_STREAM) return false;
-        return pairs() || ((kind == K_AA_EVEN || kind == K_AA_ODD) && bundle_pairs());
+        return pairs() || bundle_pairs();
     }
     size_t main_blocks_for(int kind) const {
         if (kind == K_AA_ODD && tma()) return ntma;

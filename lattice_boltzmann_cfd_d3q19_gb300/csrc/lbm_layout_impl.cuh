@@ -107,7 +107,8 @@ template <int LL>
 cudaError_t cells2_impl(int kind, const Params& p, bool force, bool body, dim3 grid, dim3 block,
                         cudaStream_t s) {
     if constexpr (LL == LAYOUT_BUNDLE) {
-        // the bundle layout's AA steps (two cells per thread); its A-B steps are one-cell
+        // the bundle layout's AA and A-B steps (two cells per thread); AB2's streaming pass is
+        // one-cell
         if (kind == K_AA_EVEN) {
             if (force) {
                 if (body) k_aa_even2_bundle<true, true><<<grid, block, 0, s>>>(p);
@@ -123,6 +124,19 @@ cudaError_t cells2_impl(int kind, const Params& p, bool force, bool body, dim3 g
             } else {
                 if (body) k_aa_odd2_bundle<false, true, true><<<grid, block, 0, s>>>(p);
                 else k_aa_odd2_bundle<false, false, true><<<grid, block, 0, s>>>(p);
+            }
+        } else if (kind == K_AB_PULL || kind == K_AB_COLLIDE) {
+            const bool nat = kind == K_AB_COLLIDE;
+            if (force) {
+                if (body) nat ? k_ab2_bundle<true, true, true><<<grid, block, 0, s>>>(p)
+                              : k_ab2_bundle<true, true, false><<<grid, block, 0, s>>>(p);
+                else nat ? k_ab2_bundle<true, false, true><<<grid, block, 0, s>>>(p)
+                         : k_ab2_bundle<true, false, false><<<grid, block, 0, s>>>(p);
+            } else {
+                if (body) nat ? k_ab2_bundle<false, true, true><<<grid, block, 0, s>>>(p)
+                              : k_ab2_bundle<false, true, false><<<grid, block, 0, s>>>(p);
+                else nat ? k_ab2_bundle<false, false, true><<<grid, block, 0, s>>>(p)
+                         : k_ab2_bundle<false, false, false><<<grid, block, 0, s>>>(p);
             }
         } else {
             return cudaErrorNotSupported;

@@ -655,8 +655,8 @@ PAIR_CASES = [
 def test_cell_pairs_bit_identical_to_one_cell_kernels(ci, layout, scheme):
     """The two-cell kernels do the same arithmetic in the same order as the one-cell kernels:
     identical populations after every number of steps; the force (partial sums grouped per
-    thread) within 1e-5 relative.  In the bundle layout the AA steps have two-cell kernels (the
-    A-B steps run one cell per thread either way)."""
+    thread) within 1e-5 relative.  In the bundle layout every step but AB2's streaming pass has a
+    two-cell kernel."""
     nx, ny, nz, faces, solid, inlet, moving = PAIR_CASES[ci]
     case = mixed_case(nx, ny, nz, faces, 700 + ci, solid=solid, inlet_layer=inlet, moving=moving)
     for steps in (1, 2, 5):
