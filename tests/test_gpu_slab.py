@@ -54,7 +54,7 @@ def make_ctx(nx, ny, nz, layout, flags, pairs):
 @pytest.mark.parametrize("overlap", [False, True])
 @pytest.mark.parametrize("moving", [False, True])
 @pytest.mark.parametrize("pairs", [True, False])
-@pytest.mark.parametrize("layout", ["stream", "collision", "stream_fp16"])
+@pytest.mark.parametrize("layout", ["stream", "bundle", "collision", "stream_fp16"])
 @pytest.mark.parametrize("nz, world", [(12, 2), (13, 3), (4, 4), (6, 3)])
 def test_slabs_equal_the_unsliced_context(nz, world, layout, pairs, moving, overlap):
     """With moving walls the slabs also have special cells (boundary kernel), some of them next
