@@ -128,6 +128,9 @@ struct lbm_ctx {
     bool pairs_allowed = true;
     // TMA-staged AA odd kernel: persistent grid and whether the caller allows it
     unsigned ntma = 0;
+    // 2.5D-tiled A-B pull of the collision layout: its grid (z chunks of the tiles) and blocks
+    dim3 tile_grid;
+    size_t ntile = 0;
     bool tma_allowed = false;  // opt-in: measured slower than the register kernels
     int* fault_dev = nullptr;   // set by a kernel whose bounded wait ran out (sticky)
     // test hook (LBM_TEST_STAGE_TIMEOUT=1 at lbm_create): the staged kernel announces 16 bytes
@@ -250,6 +253,11 @@ struct lbm_ctx {
     }
     // the AA odd step stages its gather through shared memory (TMA bulk copies of whole rows)
     bool tma() const { return pairs() && tma_allowed && n[0] % 16 == 0 && n[0] <= 512 && ntma > 0; }
+    // the collision layout's A-B pull stages its gather in 2.5D tiles
+    bool tiled() const {
+        return layout == LBM_LAYOUT_COLLISION && n[0] % kTileX == 0 && 19 * N <= (size_t(1) << 32) &&
+               ntile > 0;
+    }
     // blocks of the step kernels that write force partials (the boundary kernels' partials follow)
     size_t main_blocks() const { return pairs() || bundle_pairs() ? nblocks2 : nblocks; }
     // the bundle layout's AA even step also runs two cells per thread (aligned pair runs)
@@ -264,6 +272,7 @@ struct lbm_ctx {
     }
     size_t main_blocks_for(int kind) const {
         if (kind == K_AA_ODD && tma()) return ntma;
+        if (kind == K_AB_PULL && tiled()) return ntile;
         return pairs_for(kind) ? nblocks2 : nblocks;
     }
     bool body() const { return g[0] != 0.f || g[1] != 0.f || g[2] != 0.f; }
@@ -522,6 +531,8 @@ int launch_kind(lbm_ctx* c, int kind, const Params& p_in, bool force, int main_k
         const bool two = c->pairs_for(kind);
         if (kind == K_AA_ODD && c->tma())
             e = c->ops->odd_tma(p, force, c->body(), c->ntma, c->stream);
+        else if (kind == K_AB_PULL && c->tiled())
+            e = c->ops->ab_pull_tile(p, force, c->body(), c->tile_grid, c->stream);
         else if (two)
             e = c->ops->cells2(kind, p, force, c->body(), c->grid2, c->block2, c->stream);
         else
@@ -580,7 +591,10 @@ int step_once(lbm_ctx* c, bool last) {
         if (c->state == ST_NATURAL) {
             rc = launch_kind(c, K_AB_COLLIDE, p, last);
         } else {
-            rc = main_and_boundary(c, K_AB_PULL, p, last);
+            // the boundary kernel's force partials follow those of the pull's own grid
+            Params pp = p;
+            pp.part_special = c->main_blocks_for(K_AB_PULL) * kWarpsPerBlock;
+            rc = main_and_boundary(c, K_AB_PULL, pp, last);
         }
         c->cur ^= 1;
         c->state = ST_POST_AB;
@@ -769,6 +783,28 @@ lbm_ctx* lbm_create(int nx, int ny, int nz, float tau, int layout, int streaming
             cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && sms > 0) {
             const long long tiles = ((long long)ny * nz + (512 / nx) - 1) / (512 / nx);
             c->ntma = (unsigned)std::min<long long>(sms, tiles);
+        } else {
+            cudaGetLastError();
+        }
+    }
+    if (layout == LBM_LAYOUT_COLLISION && nx % kTileX == 0) {
+        // tiles of 32 x 8 cells; the z planes split into chunks so that the grid holds about 16
+        // blocks per SM (2 resident), each chunk at least 8 planes long
+        int dev = 0, sms = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && sms > 0) {
+            const long long tiles = (long long)(nx / kTileX) * ((ny + kTileY - 1) / kTileY);
+            long long chunks = (16LL * sms + tiles - 1) / tiles;
+            chunks = std::max(1LL, std::min(chunks, (long long)std::max(1, nz / 8)));
+            c->tile_grid = dim3((unsigned)(nx / kTileX), (unsigned)((ny + kTileY - 1) / kTileY),
+                                (unsigned)chunks);
+            c->ntile = (size_t)c->tile_grid.x * c->tile_grid.y * c->tile_grid.z;
+            // its shared memory (97 KB) is above the default limit: raised here, before any
+            // stream capture; without it the pull stays element-wise
+            if (c->ops->tile_prepare() != cudaSuccess) {
+                cudaGetLastError();
+                c->ntile = 0;
+            }
         } else {
             cudaGetLastError();
         }

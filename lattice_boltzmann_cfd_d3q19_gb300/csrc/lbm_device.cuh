@@ -354,6 +354,9 @@ __device__ __forceinline__ void collide2(float2 (&h)[19], const Params& p) {
 // is done leaves at once).  Lane 0 stores the warp's sum as one fp64 triple at slot
 // slot_base + (linear block index) * (warps per block) + (warp in block).
 constexpr int kWarpsPerBlock = 8;  // step kernels launch 256-thread blocks
+// tiles of the collision layout's staged A-B pull: kTileX cells along x (a warp) by kTileY rows
+constexpr int kTileX = 32;
+constexpr int kTileY = 8;
 __device__ __forceinline__ void warp_force(float fx, float fy, float fz, double* partial,
                                            size_t slot_base = 0) {
 #pragma unroll

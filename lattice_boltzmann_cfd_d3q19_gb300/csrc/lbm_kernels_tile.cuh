@@ -1,0 +1,210 @@
+// The A-B pull in the collision layout with its gather staged through shared memory in 2.5D
+// blocks.  In that layout a cell's 19 populations form one 76-byte record ([PortLBM] §3.2,
+// Fig. 2(b)), and the pull reads element q of the record of x - c_q.  Element by element, a warp's
+// request touches a sector per lane, and each source record's sectors are fetched from the L2
+// once for every cell that needs one of its elements (about 615 bytes per cell at 256^3, for the
+// 76 the cell needs).  Here a block holds whole records of its x-y tile plus a one-cell halo for
+// three z planes, copied in coalesced runs, and walks its tile along z: every record crosses the
+// L2 about (10 x 34) / (8 x 32) times per plane.
+#pragma once
+
+#include "lbm_kernels.cuh"
+
+namespace lbm {
+
+// kTileX (32: one warp per row) by kTileY rows: lbm_device.cuh
+constexpr int kTileThreads = kTileX * kTileY;
+constexpr int kHaloX = kTileX + 2;
+constexpr int kHaloY = kTileY + 2;
+// A halo row in shared memory: one pad float, then the records of x0 - 1 .. x0 + 32 in order
+// (hx = 0 .. 33 at 1 + 19 hx), so that the run x0 .. x0 + 31 starts at float 20, 16-byte aligned
+// like its source (76 (row + x0) bytes with 32 | nx), and the row is padded to 648 floats.
+constexpr int kTileRowFloats = 648;
+constexpr int kTileRunFloats = kTileX * 19;                  // 608: one row's own records
+constexpr int kTileRunPieces = kTileRunFloats / 4;           // 152 pieces of 16 bytes
+constexpr int kTilePlaneFloats = kHaloY * kTileRowFloats;    // one plane of the ring
+static_assert(1 + kHaloX * 19 <= kTileRowFloats && kTileRowFloats % 4 == 0, "halo row layout");
+constexpr int kTileSlots = 4;  // planes z - 1, z, z + 1 being read, z + 2 arriving
+constexpr size_t kTileSmemBytes = kTileSlots * kTilePlaneFloats * sizeof(float);
+static_assert(kTileY * kTileX * 19 <= kTilePlaneFloats, "a tile's results fit in one slot");
+
+// coordinate v in [-1, n] of a source row: wrapped on a PERIODIC axis, clamped onto the last
+// layer on an OPEN one (the zero-gradient source of a pull); v > n only for rows of the ragged
+// tail that no cell reads, kept in range
+__device__ __forceinline__ int tile_edge(int v, int n, bool open) {
+    if (v < 0) return open ? 0 : n - 1;
+    if (v == n) return open ? n - 1 : 0;
+    return v < n ? v : n - 1;
+}
+
+__device__ __forceinline__ void cp_async4(float* dst_shared, const float* src) {
+    const unsigned d = (unsigned)__cvta_generic_to_shared(dst_shared);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(d), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async16(float* dst_shared, const float* src) {
+    const unsigned d = (unsigned)__cvta_generic_to_shared(dst_shared);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// wait until at most `pending` of this thread's committed groups are still in flight
+template <int pending>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(pending) : "memory"); }
+
+__device__ __forceinline__ int tile_slot(int z) { return (z + kTileSlots) % kTileSlots; }  // z >= -1
+
+// Plane zs of A, rows y0 - 1 .. y0 + kTileY, into `dst` (kHaloY halo rows).  In every row thread
+// t < 152 copies the 16-byte piece t of the run x0 .. x0 + 31.  The edge records x0 - 1 and
+// x0 + 32 follow.  Where such a record is the run's neighbour in memory, it is one aligned block
+// of 80 bytes (5 pieces; the extra float lands on a pad float of the halo row, and with 32 | nx the
+// block never leaves the row).  Where it is wrapped or clamped, it is 19 single elements.
+// Asynchronous; the caller commits the group.
+__device__ __forceinline__ void tile_load_plane(const Params& p, const float* A, float* dst, int x0,
+                                                int y0, int zs) {
+    const int t = (int)threadIdx.x;
+    const bool lw = x0 > 0, rw = x0 + kTileX < p.nx;
+    const int nl = lw ? 5 : 19, nr = rw ? 5 : 19;
+    bool wide;
+    uint32_t src;  // element offset from the row's first element
+    int d;         // float offset in the halo row
+    if (t < kTileRunPieces) {
+        wide = true;
+        src = 19u * (uint32_t)x0 + 4u * (uint32_t)t;
+        d = 20 + 4 * t;
+    } else if (t < kTileRunPieces + nl) {
+        const int i = t - kTileRunPieces;
+        wide = lw;
+        if (lw) {
+            src = 19u * (uint32_t)x0 - 20u + 4u * (uint32_t)i;
+            d = 4 * i;
+        } else {
+            src = 19u * (uint32_t)tile_edge(x0 - 1, p.nx, p.open[0]) + (uint32_t)i;
+            d = 1 + i;
+        }
+    } else if (t < kTileRunPieces + nl + nr) {
+        const int i = t - kTileRunPieces - nl;
+        wide = rw;
+        if (rw) {
+            src = 19u * (uint32_t)(x0 + kTileX) + 4u * (uint32_t)i;
+            d = 1 + (kHaloX - 1) * 19 + 4 * i;
+        } else {
+            src = 19u * (uint32_t)tile_edge(x0 + kTileX, p.nx, p.open[0]) + (uint32_t)i;
+            d = 1 + (kHaloX - 1) * 19 + i;
+        }
+    } else {
+        return;
+    }
+#pragma unroll 2
+    for (int r = 0; r < kHaloY; ++r) {
+        const int y = tile_edge(y0 - 1 + r, p.ny, p.open[1]);
+        const uint32_t row = (uint32_t)p.nx * ((uint32_t)y + (uint32_t)p.ny * (uint32_t)zs);
+        const float* g = A + (19u * row + src);
+        float* s_ = dst + r * kTileRowFloats + d;
+        if (wide) cp_async16(s_, g);
+        else cp_async4(s_, g);
+    }
+}
+
+// population q of the cell at (tx, ty) of the tile from the ring: element q of the record of
+// x - c_q, or on a solid link opposite(q) element opposite(q) of its own record
+template <int Q = 0>
+__device__ __forceinline__ void tile_gather(const float* pm, const float* p0, const float* pp,
+                                            int own, uint32_t m, float (&h)[19]) {
+    constexpr int dz = cz(Q);
+    const float* src = dz > 0 ? pm : dz < 0 ? pp : p0;
+    const int off = own - cy(Q) * kTileRowFloats - cx(Q) * 19;
+    if constexpr (Q == 0) h[Q] = src[off + Q];
+    else h[Q] = solid_link<opp(Q)>(m) ? p0[own + opp(Q)] : src[off + Q];
+    if constexpr (Q < 18) tile_gather<Q + 1>(pm, p0, pp, own, m, h);
+}
+
+// Grid: (nx / 32, ceil(ny / 8), chunks); a block walks the planes of its chunk of
+// ceil(nz / chunks).  FLUID cells that are not special are pulled and collided; INLET cells store
+// the reservoir's f_eq, the others zeros (the boundary kernel, launched after this one, writes the
+// special cells).  The caller checks 32 | nx and 19 N <= 2^32.
+// Pipeline: while plane z is computed from the slots of z - 1, z and z + 1, the copies of z + 2
+// are in flight; after it, the results go through the freed slot of z - 1 to the destination in
+// one run per row, and the copies of z + 3 start into that slot.
+template <bool FORCE, bool BODY>
+__global__ void __launch_bounds__(kTileThreads, 2) k_ab_pull_tile(Params p) {
+    extern __shared__ __align__(16) float tile_smem[];
+    float* ring = tile_smem;
+    const int tx = (int)threadIdx.x & 31, ty = (int)threadIdx.x >> 5;
+    const int x0 = (int)blockIdx.x * kTileX, y0 = (int)blockIdx.y * kTileY;
+    const int len = (p.nz + (int)gridDim.z - 1) / (int)gridDim.z;
+    const int z0 = (int)blockIdx.z * len;
+    const int z1 = min(z0 + len, p.nz);
+    const int x = x0 + tx, y = y0 + ty;
+    const bool row_in = y < p.ny;  // the same for the whole warp
+    const float* A = static_cast<const float*>(p.A);
+    float* B = static_cast<float*>(p.B);
+    float fx = 0.f, fy = 0.f, fz = 0.f;
+    if (z0 < z1) {
+        // planes z0 - 1 .. z0 + 1 (one group), then z0 + 2 (the next); a plane is needed up to z1
+        for (int z = z0 - 1; z <= z0 + 1; ++z)
+            tile_load_plane(p, A, ring + tile_slot(z) * kTilePlaneFloats, x0, y0,
+                            tile_edge(z, p.nz, p.open[2]));
+        cp_async_commit();
+        if (z0 + 2 <= z1)
+            tile_load_plane(p, A, ring + tile_slot(z0 + 2) * kTilePlaneFloats, x0, y0,
+                            tile_edge(z0 + 2, p.nz, p.open[2]));
+        cp_async_commit();
+        cp_async_wait<1>();
+        __syncthreads();
+        const int own = (ty + 1) * kTileRowFloats + 1 + (tx + 1) * 19;
+        const uint32_t area = (uint32_t)p.nx * (uint32_t)p.ny;
+        uint32_t n = (uint32_t)x + (uint32_t)p.nx * ((uint32_t)y + (uint32_t)p.ny * (uint32_t)z0);
+        // the flag byte and mask of a cell are loaded one plane ahead of its use
+        uint32_t m_next = 0u;
+        uint8_t fl_next = (uint8_t)T_SOLID;
+        if (row_in) {
+            m_next = p.any_solid_link ? p.mask[n] : 0u;
+            fl_next = p.flags[n];
+        }
+        for (int z = z0; z < z1; ++z, n += area) {
+            float h[19];
+            const uint32_t m = m_next;
+            const uint8_t fl = fl_next;
+            if (row_in && z + 1 < z1) {
+                m_next = p.any_solid_link ? p.mask[n + area] : 0u;
+                fl_next = p.flags[n + area];
+            }
+            if (row_in) {
+                if ((fl & (TYPE_MASK | F_SPECIAL)) == T_FLUID) {
+                    tile_gather(ring + tile_slot(z - 1) * kTilePlaneFloats,
+                                ring + tile_slot(z) * kTilePlaneFloats,
+                                ring + tile_slot(z + 1) * kTilePlaneFloats, own, m, h);
+                    collide<BODY>(h, p);
+                    if (FORCE && m) mask_forces(m, h, fx, fy, fz);
+                } else {
+                    const bool inl = p.any_inlet && (fl & TYPE_MASK) == T_INLET;
+#pragma unroll
+                    for (int q = 0; q < 19; ++q) h[q] = inl ? p.heq_in[q] : 0.0f;
+                }
+            }
+            __syncthreads();  // every read of the slot of z - 1 is done
+            float* out = ring + tile_slot(z - 1) * kTilePlaneFloats;
+            if (row_in) {
+                float* o = out + ty * kTileRunFloats + tx * 19;
+#pragma unroll
+                for (int q = 0; q < 19; ++q) o[q] = h[q];
+            }
+            __syncwarp();
+            if (row_in) {
+                // the row's 32 records are one contiguous, 16-byte aligned run of the destination
+                float4* dst = reinterpret_cast<float4*>(B + 19u * (n - (uint32_t)tx));
+                const float4* src = reinterpret_cast<const float4*>(out + ty * kTileRunFloats);
+                for (int k = tx; k < kTileRunPieces; k += 32) dst[k] = src[k];
+            }
+            __syncthreads();  // the slot of z - 1 is free again
+            if (z + 3 <= z1)
+                tile_load_plane(p, A, ring + tile_slot(z + 3) * kTilePlaneFloats, x0, y0,
+                                tile_edge(z + 3, p.nz, p.open[2]));
+            cp_async_commit();
+            cp_async_wait<1>();  // plane z + 2 has arrived (z + 3 may still be in flight)
+            __syncthreads();
+        }
+    }
+    if (FORCE) warp_force(fx, fy, fz, p.partial, p.part_main);
+}
+
+}  // namespace lbm

@@ -35,6 +35,12 @@ struct LayoutOps {
     // AA odd step with the gather staged by TMA bulk copies (stream layouts, 16 | nx <= 512,
     // 19 N <= 2^32): `grid` persistent CTAs of 256 threads; cudaErrorNotSupported otherwise
     cudaError_t (*odd_tma)(const Params& p, bool force, bool body, unsigned grid, cudaStream_t s);
+    // A-B pull of the collision layout with its gather staged in 2.5D tiles (32 | nx,
+    // 19 N <= 2^32): `grid` = (nx / 32, ceil(ny / 8), z chunks) blocks of 256 threads;
+    // cudaErrorNotSupported for the other layouts.  tile_prepare raises the kernel's dynamic
+    // shared-memory limit on the current device (a no-op for the other layouts).
+    cudaError_t (*ab_pull_tile)(const Params& p, bool force, bool body, dim3 grid, cudaStream_t s);
+    cudaError_t (*tile_prepare)();
     // boundary kernel over the special-cell list for main kind K_AA_ODD, K_AB_PULL or K_STREAM
     cudaError_t (*special)(int kind, const Params& p, bool force, bool body, cudaStream_t s);
     // open-face pre-gather of the AA odd step, every open face in one launch

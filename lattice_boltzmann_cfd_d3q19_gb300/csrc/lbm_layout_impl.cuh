@@ -6,6 +6,7 @@
 #include "lbm_kernels.cuh"
 #include "lbm_kernels_pair.cuh"
 #include "lbm_kernels_tma.cuh"
+#include "lbm_kernels_tile.cuh"
 #include "lbm_kernels_boundary.cuh"
 #include "lbm_launch.h"
 
@@ -197,6 +198,43 @@ cudaError_t odd_tma(const Params& p, bool force, bool body, unsigned grid, cudaS
     return odd_tma_impl<L>(p, force, body, grid, s);
 }
 
+// 2.5D-tiled A-B pull of the collision layout (the caller checks 32 | nx and 19 N <= 2^32)
+template <int LL>
+cudaError_t ab_pull_tile_impl(const Params& p, bool force, bool body, dim3 grid, cudaStream_t s) {
+    if constexpr (LL != LAYOUT_COLLISION) {
+        return cudaErrorNotSupported;
+    } else {
+        if (force) {
+            if (body) k_ab_pull_tile<true, true><<<grid, kTileThreads, kTileSmemBytes, s>>>(p);
+            else k_ab_pull_tile<true, false><<<grid, kTileThreads, kTileSmemBytes, s>>>(p);
+        } else {
+            if (body) k_ab_pull_tile<false, true><<<grid, kTileThreads, kTileSmemBytes, s>>>(p);
+            else k_ab_pull_tile<false, false><<<grid, kTileThreads, kTileSmemBytes, s>>>(p);
+        }
+        return cudaGetLastError();
+    }
+}
+cudaError_t ab_pull_tile(const Params& p, bool force, bool body, dim3 grid, cudaStream_t s) {
+    return ab_pull_tile_impl<L>(p, force, body, grid, s);
+}
+template <int LL>
+cudaError_t tile_prepare_impl() {
+    if constexpr (LL != LAYOUT_COLLISION) {
+        return cudaSuccess;
+    } else {
+        const int bytes = (int)kTileSmemBytes;
+        cudaError_t e = cudaFuncSetAttribute(k_ab_pull_tile<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k_ab_pull_tile<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k_ab_pull_tile<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k_ab_pull_tile<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        return e;
+    }
+}
+cudaError_t tile_prepare() { return tile_prepare_impl<L>(); }
+
 unsigned blocks_for(size_t count) { return (unsigned)((count + 255) / 256); }
 
 #define LBM_LAUNCH_SPECIAL(KERNEL)                                                     \
@@ -284,8 +322,8 @@ cudaError_t halo_unpack(const Params& p, const void* below, const void* above, c
     return cudaGetLastError();
 }
 
-const LayoutOps kOps = {cells, cells2, odd_tma, special, pregather, pack, unpack, equilibrium, macro, check_finite,
-                        fill_inlet, halo_pack, halo_unpack};
+const LayoutOps kOps = {cells, cells2, odd_tma, ab_pull_tile, tile_prepare, special, pregather, pack, unpack,
+                        equilibrium, macro, check_finite, fill_inlet, halo_pack, halo_unpack};
 
 }  // namespace
 }  // namespace lbm
