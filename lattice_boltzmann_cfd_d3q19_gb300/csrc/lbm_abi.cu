@@ -165,7 +165,9 @@ struct lbm_ctx {
     bool overlap_allowed = true;
     bool overlap(int kind) const {
         if (!overlap_allowed || profiling || n_special == 0) return false;
-        // the two-cell pull and the staged pull of the non-SoA layouts write special cells' slots
+        // the two-cell pull and the staged pull of the non-SoA layouts write special cells' slots,
+        // and so does the tiled odd step (whole records)
+        if (kind == K_AA_ODD && tiled_odd()) return false;
         return !(kind == K_AB_PULL && (pairs() || !is_soa(layout)));
     }
     int64_t steps = 0;
@@ -258,6 +260,9 @@ struct lbm_ctx {
         return layout == LBM_LAYOUT_COLLISION && n[0] % kTileX == 0 && 19 * N <= (size_t(1) << 32) &&
                ntile > 0;
     }
+    // and its AA odd step runs in the same tiles, in place in shared memory, where no two rows of a
+    // halo tile are one row of the grid
+    bool tiled_odd() const { return tiled() && n[1] >= kTileY + 2; }
     // blocks of the step kernels that write force partials (the boundary kernels' partials follow)
     size_t main_blocks() const { return pairs() || bundle_pairs() ? nblocks2 : nblocks; }
     // the bundle layout's AA even step also runs two cells per thread (aligned pair runs)
@@ -273,6 +278,7 @@ struct lbm_ctx {
     size_t main_blocks_for(int kind) const {
         if (kind == K_AA_ODD && tma()) return ntma;
         if (kind == K_AB_PULL && tiled()) return ntile;
+        if (kind == K_AA_ODD && tiled_odd()) return ntile;
         return pairs_for(kind) ? nblocks2 : nblocks;
     }
     bool body() const { return g[0] != 0.f || g[1] != 0.f || g[2] != 0.f; }
@@ -533,6 +539,8 @@ int launch_kind(lbm_ctx* c, int kind, const Params& p_in, bool force, int main_k
             e = c->ops->odd_tma(p, force, c->body(), c->ntma, c->stream);
         else if (kind == K_AB_PULL && c->tiled())
             e = c->ops->ab_pull_tile(p, force, c->body(), c->tile_grid, c->stream);
+        else if (kind == K_AA_ODD && c->tiled_odd())
+            e = c->ops->aa_odd_tile(p, force, c->body(), c->tile_grid, c->stream);
         else if (two)
             e = c->ops->cells2(kind, p, force, c->body(), c->grid2, c->block2, c->stream);
         else

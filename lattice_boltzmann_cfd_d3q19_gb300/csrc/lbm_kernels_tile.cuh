@@ -58,8 +58,10 @@ __device__ __forceinline__ int tile_slot(int z) { return (z + kTileSlots) % kTil
 // of 80 bytes (5 pieces; the extra float lands on a pad float of the halo row, and with 32 | nx the
 // block never leaves the row).  Where it is wrapped or clamped, it is 19 single elements.
 // Asynchronous; the caller commits the group.
+// clamp: OPEN axes clamp onto the last layer (the A-B pull); otherwise every axis wraps (the AA
+// odd step, whose links across an OPEN face belong to special cells).
 __device__ __forceinline__ void tile_load_plane(const Params& p, const float* A, float* dst, int x0,
-                                                int y0, int zs) {
+                                                int y0, int zs, bool clamp = true) {
     const int t = (int)threadIdx.x;
     const bool lw = x0 > 0, rw = x0 + kTileX < p.nx;
     const int nl = lw ? 5 : 19, nr = rw ? 5 : 19;
@@ -77,7 +79,7 @@ __device__ __forceinline__ void tile_load_plane(const Params& p, const float* A,
             src = 19u * (uint32_t)x0 - 20u + 4u * (uint32_t)i;
             d = 4 * i;
         } else {
-            src = 19u * (uint32_t)tile_edge(x0 - 1, p.nx, p.open[0]) + (uint32_t)i;
+            src = 19u * (uint32_t)tile_edge(x0 - 1, p.nx, clamp && p.open[0]) + (uint32_t)i;
             d = 1 + i;
         }
     } else if (t < kTileRunPieces + nl + nr) {
@@ -87,7 +89,7 @@ __device__ __forceinline__ void tile_load_plane(const Params& p, const float* A,
             src = 19u * (uint32_t)(x0 + kTileX) + 4u * (uint32_t)i;
             d = 1 + (kHaloX - 1) * 19 + 4 * i;
         } else {
-            src = 19u * (uint32_t)tile_edge(x0 + kTileX, p.nx, p.open[0]) + (uint32_t)i;
+            src = 19u * (uint32_t)tile_edge(x0 + kTileX, p.nx, clamp && p.open[0]) + (uint32_t)i;
             d = 1 + (kHaloX - 1) * 19 + i;
         }
     } else {
@@ -95,7 +97,7 @@ __device__ __forceinline__ void tile_load_plane(const Params& p, const float* A,
     }
 #pragma unroll 2
     for (int r = 0; r < kHaloY; ++r) {
-        const int y = tile_edge(y0 - 1 + r, p.ny, p.open[1]);
+        const int y = tile_edge(y0 - 1 + r, p.ny, clamp && p.open[1]);
         const uint32_t row = (uint32_t)p.nx * ((uint32_t)y + (uint32_t)p.ny * (uint32_t)zs);
         const float* g = A + (19u * row + src);
         float* s_ = dst + r * kTileRowFloats + d;
@@ -205,6 +207,197 @@ __global__ void __launch_bounds__(kTileThreads, 2) k_ab_pull_tile(Params p) {
         }
     }
     if (FORCE) warp_force(fx, fy, fz, p.partial, p.part_main);
+}
+
+// ============================== AA odd step, collision layout, 2.5D tiles ========================
+// The AA odd step writes population q of cell x into element q of the record of x + c_q, so in the
+// collision layout a record's elements come from 19 cells and every element store of a warp hit
+// another sector: each sector was assembled in the L2 from about eight 4-byte writes.  Here a block
+// updates the records of its tile and halo in place in shared memory.  Each cell reads and writes
+// only its own slot set (the AA property), plus, on a solid link, one slot of its own record that
+// the SOLID neighbour owns and nobody else writes.  A plane is final once the plane after it has
+// been computed, and then it goes back to the buffer.
+// * Records whose 19 slots all belong to this block's cells go back whole, one contiguous run per
+//   row: x-y interior records (hx 2 .. 31, hy 2 .. 7 with the next row inside the grid) of planes
+//   strictly inside the block's chunk.
+// * Every other record goes back element by element: only the slots this block wrote, recorded
+//   in a 32-bit mask per record.
+// The whole records carry stale values in the slots of special cells, so the boundary kernel runs
+// after this kernel, not beside it.  The caller checks 32 | nx, ny >= kTileY + 2 (no two rows of a
+// halo tile are the same row of the grid) and 19 N <= 2^32.
+constexpr int kTileRecords = kHaloX * kHaloY;
+constexpr size_t kOddTileSmemBytes = kTileSmemBytes + kTileSlots * kTileRecords * sizeof(uint32_t);
+
+__device__ __forceinline__ int tile_wrap(int v, int n) {
+    v %= n;
+    return v < 0 ? v + n : v;
+}
+
+// population q of the cell from element opposite(q) of the record of x - c_q, or on a solid link
+// opposite(q) element q of its own record (the AA odd gather)
+template <int Q = 0>
+__device__ __forceinline__ void tile_odd_gather(const float* pm, const float* p0, const float* pp,
+                                                int own, uint32_t m, float (&h)[19]) {
+    constexpr int dz = cz(Q);
+    const float* src = dz > 0 ? pm : dz < 0 ? pp : p0;
+    constexpr int shift = -cy(Q) * kTileRowFloats - cx(Q) * 19 + opp(Q);
+    if constexpr (Q == 0) h[Q] = p0[own];
+    else h[Q] = solid_link<opp(Q)>(m) ? p0[own + Q] : src[own + shift];
+    if constexpr (Q < 18) tile_odd_gather<Q + 1>(pm, p0, pp, own, m, h);
+}
+
+// population q to element q of the record of x + c_q, or on a solid link q to element opposite(q)
+// of its own record (with the link's momentum exchange); the element's bit is set in its
+// record's mask
+template <bool FORCE, int Q = 0>
+__device__ __forceinline__ void tile_odd_scatter(float* pm, float* p0, float* pp, uint32_t* bm,
+                                                 uint32_t* b0, uint32_t* bp, int own, int rid,
+                                                 uint32_t m, const float (&h)[19], float& fx,
+                                                 float& fy, float& fz) {
+    constexpr int dz = cz(Q);
+    if (Q > 0 && solid_link<Q>(m)) {
+        p0[own + opp(Q)] = h[Q];
+        atomicOr(&b0[rid], 1u << opp(Q));
+        if (FORCE) accumulate_force<Q>(h[Q], fx, fy, fz);
+    } else {
+        float* dst = dz > 0 ? pp : dz < 0 ? pm : p0;
+        uint32_t* bd = dz > 0 ? bp : dz < 0 ? bm : b0;
+        dst[own + cy(Q) * kTileRowFloats + cx(Q) * 19 + Q] = h[Q];
+        atomicOr(&bd[rid + cy(Q) * kHaloX + cx(Q)], 1u << Q);
+    }
+    if constexpr (Q < 18) tile_odd_scatter<FORCE, Q + 1>(pm, p0, pp, bm, b0, bp, own, rid, m, h, fx, fy, fz);
+}
+
+// INLET producer: f_eq,q of the reservoir to element q of the record of s + c_q, links that leave
+// the grid through an OPEN face dropped (as the one-cell kernel's producer)
+template <int Q = 1>
+__device__ __forceinline__ void tile_odd_produce(const Params& p, float* pm, float* p0, float* pp,
+                                                 uint32_t* bm, uint32_t* b0, uint32_t* bp, int own,
+                                                 int rid, int x, int y, int z) {
+    if (!leaves_open(p, x, y, z, cx(Q), cy(Q), cz(Q))) {
+        constexpr int dz = cz(Q);
+        float* dst = dz > 0 ? pp : dz < 0 ? pm : p0;
+        uint32_t* bd = dz > 0 ? bp : dz < 0 ? bm : b0;
+        dst[own + cy(Q) * kTileRowFloats + cx(Q) * 19 + Q] = p.heq_in[Q];
+        atomicOr(&bd[rid + cy(Q) * kHaloX + cx(Q)], 1u << Q);
+    }
+    if constexpr (Q < 18) tile_odd_produce<Q + 1>(p, pm, p0, pp, bm, b0, bp, own, rid, x, y, z);
+}
+
+// plane pl of the ring (slot `ring_s`, masks `bits_s`) back to A; `whole`: the plane lies
+// strictly inside the chunk, so its x-y interior records go back whole.  The masks are cleared.
+__device__ __forceinline__ void tile_odd_writeback(const Params& p, float* A, const float* ring_s,
+                                                   uint32_t* bits_s, int x0, int y0, int pl,
+                                                   bool whole) {
+    const int t = (int)threadIdx.x;
+    const uint32_t gz = (uint32_t)tile_wrap(pl, p.nz);
+    if (whole) {
+        // warp w: row hy = 2 + w, records hx = 2 .. 31 (one run of 30 records)
+        const int w = t >> 5, lane = t & 31;
+        const int hy = 2 + w;
+        if (w < kTileY - 2 && y0 + hy < p.ny) {
+            const uint32_t gy = (uint32_t)(y0 + hy - 1);
+            float* dst = A + 19u * ((uint32_t)(x0 + 1) + (uint32_t)p.nx * (gy + (uint32_t)p.ny * gz));
+            const float* src = ring_s + hy * kTileRowFloats + 1 + 2 * 19;
+            for (int k = lane; k < (kTileX - 2) * 19; k += 32) dst[k] = src[k];
+        }
+    }
+    for (int rid = t; rid < kTileRecords; rid += kTileThreads) {
+        const uint32_t b = bits_s[rid];
+        if (b == 0u) continue;
+        bits_s[rid] = 0u;
+        const int hx = rid % kHaloX, hy = rid / kHaloX;
+        if (whole && hx >= 2 && hx <= kTileX - 1 && hy >= 2 && hy <= kTileY - 1 && y0 + hy < p.ny)
+            continue;
+        const uint32_t gx = (uint32_t)tile_wrap(x0 - 1 + hx, p.nx);
+        const uint32_t gy = (uint32_t)tile_wrap(y0 - 1 + hy, p.ny);
+        float* dst = A + 19u * (gx + (uint32_t)p.nx * (gy + (uint32_t)p.ny * gz));
+        const float* src = ring_s + hy * kTileRowFloats + 1 + hx * 19;
+        for (uint32_t r = b; r; r &= r - 1u) {
+            const int e = __ffs(r) - 1;
+            dst[e] = src[e];
+        }
+    }
+}
+
+// Grid: (nx / 32, ceil(ny / 8), chunks), as the tiled pull.  FLUID cells that are not special are
+// gathered, collided and scattered; INLET cells produce.
+template <bool FORCE, bool BODY>
+__global__ void __launch_bounds__(kTileThreads, 2) k_aa_odd_tile(Params p) {
+    extern __shared__ __align__(16) float tile_smem[];
+    float* ring = tile_smem;
+    uint32_t* bits = reinterpret_cast<uint32_t*>(tile_smem + kTileSlots * kTilePlaneFloats);
+    const int tx = (int)threadIdx.x & 31, ty = (int)threadIdx.x >> 5;
+    const int x0 = (int)blockIdx.x * kTileX, y0 = (int)blockIdx.y * kTileY;
+    const int len = (p.nz + (int)gridDim.z - 1) / (int)gridDim.z;
+    const int z0 = (int)blockIdx.z * len;
+    const int z1 = min(z0 + len, p.nz);
+    const int x = x0 + tx, y = y0 + ty;
+    const bool row_in = y < p.ny;  // the same for the whole warp
+    float* A = static_cast<float*>(p.A);
+    float fx = 0.f, fy = 0.f, fz = 0.f;
+    if (z0 < z1) {
+        for (int k = (int)threadIdx.x; k < kTileSlots * kTileRecords; k += kTileThreads) bits[k] = 0u;
+        for (int z = z0 - 1; z <= z0 + 1; ++z)
+            tile_load_plane(p, A, ring + tile_slot(z) * kTilePlaneFloats, x0, y0,
+                            tile_wrap(z, p.nz), false);
+        cp_async_commit();
+        if (z0 + 2 <= z1)
+            tile_load_plane(p, A, ring + tile_slot(z0 + 2) * kTilePlaneFloats, x0, y0,
+                            tile_wrap(z0 + 2, p.nz), false);
+        cp_async_commit();
+        const int own = (ty + 1) * kTileRowFloats + 1 + (tx + 1) * 19;
+        const int rid = (ty + 1) * kHaloX + (tx + 1);
+        const uint32_t area = (uint32_t)p.nx * (uint32_t)p.ny;
+        uint32_t n = (uint32_t)x + (uint32_t)p.nx * ((uint32_t)y + (uint32_t)p.ny * (uint32_t)z0);
+        uint32_t m_next = 0u;
+        uint8_t fl_next = (uint8_t)T_SOLID;
+        if (row_in) {
+            m_next = p.any_solid_link ? p.mask[n] : 0u;
+            fl_next = p.flags[n];
+        }
+        cp_async_wait<1>();
+        __syncthreads();
+        for (int z = z0; z < z1; ++z, n += area) {
+            const uint32_t m = m_next;
+            const uint8_t fl = fl_next;
+            if (row_in && z + 1 < z1) {
+                m_next = p.any_solid_link ? p.mask[n + area] : 0u;
+                fl_next = p.flags[n + area];
+            }
+            float* pm = ring + tile_slot(z - 1) * kTilePlaneFloats;
+            float* p0 = ring + tile_slot(z) * kTilePlaneFloats;
+            float* pp = ring + tile_slot(z + 1) * kTilePlaneFloats;
+            uint32_t* bm = bits + tile_slot(z - 1) * kTileRecords;
+            uint32_t* b0 = bits + tile_slot(z) * kTileRecords;
+            uint32_t* bp = bits + tile_slot(z + 1) * kTileRecords;
+            if (row_in) {
+                if ((fl & (TYPE_MASK | F_SPECIAL)) == T_FLUID) {
+                    float h[19];
+                    tile_odd_gather(pm, p0, pp, own, m, h);
+                    collide<BODY>(h, p);
+                    tile_odd_scatter<FORCE>(pm, p0, pp, bm, b0, bp, own, rid, m, h, fx, fy, fz);
+                } else if (p.any_inlet && (fl & TYPE_MASK) == T_INLET) {
+                    tile_odd_produce(p, pm, p0, pp, bm, b0, bp, own, rid, x, y, z);
+                }
+            }
+            __syncthreads();  // plane z is scattered: plane z - 1 is final
+            tile_odd_writeback(p, A, pm, bm, x0, y0, z - 1, z - 1 > z0 && z - 1 < z1 - 1);
+            __syncthreads();  // the slot of z - 1 is free again
+            if (z + 3 <= z1)
+                tile_load_plane(p, A, ring + tile_slot(z + 3) * kTilePlaneFloats, x0, y0,
+                                tile_wrap(z + 3, p.nz), false);
+            cp_async_commit();
+            cp_async_wait<1>();  // plane z + 2 has arrived (z + 3 may still be in flight)
+            __syncthreads();
+        }
+        // the chunk's last plane and the halo plane after it
+        tile_odd_writeback(p, A, ring + tile_slot(z1 - 1) * kTilePlaneFloats,
+                           bits + tile_slot(z1 - 1) * kTileRecords, x0, y0, z1 - 1, false);
+        tile_odd_writeback(p, A, ring + tile_slot(z1) * kTilePlaneFloats,
+                           bits + tile_slot(z1) * kTileRecords, x0, y0, z1, false);
+    }
+    if (FORCE) warp_force(fx, fy, fz, p.partial);
 }
 
 }  // namespace lbm

@@ -40,6 +40,9 @@ struct LayoutOps {
     // cudaErrorNotSupported for the other layouts.  tile_prepare raises the kernel's dynamic
     // shared-memory limit on the current device (a no-op for the other layouts).
     cudaError_t (*ab_pull_tile)(const Params& p, bool force, bool body, dim3 grid, cudaStream_t s);
+    // AA odd step of the collision layout in 2.5D tiles, updated in place in shared memory (32 | nx,
+    // ny >= 10, 19 N <= 2^32; the same grid); cudaErrorNotSupported for the other layouts
+    cudaError_t (*aa_odd_tile)(const Params& p, bool force, bool body, dim3 grid, cudaStream_t s);
     cudaError_t (*tile_prepare)();
     // boundary kernel over the special-cell list for main kind K_AA_ODD, K_AB_PULL or K_STREAM
     cudaError_t (*special)(int kind, const Params& p, bool force, bool body, cudaStream_t s);

@@ -218,6 +218,24 @@ cudaError_t ab_pull_tile(const Params& p, bool force, bool body, dim3 grid, cuda
     return ab_pull_tile_impl<L>(p, force, body, grid, s);
 }
 template <int LL>
+cudaError_t aa_odd_tile_impl(const Params& p, bool force, bool body, dim3 grid, cudaStream_t s) {
+    if constexpr (LL != LAYOUT_COLLISION) {
+        return cudaErrorNotSupported;
+    } else {
+        if (force) {
+            if (body) k_aa_odd_tile<true, true><<<grid, kTileThreads, kOddTileSmemBytes, s>>>(p);
+            else k_aa_odd_tile<true, false><<<grid, kTileThreads, kOddTileSmemBytes, s>>>(p);
+        } else {
+            if (body) k_aa_odd_tile<false, true><<<grid, kTileThreads, kOddTileSmemBytes, s>>>(p);
+            else k_aa_odd_tile<false, false><<<grid, kTileThreads, kOddTileSmemBytes, s>>>(p);
+        }
+        return cudaGetLastError();
+    }
+}
+cudaError_t aa_odd_tile(const Params& p, bool force, bool body, dim3 grid, cudaStream_t s) {
+    return aa_odd_tile_impl<L>(p, force, body, grid, s);
+}
+template <int LL>
 cudaError_t tile_prepare_impl() {
     if constexpr (LL != LAYOUT_COLLISION) {
         return cudaSuccess;
@@ -230,6 +248,15 @@ cudaError_t tile_prepare_impl() {
             e = cudaFuncSetAttribute(k_ab_pull_tile<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(k_ab_pull_tile<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        const int odd = (int)kOddTileSmemBytes;
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k_aa_odd_tile<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, odd);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k_aa_odd_tile<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, odd);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k_aa_odd_tile<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, odd);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k_aa_odd_tile<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, odd);
         return e;
     }
 }
@@ -322,7 +349,7 @@ cudaError_t halo_unpack(const Params& p, const void* below, const void* above, c
     return cudaGetLastError();
 }
 
-const LayoutOps kOps = {cells, cells2, odd_tma, ab_pull_tile, tile_prepare, special, pregather, pack, unpack,
+const LayoutOps kOps = {cells, cells2, odd_tma, ab_pull_tile, aa_odd_tile, tile_prepare, special, pregather, pack, unpack,
                         equilibrium, macro, check_finite, fill_inlet, halo_pack, halo_unpack};
 
 }  // namespace

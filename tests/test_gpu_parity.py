@@ -206,14 +206,16 @@ def test_split_step_calls_equal_one_call(scheme):
 @pytest.mark.parametrize("dims, faces", [((37, 6, 5), (1, 0, 0)), ((13, 9, 4), (0, 1, 1)),
                                          ((300, 3, 2), (1, 0, 1)), ((64, 5, 3), (0, 0, 0)),
                                          ((64, 9, 40), (0, 1, 0)), ((32, 16, 24), (1, 0, 1)),
-                                         ((96, 11, 9), (1, 1, 1))])
+                                         ((96, 11, 9), (1, 1, 1)), ((64, 21, 40), (0, 1, 0))])
 def test_layouts_bit_identical_to_stream(dims, faces, layout, scheme):
     """The layouts differ only in where a population is stored: the same collision in the same
     order gives identical populations in the bundle and collision layouts (the collision layout's
     own-population steps stage each warp's records through shared memory) and in the stream
     layout, on rows longer than a block, shorter than a warp and with a partial last warp.  With
     32 | nx the collision layout's A-B pull runs in 2.5D tiles: several z chunks (64 x 9 x 40,
-    32 x 16 x 24), ragged tile rows (ny not a multiple of 8), open faces on each axis."""
+    32 x 16 x 24), ragged tile rows (ny not a multiple of 8), open faces on each axis; with also
+    ny >= 10 its AA odd step runs in the same tiles, updated in place (32 x 16 x 24, 96 x 11 x 9,
+    64 x 21 x 40)."""
     nx, ny, nz = dims
     case = mixed_case(nx, ny, nz, faces, 1900 + nx, solid=0.15, inlet_layer=True, moving=0.3)
     for steps in (1, 2, 5):
