@@ -497,10 +497,12 @@ int classify(lbm_ctx* c) {
 // it starts on the planes the previous step wrote last (still in L2 on grids near its size).
 int z_reversed(const lbm_ctx* c, int kind) {
     switch (kind) {
+        // the tiled odd step runs its chunks of planes upwards, so the even step after it goes down
+        case K_AA_EVEN: return c->tiled_odd() ? 1 : 0;
         case K_AA_ODD: return 1;
         case K_AB_PULL: return c->cur;
         case K_STREAM: return 1;
-        default: return 0;  // AA even step, A-B / AB2 collision from the natural state
+        default: return 0;  // A-B / AB2 collision from the natural state
     }
 }
 
