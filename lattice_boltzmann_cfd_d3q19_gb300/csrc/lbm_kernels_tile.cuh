@@ -228,10 +228,9 @@ __global__ void __launch_bounds__(kTileThreads, 2) k_ab_pull_tile(Params p) {
 constexpr int kTileRecords = kHaloX * kHaloY;
 constexpr size_t kOddTileSmemBytes = kTileSmemBytes + kTileSlots * kTileRecords * sizeof(uint32_t);
 
-__device__ __forceinline__ int tile_wrap(int v, int n) {
-    v %= n;
-    return v < 0 ? v + n : v;
-}
+// v in [-n, 2 n): the halo coordinates of a tile (x in [-1, nx], y in [-1, ny + 8] with ny >= 10,
+// z in [-1, nz])
+__device__ __forceinline__ int tile_wrap(int v, int n) { return v < 0 ? v + n : v >= n ? v - n : v; }
 
 // population q of the cell from element opposite(q) of the record of x - c_q, or on a solid link
 // opposite(q) element q of its own record (the AA odd gather)
