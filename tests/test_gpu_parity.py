@@ -206,16 +206,17 @@ def test_split_step_calls_equal_one_call(scheme):
 @pytest.mark.parametrize("dims, faces", [((37, 6, 5), (1, 0, 0)), ((13, 9, 4), (0, 1, 1)),
                                          ((300, 3, 2), (1, 0, 1)), ((64, 5, 3), (0, 0, 0)),
                                          ((64, 9, 40), (0, 1, 0)), ((32, 16, 24), (1, 0, 1)),
-                                         ((96, 11, 9), (1, 1, 1)), ((64, 21, 40), (0, 1, 0))])
+                                         ((96, 11, 9), (1, 1, 1)), ((64, 21, 40), (0, 1, 0)),
+                                         ((32, 34, 20), (1, 0, 1))])
 def test_layouts_bit_identical_to_stream(dims, faces, layout, scheme):
     """The layouts differ only in where a population is stored: the same collision in the same
     order gives identical populations in the bundle and collision layouts (the collision layout's
     own-population steps stage each warp's records through shared memory) and in the stream
     layout, on rows longer than a block, shorter than a warp and with a partial last warp.  With
     32 | nx the collision layout's A-B pull runs in 2.5D tiles: several z chunks (64 x 9 x 40,
-    32 x 16 x 24), ragged tile rows (ny not a multiple of 8), open faces on each axis; with also
-    ny >= 10 its AA odd step runs in the same tiles, updated in place (32 x 16 x 24, 96 x 11 x 9,
-    64 x 21 x 40)."""
+    32 x 16 x 24), ragged tile rows (ny not a multiple of the tile's 8 rows), open faces on each
+    axis; with also ny >= 10 its AA odd step runs in the same tiles, updated in place (32 x 16 x
+    24, 96 x 11 x 9, 64 x 21 x 40, 32 x 34 x 20)."""
     nx, ny, nz = dims
     case = mixed_case(nx, ny, nz, faces, 1900 + nx, solid=0.15, inlet_layer=True, moving=0.3)
     for steps in (1, 2, 5):
@@ -228,13 +229,14 @@ def test_layouts_bit_identical_to_stream(dims, faces, layout, scheme):
 
 # ---- streaming is an exact permutation ---------------------------------------------------------------
 
-@pytest.mark.parametrize("dims, faces", [((21, 10, 7), (0, 0, 0)), ((64, 10, 17), (1, 0, 1))])
+@pytest.mark.parametrize("dims, faces", [((21, 10, 7), (0, 0, 0)), ((64, 20, 17), (1, 0, 1))])
 @pytest.mark.parametrize("scheme", ["AA", "AB", "AB2"])
 @pytest.mark.parametrize("layout", ["stream", "bundle", "collision"])
 def test_streaming_permutation_bit_exact(layout, scheme, dims, faces):
     """Collision off (tau = 1e30, g = 0), integer labels: every label must land exactly where the
     oracle (pinned to forward particle tracing) puts it -- neighbour indexing is bit-exact.  The
-    second grid takes the collision layout's tiled A-B pull (two z chunks, open x and z faces)."""
+    second grid takes the collision layout's tiled A-B pull and AA odd step (z chunks, open x and z
+    faces)."""
     nx, ny, nz = dims
     r = np.random.default_rng(41)
     flags = (r.uniform(size=nx * ny * nz) < 0.2).astype(np.uint8)
