@@ -72,6 +72,14 @@ def test_null_context_calls_fail_cleanly():
     assert lib.lbm_set_graph_launch(None, 1) == B.EINVAL
     assert lib.lbm_step_count(None) == -1
     assert lib.lbm_kernel_launches(None) == -1
+    # the slab-decomposition calls
+    assert lib.lbm_set_ghost_planes(None, 1) == B.EINVAL
+    assert lib.lbm_halo_elements(None) == -1
+    assert lib.lbm_halo_element_bytes(None) == B.EINVAL
+    assert lib.lbm_halo_pack(None, None, None) == B.EINVAL
+    assert lib.lbm_halo_unpack(None, None, None) == B.EINVAL
+    assert lib.lbm_slab_step_begin(None, None, None) == B.EINVAL
+    assert lib.lbm_slab_step_end(None, None, None) == B.EINVAL
     lib.lbm_destroy(None)  # NULL-safe
 
 
