@@ -282,6 +282,7 @@ __device__ __forceinline__ void pair_gather_h(const Params& p, const NbrPair& nb
 // blocks and lost, and keep the fp32 arrays at 4 blocks (the A-B pull has no packed form).
 constexpr bool kPackedHalfEven = true;
 constexpr bool kPackedHalfOdd = false;
+constexpr int kOddBlocksNoWalls = 4;
 template <int L>
 constexpr int pair_min_blocks(bool packed) { return L == LAYOUT_STREAM_FP16 && packed ? 6 : 4; }
 
@@ -748,20 +749,25 @@ __device__ __forceinline__ void odd2_produce(const Params& p, const NbrPair& nb,
     if constexpr (Q < 18) odd2_produce<L, Q + 1>(p, nb, n, x, y, z, ia, ib);
 }
 
-template <int L, bool FORCE, bool BODY, bool INLETS>
-__global__ void __launch_bounds__(256, pair_min_blocks<L>(kPackedHalfOdd)) k_aa_odd2(Params p) {
+// WALLS = false: the grid has no solid link (its near-wall path compiled out, fewer registers and
+// spills; the fp32 arrays and 4 blocks per SM stay: the packed half-precision form at 5 or 6 blocks
+// spilled 60-160 bytes and was slower, fp16 periodic 512^3 odd step 2.26 / 2.55 ms against 2.02)
+template <int L, bool WALLS>
+constexpr int odd2_min_blocks() { return WALLS ? pair_min_blocks<L>(kPackedHalfOdd) : kOddBlocksNoWalls; }
+template <int L, bool FORCE, bool BODY, bool INLETS, bool WALLS = true>
+__global__ void __launch_bounds__(256, odd2_min_blocks<L, WALLS>()) k_aa_odd2(Params p) {
     PairCoord c;
     float fx = 0.f, fy = 0.f, fz = 0.f;
     const bool in = grid_pair(p, c);
     PairFlags f{0, 0, 0u, 0u};
-    if (in) f = pair_flags(p, c.n, p.any_solid_link != 0);
+    if (in) f = pair_flags(p, c.n, WALLS && p.any_solid_link != 0);
     const bool act_a = in && (f.fa & (TYPE_MASK | F_SPECIAL)) == T_FLUID;
     const bool act_b = in && (f.fb & (TYPE_MASK | F_SPECIAL)) == T_FLUID;
     if (!act_a) f.ma = 0u;
     if (!act_b) f.mb = 0u;
     // warp-uniform code paths: any solid link in the warp; every working thread owns two
     // working cells
-    const bool wall = __any_sync(0xffffffffu, (f.ma | f.mb) != 0u);
+    const bool wall = WALLS && __any_sync(0xffffffffu, (f.ma | f.mb) != 0u);
     const bool both = __all_sync(0xffffffffu, act_a == act_b);
     if ((act_a || act_b) && L == LAYOUT_STREAM_FP16 && kPackedHalfOdd) {
         // half-precision storage: the gathered pairs stay packed; each population is relaxed in
