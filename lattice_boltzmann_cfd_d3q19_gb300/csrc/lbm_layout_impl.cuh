@@ -94,7 +94,12 @@ void launch_pair_i(int kind, const Params& p, dim3 grid, dim3 block, cudaStream_
             else
                 k_aa_odd2<LL, F, B, I><<<grid, block, 0, s>>>(p);
             break;
-        case K_AB_PULL: k_ab2<LL, F, B, false, I><<<grid, block, 0, s>>>(p); break;
+        case K_AB_PULL:
+            if (!p.any_solid_link)
+                k_ab2<LL, F, B, false, I, false><<<grid, block, 0, s>>>(p);
+            else
+                k_ab2<LL, F, B, false, I><<<grid, block, 0, s>>>(p);
+            break;
         case K_AB_COLLIDE: k_ab2<LL, F, B, true, I><<<grid, block, 0, s>>>(p); break;
     }
 }
