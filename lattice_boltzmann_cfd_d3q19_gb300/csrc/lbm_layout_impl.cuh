@@ -132,12 +132,17 @@ cudaError_t cells2_impl(int kind, const Params& p, bool force, bool body, dim3 g
                 else k_aa_even2_bundle<false, false><<<grid, block, 0, s>>>(p);
             }
         } else if (kind == K_AA_ODD) {
+            const bool w = p.any_solid_link != 0;  // without solid links: no near-wall path
             if (force) {
-                if (body) k_aa_odd2_bundle<true, true, true><<<grid, block, 0, s>>>(p);
-                else k_aa_odd2_bundle<true, false, true><<<grid, block, 0, s>>>(p);
+                if (body) w ? k_aa_odd2_bundle<true, true, true><<<grid, block, 0, s>>>(p)
+                            : k_aa_odd2_bundle<true, true, true, false><<<grid, block, 0, s>>>(p);
+                else w ? k_aa_odd2_bundle<true, false, true><<<grid, block, 0, s>>>(p)
+                       : k_aa_odd2_bundle<true, false, true, false><<<grid, block, 0, s>>>(p);
             } else {
-                if (body) k_aa_odd2_bundle<false, true, true><<<grid, block, 0, s>>>(p);
-                else k_aa_odd2_bundle<false, false, true><<<grid, block, 0, s>>>(p);
+                if (body) w ? k_aa_odd2_bundle<false, true, true><<<grid, block, 0, s>>>(p)
+                            : k_aa_odd2_bundle<false, true, true, false><<<grid, block, 0, s>>>(p);
+                else w ? k_aa_odd2_bundle<false, false, true><<<grid, block, 0, s>>>(p)
+                       : k_aa_odd2_bundle<false, false, true, false><<<grid, block, 0, s>>>(p);
             }
         } else if (kind == K_AB_PULL || kind == K_AB_COLLIDE) {
             const bool nat = kind == K_AB_COLLIDE;
