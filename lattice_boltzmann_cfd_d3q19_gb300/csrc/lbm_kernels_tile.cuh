@@ -126,7 +126,8 @@ __device__ __forceinline__ void tile_gather(const float* pm, const float* p0, co
 // Pipeline: while plane z is computed from the slots of z - 1, z and z + 1, the copies of z + 2
 // are in flight; after it, the results go through the freed slot of z - 1 to the destination in
 // one run per row, and the copies of z + 3 start into that slot.
-template <bool FORCE, bool BODY>
+// WALLS = false: the grid has no solid link (masks known zero, the bounce-back selects fold away)
+template <bool FORCE, bool BODY, bool WALLS = true>
 __global__ void __launch_bounds__(kTileThreads, 2) k_ab_pull_tile(Params p) {
     extern __shared__ __align__(16) float tile_smem[];
     float* ring = tile_smem;
@@ -159,7 +160,7 @@ __global__ void __launch_bounds__(kTileThreads, 2) k_ab_pull_tile(Params p) {
         uint32_t m_next = 0u;
         uint8_t fl_next = (uint8_t)T_SOLID;
         if (row_in) {
-            m_next = p.any_solid_link ? p.mask[n] : 0u;
+            m_next = (WALLS && p.any_solid_link) ? p.mask[n] : 0u;
             fl_next = p.flags[n];
         }
         for (int z = z0; z < z1; ++z, n += area) {
@@ -167,7 +168,7 @@ __global__ void __launch_bounds__(kTileThreads, 2) k_ab_pull_tile(Params p) {
             const uint32_t m = m_next;
             const uint8_t fl = fl_next;
             if (row_in && z + 1 < z1) {
-                m_next = p.any_solid_link ? p.mask[n + area] : 0u;
+                m_next = (WALLS && p.any_solid_link) ? p.mask[n + area] : 0u;
                 fl_next = p.flags[n + area];
             }
             if (row_in) {
@@ -321,7 +322,7 @@ __device__ __forceinline__ void tile_odd_writeback(const Params& p, float* A, co
 
 // Grid: (nx / 32, ceil(ny / 8), chunks), as the tiled pull.  FLUID cells that are not special are
 // gathered, collided and scattered; INLET cells produce.
-template <bool FORCE, bool BODY>
+template <bool FORCE, bool BODY, bool WALLS = true>
 __global__ void __launch_bounds__(kTileThreads, 2) k_aa_odd_tile(Params p) {
     extern __shared__ __align__(16) float tile_smem[];
     float* ring = tile_smem;
@@ -352,7 +353,7 @@ __global__ void __launch_bounds__(kTileThreads, 2) k_aa_odd_tile(Params p) {
         uint32_t m_next = 0u;
         uint8_t fl_next = (uint8_t)T_SOLID;
         if (row_in) {
-            m_next = p.any_solid_link ? p.mask[n] : 0u;
+            m_next = (WALLS && p.any_solid_link) ? p.mask[n] : 0u;
             fl_next = p.flags[n];
         }
         cp_async_wait<1>();
@@ -361,7 +362,7 @@ __global__ void __launch_bounds__(kTileThreads, 2) k_aa_odd_tile(Params p) {
             const uint32_t m = m_next;
             const uint8_t fl = fl_next;
             if (row_in && z + 1 < z1) {
-                m_next = p.any_solid_link ? p.mask[n + area] : 0u;
+                m_next = (WALLS && p.any_solid_link) ? p.mask[n + area] : 0u;
                 fl_next = p.flags[n + area];
             }
             float* pm = ring + tile_slot(z - 1) * kTilePlaneFloats;

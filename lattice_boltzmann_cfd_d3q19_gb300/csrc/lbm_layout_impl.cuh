@@ -222,12 +222,17 @@ cudaError_t ab_pull_tile_impl(const Params& p, bool force, bool body, dim3 grid,
     if constexpr (LL != LAYOUT_COLLISION) {
         return cudaErrorNotSupported;
     } else {
+        const bool w = p.any_solid_link != 0;  // without solid links: no bounce-back selects
         if (force) {
-            if (body) k_ab_pull_tile<true, true><<<grid, kTileThreads, kTileSmemBytes, s>>>(p);
-            else k_ab_pull_tile<true, false><<<grid, kTileThreads, kTileSmemBytes, s>>>(p);
+            if (body) w ? k_ab_pull_tile<true, true><<<grid, kTileThreads, kTileSmemBytes, s>>>(p)
+                        : k_ab_pull_tile<true, true, false><<<grid, kTileThreads, kTileSmemBytes, s>>>(p);
+            else w ? k_ab_pull_tile<true, false><<<grid, kTileThreads, kTileSmemBytes, s>>>(p)
+                   : k_ab_pull_tile<true, false, false><<<grid, kTileThreads, kTileSmemBytes, s>>>(p);
         } else {
-            if (body) k_ab_pull_tile<false, true><<<grid, kTileThreads, kTileSmemBytes, s>>>(p);
-            else k_ab_pull_tile<false, false><<<grid, kTileThreads, kTileSmemBytes, s>>>(p);
+            if (body) w ? k_ab_pull_tile<false, true><<<grid, kTileThreads, kTileSmemBytes, s>>>(p)
+                        : k_ab_pull_tile<false, true, false><<<grid, kTileThreads, kTileSmemBytes, s>>>(p);
+            else w ? k_ab_pull_tile<false, false><<<grid, kTileThreads, kTileSmemBytes, s>>>(p)
+                   : k_ab_pull_tile<false, false, false><<<grid, kTileThreads, kTileSmemBytes, s>>>(p);
         }
         return cudaGetLastError();
     }
@@ -240,12 +245,17 @@ cudaError_t aa_odd_tile_impl(const Params& p, bool force, bool body, dim3 grid, 
     if constexpr (LL != LAYOUT_COLLISION) {
         return cudaErrorNotSupported;
     } else {
+        const bool w = p.any_solid_link != 0;
         if (force) {
-            if (body) k_aa_odd_tile<true, true><<<grid, kTileThreads, kOddTileSmemBytes, s>>>(p);
-            else k_aa_odd_tile<true, false><<<grid, kTileThreads, kOddTileSmemBytes, s>>>(p);
+            if (body) w ? k_aa_odd_tile<true, true><<<grid, kTileThreads, kOddTileSmemBytes, s>>>(p)
+                        : k_aa_odd_tile<true, true, false><<<grid, kTileThreads, kOddTileSmemBytes, s>>>(p);
+            else w ? k_aa_odd_tile<true, false><<<grid, kTileThreads, kOddTileSmemBytes, s>>>(p)
+                   : k_aa_odd_tile<true, false, false><<<grid, kTileThreads, kOddTileSmemBytes, s>>>(p);
         } else {
-            if (body) k_aa_odd_tile<false, true><<<grid, kTileThreads, kOddTileSmemBytes, s>>>(p);
-            else k_aa_odd_tile<false, false><<<grid, kTileThreads, kOddTileSmemBytes, s>>>(p);
+            if (body) w ? k_aa_odd_tile<false, true><<<grid, kTileThreads, kOddTileSmemBytes, s>>>(p)
+                        : k_aa_odd_tile<false, true, false><<<grid, kTileThreads, kOddTileSmemBytes, s>>>(p);
+            else w ? k_aa_odd_tile<false, false><<<grid, kTileThreads, kOddTileSmemBytes, s>>>(p)
+                   : k_aa_odd_tile<false, false, false><<<grid, kTileThreads, kOddTileSmemBytes, s>>>(p);
         }
         return cudaGetLastError();
     }
@@ -266,7 +276,23 @@ cudaError_t tile_prepare_impl() {
             e = cudaFuncSetAttribute(k_ab_pull_tile<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(k_ab_pull_tile<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k_ab_pull_tile<true, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k_ab_pull_tile<true, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k_ab_pull_tile<false, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k_ab_pull_tile<false, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
         const int odd = (int)kOddTileSmemBytes;
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k_aa_odd_tile<true, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, odd);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k_aa_odd_tile<true, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, odd);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k_aa_odd_tile<false, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, odd);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k_aa_odd_tile<false, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, odd);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(k_aa_odd_tile<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, odd);
         if (e == cudaSuccess)
