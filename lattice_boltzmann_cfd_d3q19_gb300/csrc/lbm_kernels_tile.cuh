@@ -222,7 +222,9 @@ __global__ void __launch_bounds__(kTileThreads, 2) k_ab_pull_tile(Params p) {
 //   row: x-y interior records (hx 2 .. 31, hy 2 .. 7 with the next row inside the grid) of planes
 //   strictly inside the block's chunk.
 // * Every other record goes back element by element: only the slots this block wrote, recorded
-//   in a 32-bit mask per record.
+//   in a 32-bit mask per record.  On a grid without solid links the slots follow from geometry
+//   (each has one writer, x - c_q) and no mask is kept: the write-back takes them per axis, and the
+//   160 such records of a plane inside the chunk go one to a thread.
 // The whole records carry stale values in the slots of special cells, so the boundary kernel runs
 // after this kernel, not beside it.  The caller checks 32 | nx, ny >= kTileY + 2 (no two rows of a
 // halo tile are the same row of the grid) and 19 N <= 2^32.
@@ -247,9 +249,9 @@ __device__ __forceinline__ void tile_odd_gather(const float* pm, const float* p0
 }
 
 // population q to element q of the record of x + c_q, or on a solid link q to element opposite(q)
-// of its own record (with the link's momentum exchange); the element's bit is set in its
-// record's mask
-template <bool FORCE, int Q = 0>
+// of its own record (with the link's momentum exchange); BITS: the element's bit is set in its
+// record's mask (on a grid without solid links the elements written follow from geometry instead)
+template <bool FORCE, bool BITS, int Q = 0>
 __device__ __forceinline__ void tile_odd_scatter(float* pm, float* p0, float* pp, uint32_t* bm,
                                                  uint32_t* b0, uint32_t* bp, int own, int rid,
                                                  uint32_t m, const float (&h)[19], float& fx,
@@ -257,31 +259,69 @@ __device__ __forceinline__ void tile_odd_scatter(float* pm, float* p0, float* pp
     constexpr int dz = cz(Q);
     if (Q > 0 && solid_link<Q>(m)) {
         p0[own + opp(Q)] = h[Q];
-        atomicOr(&b0[rid], 1u << opp(Q));
+        if (BITS) atomicOr(&b0[rid], 1u << opp(Q));
         if (FORCE) accumulate_force<Q>(h[Q], fx, fy, fz);
     } else {
         float* dst = dz > 0 ? pp : dz < 0 ? pm : p0;
-        uint32_t* bd = dz > 0 ? bp : dz < 0 ? bm : b0;
         dst[own + cy(Q) * kTileRowFloats + cx(Q) * 19 + Q] = h[Q];
-        atomicOr(&bd[rid + cy(Q) * kHaloX + cx(Q)], 1u << Q);
+        if (BITS) {
+            uint32_t* bd = dz > 0 ? bp : dz < 0 ? bm : b0;
+            atomicOr(&bd[rid + cy(Q) * kHaloX + cx(Q)], 1u << Q);
+        }
     }
-    if constexpr (Q < 18) tile_odd_scatter<FORCE, Q + 1>(pm, p0, pp, bm, b0, bp, own, rid, m, h, fx, fy, fz);
+    if constexpr (Q < 18)
+        tile_odd_scatter<FORCE, BITS, Q + 1>(pm, p0, pp, bm, b0, bp, own, rid, m, h, fx, fy, fz);
 }
 
 // INLET producer: f_eq,q of the reservoir to element q of the record of s + c_q, links that leave
 // the grid through an OPEN face dropped (as the one-cell kernel's producer)
-template <int Q = 1>
+template <bool BITS, int Q = 1>
 __device__ __forceinline__ void tile_odd_produce(const Params& p, float* pm, float* p0, float* pp,
                                                  uint32_t* bm, uint32_t* b0, uint32_t* bp, int own,
                                                  int rid, int x, int y, int z) {
     if (!leaves_open(p, x, y, z, cx(Q), cy(Q), cz(Q))) {
         constexpr int dz = cz(Q);
         float* dst = dz > 0 ? pp : dz < 0 ? pm : p0;
-        uint32_t* bd = dz > 0 ? bp : dz < 0 ? bm : b0;
         dst[own + cy(Q) * kTileRowFloats + cx(Q) * 19 + Q] = p.heq_in[Q];
-        atomicOr(&bd[rid + cy(Q) * kHaloX + cx(Q)], 1u << Q);
+        if (BITS) {
+            uint32_t* bd = dz > 0 ? bp : dz < 0 ? bm : b0;
+            atomicOr(&bd[rid + cy(Q) * kHaloX + cx(Q)], 1u << Q);
+        }
     }
-    if constexpr (Q < 18) tile_odd_produce<Q + 1>(p, pm, p0, pp, bm, b0, bp, own, rid, x, y, z);
+    if constexpr (Q < 18) tile_odd_produce<BITS, Q + 1>(p, pm, p0, pp, bm, b0, bp, own, rid, x, y, z);
+}
+
+// the elements of mask b of record rid of the ring's plane `ring_s` to plane gz of A
+__device__ __forceinline__ void tile_odd_put(const Params& p, float* A, const float* ring_s, int x0,
+                                             int y0, uint32_t gz, int rid, uint32_t b) {
+    const int hx = rid % kHaloX, hy = rid / kHaloX;
+    const uint32_t gx = (uint32_t)tile_wrap(x0 - 1 + hx, p.nx);
+    const uint32_t gy = (uint32_t)tile_wrap(y0 - 1 + hy, p.ny);
+    float* dst = A + 19u * (gx + (uint32_t)p.nx * (gy + (uint32_t)p.ny * gz));
+    const float* src = ring_s + hy * kTileRowFloats + 1 + hx * 19;
+    for (uint32_t r = b; r; r &= r - 1u) {
+        const int e = __ffs(r) - 1;
+        dst[e] = src[e];
+    }
+}
+
+// `whole`: the x-y interior records of plane gz (hx 2 .. 31, hy 2 .. 7 with the next row inside
+// the grid) back to A in contiguous runs, warp w taking row hy = 2 + w (30 records)
+__device__ __forceinline__ void tile_odd_put_whole(const Params& p, float* A, const float* ring_s,
+                                                   int x0, int y0, uint32_t gz) {
+    const int t = (int)threadIdx.x;
+    const int w = t >> 5, lane = t & 31;
+    const int hy = 2 + w;
+    if (w < kTileY - 2 && y0 + hy < p.ny) {
+        const uint32_t gy = (uint32_t)(y0 + hy - 1);
+        float* dst = A + 19u * ((uint32_t)(x0 + 1) + (uint32_t)p.nx * (gy + (uint32_t)p.ny * gz));
+        const float* src = ring_s + hy * kTileRowFloats + 1 + 2 * 19;
+        for (int k = lane; k < (kTileX - 2) * 19; k += 32) dst[k] = src[k];
+    }
+}
+__device__ __forceinline__ bool tile_whole_record(int rid, int y0, int ny) {
+    const int hx = rid % kHaloX, hy = rid / kHaloX;
+    return hx >= 2 && hx <= kTileX - 1 && hy >= 2 && hy <= kTileY - 1 && y0 + hy < ny;
 }
 
 // plane pl of the ring (slot `ring_s`, masks `bits_s`) back to A; `whole`: the plane lies
@@ -289,35 +329,90 @@ __device__ __forceinline__ void tile_odd_produce(const Params& p, float* pm, flo
 __device__ __forceinline__ void tile_odd_writeback(const Params& p, float* A, const float* ring_s,
                                                    uint32_t* bits_s, int x0, int y0, int pl,
                                                    bool whole) {
-    const int t = (int)threadIdx.x;
     const uint32_t gz = (uint32_t)tile_wrap(pl, p.nz);
-    if (whole) {
-        // warp w: row hy = 2 + w, records hx = 2 .. 31 (one run of 30 records)
-        const int w = t >> 5, lane = t & 31;
-        const int hy = 2 + w;
-        if (w < kTileY - 2 && y0 + hy < p.ny) {
-            const uint32_t gy = (uint32_t)(y0 + hy - 1);
-            float* dst = A + 19u * ((uint32_t)(x0 + 1) + (uint32_t)p.nx * (gy + (uint32_t)p.ny * gz));
-            const float* src = ring_s + hy * kTileRowFloats + 1 + 2 * 19;
-            for (int k = lane; k < (kTileX - 2) * 19; k += 32) dst[k] = src[k];
-        }
-    }
-    for (int rid = t; rid < kTileRecords; rid += kTileThreads) {
+    if (whole) tile_odd_put_whole(p, A, ring_s, x0, y0, gz);
+    for (int rid = (int)threadIdx.x; rid < kTileRecords; rid += kTileThreads) {
         const uint32_t b = bits_s[rid];
         if (b == 0u) continue;
         bits_s[rid] = 0u;
-        const int hx = rid % kHaloX, hy = rid / kHaloX;
-        if (whole && hx >= 2 && hx <= kTileX - 1 && hy >= 2 && hy <= kTileY - 1 && y0 + hy < p.ny)
-            continue;
-        const uint32_t gx = (uint32_t)tile_wrap(x0 - 1 + hx, p.nx);
-        const uint32_t gy = (uint32_t)tile_wrap(y0 - 1 + hy, p.ny);
-        float* dst = A + 19u * (gx + (uint32_t)p.nx * (gy + (uint32_t)p.ny * gz));
-        const float* src = ring_s + hy * kTileRowFloats + 1 + hx * 19;
-        for (uint32_t r = b; r; r &= r - 1u) {
-            const int e = __ffs(r) - 1;
-            dst[e] = src[e];
+        if (whole && tile_whole_record(rid, y0, p.ny)) continue;
+        tile_odd_put(p, A, ring_s, x0, y0, gz, rid, b);
+    }
+}
+
+// On a grid without solid links every element of the AA odd step has one writer by geometry:
+// element q of the record of x is written by the cell x - c_q, whatever that cell's type (a cell
+// that is not updated leaves the value loaded with the plane, which goes back unchanged; the
+// special cells' boundary kernel runs after this kernel).  So the elements a block writes back
+// are those whose writer lies in its tile and chunk, with no per-element record: along one axis,
+// a record at position p of a span of t cells (p = -1 and p = t its halo) takes the elements
+// whose c along the axis has p - c in [0, t - 1].
+constexpr uint32_t tile_vel_mask(int axis, int c) {
+    uint32_t m = 0u;
+    for (int q = 0; q < 19; ++q)
+        if ((axis == 0 ? cx(q) : axis == 1 ? cy(q) : cz(q)) == c) m |= 1u << q;
+    return m;
+}
+template <int AXIS>
+__device__ __forceinline__ uint32_t tile_axis_mask(int pos, int t) {
+    constexpr uint32_t lo = tile_vel_mask(AXIS, -1), mid = tile_vel_mask(AXIS, 0),
+                       hi = tile_vel_mask(AXIS, 1);
+    return (pos >= -1 && pos <= t - 2 ? lo : 0u) | (pos >= 0 && pos <= t - 1 ? mid : 0u) |
+           (pos >= 1 && pos <= t ? hi : 0u);
+}
+__device__ __forceinline__ uint32_t tile_xy_mask(int rid, int ty_n) {
+    const int hx = rid % kHaloX, hy = rid / kHaloX;
+    return tile_axis_mask<0>(hx - 1, kTileX) & tile_axis_mask<1>(hy - 1, ty_n);
+}
+// The records of a plane that do not go back whole, when all kTileY rows of the tile are in the
+// grid: halo rows hy = 0 and 9 (c 0 .. 67), the columns hx = 0, 1, 32, 33 of rows 2 .. 7
+// (c 68 .. 91), edge rows hy = 1 and 8 (c 92 .. 159); given to threads 96 .. 255, so that warps 6
+// and 7, which hold no whole row, take the edge rows, whose records have 14 elements each.
+constexpr int kTileEdgeRecords = 4 * kHaloX + 4 * (kTileY - 2);
+static_assert(kTileEdgeRecords == 160 && kTileThreads - 96 == kTileEdgeRecords, "edge record list");
+__device__ __forceinline__ int tile_edge_record(int c) {
+    if (c < 2 * kHaloX) return (c < kHaloX ? 0 : (kHaloY - 1) * kHaloX) + c % kHaloX;
+    if (c < 2 * kHaloX + 4 * (kTileY - 2)) {
+        const int i = c - 2 * kHaloX, k = i & 3;
+        return (2 + (i >> 2)) * kHaloX + (k < 2 ? k : kTileX - 2 + k);
+    }
+    const int i = c - 2 * kHaloX - 4 * (kTileY - 2);
+    return (i < kHaloX ? 1 : kTileY) * kHaloX + i % kHaloX;
+}
+// A thread's records of the static write-back and their x-y masks: rid = t and t + 256 of a plane
+// written record by record, and its record of the list above (thread t >= 96, full tiles)
+struct TileOwned {
+    uint32_t m0 = 0u, m1 = 0u, me = 0u;
+    int re = 0;
+    __device__ __forceinline__ TileOwned(int y0, int ny) {
+        const int t = (int)threadIdx.x;
+        const int ty_n = min(kTileY, ny - y0);
+        m0 = tile_xy_mask(t, ty_n);
+        if (t + kTileThreads < kTileRecords) m1 = tile_xy_mask(t + kTileThreads, ty_n);
+        if (t >= kTileThreads - kTileEdgeRecords && ty_n == kTileY) {
+            re = tile_edge_record(t - (kTileThreads - kTileEdgeRecords));
+            me = tile_xy_mask(re, ty_n);
         }
     }
+};
+// plane pl of the ring back to A on a grid without solid links; mz: the plane's z mask
+__device__ __forceinline__ void tile_odd_writeback_static(const Params& p, float* A,
+                                                          const float* ring_s, int x0, int y0,
+                                                          int pl, uint32_t mz, bool whole,
+                                                          const TileOwned& o) {
+    const uint32_t gz = (uint32_t)tile_wrap(pl, p.nz);
+    const int t = (int)threadIdx.x;
+    if (whole) {
+        tile_odd_put_whole(p, A, ring_s, x0, y0, gz);
+        if (y0 + kTileY <= p.ny) {
+            if (o.me) tile_odd_put(p, A, ring_s, x0, y0, gz, o.re, o.me);
+            return;
+        }
+    }
+    if (const uint32_t b = o.m0 & mz; b && !(whole && tile_whole_record(t, y0, p.ny)))
+        tile_odd_put(p, A, ring_s, x0, y0, gz, t, b);
+    if (const uint32_t b = o.m1 & mz; b && !(whole && tile_whole_record(t + kTileThreads, y0, p.ny)))
+        tile_odd_put(p, A, ring_s, x0, y0, gz, t + kTileThreads, b);
 }
 
 // Grid: (nx / 32, ceil(ny / 8), chunks), as the tiled pull.  FLUID cells that are not special are
@@ -337,7 +432,9 @@ __global__ void __launch_bounds__(kTileThreads, 2) k_aa_odd_tile(Params p) {
     float* A = static_cast<float*>(p.A);
     float fx = 0.f, fy = 0.f, fz = 0.f;
     if (z0 < z1) {
-        for (int k = (int)threadIdx.x; k < kTileSlots * kTileRecords; k += kTileThreads) bits[k] = 0u;
+        if (WALLS)
+            for (int k = (int)threadIdx.x; k < kTileSlots * kTileRecords; k += kTileThreads) bits[k] = 0u;
+        const TileOwned owned(y0, p.ny);  // the geometric write-back (grids without solid links)
         for (int z = z0 - 1; z <= z0 + 1; ++z)
             tile_load_plane(p, A, ring + tile_slot(z) * kTilePlaneFloats, x0, y0,
                             tile_wrap(z, p.nz), false);
@@ -376,13 +473,18 @@ __global__ void __launch_bounds__(kTileThreads, 2) k_aa_odd_tile(Params p) {
                     float h[19];
                     tile_odd_gather(pm, p0, pp, own, m, h);
                     collide<BODY>(h, p);
-                    tile_odd_scatter<FORCE>(pm, p0, pp, bm, b0, bp, own, rid, m, h, fx, fy, fz);
+                    tile_odd_scatter<FORCE, WALLS>(pm, p0, pp, bm, b0, bp, own, rid, m, h, fx, fy, fz);
                 } else if (p.any_inlet && (fl & TYPE_MASK) == T_INLET) {
-                    tile_odd_produce(p, pm, p0, pp, bm, b0, bp, own, rid, x, y, z);
+                    tile_odd_produce<WALLS>(p, pm, p0, pp, bm, b0, bp, own, rid, x, y, z);
                 }
             }
             __syncthreads();  // plane z is scattered: plane z - 1 is final
-            tile_odd_writeback(p, A, pm, bm, x0, y0, z - 1, z - 1 > z0 && z - 1 < z1 - 1);
+            if (WALLS)
+                tile_odd_writeback(p, A, pm, bm, x0, y0, z - 1, z - 1 > z0 && z - 1 < z1 - 1);
+            else
+                tile_odd_writeback_static(p, A, pm, x0, y0, z - 1,
+                                          tile_axis_mask<2>(z - 1 - z0, z1 - z0),
+                                          z - 1 > z0 && z - 1 < z1 - 1, owned);
             __syncthreads();  // the slot of z - 1 is free again
             if (z + 3 <= z1)
                 tile_load_plane(p, A, ring + tile_slot(z + 3) * kTilePlaneFloats, x0, y0,
@@ -392,10 +494,14 @@ __global__ void __launch_bounds__(kTileThreads, 2) k_aa_odd_tile(Params p) {
             __syncthreads();
         }
         // the chunk's last plane and the halo plane after it
-        tile_odd_writeback(p, A, ring + tile_slot(z1 - 1) * kTilePlaneFloats,
-                           bits + tile_slot(z1 - 1) * kTileRecords, x0, y0, z1 - 1, false);
-        tile_odd_writeback(p, A, ring + tile_slot(z1) * kTilePlaneFloats,
-                           bits + tile_slot(z1) * kTileRecords, x0, y0, z1, false);
+        for (int pl = z1 - 1; pl <= z1; ++pl) {
+            const float* ring_s = ring + tile_slot(pl) * kTilePlaneFloats;
+            if (WALLS)
+                tile_odd_writeback(p, A, ring_s, bits + tile_slot(pl) * kTileRecords, x0, y0, pl, false);
+            else
+                tile_odd_writeback_static(p, A, ring_s, x0, y0, pl,
+                                          tile_axis_mask<2>(pl - z0, z1 - z0), false, owned);
+        }
     }
     if (FORCE) warp_force(fx, fy, fz, p.partial);
 }

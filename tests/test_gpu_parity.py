@@ -227,6 +227,35 @@ def test_layouts_bit_identical_to_stream(dims, faces, layout, scheme):
         assert np.abs(Fl - Fs).max() <= 1e-6 * max(1.0, float(np.abs(Fs).max())), (steps, Fl, Fs)
 
 
+@pytest.mark.parametrize("scheme", ["AA", "AB"])
+@pytest.mark.parametrize("walls", ["moving_only", "none_inlet", "none"])
+@pytest.mark.parametrize("dims, faces", [((32, 16, 24), (1, 0, 1)), ((96, 11, 9), (1, 1, 1)),
+                                         ((64, 21, 40), (0, 1, 0)), ((32, 34, 20), (1, 0, 1)),
+                                         ((64, 20, 17), (0, 0, 0))])
+def test_collision_tiles_without_solid_links(dims, faces, walls, scheme):
+    """A grid without SOLID cells runs the collision layout's tiled kernels without the
+    bounce-back path; the tiled AA odd step then writes back the elements whose writer (the cell
+    x - c_q of element q of the record of x) lies in the block's tile and chunk.  Moving walls
+    only (their neighbours are special cells, stepped by the boundary kernel after the tiled
+    step), an inlet layer (producers) or neither; open faces, ragged tile rows, z chunks, nx = 32
+    (a halo column is the grid's other edge column).  Bit-identical to the stream layout, and
+    within the parity bar of the oracle."""
+    nx, ny, nz = dims
+    moving = walls == "moving_only"
+    case = mixed_case(nx, ny, nz, faces, 2300 + nx + ny, solid=0.15 if moving else 0.0,
+                      inlet_layer=walls != "none", moving=1.0 if moving else 0.0)
+    assert not (case.flags == wl.SOLID).any()
+    for steps in (1, 2, 5):
+        fs, Fs = case.run_gpu(steps, "stream", scheme, want_force=True, pairs=False)
+        fc, Fc = case.run_gpu(steps, "collision", scheme, want_force=True)
+        fl = case.fluid
+        assert np.array_equal(fc[:, fl], fs[:, fl]), (steps, np.abs(fc[:, fl] - fs[:, fl]).max())
+        assert np.abs(Fc - Fs).max() <= 1e-6 * max(1.0, float(np.abs(Fs).max())), (steps, Fc, Fs)
+    fo, Fo = case.run_oracle(5, want_force=True)
+    assert max_fluid_diff(case, fc, fo) <= TOL_F, max_fluid_diff(case, fc, fo)
+    assert np.abs(Fc - Fo).max() <= 1e-4 * max(1.0, float(np.abs(Fo).max())), (Fc, Fo)
+
+
 # ---- streaming is an exact permutation ---------------------------------------------------------------
 
 @pytest.mark.parametrize("dims, faces", [((21, 10, 7), (0, 0, 0)), ((64, 20, 17), (1, 0, 1))])
