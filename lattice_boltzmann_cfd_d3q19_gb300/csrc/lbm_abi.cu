@@ -1278,6 +1278,23 @@ static int launch_planes(lbm_ctx* c, int kind, const Params& p0, int z0, int dz,
     return LBM_OK;
 }
 
+// Force partial triples of a slab step (the launches of lbm_slab_step_begin): the main kernel over
+// the owned planes 1 .. nz - 2, and for the pull the boundary kernel over the special cells, split
+// at the edge planes into `edges` + 1 ranges (one range for a slab that owns one plane).
+static size_t slab_step_triples(const lbm_ctx* c, int kind, int edges) {
+    const bool two = c->pairs_for(kind);
+    const dim3 g = two ? c->grid2 : c->grid;
+    size_t blocks = (size_t)g.x * g.y * (size_t)(c->n[2] - 2);
+    if (kind == K_AB_PULL) {
+        if (edges == 2)
+            blocks += special_blocks(c->sp_lo_end) + special_blocks(c->n_special - c->sp_hi_begin) +
+                      special_blocks(c->sp_hi_begin - c->sp_lo_end);
+        else
+            blocks += special_blocks(c->n_special);
+    }
+    return blocks * kWarpsPerBlock;
+}
+
 int lbm_slab_step_begin(lbm_ctx* c, void* lo, void* hi) {
     if (c && c->split)
         return fail(LBM_ESTATE, "lbm_slab_step_begin: the previous slab step is still open");
@@ -1290,6 +1307,11 @@ int lbm_slab_step_begin(lbm_ctx* c, void* lo, void* hi) {
     // the edge planes 1 and nz - 2 (one plane when the slab owns one), their special cells, and
     // the pack of their outgoing populations, on the context stream
     const int edges = nz - 2 > 1 ? 2 : 1;
+    // the kernels' force partials must fit before any of them is launched
+    const size_t need = slab_step_triples(c, kind, edges);
+    if (need > c->partial_cap)
+        return fail(LBM_ESTATE, "lbm_slab_step_begin: %zu force partials exceed the %zu allocated",
+                    need, c->partial_cap);
     size_t slot = 0;
     int rc = launch_planes(c, kind, p, 1, nz - 3, edges, 0, 0, slot, c->stream);
     if (rc == LBM_OK) {
@@ -1316,9 +1338,6 @@ int lbm_slab_step_begin(lbm_ctx* c, void* lo, void* hi) {
         return rc;
     }
     if (e != cudaSuccess) return cuda_fail(e, "lbm_slab_step_begin: join");
-    if (slot > c->partial_cap)
-        return fail(LBM_ESTATE, "lbm_slab_step_begin: %zu force partials exceed the %zu allocated",
-                    slot, c->partial_cap);
     c->force_triples = slot;
     c->split = true;
     return LBM_OK;
