@@ -162,8 +162,10 @@ def test_lid_driven_cavity_256_windows_and_mass():
 @pytest.mark.parametrize("layout", ["stream", "bundle", "collision"])
 def test_degenerate_grids(layout):
     """Grids of one cell, one row, one plane (a warp holding one or a few cells), in every layout;
-    and a two-cell row between an inlet and an open face."""
-    for (nx, ny, nz) in [(1, 1, 1), (2, 1, 1), (1, 3, 1), (2, 2, 2), (5, 1, 7)]:
+    a thin 256 x 1 x 7 grid, whose tiled collision-layout pull has more blocks than the one-cell
+    grid (its force partials are sized for both); and a two-cell row between an inlet and an open
+    face."""
+    for (nx, ny, nz) in [(1, 1, 1), (2, 1, 1), (1, 3, 1), (2, 2, 2), (5, 1, 7), (256, 1, 7)]:
         case = Case(nx, ny, nz, 0.7, random_state(nx * ny * nz, 7), g=(1e-4, 0, 0))
         fo, _ = case.run_oracle(5)
         for scheme in SCHEMES:
@@ -207,7 +209,7 @@ def test_split_step_calls_equal_one_call(scheme):
                                          ((300, 3, 2), (1, 0, 1)), ((64, 5, 3), (0, 0, 0)),
                                          ((64, 9, 40), (0, 1, 0)), ((32, 16, 24), (1, 0, 1)),
                                          ((96, 11, 9), (1, 1, 1)), ((64, 21, 40), (0, 1, 0)),
-                                         ((32, 34, 20), (1, 0, 1))])
+                                         ((32, 34, 20), (1, 0, 1)), ((32, 12, 6), (0, 0, 1))])
 def test_layouts_bit_identical_to_stream(dims, faces, layout, scheme):
     """The layouts differ only in where a population is stored: the same collision in the same
     order gives identical populations in the bundle and collision layouts (the collision layout's
@@ -216,7 +218,8 @@ def test_layouts_bit_identical_to_stream(dims, faces, layout, scheme):
     32 | nx the collision layout's A-B pull runs in 2.5D tiles: several z chunks (64 x 9 x 40,
     32 x 16 x 24), ragged tile rows (ny not a multiple of the tile's 8 rows), open faces on each
     axis; with also ny >= 10 its AA odd step runs in the same tiles, updated in place (32 x 16 x
-    24, 96 x 11 x 9, 64 x 21 x 40, 32 x 34 x 20)."""
+    24, 96 x 11 x 9, 64 x 21 x 40, 32 x 34 x 20, and 32 x 12 x 6 in one chunk whose halo planes
+    wrap onto its own planes)."""
     nx, ny, nz = dims
     case = mixed_case(nx, ny, nz, faces, 1900 + nx, solid=0.15, inlet_layer=True, moving=0.3)
     for steps in (1, 2, 5):
@@ -231,14 +234,14 @@ def test_layouts_bit_identical_to_stream(dims, faces, layout, scheme):
 @pytest.mark.parametrize("walls", ["moving_only", "none_inlet", "none"])
 @pytest.mark.parametrize("dims, faces", [((32, 16, 24), (1, 0, 1)), ((96, 11, 9), (1, 1, 1)),
                                          ((64, 21, 40), (0, 1, 0)), ((32, 34, 20), (1, 0, 1)),
-                                         ((64, 20, 17), (0, 0, 0))])
+                                         ((64, 20, 17), (0, 0, 0)), ((32, 12, 6), (0, 0, 1))])
 def test_collision_tiles_without_solid_links(dims, faces, walls, scheme):
     """A grid without SOLID cells runs the collision layout's tiled kernels without the
     bounce-back path; the tiled AA odd step then writes back the elements whose writer (the cell
     x - c_q of element q of the record of x) lies in the block's tile and chunk.  Moving walls
     only (their neighbours are special cells, stepped by the boundary kernel after the tiled
-    step), an inlet layer (producers) or neither; open faces, ragged tile rows, z chunks, nx = 32
-    (a halo column is the grid's other edge column).  Bit-identical to the stream layout, and
+    step), an inlet layer (producers) or neither; open faces, ragged tile rows, several z chunks
+    and one (32 x 12 x 6), nx = 32 (a halo column is the grid's other edge column).  Bit-identical to the stream layout, and
     within the parity bar of the oracle."""
     nx, ny, nz = dims
     moving = walls == "moving_only"
