@@ -99,3 +99,28 @@ def test_code_tokens_ignore_comments_not_code():
     assert bench.code_tokens(a) != bench.code_tokens(a.replace("2.0f", "3.0f"))
     s = 'const char* u = "x // y /* z */"; char c = \'"\';'
     assert bench.code_tokens(s) == s
+
+
+def test_reference_arm_prints_the_contract_line(capsys, monkeypatch):
+    """`bench.py --impl reference` times the CPU oracle on a bounded slab of the benchmark's
+    porous medium and prints one JSON line with the contract's keys; under torchrun the ranks
+    other than 0 print nothing."""
+    import json
+    for k in ("WORLD_SIZE", "RANK", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+    bench.main(["--impl", "reference", "--steps", "1", "--warmup", "3"])
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC
+    assert line["value"] > 0 and line["unit"] == bench.UNIT and line["n_gpus"] == 1
+    assert (line["steps"], line["warmup"]) == (1, 3) and line["higher_is_better"] is True
+    assert line["vs_baseline"] is None and line["dtype"] == "f64" and line["data"] == "synthetic"
+    assert "workload" in line["config"] and "sample" in line["config"]
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == line["value"] and cb["cores"] >= 1
+    assert cb["sample"] == line["config"]["sample"]
+    assert line["e2e"] == {"value": line["value"], "unit": line["unit"],
+                           "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    monkeypatch.setenv("RANK", "1")
+    bench.main(["--impl", "reference", "--steps", "1", "--warmup", "3"])
+    assert capsys.readouterr().out == ""
